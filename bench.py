@@ -1,0 +1,495 @@
+"""Benchmark of the paged decode hot path on GB300.
+
+One step = one decode step of the workload through the library: the slot
+map of the new tokens, then for every layer the cache write of the new
+tokens and the paged decode (partition pass + merge).  The headline metric
+is paged-decode KV GB/s: algorithmic bytes of all decode calls of the step
+(q + the gathered K/V of the c_s live tokens + out + block-table entries and
+context lengths) over the step time; also reported as % of the measured HBM
+peak, attention tokens/s per layer and us per layer.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c3|c5|c2|c4|c1]
+    python bench.py --impl reference ...   # the CPU oracle as the reference arm
+
+N > 1 runs under torch.distributed.run: every rank runs its own replica of
+the workload (sequences shard across GPUs with no exchange: weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import configs  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c3", choices=["c1", "c2", "c3", "c4", "c5"])
+    ap.add_argument("--layers", type=int, default=0, help="use only the first L layers (profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--partition-tokens", type=int, default=0)
+    ap.add_argument("--graph", action="store_true", help="replay each step as one CUDA graph")
+    return ap.parse_args()
+
+
+def make_workload(name: str, layers: int):
+    cid = int(name[1:])
+    if cid == 3:
+        return configs.config3(layers or 40)
+    if cid == 5:
+        return configs.config5(layers or 32)
+    return configs.ALL[cid]()
+
+
+def decode_bytes(w, bt, ctx) -> int:
+    """Algorithmic bytes of one decode call: per (s, h): q (2D) + K and V of the c_s live
+    tokens (2 * c_s * D * 2) + out (2D); per s: ceil(c_s/B) table entries and one context length."""
+    S, H, D, B = w.num_seqs, w.num_heads, w.head_dim, w.block_size
+    ctx = np.asarray(ctx, dtype=np.int64)
+    per_pair = 2 * D + 4 * ctx * D + 2 * D
+    return int(H * per_pair.sum() + 4 * (-(-ctx // B)).sum() + 4 * S)
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "paged_kv_cache_158_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def committed_traffic(workload_name: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(workload_name)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = os.path.join("/tmp", f"pa_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.uuid:
+            cmd.insert(1, f"--id={self.uuid}")
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Max of a per-rank scalar (timing only; no data-path collective)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(bytes_per_rank_step: int, world: int, ms_per_step_max: float) -> float:
+    """Whole-job GB/s: every rank processed bytes_per_rank_step per step; the job's step
+    time is the slowest rank's."""
+    return bytes_per_rank_step * world / (ms_per_step_max * 1e-3) / 1e9
+
+
+# ---------------------------------------------------------------- our arm
+
+class Step:
+    """Device state and the launch sequence of one decode step."""
+
+    def __init__(self, w, device):
+        import torch
+
+        import paged_kv_cache_158_gb300 as pa
+        from paged_kv_cache_158_gb300.pool import BlockManager
+        from workloads import gpu
+
+        self.pa, self.w, self.dev = pa, w, device
+        dw = gpu.materialize(w, device=device)
+        self.dw = dw
+        self.copy_pairs = None
+        if w.block_tables is None:          # shared-prefix workload: the block manager plans
+            bm = BlockManager(w.num_blocks, w.block_size, w.num_seqs, w.max_blocks_per_seq, w.free_order)
+            bm.add_sequence(0)
+            bm.append_tokens(0, w.prefix_len)
+            for s in range(1, w.num_seqs):
+                bm.fork(0, s)
+            for s in range(w.num_seqs):
+                bm.append_tokens(s, int(w.suffix_lens[s]))
+            self.copy_pairs = torch.from_numpy(bm.take_copies()).to(device)
+            dw.block_tables = torch.from_numpy(bm.block_tables()).to(device)
+        self.bt_host = dw.block_tables.cpu().numpy()
+        self.ctx_host = w.context_lens.copy()
+        self.max_ctx = int(self.ctx_host.max())
+        L = len(dw.layers)
+        self.outs = [torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=device)
+                     for _ in range(L)]
+        self.slots = torch.empty(dw.token_seq.numel(), dtype=torch.int64, device=device)
+        self.ws = pa.decode_workspace(w.num_seqs, w.num_heads, w.head_dim, self.max_ctx, device)
+        self.bytes_per_decode = decode_bytes(w, self.bt_host, self.ctx_host)
+        self.max_parts = -(-self.max_ctx // pa.pa_decode_partition_tokens(w.num_seqs, w.num_heads, self.max_ctx))
+        self.stream = torch.cuda.current_stream(device)
+
+    def launches_per_step(self) -> int:
+        L = len(self.dw.layers)
+        per_layer = 1 + 1 + (1 if self.max_parts > 1 else 0)
+        return 1 + L * per_layer + (1 if self.copy_pairs is not None else 0)
+
+    def run(self, decode_events=None):
+        pa, w, dw = self.pa, self.w, self.dw
+        if self.copy_pairs is not None:
+            pa.pa_copy_blocks(dw.key_caches, dw.value_caches, self.copy_pairs, self.stream)
+        pa.pa_slot_mapping(self.slots, dw.block_tables, dw.token_seq, dw.token_pos, w.block_size,
+                           w.num_blocks, self.stream)
+        for i in range(len(dw.layers)):
+            pa.pa_reshape_and_cache(dw.keys_new[i], dw.values_new[i], dw.key_caches[i], dw.value_caches[i],
+                                    self.slots, self.stream)
+            if decode_events is not None:
+                decode_events[i][0].record(self.stream)
+            pa.pa_decode(self.outs[i], dw.queries[i], dw.key_caches[i], dw.value_caches[i], dw.block_tables,
+                         dw.context_lens, w.scale, self.max_ctx, self.ws, self.stream)
+            if decode_events is not None:
+                decode_events[i][1].record(self.stream)
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import paged_kv_cache_158_gb300 as pa
+
+    device = torch.device("cuda", local if world > 1 else 0)
+    if args.partition_tokens:
+        pa.pa_decode_set_partition_tokens(args.partition_tokens)
+    w = make_workload(args.workload, args.layers)
+    st = Step(w, device)
+    L = len(st.dw.layers)
+    for _ in range(args.warmup):
+        st.run()
+    torch.cuda.synchronize(device)
+    status, bits = pa.pa_check_errors()
+    if status != pa.PA_OK:
+        raise RuntimeError(f"device error word after warm-up: {pa.pa_status_string(status)} 0x{bits:x}")
+
+    graph = None
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            st.stream = torch.cuda.current_stream(device)
+            st.run()
+        st.stream = torch.cuda.current_stream(device)
+        graph.replay()
+        torch.cuda.synchronize(device)
+
+    K = args.steps
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+          for _ in range(K)] if graph is None else None
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(st.stream)
+    for k in range(K):
+        if graph is not None:
+            graph.replay()
+        else:
+            st.run(ev[k])
+    t1.record(st.stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    ms_total_max = max_over_ranks(ms_total, world)
+    status, bits = pa.pa_check_errors()
+    if status != pa.PA_OK:
+        raise RuntimeError(f"device error word after timing: {pa.pa_status_string(status)} 0x{bits:x}")
+
+    ms_step = ms_total_max / K
+    bytes_step = st.bytes_per_decode * L
+    value = weak_scaling_value(bytes_step, world, ms_step)
+    peak, peak_kind = measured_peak()
+    if ev is not None:
+        dec_ms = [a.elapsed_time(b) for row in ev for a, b in row]
+        dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    else:
+        dec_avg_ms = ms_step / L
+    achieved = st.bytes_per_decode / (dec_avg_ms * 1e-3) / 1e9
+    ctx_tokens = int(st.ctx_host.sum())
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(st, args, world, device)
+
+    line = {
+        "metric": "paged-decode KV GB/s (algorithmic q + gathered K/V + out bytes over step time)",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16 in, f32 accumulate",
+        "data": "synthetic (seeded SplitMix64 / Box-Muller values, seeded block tables)",
+        "config": {
+            "workload": w.name,
+            "layers": L, "num_seqs": w.num_seqs, "num_heads": w.num_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "num_blocks_per_layer": w.num_blocks,
+            "context_tokens": ctx_tokens, "max_context_len": st.max_ctx,
+            "partition_tokens": pa.pa_decode_partition_tokens(w.num_seqs, w.num_heads, st.max_ctx),
+            "l2": "inputs larger than L2: each layer's cache is read once per step",
+            "kv_pool_gb": round(w.pool_bytes_all_layers() / 1e9, 3),
+            "cuda_graph": bool(args.graph),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
+        "us_per_layer": round(ms_step * 1e3 / L, 3),
+        "decode_tokens_per_s_per_layer": round(w.num_seqs / (ms_step * 1e-3 / L), 1),
+        "context_tokens_per_s_per_layer": round(ctx_tokens / (ms_step * 1e-3 / L), 1),
+        "decode_bytes_per_layer": st.bytes_per_decode,
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "pa_decode (partition + merge kernels)",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "launch_us": round(dec_avg_ms * 1e3, 3),
+            "traffic": committed_traffic(w.name),
+        },
+        "clocks": clk,
+        "gpu_launches": st.launches_per_step() * K,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=12.0)
+    return line
+
+
+def measure_e2e(st, args, world, device):
+    """Same metric through the public API with the step's inputs in pinned host memory:
+    every step copies q / new K,V / token ids / tables / lengths host->device, runs the
+    step and reads every layer's output back."""
+    import torch
+    dw = st.dw
+    pin = lambda t: t.detach().cpu().pin_memory()  # noqa: E731
+    h_q = [pin(t) for t in dw.queries]
+    h_k = [pin(t) for t in dw.keys_new]
+    h_v = [pin(t) for t in dw.values_new]
+    h_small = [pin(t) for t in (dw.token_seq, dw.token_pos, dw.block_tables, dw.context_lens)]
+    d_small = [dw.token_seq, dw.token_pos, dw.block_tables, dw.context_lens]
+    h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in st.outs]
+    h2d = sum(t.numel() * t.element_size() for t in h_q + h_k + h_v + h_small)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    K = max(3, min(args.steps, 100))
+    s = st.stream
+
+    def one():
+        for hs, ds in zip(h_small, d_small):
+            ds.copy_(hs, non_blocking=True)
+        for i in range(len(dw.layers)):
+            dw.queries[i].copy_(h_q[i], non_blocking=True)
+            dw.keys_new[i].copy_(h_k[i], non_blocking=True)
+            dw.values_new[i].copy_(h_v[i], non_blocking=True)
+        st.run()
+        for i in range(len(dw.layers)):
+            h_out[i].copy_(st.outs[i], non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize(device)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        one()
+    torch.cuda.synchronize(device)
+    dt = max_over_ranks(time.perf_counter() - t0, world) / K
+    L = len(dw.layers)
+    return {"value": round(st.bytes_per_decode * L * world / dt / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(dt * 1e3, 4), "steps": K,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample(w):
+    """Host inputs of the bounded sample: layer 0 of the workload, every sequence and head."""
+    import oracle
+    from workloads import gpu
+    if w.block_tables is None:
+        raise ValueError("the CPU baseline sample needs static block tables")
+    kc, vc = gpu.host_pool(w, 0)
+    q, _, _ = gpu.host_small(w, 0)
+    return oracle, q, kc, vc
+
+
+def cpu_baseline(w, budget_s: float):
+    oracle, q, kc, vc = oracle_sample(w)
+    nbytes = decode_bytes(w, w.block_tables, w.context_lens)
+    reps, t_total = 0, 0.0
+    while t_total < budget_s or reps < 1:
+        t0 = time.perf_counter()
+        _, _, rc = oracle.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, want64=False)
+        t_total += time.perf_counter() - t0
+        reps += 1
+        assert rc == 0
+    return {"value": round(nbytes * reps / t_total / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{w.name} layer 0 decode (all {w.num_seqs} seqs x {w.num_heads} heads), "
+                      f"{reps} repetitions, {t_total:.1f} s",
+            "host_cpus": os.cpu_count()}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = make_workload(args.workload, 1)
+    oracle, q, kc, vc = oracle_sample(w)
+    nbytes = decode_bytes(w, w.block_tables, w.context_lens)
+    for _ in range(args.warmup):
+        oracle.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, want64=False)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, want64=False)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = nbytes / dt / 1e9
+    sample = f"{w.name} layer 0 decode per step (all {w.num_seqs} seqs x {w.num_heads} heads)"
+    return {
+        "impl": "reference",
+        "metric": "paged-decode KV GB/s (algorithmic q + gathered K/V + out bytes over step time)",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "layers": 1, "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    world_env = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        line = run_reference(args, int(os.environ.get("RANK", "0")), world_env)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    rank, world, local = dist_setup(args.gpus)
+    line = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,204 @@
+/*
+ * pa.h — C ABI of libpa.so, a GB300 (sm_103a) library for the PagedAttention
+ * decode hot path: single-query attention over a paged fp16 KV cache, the
+ * cache write that scatters new tokens into their slots, the copy-on-write
+ * block copy, and the slot map.
+ *
+ * Sources (page title, section):
+ *   [P1] "深入解析LLM推理引擎：从PagedAttention到调度优化"
+ *   [P2] "vLLM推理加速深度解读：PagedAttention如何提升10x吞吐量"
+ *   [P3] "vLLM基础架构：核心组件、PagedAttention原理、KV Cache管理与连续批处理机制"
+ *
+ * Conventions for every call:
+ *   - All array pointers are device memory owned by the caller, C-contiguous,
+ *     16-byte aligned unless stated otherwise.  The library keeps no pointer
+ *     after a call returns and allocates no device memory.
+ *   - fp16 arrays are IEEE binary16; int32 / int64 arrays as named.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and never synchronise it, except pa_check_errors.
+ *   - Host-detectable errors (null pointer, misalignment, unsupported shape,
+ *     too small a workspace) return a status and launch nothing.
+ *   - Index errors found on the device (a block id outside [0, num_blocks),
+ *     a slot past the pool, a context length past the block table) never
+ *     trap: the offending item is skipped, a bit is set in the library's
+ *     device error word, and pa_check_errors reports it.
+ *   - Cache layout per layer: key_cache and value_cache are fp16
+ *     [num_blocks][num_heads][block_size][head_dim]; one (block, head) tile
+ *     of block_size * head_dim values is contiguous.
+ *   - Supported shapes: head_dim in {64, 128}; block_size in {4, 8, 16, 32}.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (same underlying type, without including CUDA headers). */
+typedef struct CUstream_st* pa_stream_t;
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,  /* null pointer, misaligned pointer, bad size, small workspace */
+  PA_ERR_UNSUPPORTED = 2,  /* head_dim or block_size outside the supported set           */
+  PA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed                        */
+  PA_ERR_OUT_OF_RANGE = 4, /* the device found an index outside its array (see bits)      */
+  PA_ERR_TIMEOUT = 5       /* a bounded wait inside a kernel gave up (see bits)           */
+} pa_status;
+
+/* Bits of the device error word, as returned by pa_check_errors. */
+#define PA_ERRBIT_BLOCK_ID 0x1u  /* decode: a block-table entry outside [0, num_blocks)        */
+#define PA_ERRBIT_CONTEXT 0x2u   /* decode: context_len < 0, > max_blocks_per_seq*block_size,
+                                    or > max_context_len                                      */
+#define PA_ERRBIT_SLOT 0x4u      /* cache write: slot >= num_blocks*block_size                 */
+#define PA_ERRBIT_COPY 0x8u      /* block copy: a src/dst id outside [0, num_blocks)           */
+#define PA_ERRBIT_TOKEN 0x10u    /* slot map: sequence, position or table entry out of range   */
+#define PA_ERRBIT_TIMEOUT 0x20u  /* a kernel's bounded wait on its own copies gave up          */
+
+/*
+ * Bytes of device scratch pa_decode needs for this batch shape.  The decode
+ * splits each sequence's context into partitions and keeps, per partition,
+ * the running maximum, the softmax denominator and the unnormalised output
+ * (fp32), plus a small work counter.  0 on invalid arguments.
+ */
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len);
+
+/*
+ * Decode attention over the paged cache [P2 §2.1 attention formula; P2 §2.3
+ * paged formula and address map K_paged[i] = K_physical[BlockTable[i div B]][i mod B];
+ * P1 §3.3 gather through the block table at attention time]:
+ *
+ *   out[s,h,:] = softmax( scale * q[s,h,:] . K_paged[s,h,i,:] for i < c_s ) . V_paged[s,h,:,:]
+ *
+ * with c_s = context_lens[s] (it counts the token written just before this
+ * call), K_paged[s,h,i,:] = key_cache[block_tables[s][i / block_size]][h][i % block_size][:]
+ * and the same for V.  A sequence with c_s == 0 gets a zero row.
+ *
+ *   out            fp16 [num_seqs][num_heads][head_dim]          (written)
+ *   query          fp16 [num_seqs][num_heads][head_dim]
+ *   key_cache,
+ *   value_cache    fp16 [num_blocks][num_heads][block_size][head_dim]
+ *   block_tables   int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                  ceil(c_s / block_size) are never read (any value)
+ *   context_lens   int32 [num_seqs]
+ *   scale          multiplier of q.k (normally 1/sqrt(head_dim))
+ *   max_context_len  host-side upper bound of context_lens (sizes the launch;
+ *                  a larger c_s is clipped and flagged PA_ERRBIT_CONTEXT)
+ *   workspace      device scratch of at least pa_decode_workspace_size(...)
+ *                  bytes, 16-byte aligned; contents on entry are ignored and
+ *                  undefined on exit.  Calls that share one workspace must
+ *                  not overlap on the GPU.
+ *
+ * Arithmetic: fp16 inputs, fp32 dot products, online softmax and
+ * accumulation; the result is rounded once to fp16 (nearest even).  The
+ * summation order depends only on logical token positions, so results are
+ * bit-identical under any relabelling of physical blocks and between shared
+ * and privately copied blocks with equal contents.
+ */
+pa_status pa_decode(void* out, const void* query, const void* key_cache, const void* value_cache,
+                    const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* context_lens, int num_seqs, int num_heads, int head_dim,
+                    int block_size, int num_blocks, float scale, int max_context_len,
+                    void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * Cache write [P1 §3.2: a block fills token by token, a new block is taken
+ * when the last one is full; P3 §2.3: blocks are taken on demand every
+ * block_size tokens]: token t's key and value vectors for every head go to
+ * slot slot_mapping[t], i.e.
+ *
+ *   key_cache[slot / block_size][h][slot % block_size][:] = key[t][h][:]   (same for value)
+ *
+ * slot_mapping[t] < 0 marks a padding token: skipped, not an error.  A slot
+ * >= num_blocks * block_size is skipped and flagged PA_ERRBIT_SLOT.  Two
+ * tokens with the same slot race (the result is one of them).
+ *
+ *   key, value     fp16 [num_tokens][num_heads][head_dim]
+ *   key_cache,
+ *   value_cache    fp16 [num_blocks][num_heads][block_size][head_dim] (updated)
+ *   slot_mapping   int64 [num_tokens]
+ * num_tokens == 0 is a no-op.  Bit-exact copy; nothing else is touched.
+ */
+pa_status pa_reshape_and_cache(const void* key, const void* value, void* key_cache,
+                               void* value_cache, const int64_t* slot_mapping, int num_tokens,
+                               int num_heads, int head_dim, int block_size, int num_blocks,
+                               pa_stream_t stream);
+
+/*
+ * Copy-on-write block copy [P3 §2.3: a shared block stays shared until a
+ * request writes different content into it; then the block is copied and
+ * that request's table is repointed; P3 §2.1 components table: the block
+ * manager owns allocation, release and copy-on-write]: for every pair p
+ * and every layer l,
+ *
+ *   key_caches[l][dst_p][:][:][:] = key_caches[l][src_p][:][:][:]   (same for value_caches)
+ *
+ * with (src_p, dst_p) = (block_mapping[2p], block_mapping[2p+1]).
+ *
+ *   key_caches,
+ *   value_caches   HOST arrays of num_layers device pointers, each to an fp16
+ *                  [num_blocks][num_heads][block_size][head_dim] cache
+ *   block_mapping  device int64 [num_pairs][2]
+ * Preconditions (not checked: the mapping lives on the device): destination
+ * ids are distinct and no destination is also a source in the same call;
+ * otherwise copies race.  An id outside [0, num_blocks) skips that pair and
+ * sets PA_ERRBIT_COPY.  num_pairs == 0 is a no-op.  Bit-exact.
+ */
+pa_status pa_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
+                         const int64_t* block_mapping, int num_pairs, int num_heads, int head_dim,
+                         int block_size, int num_blocks, pa_stream_t stream);
+
+/*
+ * Slot map [P2 §2.3 address map; P1 §3.2 worked block-table example]: for
+ * token t of sequence s = token_seq[t] at logical position pos = token_pos[t],
+ *
+ *   slot_mapping[t] = block_tables[s][pos / block_size] * block_size + pos % block_size
+ *
+ * token_seq[t] < 0 marks a padding token and yields -1.  A sequence outside
+ * [0, num_seqs), a position outside the table, or a table entry outside
+ * [0, num_blocks) yields -1 and sets PA_ERRBIT_TOKEN.
+ *
+ *   slot_mapping   int64 [num_tokens] (written)
+ *   block_tables   int32 [num_seqs][max_blocks_per_seq]
+ *   token_seq,
+ *   token_pos      int32 [num_tokens]
+ */
+pa_status pa_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,
+                          int max_blocks_per_seq, const int32_t* token_seq,
+                          const int32_t* token_pos, int num_tokens, int num_seqs, int block_size,
+                          int num_blocks, pa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the calling device's error
+ * word.  Returns PA_ERR_CUDA if a CUDA error is pending, PA_ERR_TIMEOUT if
+ * the timeout bit is set, PA_ERR_OUT_OF_RANGE if any other bit is set, else
+ * PA_OK.  If error_bits is not NULL it receives the word (0 when clean).
+ */
+pa_status pa_check_errors(pa_stream_t stream, uint32_t* error_bits);
+
+/* A static, human-readable name of a status. */
+const char* pa_status_string(pa_status status);
+
+/*
+ * Tokens per context partition pa_decode will use for this shape on the
+ * current device (a multiple of 32).  Exposed so callers can reason about
+ * workspace use; 0 on invalid arguments.
+ */
+int pa_decode_partition_tokens(int num_seqs, int num_heads, int max_context_len);
+
+/*
+ * Process-wide override of the partition size used by pa_decode and
+ * pa_decode_workspace_size (rounded up to a multiple of 32; 0 restores the
+ * automatic choice).  Meant for tuning and for tests that force many
+ * partitions on small inputs.  Not thread-safe with concurrent decodes.
+ */
+void pa_decode_set_partition_tokens(int tokens);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,193 @@
+"""GB300 paged-attention decode library: Python binding of libpa.so.
+
+The functions below carry the C ABI's names (see include/pa.h) and only
+marshal arguments: torch tensors supply device pointers and shapes, the
+current torch CUDA stream is passed unless one is given.  Every computation
+runs in the library's CUDA kernels; there is no CPU fallback, and importing
+this package fails if the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+LIB_PATH = _build.OUT
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing; build it first "
+                      "(python -c 'import __graft_entry__ as g; g.build()')")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_vp, _i32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+
+_lib.pa_decode_workspace_size.argtypes = [_i32, _i32, _i32, _i32]
+_lib.pa_decode_workspace_size.restype = _sz
+_lib.pa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                           ctypes.c_float, _i32, _vp, _sz, _vp]
+_lib.pa_decode.restype = _i32
+_lib.pa_reshape_and_cache.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp]
+_lib.pa_reshape_and_cache.restype = _i32
+_lib.pa_copy_blocks.argtypes = [_vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _vp]
+_lib.pa_copy_blocks.restype = _i32
+_lib.pa_slot_mapping.argtypes = [_vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _vp]
+_lib.pa_slot_mapping.restype = _i32
+_lib.pa_check_errors.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
+_lib.pa_check_errors.restype = _i32
+_lib.pa_status_string.argtypes = [_i32]
+_lib.pa_status_string.restype = ctypes.c_char_p
+_lib.pa_decode_partition_tokens.argtypes = [_i32, _i32, _i32]
+_lib.pa_decode_partition_tokens.restype = _i32
+_lib.pa_decode_set_partition_tokens.argtypes = [_i32]
+_lib.pa_decode_set_partition_tokens.restype = None
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_OUT_OF_RANGE, PA_ERR_TIMEOUT = range(6)
+PA_ERRBIT_BLOCK_ID, PA_ERRBIT_CONTEXT, PA_ERRBIT_SLOT = 0x1, 0x2, 0x4
+PA_ERRBIT_COPY, PA_ERRBIT_TOKEN, PA_ERRBIT_TIMEOUT = 0x8, 0x10, 0x20
+
+
+class PAError(RuntimeError):
+    def __init__(self, status: int, what: str, bits: int = 0):
+        self.status = status
+        self.bits = bits
+        super().__init__(f"{what}: {pa_status_string(status)}" + (f" (bits 0x{bits:x})" if bits else ""))
+
+
+def pa_status_string(status: int) -> str:
+    return _lib.pa_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != PA_OK:
+        raise PAError(status, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: torch.Tensor, name: str, dtype: torch.dtype) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def pa_decode_workspace_size(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int) -> int:
+    return int(_lib.pa_decode_workspace_size(num_seqs, num_heads, head_dim, max_context_len))
+
+
+def pa_decode_partition_tokens(num_seqs: int, num_heads: int, max_context_len: int) -> int:
+    return int(_lib.pa_decode_partition_tokens(num_seqs, num_heads, max_context_len))
+
+
+def pa_decode_set_partition_tokens(tokens: int) -> None:
+    _lib.pa_decode_set_partition_tokens(int(tokens))
+
+
+def decode_workspace(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,
+                     device=None) -> torch.Tensor:
+    """A device byte buffer of pa_decode_workspace_size(...) bytes (allocated by torch)."""
+    n = pa_decode_workspace_size(num_seqs, num_heads, head_dim, max_context_len)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def pa_decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+              value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+              scale: float, max_context_len: int, workspace: torch.Tensor, stream=None) -> None:
+    """out[S,H,D] = paged decode attention (see pa_decode in include/pa.h)."""
+    S, H, D = query.shape
+    NB, H2, B, D2 = key_cache.shape
+    if (H2, D2) != (H, D) or tuple(value_cache.shape) != tuple(key_cache.shape):
+        raise ValueError("cache shape does not match query")
+    if tuple(out.shape) != (S, H, D) or block_tables.dim() != 2 or block_tables.shape[0] != S:
+        raise ValueError("out / block_tables shape")
+    if context_lens.shape != (S,):
+        raise ValueError("context_lens shape")
+    st = _lib.pa_decode(_ptr(out, "out", torch.float16), _ptr(query, "query", torch.float16),
+                        _ptr(key_cache, "key_cache", torch.float16),
+                        _ptr(value_cache, "value_cache", torch.float16),
+                        _ptr(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+                        _ptr(context_lens, "context_lens", torch.int32), S, H, D, B, NB,
+                        float(scale), int(max_context_len), _ptr(workspace, "workspace", torch.uint8),
+                        workspace.numel(), _stream(stream))
+    _check(st, "pa_decode")
+
+
+def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
+                         value_cache: torch.Tensor, slot_mapping: torch.Tensor, stream=None) -> None:
+    """Scatter key/value [T,H,D] into their slots of the paged caches."""
+    T, H, D = key.shape
+    NB, H2, B, D2 = key_cache.shape
+    if (H2, D2) != (H, D) or tuple(value.shape) != (T, H, D) or slot_mapping.shape != (T,):
+        raise ValueError("shape mismatch")
+    st = _lib.pa_reshape_and_cache(_ptr(key, "key", torch.float16), _ptr(value, "value", torch.float16),
+                                   _ptr(key_cache, "key_cache", torch.float16),
+                                   _ptr(value_cache, "value_cache", torch.float16),
+                                   _ptr(slot_mapping, "slot_mapping", torch.int64), T, H, D, B, NB,
+                                   _stream(stream))
+    _check(st, "pa_reshape_and_cache")
+
+
+def pa_copy_blocks(key_caches, value_caches, block_mapping: torch.Tensor, stream=None) -> None:
+    """Copy-on-write block copy across all layers; block_mapping is int64 [P, 2] (src, dst)."""
+    L = len(key_caches)
+    if len(value_caches) != L or L == 0:
+        raise ValueError("need one value cache per key cache")
+    NB, H, B, D = key_caches[0].shape
+    for t in list(key_caches) + list(value_caches):
+        if tuple(t.shape) != (NB, H, B, D):
+            raise ValueError("all caches must share one shape")
+    kp = (ctypes.c_void_p * L)(*[_ptr(t, "key_caches[i]", torch.float16) for t in key_caches])
+    vp = (ctypes.c_void_p * L)(*[_ptr(t, "value_caches[i]", torch.float16) for t in value_caches])
+    if block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
+        raise ValueError("block_mapping must be [P, 2]")
+    st = _lib.pa_copy_blocks(kp, vp, L, _ptr(block_mapping, "block_mapping", torch.int64),
+                             block_mapping.shape[0], H, D, B, NB, _stream(stream))
+    _check(st, "pa_copy_blocks")
+
+
+def pa_slot_mapping(slot_mapping: torch.Tensor, block_tables: torch.Tensor, token_seq: torch.Tensor,
+                    token_pos: torch.Tensor, block_size: int, num_blocks: int, stream=None) -> None:
+    """slot_mapping[t] = block_tables[seq][pos // B] * B + pos % B for each new token."""
+    T = token_seq.shape[0]
+    if token_pos.shape != (T,) or slot_mapping.shape != (T,) or block_tables.dim() != 2:
+        raise ValueError("shape mismatch")
+    st = _lib.pa_slot_mapping(_ptr(slot_mapping, "slot_mapping", torch.int64),
+                              _ptr(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+                              _ptr(token_seq, "token_seq", torch.int32),
+                              _ptr(token_pos, "token_pos", torch.int32), T, block_tables.shape[0],
+                              int(block_size), int(num_blocks), _stream(stream))
+    _check(st, "pa_slot_mapping")
+
+
+def pa_check_errors(stream=None) -> tuple[int, int]:
+    """Synchronise the stream and read + clear the device error word: (status, bits)."""
+    bits = ctypes.c_uint32(0)
+    st = _lib.pa_check_errors(_stream(stream), ctypes.byref(bits))
+    return int(st), int(bits.value)
+
+
+def raise_on_device_errors(stream=None) -> None:
+    st, bits = pa_check_errors(stream)
+    if st != PA_OK:
+        raise PAError(st, "device error word", bits)
+
+
+__all__ = [
+    "pa_decode", "pa_reshape_and_cache", "pa_copy_blocks", "pa_slot_mapping", "pa_check_errors",
+    "pa_status_string", "pa_decode_workspace_size", "pa_decode_partition_tokens",
+    "pa_decode_set_partition_tokens", "decode_workspace", "raise_on_device_errors", "PAError",
+]

@@ -1,0 +1,318 @@
+// C ABI of libpa.so: argument checks, launch planning and the device error
+// word.  Every computation runs in the kernels of the other translation
+// units; this file only validates, sizes and launches.
+#include <atomic>
+#include <mutex>
+
+#include "pa_internal.h"
+
+namespace pa {
+cudaError_t launch_decode_partition_d64(const DecodeParams&, int, int, size_t, cudaStream_t);
+cudaError_t launch_decode_partition_d128(const DecodeParams&, int, int, size_t, cudaStream_t);
+cudaError_t launch_decode_reduce_d64(const DecodeParams&, int, int, cudaStream_t);
+cudaError_t launch_decode_reduce_d128(const DecodeParams&, int, int, cudaStream_t);
+int decode_ctas_per_sm_d64(int, size_t);
+int decode_ctas_per_sm_d128(int, size_t);
+size_t decode_fixed_smem_d64(int);
+size_t decode_fixed_smem_d128(int);
+cudaError_t decode_prepare_d64();
+cudaError_t decode_prepare_d128();
+
+cudaError_t launch_decode_partition(const DecodeParams& p, int head_dim, int block_size, int grid,
+                                    size_t smem, cudaStream_t st) {
+  return head_dim == 64 ? launch_decode_partition_d64(p, block_size, grid, smem, st)
+                        : launch_decode_partition_d128(p, block_size, grid, smem, st);
+}
+
+cudaError_t launch_decode_reduce(const DecodeParams& p, int head_dim, int block_size,
+                                 int total_seqs, cudaStream_t st) {
+  return head_dim == 64 ? launch_decode_reduce_d64(p, block_size, total_seqs, st)
+                        : launch_decode_reduce_d128(p, block_size, total_seqs, st);
+}
+
+size_t decode_smem_bytes(int head_dim, int block_size, int part_tokens, int seqs_in_launch) {
+  const size_t fixed =
+      head_dim == 64 ? decode_fixed_smem_d64(block_size) : decode_fixed_smem_d128(block_size);
+  const size_t bt = 2 * (size_t)(part_tokens / block_size + 1) * 4;
+  const size_t seq = (2 * (size_t)seqs_in_launch + 1) * 4;
+  return (fixed + bt + seq + 15) & ~size_t(15);
+}
+
+int decode_ctas_per_sm(int head_dim, int block_size, size_t smem) {
+  return head_dim == 64 ? decode_ctas_per_sm_d64(block_size, smem)
+                        : decode_ctas_per_sm_d128(block_size, smem);
+}
+
+cudaError_t decode_prepare_device(int) {
+  cudaError_t e = decode_prepare_d64();
+  if (e != cudaSuccess) return e;
+  return decode_prepare_d128();
+}
+
+}  // namespace pa
+
+// The library's device error word: one per device (a static device variable
+// is instantiated in every context that loads the module).
+static __device__ unsigned int g_pa_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_err_ptr[kMaxDevices];
+int g_sms[kMaxDevices];
+bool g_prepared[kMaxDevices];
+std::atomic<int> g_part_override{0};
+
+struct DeviceState {
+  unsigned int* err;
+  int sms;
+};
+
+pa_status device_state(DeviceState* out, bool prepare_decode) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pa_error_word) != cudaSuccess) return PA_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PA_ERR_CUDA;
+    g_sms[dev] = sms;
+    g_err_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  if (prepare_decode && !g_prepared[dev]) {
+    if (pa::decode_prepare_device(dev) != cudaSuccess) return PA_ERR_CUDA;
+    g_prepared[dev] = true;
+  }
+  out->err = g_err_ptr[dev];
+  out->sms = g_sms[dev];
+  return PA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
+bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7) == 0; }
+bool head_dim_ok(int d) { return d == 64 || d == 128; }
+bool block_size_ok(int b) { return b == 4 || b == 8 || b == 16 || b == 32; }
+
+int part_tokens_for(int num_seqs, int num_heads, int max_context_len) {
+  (void)num_seqs;
+  (void)num_heads;
+  (void)max_context_len;
+  const int o = g_part_override.load(std::memory_order_relaxed);
+  if (o > 0) return (o + 31) / 32 * 32;
+  return 256;
+}
+
+struct WsLayout {
+  int part_tokens;
+  int max_parts;
+  int launches;
+  size_t counters_off, ml_off, o_off, total;
+};
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+WsLayout ws_layout(int S, int H, int D, int max_context_len) {
+  WsLayout w{};
+  w.part_tokens = part_tokens_for(S, H, max_context_len);
+  w.max_parts = max_context_len > 0 ? (max_context_len + w.part_tokens - 1) / w.part_tokens : 1;
+  w.launches = (S + pa::kMaxSeqsPerLaunch - 1) / pa::kMaxSeqsPerLaunch;
+  if (w.launches < 1) w.launches = 1;
+  w.counters_off = 0;
+  size_t off = round256((size_t)w.launches * 4);
+  w.ml_off = off;
+  w.o_off = off;
+  if (w.max_parts > 1) {
+    const size_t slots = (size_t)S * H * w.max_parts;
+    w.o_off = round256(off + slots * 2 * 4);
+    off = round256(w.o_off + slots * (size_t)D * 4);
+  }
+  w.total = off;
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_status_string(pa_status status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_OUT_OF_RANGE: return "PA_ERR_OUT_OF_RANGE";
+    case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
+  }
+  return "PA_ERR_UNKNOWN";
+}
+
+int pa_decode_partition_tokens(int num_seqs, int num_heads, int max_context_len) {
+  if (num_seqs < 0 || num_heads <= 0 || max_context_len < 0) return 0;
+  return part_tokens_for(num_seqs, num_heads, max_context_len);
+}
+
+void pa_decode_set_partition_tokens(int tokens) {
+  g_part_override.store(tokens > 0 ? tokens : 0, std::memory_order_relaxed);
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len) {
+  if (num_seqs < 0 || num_heads <= 0 || !head_dim_ok(head_dim) || max_context_len < 0) return 0;
+  return ws_layout(num_seqs, num_heads, head_dim, max_context_len).total;
+}
+
+pa_status pa_decode(void* out, const void* query, const void* key_cache, const void* value_cache,
+                    const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* context_lens, int num_seqs, int num_heads, int head_dim,
+                    int block_size, int num_blocks, float scale, int max_context_len,
+                    void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  if (!head_dim_ok(head_dim) || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+  if (num_seqs < 0 || num_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 ||
+      max_context_len < 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens || !workspace)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache) ||
+      !aligned16(workspace) || !aligned4(block_tables) || !aligned4(context_lens))
+    return PA_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(num_seqs, num_heads, head_dim, max_context_len);
+  if (workspace_bytes < w.total) return PA_ERR_INVALID_ARG;
+  if ((long long)num_seqs * num_heads * w.max_parts >= (1LL << 31)) return PA_ERR_UNSUPPORTED;
+
+  DeviceState ds;
+  pa_status st = device_state(&ds, true);
+  if (st != PA_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  pa::DecodeParams p{};
+  p.out = out;
+  p.query = query;
+  p.key_cache = key_cache;
+  p.value_cache = value_cache;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.ws_ml = reinterpret_cast<float*>(ws + w.ml_off);
+  p.ws_o = reinterpret_cast<float*>(ws + w.o_off);
+  p.err = ds.err;
+  p.num_heads = num_heads;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.max_context_len = max_context_len;
+  p.part_tokens = w.part_tokens;
+  p.max_parts = w.max_parts;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634073599246810019);
+
+  unsigned int* counters = reinterpret_cast<unsigned int*>(ws + w.counters_off);
+  if (cudaMemsetAsync(counters, 0, (size_t)w.launches * 4, cs) != cudaSuccess) return PA_ERR_CUDA;
+  for (int b = 0; b < w.launches; ++b) {
+    p.seq_begin = b * pa::kMaxSeqsPerLaunch;
+    p.num_seqs = num_seqs - p.seq_begin < pa::kMaxSeqsPerLaunch ? num_seqs - p.seq_begin
+                                                                 : pa::kMaxSeqsPerLaunch;
+    p.counter = counters + b;
+    const size_t smem = pa::decode_smem_bytes(head_dim, block_size, w.part_tokens, p.num_seqs);
+    const int per_sm = pa::decode_ctas_per_sm(head_dim, block_size, smem);
+    long long grid = (long long)per_sm * ds.sms;
+    const long long items_ub = (long long)p.num_seqs * num_heads * w.max_parts;
+    if (grid > items_ub) grid = items_ub;
+    if (pa::launch_decode_partition(p, head_dim, block_size, (int)grid, smem, cs) != cudaSuccess)
+      return PA_ERR_CUDA;
+  }
+  if (w.max_parts > 1) {
+    p.seq_begin = 0;
+    p.num_seqs = num_seqs;
+    if (pa::launch_decode_reduce(p, head_dim, block_size, num_seqs, cs) != cudaSuccess)
+      return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+pa_status pa_reshape_and_cache(const void* key, const void* value, void* key_cache,
+                               void* value_cache, const int64_t* slot_mapping, int num_tokens,
+                               int num_heads, int head_dim, int block_size, int num_blocks,
+                               pa_stream_t stream) {
+  if (!head_dim_ok(head_dim) || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+  if (num_tokens < 0 || num_heads <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache) ||
+      !aligned8(slot_mapping))
+    return PA_ERR_INVALID_ARG;
+  DeviceState ds;
+  pa_status st = device_state(&ds, false);
+  if (st != PA_OK) return st;
+  return pa::launch_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, num_tokens,
+                                      num_heads, head_dim, block_size, num_blocks, ds.err,
+                                      reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+pa_status pa_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
+                         const int64_t* block_mapping, int num_pairs, int num_heads, int head_dim,
+                         int block_size, int num_blocks, pa_stream_t stream) {
+  if (!head_dim_ok(head_dim) || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+  if (num_layers < 0 || num_pairs < 0 || num_heads <= 0 || num_blocks <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_layers == 0 || num_pairs == 0) return PA_OK;
+  if (!key_caches || !value_caches || !block_mapping || !aligned8(block_mapping))
+    return PA_ERR_INVALID_ARG;
+  for (int l = 0; l < num_layers; ++l) {
+    if (!key_caches[l] || !value_caches[l] || !aligned16(key_caches[l]) ||
+        !aligned16(value_caches[l]))
+      return PA_ERR_INVALID_ARG;
+  }
+  DeviceState ds;
+  pa_status st = device_state(&ds, false);
+  if (st != PA_OK) return st;
+  return pa::launch_copy_blocks(key_caches, value_caches, num_layers, block_mapping, num_pairs,
+                                num_heads, head_dim, block_size, num_blocks, ds.err,
+                                reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+pa_status pa_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,
+                          int max_blocks_per_seq, const int32_t* token_seq,
+                          const int32_t* token_pos, int num_tokens, int num_seqs, int block_size,
+                          int num_blocks, pa_stream_t stream) {
+  if (!block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+  if (num_tokens < 0 || num_seqs < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!slot_mapping || !block_tables || !token_seq || !token_pos || !aligned8(slot_mapping) ||
+      !aligned4(block_tables) || !aligned4(token_seq) || !aligned4(token_pos))
+    return PA_ERR_INVALID_ARG;
+  DeviceState ds;
+  pa_status st = device_state(&ds, false);
+  if (st != PA_OK) return st;
+  return pa::launch_slot_mapping(slot_mapping, block_tables, max_blocks_per_seq, token_seq,
+                                 token_pos, num_tokens, num_seqs, block_size, num_blocks, ds.err,
+                                 reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+pa_status pa_check_errors(pa_stream_t stream, uint32_t* error_bits) {
+  if (error_bits) *error_bits = 0;
+  DeviceState ds;
+  pa_status st = device_state(&ds, false);
+  if (st != PA_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpy(&word, ds.err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (word != 0 && cudaMemset(ds.err, 0, sizeof(word)) != cudaSuccess) return PA_ERR_CUDA;
+  if (error_bits) *error_bits = word;
+  if (word & PA_ERRBIT_TIMEOUT) return PA_ERR_TIMEOUT;
+  return word ? PA_ERR_OUT_OF_RANGE : PA_OK;
+}
+
+}  // extern "C"

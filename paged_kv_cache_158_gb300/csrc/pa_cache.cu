@@ -1,0 +1,180 @@
+// Cache write, copy-on-write block copy and slot map for sm_103a.
+//
+// All three are bit copies or integer index arithmetic over KB- to MB-scale
+// data: they are bound by launch latency or by HBM, and move 16-byte
+// vectors with fully coalesced accesses.
+#include <cuda_fp16.h>
+
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+// ---- cache write ("深入解析LLM推理引擎：从PagedAttention到调度优化" §3.2;
+// "vLLM基础架构：核心组件、PagedAttention原理、KV Cache管理与连续批处理机制" §2.3)
+// Thread i moves 16-byte vector i of the [T][H][D] key/value inputs to its
+// slot: block slot/B, offset slot%B, same head and dimensions.
+template <int D>
+__global__ void __launch_bounds__(256)
+    reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                             uint4* __restrict__ key_cache, uint4* __restrict__ value_cache,
+                             const int64_t* __restrict__ slot_mapping, int num_tokens,
+                             int num_heads, int log2_block, long long num_slots,
+                             unsigned int* err) {
+  constexpr int V = D / 8;  // 16-byte vectors per head row
+  const long long per_token = (long long)num_heads * V;
+  const long long total = (long long)num_tokens * per_token;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const long long t = i / per_token;
+    const int rem = (int)(i - t * per_token);
+    const long long slot = slot_mapping[t];
+    if (slot < 0) continue;  // padding token
+    if (slot >= num_slots) {
+      if (rem == 0) atomicOr(err, PA_ERRBIT_SLOT);
+      continue;
+    }
+    const int h = rem / V;
+    const int v = rem - h * V;
+    const long long blk = slot >> log2_block;
+    const long long off = slot & ((1 << log2_block) - 1);
+    const long long dst = ((blk * num_heads + h) << log2_block | off) * V + v;
+    key_cache[dst] = key[i];
+    value_cache[dst] = value[i];
+  }
+}
+
+// ---- copy-on-write block copy
+// ("vLLM基础架构：核心组件、PagedAttention原理、KV Cache管理与连续批处理机制" §2.3)
+// blockIdx.y = pair, blockIdx.z = layer * 2 + (0 key | 1 value); blockIdx.x
+// and the threads stride over the block's H*B*D/8 16-byte vectors.
+struct LayerPtrs {
+  uint4* k[kCopyMaxLayers];
+  uint4* v[kCopyMaxLayers];
+};
+
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(LayerPtrs ptrs, const int64_t* __restrict__ block_mapping, int pair_base,
+                       long long block_vecs, long long num_blocks, unsigned int* err) {
+  const int pair = pair_base + blockIdx.y;
+  const int layer = blockIdx.z >> 1;
+  const long long src = block_mapping[2 * pair];
+  const long long dst = block_mapping[2 * pair + 1];
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (blockIdx.x == 0 && blockIdx.z == 0 && threadIdx.x == 0) atomicOr(err, PA_ERRBIT_COPY);
+    return;
+  }
+  uint4* base = (blockIdx.z & 1) ? ptrs.v[layer] : ptrs.k[layer];
+  const uint4* s = base + src * block_vecs;
+  uint4* d = base + dst * block_vecs;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < block_vecs; i += stride)
+    d[i] = s[i];
+}
+
+// ---- slot map ("vLLM推理加速深度解读：PagedAttention如何提升10x吞吐量" §2.3)
+__global__ void __launch_bounds__(256)
+    slot_mapping_kernel(int64_t* __restrict__ slot_mapping, const int32_t* __restrict__ block_tables,
+                        int max_blocks, const int32_t* __restrict__ token_seq,
+                        const int32_t* __restrict__ token_pos, int num_tokens, int num_seqs,
+                        int block_size, int num_blocks, unsigned int* err) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= num_tokens) return;
+  const int s = token_seq[t];
+  const int pos = token_pos[t];
+  int64_t slot = -1;
+  if (s >= 0) {
+    bool ok = s < num_seqs && pos >= 0 && pos / block_size < max_blocks;
+    if (ok) {
+      const int phys = block_tables[(long long)s * max_blocks + pos / block_size];
+      ok = phys >= 0 && phys < num_blocks;
+      if (ok) slot = (int64_t)phys * block_size + pos % block_size;
+    }
+    if (!ok) atomicOr(err, PA_ERRBIT_TOKEN);
+  }
+  slot_mapping[t] = slot;
+}
+
+int log2_exact(int x) {
+  int l = 0;
+  while ((1 << l) < x) ++l;
+  return l;
+}
+
+int sm_count() {
+  int dev = 0, n = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n;
+}
+
+}  // namespace
+
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* key_cache,
+                                     void* value_cache, const int64_t* slot_mapping,
+                                     int num_tokens, int num_heads, int head_dim, int block_size,
+                                     int num_blocks, unsigned int* err, cudaStream_t stream) {
+  const long long vecs = (long long)num_tokens * num_heads * (head_dim / 8);
+  if (vecs == 0) return cudaSuccess;
+  const int threads = 256;
+  long long blocks = (vecs + threads - 1) / threads;
+  const long long cap = (long long)sm_count() * 16;
+  if (blocks > cap) blocks = cap;
+  const int lb = log2_exact(block_size);
+  const long long slots = (long long)num_blocks * block_size;
+  auto k = static_cast<const uint4*>(key);
+  auto v = static_cast<const uint4*>(value);
+  auto kc = static_cast<uint4*>(key_cache);
+  auto vc = static_cast<uint4*>(value_cache);
+  if (head_dim == 64)
+    reshape_and_cache_kernel<64><<<(int)blocks, threads, 0, stream>>>(
+        k, v, kc, vc, slot_mapping, num_tokens, num_heads, lb, slots, err);
+  else
+    reshape_and_cache_kernel<128><<<(int)blocks, threads, 0, stream>>>(
+        k, v, kc, vc, slot_mapping, num_tokens, num_heads, lb, slots, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
+                               const int64_t* block_mapping, int num_pairs, int num_heads,
+                               int head_dim, int block_size, int num_blocks, unsigned int* err,
+                               cudaStream_t stream) {
+  if (num_pairs == 0 || num_layers == 0) return cudaSuccess;
+  const long long block_vecs = (long long)num_heads * block_size * head_dim / 8;
+  const int threads = 256;
+  long long xblocks = (block_vecs + threads - 1) / threads;
+  if (xblocks > 64) xblocks = 64;
+  for (int l0 = 0; l0 < num_layers; l0 += kCopyMaxLayers) {
+    const int nl = num_layers - l0 < kCopyMaxLayers ? num_layers - l0 : kCopyMaxLayers;
+    LayerPtrs ptrs{};
+    for (int i = 0; i < nl; ++i) {
+      ptrs.k[i] = static_cast<uint4*>(key_caches[l0 + i]);
+      ptrs.v[i] = static_cast<uint4*>(value_caches[l0 + i]);
+    }
+    for (int p0 = 0; p0 < num_pairs; p0 += 65535) {
+      const int np = num_pairs - p0 < 65535 ? num_pairs - p0 : 65535;
+      dim3 grid((unsigned)xblocks, (unsigned)np, (unsigned)(2 * nl));
+      copy_blocks_kernel<<<grid, threads, 0, stream>>>(ptrs, block_mapping, p0, block_vecs,
+                                                       num_blocks, err);
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,
+                                int max_blocks, const int32_t* token_seq,
+                                const int32_t* token_pos, int num_tokens, int num_seqs,
+                                int block_size, int num_blocks, unsigned int* err,
+                                cudaStream_t stream) {
+  if (num_tokens == 0) return cudaSuccess;
+  const int threads = 256;
+  const int blocks = (num_tokens + threads - 1) / threads;
+  slot_mapping_kernel<<<blocks, threads, 0, stream>>>(slot_mapping, block_tables, max_blocks,
+                                                      token_seq, token_pos, num_tokens, num_seqs,
+                                                      block_size, num_blocks, err);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

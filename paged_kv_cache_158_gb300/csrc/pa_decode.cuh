@@ -1,0 +1,504 @@
+// Paged decode attention for sm_103a: partition pass + log-sum-exp merge.
+//
+// What is computed ("vLLM推理加速深度解读：PagedAttention如何提升10x吞吐量"
+// §2.1 and §2.3): for each sequence s and head h,
+//   out = softmax(scale * q . K_paged^T) V_paged,
+//   K_paged[i] = key_cache[block_tables[s][i / B]][h][i % B]   (same for V).
+//
+// Design (GB300):
+//  * Work items are (sequence, head, context partition) triples of at most
+//    `part_tokens` tokens.  A persistent grid of CTAs (resident CTAs per SM x
+//    SM count) takes items from an atomic counter, so skewed batches balance
+//    to within one item and no CTA is launched for an empty partition.
+//  * Each CTA has NW warps.  A partition is cut into chunks of TC tokens
+//    (TC = min(B, 16)) lying inside one physical block; chunk j goes to warp
+//    j mod NW.  Each warp runs its own ring of NST shared-memory stages: lane
+//    0 issues two 1-D bulk copies per chunk (the K rows and the V rows of one
+//    (block, head) tile, contiguous in the [NB][H][B][D] layout) completing on
+//    the stage's mbarrier; only the live rows of a ragged last chunk are
+//    copied.  The partition's block-table slice sits in shared memory; the
+//    next item's slice is prefetched with cp.async while the current item
+//    runs.
+//  * Inside a warp each lane owns 8 dimensions (16 bytes) of a token row;
+//    D/8 lanes cover one row.  q.k uses fp16 x fp16 -> fp32 fused
+//    multiply-adds; the per-lane partial dots are combined by a shuffle
+//    reduce-scatter, after which each lane holds one token's logit.  The
+//    online softmax keeps (m, l) in fp32 in base-2 units (logits are scaled
+//    by scale*log2(e) and exponentiated with ex2), with shuffle max/sum
+//    reductions.  p.V accumulates in fp32, 8 dimensions per lane.
+//  * At the end of an item the warps' (m, l, o) merge in shared memory.  A
+//    sequence with one partition writes fp16 output directly; otherwise the
+//    partition's (m, l, o) go to the workspace and a second kernel merges
+//    the partitions (log-sum-exp weights), one warp per (sequence, head).
+//  * The summation order depends only on logical token positions, so the
+//    result is bit-identical under any relabelling of physical blocks.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+template <int D, int B>
+struct DecodeTraits {
+  static constexpr int NW = 4;                // warps per CTA
+  static constexpr int NST = 3;               // stages per warp
+  static constexpr int THREADS = NW * 32;
+  static constexpr int TC = B < 16 ? B : 16;  // tokens per chunk (inside one block)
+  static constexpr int LR = D / 8;            // lanes per token row (16 bytes each)
+  static constexpr int RI = 32 / LR;          // token rows per warp-wide load
+  static constexpr int TPL = TC / RI;         // token rows per lane
+  static constexpr int DUP = LR / TPL;        // lanes sharing a logit after the reduction
+  static constexpr int CHUNK_ELEMS = TC * D;
+  static constexpr int STAGE_BYTES = 2 * CHUNK_ELEMS * 2;  // K rows then V rows
+  static_assert(D == 64 || D == 128, "head_dim");
+  static_assert(TPL >= 1 && TPL <= LR && (TPL & (TPL - 1)) == 0, "lane layout");
+
+  // Fixed part of the dynamic shared memory (bytes), in layout order.
+  static constexpr size_t kStages = size_t(NW) * NST * STAGE_BYTES;
+  static constexpr size_t kBars = size_t(NW) * NST * 8;
+  static constexpr size_t kP = size_t(NW) * TC * 4;
+  static constexpr int MS = D + 4;            // merge stride (floats): o[D], m, l, pad
+  static constexpr size_t kMerge = 2 * size_t(NW) * MS * 4;
+  static constexpr size_t kMisc = 16 * 4;  // item ring, warp sums, failure flag
+  static constexpr size_t kFixed = kStages + kBars + kP + kMerge + kMisc;
+};
+
+// Effective context length: clipped to what the table and the launch cover.
+__device__ __forceinline__ int effective_len(int c, const DecodeParams& a, int B, bool report) {
+  int e = 0;
+  if (c < 0) { c = 0; e = 1; }
+  const long long cap_table = (long long)a.max_blocks * B;
+  if (c > cap_table) { c = (int)cap_table; e = 1; }
+  if (c > a.max_context_len) { c = a.max_context_len; e = 1; }
+  if (report && e) atomicOr(a.err, PA_ERRBIT_CONTEXT);
+  return c;
+}
+
+__device__ __forceinline__ int num_parts(int c, int part_tokens) {
+  return c > 0 ? (c + part_tokens - 1) / part_tokens : 1;  // an empty sequence is one item
+}
+
+struct ItemInfo {
+  int s;        // sequence within the launch
+  int h;
+  int p;        // partition
+  int c;        // effective context length
+  int t_begin, t_end;
+  int n_parts;
+  int blk0;     // first logical block of the partition
+  int nblk;     // logical blocks it touches
+};
+
+template <int B>
+__device__ __forceinline__ ItemInfo locate_item(int item, const int* cum, const int* ctx_s,
+                                                int nseq, int H, int part_tokens) {
+  int lo = 0, hi = nseq - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cum[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  ItemInfo it;
+  it.s = lo;
+  it.c = ctx_s[lo];
+  it.n_parts = num_parts(it.c, part_tokens);
+  const int within = item - cum[lo];
+  it.h = within / it.n_parts;
+  it.p = within - it.h * it.n_parts;
+  it.t_begin = it.p * part_tokens;
+  it.t_end = min(it.c, it.t_begin + part_tokens);
+  it.blk0 = it.t_begin / B;
+  it.nblk = it.t_end > it.t_begin ? (it.t_end - 1) / B - it.blk0 + 1 : 0;
+  return it;
+}
+
+template <int D, int B>
+__device__ __forceinline__ void issue_chunk(const DecodeParams& a, const ItemInfo& it,
+                                            const int* bt, int chunk, __half* stage, uint32_t bar,
+                                            uint64_t policy) {
+  using T = DecodeTraits<D, B>;
+  const int t0 = it.t_begin + chunk * T::TC;
+  const int rows = min(T::TC, it.t_end - t0);
+  const int phys = bt[t0 / B - it.blk0];
+  if (phys < 0 || phys >= a.num_blocks) {
+    atomicOr(a.err, PA_ERRBIT_BLOCK_ID);
+    mbar_arrive(bar);  // completes the phase with no data; the chunk is skipped
+    return;
+  }
+  const size_t off = (((size_t)phys * a.num_heads + it.h) * B + (t0 % B)) * D;
+  const uint32_t bytes = (uint32_t)rows * D * 2;
+  mbar_arrive_expect_tx(bar, 2 * bytes);
+  bulk_g2s_hint(smem_u32(stage), static_cast<const __half*>(a.key_cache) + off, bytes, bar, policy);
+  bulk_g2s_hint(smem_u32(stage + T::CHUNK_ELEMS), static_cast<const __half*>(a.value_cache) + off,
+                bytes, bar, policy);
+}
+
+// One chunk for one warp: logits, online-softmax update, p.V accumulation.
+template <int D, int B, bool FULL>
+__device__ __forceinline__ void process_chunk(const __half* Ks, const __half* Vs, int rows,
+                                              const uint4& q, float scale_log2, float* p_w,
+                                              int lane, float& m, float& l, float (&o)[8]) {
+  using T = DecodeTraits<D, B>;
+  const int cidx = lane % T::LR;  // which 8 dimensions
+  const int r = lane / T::LR;     // which row group
+
+  // Partial dots over this lane's 8 dimensions for its TPL rows.
+  float v[T::TPL];
+#pragma unroll
+  for (int k = 0; k < T::TPL; ++k) {
+    const int t = r + T::RI * k;
+    v[k] = dot8_f16(q, lds128(Ks + t * D + 8 * cidx));
+  }
+  // Reduce-scatter over the LR lanes of the row group: at each halving step a
+  // lane keeps one half of its values and adds its partner's copy of it.
+#pragma unroll
+  for (int cnt = T::TPL, msk = T::LR / 2; cnt > 1; cnt >>= 1, msk >>= 1) {
+    const bool upper = (lane & msk) != 0;
+#pragma unroll
+    for (int i = 0; i < cnt / 2; ++i) {
+      const float send = upper ? v[i] : v[i + cnt / 2];
+      const float keep = upper ? v[i + cnt / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(kFullMask, send, msk);
+    }
+  }
+#pragma unroll
+  for (int msk = T::DUP / 2; msk >= 1; msk >>= 1) v[0] += __shfl_xor_sync(kFullMask, v[0], msk);
+
+  const int kl = cidx / T::DUP;          // this lane's logit: row r + RI*kl
+  const int tl = r + T::RI * kl;
+  float x = v[0] * scale_log2;
+  if (!FULL && tl >= rows) x = -INFINITY;
+
+  float cm = x;
+#pragma unroll
+  for (int msk = T::DUP; msk < 32; msk <<= 1) cm = fmaxf(cm, __shfl_xor_sync(kFullMask, cm, msk));
+  const float m_new = fmaxf(m, cm);
+  const float alpha = exp2_approx(m - m_new);  // 0 on the first chunk (m = -inf)
+  const float pv = exp2_approx(x - m_new);     // 0 for masked rows
+  float ps = pv;
+#pragma unroll
+  for (int msk = T::DUP; msk < 32; msk <<= 1) ps += __shfl_xor_sync(kFullMask, ps, msk);
+  l = l * alpha + ps;
+  m = m_new;
+
+  if ((cidx % T::DUP) == 0) p_w[r * T::TPL + kl] = pv;
+  __syncwarp();
+  float pk[T::TPL];
+#pragma unroll
+  for (int k = 0; k < T::TPL; ++k) pk[k] = p_w[r * T::TPL + k];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i] *= alpha;
+#pragma unroll
+  for (int k = 0; k < T::TPL; ++k) {
+    const int t = r + T::RI * k;
+    if (FULL || t < rows) {
+      const uint4 vv = lds128(Vs + t * D + 8 * cidx);
+      const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = half2_bits_to_float2(w[j]);
+        o[2 * j] = fmaf(pk[k], f.x, o[2 * j]);
+        o[2 * j + 1] = fmaf(pk[k], f.y, o[2 * j + 1]);
+      }
+    }
+  }
+}
+
+template <int D, int B>
+__global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
+    decode_partition_kernel(const DecodeParams a) {
+  using T = DecodeTraits<D, B>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* cur_ptr = smem;
+  __half* stages = reinterpret_cast<__half*>(cur_ptr);
+  cur_ptr += T::kStages;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(cur_ptr);
+  cur_ptr += T::kBars;
+  float* p_s = reinterpret_cast<float*>(cur_ptr);
+  cur_ptr += T::kP;
+  float* merge = reinterpret_cast<float*>(cur_ptr);
+  cur_ptr += T::kMerge;
+  int* misc = reinterpret_cast<int*>(cur_ptr);  // [0..1] item ring, [4..7] warp sums, [8] failed
+  cur_ptr += T::kMisc;
+  const int bt_cap = a.part_tokens / B + 1;
+  int* bt_s = reinterpret_cast<int*>(cur_ptr);  // 2 x bt_cap
+  cur_ptr += 2 * bt_cap * 4;
+  int* cum = reinterpret_cast<int*>(cur_ptr);   // nseq + 1
+  int* ctx_s = cum + (a.num_seqs + 1);          // nseq
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int nseq = a.num_seqs;
+  const int H = a.num_heads;
+  const int P = a.part_tokens;
+
+  // ---- per-sequence item counts and their exclusive prefix sums ---------
+  {
+    constexpr int PER = (kMaxSeqsPerLaunch + T::THREADS - 1) / T::THREADS;
+    int vals[PER];
+    int local = 0;
+    const int base = tid * PER;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int i = base + j;
+      int v = 0;
+      if (i < nseq) {
+        const int c = effective_len(a.context_lens[a.seq_begin + i], a, B, blockIdx.x == 0);
+        ctx_s[i] = c;
+        v = H * num_parts(c, P);
+      }
+      vals[j] = v;
+      local += v;
+    }
+    int x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFullMask, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) misc[4 + warp] = x;
+    if (lane == 0) {
+      for (int j = 0; j < T::NST; ++j) mbar_init(smem_u32(&bars[warp * T::NST + j]), 1);
+    }
+    if (tid == 0) misc[8] = 0;
+    fence_mbar_init();
+    __syncthreads();
+    int run = x - local;
+    for (int w = 0; w < warp; ++w) run += misc[4 + w];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int i = base + j;
+      if (i < nseq) {
+        cum[i] = run;
+        run += vals[j];
+        if (i == nseq - 1) cum[nseq] = run;
+      }
+    }
+  }
+  if (tid == 0) {
+    misc[0] = (int)atomicAdd(a.counter, 1u);
+    misc[1] = (int)atomicAdd(a.counter, 1u);
+  }
+  __syncthreads();
+  const int total = cum[nseq];
+  int cur = misc[0];
+  int nxt = misc[1];
+  if (cur >= total) return;
+
+  // First item's block-table slice (synchronous).
+  ItemInfo it = locate_item<B>(cur, cum, ctx_s, nseq, H, P);
+  {
+    const int32_t* row = a.block_tables + (size_t)(a.seq_begin + it.s) * a.max_blocks;
+    for (int i = tid; i < it.nblk; i += T::THREADS) bt_s[i] = row[it.blk0 + i];
+  }
+  __syncthreads();
+
+  const uint64_t policy = policy_evict_first();
+  __half* my_stages = stages + (size_t)warp * T::NST * (2 * T::CHUNK_ELEMS);
+  uint64_t* my_bars = bars + warp * T::NST;
+  float* my_p = p_s + warp * T::TC;
+  const int cidx = lane % T::LR;
+  const int rgrp = lane / T::LR;
+  uint32_t u = 0;  // chunks this warp has consumed so far (stage/phase bookkeeping)
+  int buf = 0;
+  int iter = 0;
+
+  while (true) {
+    // Prefetch the next item's block-table slice into the other buffer.
+    ItemInfo nx;
+    const bool has_next = nxt < total;
+    if (has_next) {
+      nx = locate_item<B>(nxt, cum, ctx_s, nseq, H, P);
+      const int32_t* row = a.block_tables + (size_t)(a.seq_begin + nx.s) * a.max_blocks;
+      int* dst = bt_s + (buf ^ 1) * bt_cap;
+      for (int i = tid; i < nx.nblk; i += T::THREADS) cp_async_4(dst + i, row + nx.blk0 + i);
+    }
+    cp_async_commit();
+    if (tid == 0) misc[2 + (iter & 1)] = (int)atomicAdd(a.counter, 1u);
+
+    const int* bt = bt_s + buf * bt_cap;
+    const size_t sh = (size_t)(a.seq_begin + it.s) * H + it.h;
+    const int n_chunks = (it.t_end - it.t_begin + T::TC - 1) / T::TC;
+    const int n_my = warp < n_chunks ? (n_chunks - 1 - warp) / T::NW + 1 : 0;
+
+    if (lane == 0) {
+      const int pre = min(T::NST, n_my);
+      for (int i = 0; i < pre; ++i) {
+        const int st = (u + i) % T::NST;
+        issue_chunk<D, B>(a, it, bt, warp + i * T::NW, my_stages + st * 2 * T::CHUNK_ELEMS,
+                          smem_u32(&my_bars[st]), policy);
+      }
+    }
+    const uint4 q = *reinterpret_cast<const uint4*>(static_cast<const __half*>(a.query) +
+                                                    sh * D + 8 * cidx);
+    float m = -INFINITY, l = 0.f;
+    float o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = 0.f;
+
+    for (int i = 0; i < n_my; ++i) {
+      const uint32_t ui = u + i;
+      const int st = ui % T::NST;
+      const uint32_t bar = smem_u32(&my_bars[st]);
+      bool ok = mbar_wait_bounded(bar, (ui / T::NST) & 1);
+      ok = __all_sync(kFullMask, ok);
+      if (!ok) {
+        // Drain this warp's copies still in flight (bounded), then give up.
+        for (int k = i + 1; k < min(i + T::NST, n_my); ++k)
+          mbar_wait_bounded(smem_u32(&my_bars[(u + k) % T::NST]), ((u + k) / T::NST) & 1);
+        if (lane == 0) {
+          atomicOr(a.err, PA_ERRBIT_TIMEOUT);
+          misc[8] = 1;
+        }
+        break;
+      }
+      const int chunk = warp + i * T::NW;
+      const int t0 = it.t_begin + chunk * T::TC;
+      const int rows = min(T::TC, it.t_end - t0);
+      const int phys = bt[t0 / B - it.blk0];
+      if (phys >= 0 && phys < a.num_blocks) {
+        const __half* Ks = my_stages + st * 2 * T::CHUNK_ELEMS;
+        if (rows == T::TC)
+          process_chunk<D, B, true>(Ks, Ks + T::CHUNK_ELEMS, rows, q, a.scale_log2, my_p, lane, m,
+                                    l, o);
+        else
+          process_chunk<D, B, false>(Ks, Ks + T::CHUNK_ELEMS, rows, q, a.scale_log2, my_p, lane,
+                                     m, l, o);
+      }
+      __syncwarp();
+      if (lane == 0 && i + T::NST < n_my) {
+        issue_chunk<D, B>(a, it, bt, warp + (i + T::NST) * T::NW,
+                          my_stages + st * 2 * T::CHUNK_ELEMS, bar, policy);
+      }
+    }
+    u += n_my;
+
+    // Combine the row groups, then publish this warp's (m, l, o).
+#pragma unroll
+    for (int msk = T::LR; msk < 32; msk <<= 1) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] += __shfl_xor_sync(kFullMask, o[i], msk);
+    }
+    float* mw = merge + (iter & 1) * T::NW * T::MS + warp * T::MS;
+    if (rgrp == 0) {
+      reinterpret_cast<float4*>(mw + 8 * cidx)[0] = make_float4(o[0], o[1], o[2], o[3]);
+      reinterpret_cast<float4*>(mw + 8 * cidx)[1] = make_float4(o[4], o[5], o[6], o[7]);
+    }
+    if (lane == 0) {
+      mw[D] = m;
+      mw[D + 1] = l;
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    // Merge the warps of this item and write it out.
+    const float* mb = merge + (iter & 1) * T::NW * T::MS;
+    for (int d = tid; d < D; d += T::THREADS) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < T::NW; ++w) M = fmaxf(M, mb[w * T::MS + D]);
+      float L = 0.f, O = 0.f;
+#pragma unroll
+      for (int w = 0; w < T::NW; ++w) {
+        const float mwv = mb[w * T::MS + D];
+        const float sc = (mwv == -INFINITY) ? 0.f : exp2_approx(mwv - M);
+        L = fmaf(sc, mb[w * T::MS + D + 1], L);
+        O = fmaf(sc, mb[w * T::MS + d], O);
+      }
+      if (it.n_parts == 1) {
+        const float r = (it.c > 0 && L > 0.f) ? O / L : 0.f;
+        static_cast<__half*>(a.out)[sh * D + d] = __float2half_rn(r);
+      } else {
+        const size_t slot = sh * a.max_parts + it.p;
+        a.ws_o[slot * D + d] = O;
+        if (d == 0) {
+          a.ws_ml[slot * 2] = M;
+          a.ws_ml[slot * 2 + 1] = L;
+        }
+      }
+    }
+    if (misc[8] != 0 || !has_next) break;
+    cur = nxt;
+    nxt = misc[2 + (iter & 1)];
+    it = nx;
+    buf ^= 1;
+    ++iter;
+  }
+}
+
+// Merge the partitions of each (sequence, head): one warp per pair.
+template <int D, int B>
+__global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams a, int total_seqs) {
+  constexpr int DPL = D / 32;
+  const int lane = threadIdx.x & 31;
+  const long long pair = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (pair >= (long long)total_seqs * a.num_heads) return;
+  const int s = (int)(pair / a.num_heads);
+  const int c = effective_len(a.context_lens[s], a, B, false);
+  const int n = num_parts(c, a.part_tokens);
+  if (n <= 1) return;
+  const float* ml = a.ws_ml + (size_t)pair * a.max_parts * 2;
+  const float* ob = a.ws_o + (size_t)pair * a.max_parts * D;
+  float M = -INFINITY;
+  for (int p = 0; p < n; ++p) M = fmaxf(M, ml[2 * p]);
+  float L = 0.f;
+  float acc[DPL];
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+  for (int p = 0; p < n; ++p) {
+    const float mp = ml[2 * p];
+    const float w = (mp == -INFINITY) ? 0.f : exp2_approx(mp - M);
+    L = fmaf(w, ml[2 * p + 1], L);
+    const float* op = ob + (size_t)p * D + lane * DPL;
+    if constexpr (DPL == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(op);
+      acc[0] = fmaf(w, v.x, acc[0]);
+      acc[1] = fmaf(w, v.y, acc[1]);
+      acc[2] = fmaf(w, v.z, acc[2]);
+      acc[3] = fmaf(w, v.w, acc[3]);
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(op);
+      acc[0] = fmaf(w, v.x, acc[0]);
+      acc[1] = fmaf(w, v.y, acc[1]);
+    }
+  }
+  __half* out = static_cast<__half*>(a.out) + (size_t)pair * D + lane * DPL;
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) out[i] = __float2half_rn(L > 0.f ? acc[i] / L : 0.f);
+}
+
+template <int D, int B>
+cudaError_t launch_partition_t(const DecodeParams& p, int grid, size_t smem, cudaStream_t st) {
+  decode_partition_kernel<D, B><<<grid, DecodeTraits<D, B>::THREADS, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D, int B>
+cudaError_t launch_reduce_t(const DecodeParams& p, int total_seqs, cudaStream_t st) {
+  const long long warps = (long long)total_seqs * p.num_heads;
+  const int blocks = (int)((warps + 3) / 4);
+  decode_reduce_kernel<D, B><<<blocks, 128, 0, st>>>(p, total_seqs);
+  return cudaGetLastError();
+}
+
+template <int D, int B>
+int ctas_per_sm_t(size_t smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_partition_kernel<D, B>,
+                                                    DecodeTraits<D, B>::THREADS, smem) !=
+      cudaSuccess)
+    return 1;
+  return n > 0 ? n : 1;
+}
+
+template <int D, int B>
+cudaError_t prepare_t() {
+  return cudaFuncSetAttribute(decode_partition_kernel<D, B>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+}
+
+}  // namespace pa

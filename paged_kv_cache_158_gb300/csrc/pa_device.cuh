@@ -1,0 +1,158 @@
+// Device helpers for the sm_103a kernels: shared-memory barriers, 1-D bulk
+// copies (the TMA engine's untiled form), bounded waits, fp16 arithmetic.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "pa_internal.h"
+
+namespace pa {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+// A wait on the library's own copies gives up after this long (ns) and
+// reports PA_ERRBIT_TIMEOUT instead of hanging the GPU.
+constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- mbarrier (shared::cta) ---------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Makes barrier initialisation visible to the asynchronous (bulk-copy) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "  selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete, for at most
+// kWaitLimitNs.  Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+// ---- 1-D bulk copy global -> shared, completing on an mbarrier ----------
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_smem),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Same, with an L2 eviction-priority policy from createpolicy (streamed data).
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst_smem, const void* src, uint32_t bytes,
+                                              uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], "
+      "%2, [%3], %4;" ::"r"(dst_smem),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// ---- asynchronous 4-byte global -> shared copies (block-table prefetch) --
+
+__device__ __forceinline__ void cp_async_4(void* dst_smem, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// ---- arithmetic ----------------------------------------------------------
+
+// 2^x (the SFU's approximate exponential; relative error about 2^-22).
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// acc + a.lo*b.lo + a.hi*b.hi for two packed fp16 pairs, each product added
+// with one fp32 rounding (fp16 x fp16 products are exact in fp32).
+__device__ __forceinline__ float dot2_f16_f32(uint32_t a, uint32_t b, float acc) {
+  asm("{\n"
+      "  .reg .f16 a0, a1, b0, b1;\n"
+      "  mov.b32 {a0, a1}, %1;\n"
+      "  mov.b32 {b0, b1}, %2;\n"
+      "  fma.rn.f32.f16 %0, a0, b0, %0;\n"
+      "  fma.rn.f32.f16 %0, a1, b1, %0;\n"
+      "}\n"
+      : "+f"(acc)
+      : "r"(a), "r"(b));
+  return acc;
+}
+
+// Dot product of 8 fp16 pairs (one 16-byte vector each), fp32 accumulate,
+// dimensions in increasing order.
+__device__ __forceinline__ float dot8_f16(const uint4& a, const uint4& b) {
+  float acc = 0.f;
+  acc = dot2_f16_f32(a.x, b.x, acc);
+  acc = dot2_f16_f32(a.y, b.y, acc);
+  acc = dot2_f16_f32(a.z, b.z, acc);
+  acc = dot2_f16_f32(a.w, b.w, acc);
+  return acc;
+}
+
+__device__ __forceinline__ float2 half2_bits_to_float2(uint32_t u) {
+  __half2 h;
+  *reinterpret_cast<uint32_t*>(&h) = u;
+  return __half22float2(h);
+}
+
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
+}  // namespace pa

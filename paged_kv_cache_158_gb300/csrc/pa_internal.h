@@ -1,0 +1,71 @@
+// Internal declarations shared by the library's translation units (not part
+// of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+// Sequences handled by one launch of the partition kernel: their per-sequence
+// item counts and prefix sums live in shared memory.
+constexpr int kMaxSeqsPerLaunch = 1024;
+// Layers handled by one launch of the block-copy kernel (pointer table passed
+// by value as a kernel parameter).
+constexpr int kCopyMaxLayers = 32;
+
+struct DecodeParams {
+  void* out;                  // fp16 [S][H][D]
+  const void* query;          // fp16 [S][H][D]
+  const void* key_cache;      // fp16 [NB][H][B][D]
+  const void* value_cache;    // fp16 [NB][H][B][D]
+  const int32_t* block_tables;  // [S][max_blocks]
+  const int32_t* context_lens;  // [S]
+  float* ws_ml;               // [S][H][max_parts][2]: running max (base-2 units) and sum
+  float* ws_o;                // [S][H][max_parts][D]: unnormalised output
+  unsigned int* counter;      // work counter of this launch (zeroed before it)
+  unsigned int* err;          // device error word
+  int seq_begin;              // first sequence of this launch
+  int num_seqs;               // sequences in this launch
+  int num_heads;
+  int max_blocks;             // block-table row length
+  int num_blocks;             // pool size
+  int max_context_len;        // host bound; larger lengths are clipped and flagged
+  int part_tokens;            // tokens per partition (multiple of 32)
+  int max_parts;              // ceil(max_context_len / part_tokens)
+  float scale_log2;           // scale * log2(e): logits are kept in base-2 units
+};
+
+// Partition-kernel launch: picks the instantiation for (head_dim, block_size).
+cudaError_t launch_decode_partition(const DecodeParams& p, int head_dim, int block_size,
+                                    int grid, size_t smem_bytes, cudaStream_t stream);
+// LSE-merge launch over all (seq, head) pairs of the batch.
+cudaError_t launch_decode_reduce(const DecodeParams& p, int head_dim, int block_size,
+                                 int total_seqs, cudaStream_t stream);
+// Dynamic shared memory of the partition kernel.
+size_t decode_smem_bytes(int head_dim, int block_size, int part_tokens, int seqs_in_launch);
+// Resident CTAs per SM of the partition kernel for that shared-memory size.
+int decode_ctas_per_sm(int head_dim, int block_size, size_t smem_bytes);
+// One-time per-device kernel attributes (dynamic shared memory opt-in).
+cudaError_t decode_prepare_device(int device);
+
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* key_cache,
+                                     void* value_cache, const int64_t* slot_mapping,
+                                     int num_tokens, int num_heads, int head_dim, int block_size,
+                                     int num_blocks, unsigned int* err, cudaStream_t stream);
+
+cudaError_t launch_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
+                               const int64_t* block_mapping, int num_pairs, int num_heads,
+                               int head_dim, int block_size, int num_blocks, unsigned int* err,
+                               cudaStream_t stream);
+
+cudaError_t launch_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,
+                                int max_blocks, const int32_t* token_seq,
+                                const int32_t* token_pos, int num_tokens, int num_seqs,
+                                int block_size, int num_blocks, unsigned int* err,
+                                cudaStream_t stream);
+
+}  // namespace pa

@@ -13,10 +13,8 @@ def pytest_configure(config):
 
 
 @pytest.fixture(scope="session", autouse=True)
-def _host_libraries():
-    """The oracle (gcc) and the input generator (nvcc, host + device code) are
-    built once per session if missing or stale."""
-    from oracle import _build as oracle_build
-    from workloads import _build as synth_build
-    oracle_build.build()
-    synth_build.build()
+def _native_libraries():
+    """The CUDA library, the input generator and the oracle are built once per
+    session if missing or stale (nvcc cross-compiles without a GPU)."""
+    import __graft_entry__
+    __graft_entry__.build()

@@ -1,0 +1,90 @@
+"""The C-ABI library loads without a GPU, exports every entry point that
+include/pa.h declares, and rejects bad arguments on the host before any
+CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa.h")
+LIB = os.path.join(ROOT, "paged_kv_cache_158_gb300", "_lib", "libpa.so")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["pa_decode", "pa_decode_workspace_size", "pa_reshape_and_cache", "pa_copy_blocks",
+              "pa_slot_mapping", "pa_check_errors", "pa_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(LIB)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_sizes_on_host():
+    lib = ctypes.CDLL(LIB)
+    lib.pa_status_string.restype = ctypes.c_char_p
+    assert lib.pa_status_string(0) == b"PA_OK"
+    assert lib.pa_status_string(4) == b"PA_ERR_OUT_OF_RANGE"
+    lib.pa_decode_workspace_size.restype = ctypes.c_size_t
+    assert lib.pa_decode_workspace_size(32, 40, 128, 1024) > 0
+    assert lib.pa_decode_workspace_size(32, 40, 96, 1024) == 0       # unsupported head_dim
+    assert lib.pa_decode_workspace_size(-1, 40, 128, 1024) == 0
+
+
+def test_bad_arguments_are_rejected_before_any_launch():
+    lib = ctypes.CDLL(LIB)
+    vp = ctypes.c_void_p
+    f = lib.pa_decode
+    f.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int, vp, ctypes.c_size_t, vp]
+    good = 0x10000
+    # unsupported head_dim / block_size
+    assert f(good, good, good, good, good, 4, good, 2, 2, 96, 16, 8, 0.1, 64, good, 1 << 20, None) == 2
+    assert f(good, good, good, good, good, 4, good, 2, 2, 128, 12, 8, 0.1, 64, good, 1 << 20, None) == 2
+    # null / misaligned pointers, negative sizes, small workspace
+    assert f(None, good, good, good, good, 4, good, 2, 2, 128, 16, 8, 0.1, 64, good, 1 << 20, None) == 1
+    assert f(good + 2, good, good, good, good, 4, good, 2, 2, 128, 16, 8, 0.1, 64, good, 1 << 20, None) == 1
+    assert f(good, good, good, good, good, 4, good, 2, -2, 128, 16, 8, 0.1, 64, good, 1 << 20, None) == 1
+    assert f(good, good, good, good, good, 4, good, 2, 2, 128, 16, 8, 0.1, 64, good, 8, None) == 1
+    # zero sequences is a no-op
+    assert f(None, None, None, None, None, 4, None, 0, 2, 128, 16, 8, 0.1, 64, None, 0, None) == 0
+    g = lib.pa_reshape_and_cache
+    g.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 5 + [vp]
+    assert g(good, good, good, good, good, 3, 2, 128, 5, 8, None) == 2
+    assert g(good, good, good, good, good + 4, 3, 2, 128, 16, 8, None) == 1
+    assert g(None, None, None, None, None, 0, 2, 128, 16, 8, None) == 0
+    h = lib.pa_copy_blocks
+    h.argtypes = [vp, vp, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, vp]
+    ptrs = (ctypes.c_void_p * 1)(good + 8)
+    assert h(ptrs, ptrs, 1, good, 2, 2, 128, 16, 8, None) == 1        # misaligned cache pointer
+    assert h(None, None, 0, None, 0, 2, 128, 16, 8, None) == 0
+    s = lib.pa_slot_mapping
+    s.argtypes = [vp, vp, ctypes.c_int, vp, vp] + [ctypes.c_int] * 4 + [vp]
+    assert s(good, good, 4, good, good, 3, 2, 6, 8, None) == 2
+    assert s(good + 4, good, 4, good, good, 3, 2, 16, 8, None) == 1
+
+
+def test_python_binding_refuses_to_run_without_library(tmp_path, monkeypatch):
+    """The product path has no fallback: with the library absent, the import fails."""
+    import importlib.util
+    import shutil
+    pkg = tmp_path / "paged_kv_cache_158_gb300"
+    shutil.copytree(os.path.join(ROOT, "paged_kv_cache_158_gb300"), pkg,
+                    ignore=shutil.ignore_patterns("_lib", "_build", "__pycache__"))
+    spec = importlib.util.spec_from_file_location("pa_copy_without_lib", pkg / "__init__.py",
+                                                  submodule_search_locations=[str(pkg)])
+    mod = importlib.util.module_from_spec(spec)
+    with pytest.raises(ImportError):
+        spec.loader.exec_module(mod)

@@ -1,0 +1,99 @@
+"""Shared-prefix workload with copy-on-write, end to end on the GPU: the
+product block manager plans, the GPU copies blocks, maps slots, writes the
+suffix tokens and decodes.  The oracle replays the pages' block manager on
+its own and runs its own copy / slot map / cache write / decode on the host.
+Pools must match bit for bit, outputs within tolerance; decoding with the
+prefix shared must give the same bits as with private copies."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_158_gb300 as pa
+from oracle.block_model import shared_prefix_flow
+from pa_testlib import decode_gate, u16
+from paged_kv_cache_158_gb300.pool import BlockManager
+from workloads import configs, gpu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def product_plan(w):
+    bm = BlockManager(w.num_blocks, w.block_size, w.num_seqs, w.max_blocks_per_seq, w.free_order)
+    bm.add_sequence(0)
+    bm.append_tokens(0, w.prefix_len)
+    for s in range(1, w.num_seqs):
+        bm.fork(0, s)
+    for s in range(w.num_seqs):
+        bm.append_tokens(s, int(w.suffix_lens[s]))
+    return bm.take_copies(), bm.block_tables(), bm.context_lens()
+
+
+def gpu_step(w, dw, pairs, bt, ctx):
+    bt_d = torch.from_numpy(bt).to(DEV)
+    ctx_d = torch.from_numpy(ctx).to(DEV)
+    pa.pa_copy_blocks(dw.key_caches, dw.value_caches, torch.from_numpy(pairs).to(DEV))
+    slots = torch.empty(dw.token_seq.numel(), dtype=torch.int64, device=DEV)
+    pa.pa_slot_mapping(slots, bt_d, dw.token_seq, dw.token_pos, w.block_size, w.num_blocks)
+    pa.pa_reshape_and_cache(dw.keys_new[0], dw.values_new[0], dw.key_caches[0], dw.value_caches[0], slots)
+    out = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=DEV)
+    ws = pa.decode_workspace(w.num_seqs, w.num_heads, w.head_dim, int(ctx.max()))
+    pa.pa_decode(out, dw.queries[0], dw.key_caches[0], dw.value_caches[0], bt_d, ctx_d, w.scale,
+                 int(ctx.max()), ws)
+    return out
+
+
+def test_shared_prefix_copy_on_write_against_oracle():
+    w = configs.config4()
+    pairs, bt, ctx = product_plan(w)
+    assert pairs.shape == (w.num_seqs - 1, 2)
+    dw = gpu.materialize(w, device=DEV)
+    out = gpu_step(w, dw, pairs, bt, ctx)
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+    model, appended = shared_prefix_flow(w.num_seqs, w.prefix_len, w.suffix_lens, w.num_blocks,
+                                         w.block_size, w.free_order)
+    mbt = model.table_array(range(w.num_seqs), w.max_blocks_per_seq)
+    kc, vc = gpu.host_pool(w, 0)
+    q, kn, vn = gpu.host_small(w, 0)
+    assert oracle.copy_blocks([kc], [vc], np.array(model.copies, dtype=np.int64)) == 0
+    seqs = np.array([s for s, _ in appended], dtype=np.int32)
+    pos = np.array([p for _, p in appended], dtype=np.int32)
+    slots, rc = oracle.slot_mapping(mbt, seqs, pos, w.block_size, w.num_blocks)
+    assert rc == 0
+    assert oracle.reshape_and_cache(kc, vc, kn, vn, slots, w.block_size) == 0
+    assert np.array_equal(u16(dw.key_caches[0]), kc)
+    assert np.array_equal(u16(dw.value_caches[0]), vc)
+    mctx = np.array([model.lengths[s] for s in range(w.num_seqs)], dtype=np.int32)
+    _, ref64, rc = oracle.decode(q, kc, vc, mbt, mctx, w.scale)
+    assert rc == 0
+    decode_gate(out, ref64, w.name)
+
+
+def test_shared_prefix_identity_bit_exact():
+    """Same bits whether the 32 full prefix blocks are shared by reference or
+    every sequence holds private copies of them."""
+    w = configs.config4()
+    pairs, bt, ctx = product_plan(w)
+    dw = gpu.materialize(w, device=DEV)
+    shared = gpu_step(w, dw, pairs, bt, ctx).clone()
+    full = w.prefix_len // w.block_size
+    S = w.num_seqs
+    NB = w.num_blocks
+    kc = torch.cat([dw.key_caches[0], torch.empty((S * full,) + tuple(dw.key_caches[0].shape[1:]),
+                                                  dtype=torch.float16, device=DEV)])
+    vc = torch.cat([dw.value_caches[0], torch.empty_like(kc[NB:])])
+    bt2 = bt.copy()
+    src = torch.from_numpy(bt[0, :full].astype(np.int64)).to(DEV)
+    for s in range(S):
+        ids = np.arange(NB + s * full, NB + (s + 1) * full)
+        kc[torch.from_numpy(ids).to(DEV)] = kc[src]
+        vc[torch.from_numpy(ids).to(DEV)] = vc[src]
+        bt2[s, :full] = ids
+    out = torch.empty_like(shared)
+    ws = pa.decode_workspace(S, w.num_heads, w.head_dim, int(ctx.max()))
+    pa.pa_decode(out, dw.queries[0], kc, vc, torch.from_numpy(bt2).to(DEV), torch.from_numpy(ctx).to(DEV),
+                 w.scale, int(ctx.max()), ws)
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+    assert torch.equal(shared.view(torch.int16), out.view(torch.int16))

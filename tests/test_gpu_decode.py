@@ -1,0 +1,200 @@
+"""GPU parity of paged decode against the oracle, element by element on
+small and mid-size inputs (several tiles, ragged tails, many partitions)
+and on sampled outputs at the full workload sizes in the benchmark's launch
+configuration; plus the invariants the pages fix (permutation of physical
+blocks, run-to-run determinism) and edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_158_gb300 as pa
+from pa_testlib import (decode_gate, live_slot_mask, poison_dead_slots_device, poison_dead_slots_host,
+                        sampled_oracle, u16)
+from workloads import configs, gpu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def _reset():
+    pa.pa_decode_set_partition_tokens(0)
+    pa.pa_check_errors()
+    yield
+    pa.pa_decode_set_partition_tokens(0)
+    torch.cuda.synchronize()
+
+
+def run_decode(dw, layer_idx=0, out=None):
+    w = dw.w
+    out = out if out is not None else torch.empty((w.num_seqs, w.num_heads, w.head_dim),
+                                                  dtype=torch.float16, device=DEV)
+    ws = pa.decode_workspace(w.num_seqs, w.num_heads, w.head_dim, w.max_context_len)
+    pa.pa_decode(out, dw.queries[layer_idx], dw.key_caches[layer_idx], dw.value_caches[layer_idx],
+                 dw.block_tables, dw.context_lens, w.scale, w.max_context_len, ws)
+    return out
+
+
+def cache_write(dw, layer_idx=0):
+    w = dw.w
+    slots = torch.empty(dw.token_seq.numel(), dtype=torch.int64, device=DEV)
+    pa.pa_slot_mapping(slots, dw.block_tables, dw.token_seq, dw.token_pos, w.block_size, w.num_blocks)
+    pa.pa_reshape_and_cache(dw.keys_new[layer_idx], dw.values_new[layer_idx], dw.key_caches[layer_idx],
+                            dw.value_caches[layer_idx], slots)
+
+
+def full_oracle(w, layer=0, poison=True, write_new=True):
+    kc, vc = gpu.host_pool(w, layer)
+    q, kn, vn = gpu.host_small(w, layer)
+    if write_new:
+        seqs, pos = w.new_tokens()
+        slots, rc = oracle.slot_mapping(w.block_tables, seqs, pos, w.block_size, w.num_blocks)
+        assert rc == 0
+        assert oracle.reshape_and_cache(kc, vc, kn, vn, slots, w.block_size) == 0
+    if poison:
+        poison_dead_slots_host(kc, vc, live_slot_mask(w.block_tables, w.context_lens, w.num_blocks,
+                                                      w.block_size))
+    return oracle.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale)
+
+
+SMALL = [(d, b) for d in (64, 128) for b in (4, 8, 16, 32)]
+
+
+@pytest.mark.parametrize("part", [0, 32, 96])
+@pytest.mark.parametrize("D,B", SMALL)
+def test_decode_small_random(D, B, part):
+    """Ragged contexts (including 0 and 1), NaN in every dead slot, forced
+    small partitions so several partitions and the merge kernel run."""
+    pa.pa_decode_set_partition_tokens(part)
+    w = configs.small_random(1000 + D + B + part, 7, 3, D, B, 300, min_context=0)
+    w.context_lens[0], w.context_lens[1] = 0, 1
+    w.block_tables[0, :] = -1
+    dw = gpu.materialize(w, device=DEV)
+    mask = live_slot_mask(w.block_tables, w.context_lens, w.num_blocks, B)
+    poison_dead_slots_device(dw.key_caches[0], dw.value_caches[0], mask)
+    out = run_decode(dw)
+    _, ref64, rc = full_oracle(w, write_new=False)
+    assert rc == 0
+    decode_gate(out, ref64, f"D{D} B{B} part{part}")
+    assert u16(out)[0].max() == 0                      # empty context: zero row
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_decode_step_workload_all_outputs(cfg):
+    """Slot map + cache write + decode of workloads 1 and 2, every output."""
+    w = configs.ALL[cfg]()
+    dw = gpu.materialize(w, device=DEV)
+    poison_dead_slots_device(dw.key_caches[0], dw.value_caches[0],
+                             live_slot_mask(w.block_tables, w.context_lens, w.num_blocks, w.block_size))
+    cache_write(dw)
+    out = run_decode(dw)
+    _, ref64, rc = full_oracle(w)
+    assert rc == 0
+    decode_gate(out, ref64, w.name)
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+def test_decode_workload3_full_size_sampled():
+    """LLaMA-13B shape at full size (all 40 layers resident), bench launch
+    configuration; sampled sequences of three layers against the oracle."""
+    w = configs.config3()
+    dw = gpu.materialize(w, device=DEV)
+    rng = np.random.default_rng(3)
+    for li in (0, 17, 39):
+        cache_write(dw, li)
+        out = run_decode(dw, li)
+        seqs = np.sort(rng.choice(w.num_seqs, 3, replace=False))
+        ref64 = sampled_oracle(w, li, seqs)
+        decode_gate(out[torch.from_numpy(seqs).to(DEV)], ref64, f"{w.name} layer {li}")
+        assert torch.isfinite(out).all()
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+    del dw
+    torch.cuda.empty_cache()
+
+
+def test_decode_workload5_full_size_sampled():
+    """Long-context skewed batch at full size per layer (3.4 GB), bench launch
+    configuration; the longest, the shortest and random sequences."""
+    w = configs.config5()
+    dw = gpu.materialize(w, layers=[0, 31], device=DEV)
+    order = np.argsort(w.context_lens)
+    rng = np.random.default_rng(5)
+    for li in (0, 1):
+        cache_write(dw, li)
+        out = run_decode(dw, li)
+        seqs = np.unique(np.concatenate([order[:1], order[-2:], rng.choice(w.num_seqs, 2)]))
+        ref64 = sampled_oracle(w, dw.layers[li], seqs)
+        decode_gate(out[torch.from_numpy(seqs).to(DEV)], ref64, f"{w.name} layer {dw.layers[li]}")
+        assert torch.isfinite(out).all()
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+    del dw
+    torch.cuda.empty_cache()
+
+
+def test_decode_permutation_invariance_bit_exact():
+    w = configs.config2()
+    dw = gpu.materialize(w, device=DEV)
+    a = run_decode(dw).clone()
+    perm = torch.from_numpy(np.random.default_rng(1).permutation(w.num_blocks)).to(DEV)
+    kc2 = torch.empty_like(dw.key_caches[0])
+    vc2 = torch.empty_like(dw.value_caches[0])
+    kc2[perm] = dw.key_caches[0]
+    vc2[perm] = dw.value_caches[0]
+    bt = dw.block_tables.long()
+    bt2 = torch.where(bt >= 0, perm[bt.clamp(min=0)], bt).int()
+    dw.key_caches[0], dw.value_caches[0], dw.block_tables = kc2, vc2, bt2.contiguous()
+    b = run_decode(dw)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_decode_run_to_run_deterministic():
+    w = configs.config5(num_layers=1)
+    dw = gpu.materialize(w, device=DEV)
+    a = run_decode(dw).clone()
+    for _ in range(3):
+        assert torch.equal(a.view(torch.int16), run_decode(dw).view(torch.int16))
+
+
+def test_decode_single_token_returns_value_bits():
+    w = configs.small_random(77, 6, 4, 128, 16, 1, min_context=1)
+    dw = gpu.materialize(w, device=DEV)
+    out = run_decode(dw)
+    vc = u16(dw.value_caches[0])
+    for s in range(w.num_seqs):
+        assert np.array_equal(u16(out)[s], vc[w.block_tables[s, 0], :, 0, :])
+
+
+def test_decode_out_of_range_block_id_is_flagged_not_fatal():
+    w = configs.small_random(78, 3, 2, 128, 16, 80, min_context=40)
+    w.block_tables[1, 1] = w.num_blocks + 5
+    dw = gpu.materialize(w, device=DEV)
+    run_decode(dw)
+    st, bits = pa.pa_check_errors()
+    assert st == pa.PA_ERR_OUT_OF_RANGE and bits & pa.PA_ERRBIT_BLOCK_ID
+    # the other sequences are unaffected
+    out = run_decode(dw)
+    pa.pa_check_errors()
+    clean_bt = w.block_tables.copy()
+    clean_bt[1, :] = 0
+    q = gpu.host_small(w, 0)[0]
+    kc, vc = gpu.host_pool(w, 0)
+    _, ref64, _ = oracle.decode(q, kc, vc, clean_bt, w.context_lens, w.scale)
+    for s in (0, 2):
+        decode_gate(out[s:s + 1], ref64[s:s + 1], "unaffected sequence")
+
+
+def test_decode_context_beyond_max_is_clipped_and_flagged():
+    w = configs.small_random(79, 2, 2, 64, 16, 64, min_context=64)
+    dw = gpu.materialize(w, device=DEV)
+    out = torch.empty((2, 2, 64), dtype=torch.float16, device=DEV)
+    ws = pa.decode_workspace(2, 2, 64, 48)
+    pa.pa_decode(out, dw.queries[0], dw.key_caches[0], dw.value_caches[0], dw.block_tables,
+                 dw.context_lens, w.scale, 48, ws)
+    st, bits = pa.pa_check_errors()
+    assert st == pa.PA_ERR_OUT_OF_RANGE and bits == pa.PA_ERRBIT_CONTEXT
+    q = gpu.host_small(w, 0)[0]
+    kc, vc = gpu.host_pool(w, 0)
+    _, ref64, _ = oracle.decode(q, kc, vc, w.block_tables, np.full(2, 48, np.int32), w.scale)
+    decode_gate(out, ref64, "clipped to max_context_len")
