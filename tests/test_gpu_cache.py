@@ -71,7 +71,7 @@ CACHE_SHAPES = [(d, b) for d in (64, 128) for b in (4, 8, 16, 32)]
 @pytest.mark.parametrize("D,B", CACHE_SHAPES)
 def test_reshape_and_cache_bit_exact_random(D, B):
     rng = np.random.default_rng(D * 100 + B)
-    NB, H, T = 37, 3, 150
+    NB, H, T = 64, 3, 150
     kc = rng.integers(0, 1 << 16, (NB, H, B, D), dtype=np.uint64).astype(np.uint16)
     vc = rng.integers(0, 1 << 16, (NB, H, B, D), dtype=np.uint64).astype(np.uint16)
     k = rng.integers(0, 1 << 16, (T, H, D), dtype=np.uint64).astype(np.uint16)
