@@ -104,6 +104,39 @@ pa_status pa_decode(void* out, const void* query, const void* key_cache, const v
                     int block_size, int num_blocks, float scale, int max_context_len,
                     void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
+/* Size of the fixed scratch area pa_decode_noalloc uses (32 MiB per device). */
+#define PA_DECODE_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * pa_decode without a workspace argument, for callers that cannot allocate
+ * device memory at the moment they decode: code running inside a CUDA graph
+ * capture in global mode (cudaMalloc is an error there), processes that give
+ * all of HBM to the KV pool up front and keep no allocator headroom, and hot
+ * paths that must not call cudaMalloc/cudaFree because those may synchronise
+ * the device.  The pages have no counterpart; it is a deployment convenience.
+ *
+ * Same arguments, result and arithmetic as pa_decode.  The scratch is a fixed
+ * array of PA_DECODE_NOALLOC_SCRATCH_BYTES in the library's own device memory
+ * (a __device__ variable: each device that loads the library holds it until
+ * the process exits).  This call allocates nothing and calls no allocating
+ * routine.
+ *   - If pa_decode_workspace_size(num_seqs, num_heads, head_dim,
+ *     max_context_len) exceeds PA_DECODE_NOALLOC_SCRATCH_BYTES the call
+ *     returns PA_ERR_UNSUPPORTED and launches nothing.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before capturing a stream on that device.
+ *   - All calls on a device share the one array, which keeps the previous
+ *     call's contents; the work counters are zeroed by every call.  Calls
+ *     that overlap on the GPU (e.g. on two streams) race on the array and
+ *     must be serialised by the caller.
+ */
+pa_status pa_decode_noalloc(void* out, const void* query, const void* key_cache,
+                            const void* value_cache, const int32_t* block_tables,
+                            int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                            int num_heads, int head_dim, int block_size, int num_blocks,
+                            float scale, int max_context_len, pa_stream_t stream);
+
 /*
  * Cache write [P1 §3.2: a block fills token by token, a new block is taken
  * when the last one is full; P3 §2.3: blocks are taken on demand every

@@ -1,0 +1,68 @@
+"""pa_decode_noalloc, the decode entry point for callers that cannot allocate
+device memory when they decode (inside a global-mode graph capture, with all
+of HBM given to the KV pool, or on a path where cudaMalloc/cudaFree may not
+synchronise the device).  It must give the same result as pa_decode with a
+caller-allocated workspace, on two calls in a row (the fixed scratch keeps the
+previous call's contents), and refuse shapes whose scratch would not fit.
+
+Called through the C ABI with ctypes.  Collected last on purpose."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_158_gb300 as pa
+from pa_testlib import ATOL, RTOL
+from workloads import configs, gpu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _entry():
+    f = ctypes.CDLL(pa.LIB_PATH).pa_decode_noalloc
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32, vp]
+    f.restype = i32
+    return f
+
+
+def _call(f, w, out, q, kc, vc, bt, ctx):
+    return f(out.data_ptr(), q.data_ptr(), kc.data_ptr(), vc.data_ptr(), bt.data_ptr(), bt.shape[1],
+             ctx.data_ptr(), w.num_seqs, w.num_heads, w.head_dim, w.block_size, w.num_blocks,
+             w.scale, w.max_context_len, torch.cuda.current_stream().cuda_stream)
+
+
+def test_noalloc_decode_matches_workspace_decode_twice():
+    f = _entry()
+    w = configs.config2()            # c up to 500 tokens: two partitions, so the merge uses scratch
+    assert pa.pa_decode_workspace_size(w.num_seqs, w.num_heads, w.head_dim, w.max_context_len) > 4096
+    dw = gpu.materialize(w, layers=[0, 1], device=DEV)
+    ws = pa.decode_workspace(w.num_seqs, w.num_heads, w.head_dim, w.max_context_len)
+    for i in (0, 1):                 # two calls in a row, different inputs
+        ref = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=DEV)
+        pa.pa_decode(ref, dw.queries[i], dw.key_caches[i], dw.value_caches[i], dw.block_tables,
+                     dw.context_lens, w.scale, w.max_context_len, ws)
+        got = torch.full_like(ref, float("nan"))
+        assert _call(f, w, got, dw.queries[i], dw.key_caches[i], dw.value_caches[i], dw.block_tables,
+                     dw.context_lens) == pa.PA_OK
+        torch.cuda.synchronize()
+        g = got.float().cpu().numpy()
+        r = ref.float().cpu().numpy()
+        assert np.all(np.isfinite(g))
+        assert np.all(np.abs(g - r) <= ATOL + RTOL * np.abs(r))
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+def test_noalloc_refuses_shapes_beyond_its_scratch():
+    f = _entry()
+    w = configs.config5(num_layers=1)   # 256 x 32 pairs up to 4096 tokens: more than 32 MiB of scratch
+    assert pa.pa_decode_workspace_size(w.num_seqs, w.num_heads, w.head_dim, w.max_context_len) > (32 << 20)
+    out = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=DEV)
+    q = torch.empty_like(out)
+    kc = torch.empty((16, w.num_heads, w.block_size, w.head_dim), dtype=torch.float16, device=DEV)
+    bt = torch.from_numpy(w.block_tables).to(DEV)
+    ctx = torch.from_numpy(w.context_lens).to(DEV)
+    assert _call(f, w, out, q, kc, kc, bt, ctx) == pa.PA_ERR_UNSUPPORTED
