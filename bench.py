@@ -229,7 +229,7 @@ class Step:
 
     def launches_per_step(self) -> int:
         L = len(self.dw.layers)
-        per_layer = 1 + 1 + (1 if self.max_parts > 1 else 0)
+        per_layer = 1 + 1 + (1 if self.max_parts > 1 else 0)   # cache write, partition, merge
         return 1 + L * per_layer + (1 if self.copy_pairs is not None else 0)
 
     def run(self, decode_events=None):
@@ -355,7 +355,7 @@ def run_ours(args, rank, world, local):
         "decode_bytes_per_layer": st.bytes_per_decode,
         "roofline": {
             "bound": "hbm",
-            "kernel": "pa_decode (partition + merge kernels)",
+            "kernel": "pa_decode (partition + merge kernels; events bracket the call)",
             "achieved": round(achieved, 2),
             "peak": peak,
             "peak_kind": peak_kind,

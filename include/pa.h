@@ -62,7 +62,8 @@ typedef enum pa_status {
  * Bytes of device scratch pa_decode needs for this batch shape.  The decode
  * splits each sequence's context into partitions and keeps, per partition,
  * the running maximum, the softmax denominator and the unnormalised output
- * (fp32), plus a small work counter.  0 on invalid arguments.
+ * (fp32), plus a work counter that every call zeroes before its kernels
+ * run.  0 on invalid arguments.
  */
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len);
 

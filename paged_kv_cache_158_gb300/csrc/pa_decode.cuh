@@ -16,9 +16,14 @@
 //    0 issues two 1-D bulk copies per chunk (the K rows and the V rows of one
 //    (block, head) tile, contiguous in the [NB][H][B][D] layout) completing on
 //    the stage's mbarrier; only the live rows of a ragged last chunk are
-//    copied.  The partition's block-table slice sits in shared memory; the
-//    next item's slice is prefetched with cp.async while the current item
-//    runs.
+//    copied.  A warp's chunk stream runs across items: as soon as a stage is
+//    free and the current item has no chunk left for the warp, lane 0 issues
+//    the warp's first chunks of the next item, so copies stay in flight
+//    through the end-of-item barrier and merge.
+//  * The partition's block-table slice sits in shared memory; the next
+//    item's slice is prefetched with cp.async while the current item runs
+//    (the few entries needed to start the next item early are loaded into
+//    registers by lane 0).
 //  * Inside a warp each lane owns 8 dimensions (16 bytes) of a token row;
 //    D/8 lanes cover one row.  q.k uses fp16 x fp16 -> fp32 fused
 //    multiply-adds; the per-lane partial dots are combined by a shuffle
@@ -28,8 +33,12 @@
 //    reductions.  p.V accumulates in fp32, 8 dimensions per lane.
 //  * At the end of an item the warps' (m, l, o) merge in shared memory.  A
 //    sequence with one partition writes fp16 output directly; otherwise the
-//    partition's (m, l, o) go to the workspace and a second kernel merges
-//    the partitions (log-sum-exp weights), one warp per (sequence, head).
+//    partition's (m, l, o) go to the workspace and a second kernel merges the
+//    partitions (log-sum-exp weights), one warp per (sequence, head).  Two
+//    in-kernel merges were built and measured slower: merging item by item
+//    (a GPU-scope fence and an arrival atomic after every partition stall all
+//    four warps), and deferring each CTA's merges to when it runs out of work
+//    (the pending merges form a serial latency chain in the kernel's tail).
 //  * The summation order depends only on logical token positions, so the
 //    result is bit-identical under any relabelling of physical blocks.
 #pragma once
@@ -56,6 +65,7 @@ struct DecodeTraits {
   static constexpr int STAGE_BYTES = 2 * CHUNK_ELEMS * 2;  // K rows then V rows
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(TPL >= 1 && TPL <= LR && (TPL & (TPL - 1)) == 0, "lane layout");
+  static_assert(NST == 3, "next-item block ids are kept in three registers");
 
   // Fixed part of the dynamic shared memory (bytes), in layout order.
   static constexpr size_t kStages = size_t(NW) * NST * STAGE_BYTES;
@@ -63,7 +73,7 @@ struct DecodeTraits {
   static constexpr size_t kP = size_t(NW) * TC * 4;
   static constexpr int MS = D + 4;            // merge stride (floats): o[D], m, l, pad
   static constexpr size_t kMerge = 2 * size_t(NW) * MS * 4;
-  static constexpr size_t kMisc = 16 * 4;  // item ring, warp sums, failure flag
+  static constexpr size_t kMisc = 16 * 4;     // item ring, warp sums, flags
   static constexpr size_t kFixed = kStages + kBars + kP + kMerge + kMisc;
 };
 
@@ -115,14 +125,22 @@ __device__ __forceinline__ ItemInfo locate_item(int item, const int* cum, const 
   return it;
 }
 
+// Chunks of an item that warp `warp` processes (chunks warp, warp+NW, ...).
 template <int D, int B>
-__device__ __forceinline__ void issue_chunk(const DecodeParams& a, const ItemInfo& it,
-                                            const int* bt, int chunk, __half* stage, uint32_t bar,
+__device__ __forceinline__ int warp_chunks(const ItemInfo& it, int warp) {
+  using T = DecodeTraits<D, B>;
+  const int n = (it.t_end - it.t_begin + T::TC - 1) / T::TC;
+  return warp < n ? (n - 1 - warp) / T::NW + 1 : 0;
+}
+
+// Issues the bulk copies of one chunk (K rows and V rows) into a stage.
+template <int D, int B>
+__device__ __forceinline__ void issue_chunk(const DecodeParams& a, const ItemInfo& it, int phys,
+                                            int chunk, __half* stage, uint32_t bar,
                                             uint64_t policy) {
   using T = DecodeTraits<D, B>;
   const int t0 = it.t_begin + chunk * T::TC;
   const int rows = min(T::TC, it.t_end - t0);
-  const int phys = bt[t0 / B - it.blk0];
   if (phys < 0 || phys >= a.num_blocks) {
     atomicOr(a.err, PA_ERRBIT_BLOCK_ID);
     mbar_arrive(bar);  // completes the phase with no data; the chunk is skipped
@@ -221,7 +239,8 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
   cur_ptr += T::kP;
   float* merge = reinterpret_cast<float*>(cur_ptr);
   cur_ptr += T::kMerge;
-  int* misc = reinterpret_cast<int*>(cur_ptr);  // [0..1] item ring, [4..7] warp sums, [8] failed
+  // misc: [0..3] item ring, [4..7] warp sums, [8] failure flag
+  int* misc = reinterpret_cast<int*>(cur_ptr);
   cur_ptr += T::kMisc;
   const int bt_cap = a.part_tokens / B + 1;
   int* bt_s = reinterpret_cast<int*>(cur_ptr);  // 2 x bt_cap
@@ -303,14 +322,17 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
   float* my_p = p_s + warp * T::TC;
   const int cidx = lane % T::LR;
   const int rgrp = lane / T::LR;
-  uint32_t u = 0;  // chunks this warp has consumed so far (stage/phase bookkeeping)
+  // Per-warp running chunk counts across items (warp-uniform): consumed and
+  // issued.  Chunk g of the warp's stream lives in stage g % NST and is the
+  // (g / NST)-th use of that stage's barrier.
+  uint32_t u = 0, iss = 0;
   int buf = 0;
   int iter = 0;
 
   while (true) {
-    // Prefetch the next item's block-table slice into the other buffer.
-    ItemInfo nx;
     const bool has_next = nxt < total;
+    ItemInfo nx;
+    nx.t_begin = nx.t_end = 0;
     if (has_next) {
       nx = locate_item<B>(nxt, cum, ctx_s, nseq, H, P);
       const int32_t* row = a.block_tables + (size_t)(a.seq_begin + nx.s) * a.max_blocks;
@@ -322,17 +344,44 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
 
     const int* bt = bt_s + buf * bt_cap;
     const size_t sh = (size_t)(a.seq_begin + it.s) * H + it.h;
-    const int n_chunks = (it.t_end - it.t_begin + T::TC - 1) / T::TC;
-    const int n_my = warp < n_chunks ? (n_chunks - 1 - warp) / T::NW + 1 : 0;
+    const int n_my = warp_chunks<D, B>(it, warp);
+    const int n_nx = has_next ? warp_chunks<D, B>(nx, warp) : 0;
+    const uint32_t base = u;
 
-    if (lane == 0) {
-      const int pre = min(T::NST, n_my);
-      for (int i = 0; i < pre; ++i) {
-        const int st = (u + i) % T::NST;
-        issue_chunk<D, B>(a, it, bt, warp + i * T::NW, my_stages + st * 2 * T::CHUNK_ELEMS,
-                          smem_u32(&my_bars[st]), policy);
-      }
+    // Block ids of this warp's first chunks of the next item (lane 0 only).
+    int nxp0 = -1, nxp1 = -1, nxp2 = -1;
+    if (lane == 0 && n_nx > 0) {
+      const int32_t* row = a.block_tables + (size_t)(a.seq_begin + nx.s) * a.max_blocks;
+      nxp0 = row[(nx.t_begin + warp * T::TC) / B];
+      if (n_nx > 1) nxp1 = row[(nx.t_begin + (warp + T::NW) * T::TC) / B];
+      if (n_nx > 2) nxp2 = row[(nx.t_begin + (warp + 2 * T::NW) * T::TC) / B];
     }
+    // Fill free stages: the rest of this item's chunks, then the next item's.
+    auto issue_upto = [&]() {
+      if (lane == 0) {
+        while (iss < u + T::NST) {
+          const int k = (int)(iss - base);
+          const int st = iss % T::NST;
+          __half* stage = my_stages + st * 2 * T::CHUNK_ELEMS;
+          const uint32_t bar = smem_u32(&my_bars[st]);
+          if (k < n_my) {
+            const int chunk = warp + k * T::NW;
+            const int phys = bt[(it.t_begin + chunk * T::TC) / B - it.blk0];
+            issue_chunk<D, B>(a, it, phys, chunk, stage, bar, policy);
+          } else if (k - n_my < n_nx) {
+            const int j = k - n_my;
+            const int phys = j == 0 ? nxp0 : (j == 1 ? nxp1 : nxp2);
+            issue_chunk<D, B>(a, nx, phys, warp + j * T::NW, stage, bar, policy);
+          } else {
+            break;
+          }
+          ++iss;
+        }
+      }
+      iss = __shfl_sync(kFullMask, iss, 0);
+    };
+    issue_upto();
+
     const uint4 q = *reinterpret_cast<const uint4*>(static_cast<const __half*>(a.query) +
                                                     sh * D + 8 * cidx);
     float m = -INFINITY, l = 0.f;
@@ -341,15 +390,15 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
     for (int i = 0; i < 8; ++i) o[i] = 0.f;
 
     for (int i = 0; i < n_my; ++i) {
-      const uint32_t ui = u + i;
-      const int st = ui % T::NST;
+      const int st = u % T::NST;
       const uint32_t bar = smem_u32(&my_bars[st]);
-      bool ok = mbar_wait_bounded(bar, (ui / T::NST) & 1);
+      bool ok = mbar_wait_bounded(bar, (u / T::NST) & 1);
       ok = __all_sync(kFullMask, ok);
       if (!ok) {
         // Drain this warp's copies still in flight (bounded), then give up.
-        for (int k = i + 1; k < min(i + T::NST, n_my); ++k)
-          mbar_wait_bounded(smem_u32(&my_bars[(u + k) % T::NST]), ((u + k) / T::NST) & 1);
+        for (uint32_t g = u + 1; g < iss; ++g)
+          mbar_wait_bounded(smem_u32(&my_bars[g % T::NST]), (g / T::NST) & 1);
+        u = iss;
         if (lane == 0) {
           atomicOr(a.err, PA_ERRBIT_TIMEOUT);
           misc[8] = 1;
@@ -370,12 +419,9 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
                                      m, l, o);
       }
       __syncwarp();
-      if (lane == 0 && i + T::NST < n_my) {
-        issue_chunk<D, B>(a, it, bt, warp + (i + T::NST) * T::NW,
-                          my_stages + st * 2 * T::CHUNK_ELEMS, bar, policy);
-      }
+      ++u;
+      issue_upto();
     }
-    u += n_my;
 
     // Combine the row groups, then publish this warp's (m, l, o).
 #pragma unroll
@@ -395,7 +441,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
     cp_async_wait_all();
     __syncthreads();
 
-    // Merge the warps of this item and write it out.
+    // Merge the warps of this item and write the output or the partial.
     const float* mb = merge + (iter & 1) * T::NW * T::MS;
     for (int d = tid; d < D; d += T::THREADS) {
       float M = -INFINITY;
@@ -421,7 +467,12 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
         }
       }
     }
-    if (misc[8] != 0 || !has_next) break;
+    if (misc[8] != 0 || !has_next) {
+      // No copy of this warp may still be in flight when the CTA exits.
+      for (uint32_t g = u; g < iss; ++g)
+        mbar_wait_bounded(smem_u32(&my_bars[g % T::NST]), (g / T::NST) & 1);
+      break;
+    }
     cur = nxt;
     nxt = misc[2 + (iter & 1)];
     it = nx;
@@ -430,7 +481,10 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
   }
 }
 
-// Merge the partitions of each (sequence, head): one warp per pair.
+// Merge the partitions of each (sequence, head): one warp per pair.  Lanes
+// load the partitions' (m, l) in parallel; the warp reduces max and sum by
+// shuffles, then accumulates the weighted partial outputs in partition
+// order, D/32 dimensions per lane.
 template <int D, int B>
 __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams a, int total_seqs) {
   constexpr int DPL = D / 32;
@@ -442,28 +496,40 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams a
   const int n = num_parts(c, a.part_tokens);
   if (n <= 1) return;
   const float* ml = a.ws_ml + (size_t)pair * a.max_parts * 2;
-  const float* ob = a.ws_o + (size_t)pair * a.max_parts * D;
+  const float* ob = a.ws_o + (size_t)pair * a.max_parts * D + lane * DPL;
   float M = -INFINITY;
-  for (int p = 0; p < n; ++p) M = fmaxf(M, ml[2 * p]);
+  for (int p = lane; p < n; p += 32) M = fmaxf(M, ml[2 * p]);
+#pragma unroll
+  for (int msk = 16; msk >= 1; msk >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, msk));
   float L = 0.f;
+  for (int p = lane; p < n; p += 32) {
+    const float mp = ml[2 * p];
+    L += (mp == -INFINITY ? 0.f : exp2_approx(mp - M)) * ml[2 * p + 1];
+  }
+#pragma unroll
+  for (int msk = 16; msk >= 1; msk >>= 1) L += __shfl_xor_sync(kFullMask, L, msk);
   float acc[DPL];
 #pragma unroll
   for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
-  for (int p = 0; p < n; ++p) {
-    const float mp = ml[2 * p];
-    const float w = (mp == -INFINITY) ? 0.f : exp2_approx(mp - M);
-    L = fmaf(w, ml[2 * p + 1], L);
-    const float* op = ob + (size_t)p * D + lane * DPL;
-    if constexpr (DPL == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(op);
-      acc[0] = fmaf(w, v.x, acc[0]);
-      acc[1] = fmaf(w, v.y, acc[1]);
-      acc[2] = fmaf(w, v.z, acc[2]);
-      acc[3] = fmaf(w, v.w, acc[3]);
-    } else {
-      const float2 v = *reinterpret_cast<const float2*>(op);
-      acc[0] = fmaf(w, v.x, acc[0]);
-      acc[1] = fmaf(w, v.y, acc[1]);
+  for (int p0 = 0; p0 < n; p0 += 32) {
+    const int pl = p0 + lane;
+    const float mp = pl < n ? ml[2 * pl] : -INFINITY;
+    const float wl = mp == -INFINITY ? 0.f : exp2_approx(mp - M);
+    const int cnt = min(32, n - p0);
+    for (int j = 0; j < cnt; ++j) {
+      const float w = __shfl_sync(kFullMask, wl, j);
+      const float* op = ob + (size_t)(p0 + j) * D;
+      if constexpr (DPL == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(op);
+        acc[0] = fmaf(w, v.x, acc[0]);
+        acc[1] = fmaf(w, v.y, acc[1]);
+        acc[2] = fmaf(w, v.z, acc[2]);
+        acc[3] = fmaf(w, v.w, acc[3]);
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(op);
+        acc[0] = fmaf(w, v.x, acc[0]);
+        acc[1] = fmaf(w, v.y, acc[1]);
+      }
     }
   }
   __half* out = static_cast<__half*>(a.out) + (size_t)pair * D + lane * DPL;
@@ -472,16 +538,16 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams a
 }
 
 template <int D, int B>
-cudaError_t launch_partition_t(const DecodeParams& p, int grid, size_t smem, cudaStream_t st) {
-  decode_partition_kernel<D, B><<<grid, DecodeTraits<D, B>::THREADS, smem, st>>>(p);
-  return cudaGetLastError();
-}
-
-template <int D, int B>
 cudaError_t launch_reduce_t(const DecodeParams& p, int total_seqs, cudaStream_t st) {
   const long long warps = (long long)total_seqs * p.num_heads;
   const int blocks = (int)((warps + 3) / 4);
   decode_reduce_kernel<D, B><<<blocks, 128, 0, st>>>(p, total_seqs);
+  return cudaGetLastError();
+}
+
+template <int D, int B>
+cudaError_t launch_partition_t(const DecodeParams& p, int grid, size_t smem, cudaStream_t st) {
+  decode_partition_kernel<D, B><<<grid, DecodeTraits<D, B>::THREADS, smem, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -36,33 +36,42 @@ def _call(f, w, out, q, kc, vc, bt, ctx):
 
 def test_noalloc_decode_matches_workspace_decode_twice():
     f = _entry()
-    w = configs.config2()            # c up to 500 tokens: two partitions, so the merge uses scratch
-    assert pa.pa_decode_workspace_size(w.num_seqs, w.num_heads, w.head_dim, w.max_context_len) > 4096
-    dw = gpu.materialize(w, layers=[0, 1], device=DEV)
-    ws = pa.decode_workspace(w.num_seqs, w.num_heads, w.head_dim, w.max_context_len)
-    for i in (0, 1):                 # two calls in a row, different inputs
-        ref = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=DEV)
-        pa.pa_decode(ref, dw.queries[i], dw.key_caches[i], dw.value_caches[i], dw.block_tables,
-                     dw.context_lens, w.scale, w.max_context_len, ws)
-        got = torch.full_like(ref, float("nan"))
-        assert _call(f, w, got, dw.queries[i], dw.key_caches[i], dw.value_caches[i], dw.block_tables,
-                     dw.context_lens) == pa.PA_OK
-        torch.cuda.synchronize()
-        g = got.float().cpu().numpy()
-        r = ref.float().cpu().numpy()
-        assert np.all(np.isfinite(g))
-        assert np.all(np.abs(g - r) <= ATOL + RTOL * np.abs(r))
-        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
-    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+    w = configs.config2()
+    # 128-token partitions: every sequence (200..500 tokens) has several, so the
+    # partial results and the merge go through the scratch area.
+    pa.pa_decode_set_partition_tokens(128)
+    try:
+        assert pa.pa_decode_workspace_size(w.num_seqs, w.num_heads, w.head_dim, w.max_context_len) > 4096
+        dw = gpu.materialize(w, layers=[0, 1], device=DEV)
+        ws = pa.decode_workspace(w.num_seqs, w.num_heads, w.head_dim, w.max_context_len)
+        for i in (0, 1):                 # two calls in a row, different inputs
+            ref = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=DEV)
+            pa.pa_decode(ref, dw.queries[i], dw.key_caches[i], dw.value_caches[i], dw.block_tables,
+                         dw.context_lens, w.scale, w.max_context_len, ws)
+            got = torch.full_like(ref, float("nan"))
+            assert _call(f, w, got, dw.queries[i], dw.key_caches[i], dw.value_caches[i],
+                         dw.block_tables, dw.context_lens) == pa.PA_OK
+            torch.cuda.synchronize()
+            g = got.float().cpu().numpy()
+            r = ref.float().cpu().numpy()
+            assert np.all(np.isfinite(g))
+            assert np.all(np.abs(g - r) <= ATOL + RTOL * np.abs(r))
+            assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+        assert pa.pa_check_errors() == (pa.PA_OK, 0)
+    finally:
+        pa.pa_decode_set_partition_tokens(0)
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch():
+    """1024 sequences x 64 heads up to 4096 tokens needs far more than 32 MiB of
+    partials; the call is refused on the host and launches nothing."""
     f = _entry()
-    w = configs.config5(num_layers=1)   # 256 x 32 pairs up to 4096 tokens: more than 32 MiB of scratch
-    assert pa.pa_decode_workspace_size(w.num_seqs, w.num_heads, w.head_dim, w.max_context_len) > (32 << 20)
-    out = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=DEV)
-    q = torch.empty_like(out)
-    kc = torch.empty((16, w.num_heads, w.block_size, w.head_dim), dtype=torch.float16, device=DEV)
-    bt = torch.from_numpy(w.block_tables).to(DEV)
-    ctx = torch.from_numpy(w.context_lens).to(DEV)
-    assert _call(f, w, out, q, kc, kc, bt, ctx) == pa.PA_ERR_UNSUPPORTED
+    S, H, D, B, NB, ctx_max = 1024, 64, 128, 16, 8, 4096
+    assert pa.pa_decode_workspace_size(S, H, D, ctx_max) > (32 << 20)
+    dummy = torch.zeros(64, dtype=torch.float16, device=DEV)
+    ints = torch.zeros(64, dtype=torch.int32, device=DEV)
+    p = dummy.data_ptr()
+    rc = f(p, p, p, p, ints.data_ptr(), 1, ints.data_ptr(), S, H, D, B, NB, 0.1, ctx_max,
+           torch.cuda.current_stream().cuda_stream)
+    assert rc == pa.PA_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
