@@ -217,7 +217,7 @@ pa_status pa_decode(void* out, const void* query, const void* key_cache, const v
   p.scale_log2 = (float)((double)scale * 1.4426950408889634073599246810019);
 
   unsigned int* counters = reinterpret_cast<unsigned int*>(ws + w.counters_off);
-  if (cudaMemsetAsync(ws, 0, w.zero_bytes, cs) != cudaSuccess) return PA_ERR_CUDA;
+  if (pa::launch_zero_words(counters, (int)(w.zero_bytes / 4), cs) != cudaSuccess) return PA_ERR_CUDA;
   for (int b = 0; b < w.launches; ++b) {
     p.seq_begin = b * pa::kMaxSeqsPerLaunch;
     p.num_seqs = num_seqs - p.seq_begin < pa::kMaxSeqsPerLaunch ? num_seqs - p.seq_begin

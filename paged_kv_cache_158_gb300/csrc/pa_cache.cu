@@ -5,7 +5,9 @@
 // vectors with fully coalesced accesses.
 #include <cuda_fp16.h>
 
+#include "pa_device.cuh"
 #include "pa_internal.h"
+#include "pa_launch.cuh"
 
 namespace pa {
 namespace {
@@ -22,6 +24,8 @@ __global__ void __launch_bounds__(256)
                              int num_heads, int log2_block, long long num_slots,
                              unsigned int* err) {
   constexpr int V = D / 8;  // 16-byte vectors per head row
+  pdl_wait();
+  pdl_launch_dependents();
   const long long per_token = (long long)num_heads * V;
   const long long total = (long long)num_tokens * per_token;
   const long long stride = (long long)gridDim.x * blockDim.x;
@@ -56,6 +60,8 @@ struct LayerPtrs {
 __global__ void __launch_bounds__(256)
     copy_blocks_kernel(LayerPtrs ptrs, const int64_t* __restrict__ block_mapping, int pair_base,
                        long long block_vecs, long long num_blocks, unsigned int* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int pair = pair_base + blockIdx.y;
   const int layer = blockIdx.z >> 1;
   const long long src = block_mapping[2 * pair];
@@ -78,6 +84,8 @@ __global__ void __launch_bounds__(256)
                         int max_blocks, const int32_t* __restrict__ token_seq,
                         const int32_t* __restrict__ token_pos, int num_tokens, int num_seqs,
                         int block_size, int num_blocks, unsigned int* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= num_tokens) return;
   const int s = token_seq[t];
@@ -95,6 +103,14 @@ __global__ void __launch_bounds__(256)
   slot_mapping[t] = slot;
 }
 
+// Zeroes n 32-bit words (the decode workspace's work counters); a kernel
+// rather than a memset so the decode call stays one chain of kernels.
+__global__ void __launch_bounds__(128) zero_words_kernel(unsigned int* __restrict__ w, int n) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) w[i] = 0u;
+}
+
 int log2_exact(int x) {
   int l = 0;
   while ((1 << l) < x) ++l;
@@ -109,6 +125,11 @@ int sm_count() {
 }
 
 }  // namespace
+
+cudaError_t launch_zero_words(unsigned int* words, int n, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  return launch_pdl(zero_words_kernel, dim3(1), dim3(128), 0, stream, words, n);
+}
 
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* key_cache,
                                      void* value_cache, const int64_t* slot_mapping,
@@ -127,12 +148,10 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k
   auto kc = static_cast<uint4*>(key_cache);
   auto vc = static_cast<uint4*>(value_cache);
   if (head_dim == 64)
-    reshape_and_cache_kernel<64><<<(int)blocks, threads, 0, stream>>>(
-        k, v, kc, vc, slot_mapping, num_tokens, num_heads, lb, slots, err);
-  else
-    reshape_and_cache_kernel<128><<<(int)blocks, threads, 0, stream>>>(
-        k, v, kc, vc, slot_mapping, num_tokens, num_heads, lb, slots, err);
-  return cudaGetLastError();
+    return launch_pdl(reshape_and_cache_kernel<64>, dim3((unsigned)blocks), dim3(threads), 0,
+                      stream, k, v, kc, vc, slot_mapping, num_tokens, num_heads, lb, slots, err);
+  return launch_pdl(reshape_and_cache_kernel<128>, dim3((unsigned)blocks), dim3(threads), 0, stream,
+                    k, v, kc, vc, slot_mapping, num_tokens, num_heads, lb, slots, err);
 }
 
 cudaError_t launch_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
@@ -154,9 +173,8 @@ cudaError_t launch_copy_blocks(void* const* key_caches, void* const* value_cache
     for (int p0 = 0; p0 < num_pairs; p0 += 65535) {
       const int np = num_pairs - p0 < 65535 ? num_pairs - p0 : 65535;
       dim3 grid((unsigned)xblocks, (unsigned)np, (unsigned)(2 * nl));
-      copy_blocks_kernel<<<grid, threads, 0, stream>>>(ptrs, block_mapping, p0, block_vecs,
-                                                       num_blocks, err);
-      const cudaError_t e = cudaGetLastError();
+      const cudaError_t e = launch_pdl(copy_blocks_kernel, grid, dim3(threads), 0, stream, ptrs,
+                                       block_mapping, p0, block_vecs, (long long)num_blocks, err);
       if (e != cudaSuccess) return e;
     }
   }
@@ -171,10 +189,9 @@ cudaError_t launch_slot_mapping(int64_t* slot_mapping, const int32_t* block_tabl
   if (num_tokens == 0) return cudaSuccess;
   const int threads = 256;
   const int blocks = (num_tokens + threads - 1) / threads;
-  slot_mapping_kernel<<<blocks, threads, 0, stream>>>(slot_mapping, block_tables, max_blocks,
-                                                      token_seq, token_pos, num_tokens, num_seqs,
-                                                      block_size, num_blocks, err);
-  return cudaGetLastError();
+  return launch_pdl(slot_mapping_kernel, dim3(blocks), dim3(threads), 0, stream, slot_mapping,
+                    block_tables, max_blocks, token_seq, token_pos, num_tokens, num_seqs,
+                    block_size, num_blocks, err);
 }
 
 }  // namespace pa

@@ -58,6 +58,7 @@
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "pa_launch.cuh"
 
 namespace pa {
 
@@ -265,6 +266,16 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
   const int H = a.num_heads;
   const int P = a.part_tokens;
 
+  if (lane == 0) {
+    for (int j = 0; j < T::NST; ++j) mbar_init(smem_u32(&bars[warp * T::NST + j]), 1);
+  }
+  if (tid == 0) misc[8] = 0;
+  fence_mbar_init();
+  // Everything below reads inputs or the workspace.
+  pdl_wait();
+  pdl_launch_dependents();
+  if (tid == 0) misc[0] = (int)atomicAdd(a.counter, 1u);
+
   // ---- per-sequence item counts and their exclusive prefix sums ---------
   {
     constexpr int PER = (kMaxSeqsPerLaunch + T::THREADS - 1) / T::THREADS;
@@ -290,11 +301,6 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
       if (lane >= o) x += y;
     }
     if (lane == 31) misc[4 + warp] = x;
-    if (lane == 0) {
-      for (int j = 0; j < T::NST; ++j) mbar_init(smem_u32(&bars[warp * T::NST + j]), 1);
-    }
-    if (tid == 0) misc[8] = 0;
-    fence_mbar_init();
     __syncthreads();
     int run = x - local;
     for (int w = 0; w < warp; ++w) run += misc[4 + w];
@@ -308,10 +314,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
       }
     }
   }
-  if (tid == 0) {
-    misc[0] = (int)atomicAdd(a.counter, 1u);
-    misc[1] = (int)atomicAdd(a.counter, 1u);
-  }
+  if (tid == 0) misc[1] = (int)atomicAdd(a.counter, 1u);
   __syncthreads();
   const int total = cum[nseq];
   int cur = misc[0];
@@ -499,6 +502,8 @@ template <int D, int B>
 __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams a, int total_seqs) {
   constexpr int DPL = D / 32;
   const int lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_launch_dependents();
   const long long pair = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (pair >= (long long)total_seqs * a.num_heads) return;
   const int s = (int)(pair / a.num_heads);
@@ -551,14 +556,13 @@ template <int D, int B>
 cudaError_t launch_reduce_t(const DecodeParams& p, int total_seqs, cudaStream_t st) {
   const long long warps = (long long)total_seqs * p.num_heads;
   const int blocks = (int)((warps + 3) / 4);
-  decode_reduce_kernel<D, B><<<blocks, 128, 0, st>>>(p, total_seqs);
-  return cudaGetLastError();
+  return launch_pdl(decode_reduce_kernel<D, B>, dim3(blocks), dim3(128), 0, st, p, total_seqs);
 }
 
 template <int D, int B>
 cudaError_t launch_partition_t(const DecodeParams& p, int grid, size_t smem, cudaStream_t st) {
-  decode_partition_kernel<D, B><<<grid, DecodeTraits<D, B>::THREADS, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(decode_partition_kernel<D, B>, dim3(grid), dim3(DecodeTraits<D, B>::THREADS),
+                    smem, st, p);
 }
 
 template <int D, int B>

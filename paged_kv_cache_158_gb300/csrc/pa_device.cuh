@@ -24,6 +24,21 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// ---- programmatic dependent launch --------------------------------------
+// Every library kernel is launched with programmatic stream serialisation:
+// it may start while the previous kernel in the stream is finishing, does
+// only CTA-local set-up, and waits here before touching global memory that
+// earlier stream work may produce or consume.  Without the launch attribute
+// both instructions are no-ops.
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel in the stream start its own set-up early (it still
+// waits for this grid to finish before touching memory).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- mbarrier (shared::cta) ---------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

@@ -52,6 +52,9 @@ int decode_ctas_per_sm(int head_dim, int block_size, size_t smem_bytes);
 // One-time per-device kernel attributes (dynamic shared memory opt-in).
 cudaError_t decode_prepare_device(int device);
 
+// Zeroes n 32-bit words on the stream (one small kernel).
+cudaError_t launch_zero_words(unsigned int* words, int n, cudaStream_t stream);
+
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* key_cache,
                                      void* value_cache, const int64_t* slot_mapping,
                                      int num_tokens, int num_heads, int head_dim, int block_size,
