@@ -47,7 +47,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--partition-tokens", type=int, default=0)
-    ap.add_argument("--graph", action="store_true", help="replay each step as one CUDA graph")
+    ap.add_argument("--eager", action="store_true", help="time eager launches only (no CUDA graph)")
     return ap.parse_args()
 
 
@@ -192,19 +192,20 @@ def weak_scaling_value(bytes_per_rank_step: int, world: int, ms_per_step_max: fl
 # ---------------------------------------------------------------- our arm
 
 class Step:
-    """Device state and the launch sequence of one decode step."""
+    """Device state of the workload and its decode step (the library's DecodeStep)."""
 
     def __init__(self, w, device):
         import torch
 
         import paged_kv_cache_158_gb300 as pa
         from paged_kv_cache_158_gb300.pool import BlockManager
+        from paged_kv_cache_158_gb300.step import DecodeStep
         from workloads import gpu
 
         self.pa, self.w, self.dev = pa, w, device
         dw = gpu.materialize(w, device=device)
         self.dw = dw
-        self.copy_pairs = None
+        copy_pairs = None
         if w.block_tables is None:          # shared-prefix workload: the block manager plans
             bm = BlockManager(w.num_blocks, w.block_size, w.num_seqs, w.max_blocks_per_seq, w.free_order)
             bm.add_sequence(0)
@@ -213,40 +214,45 @@ class Step:
                 bm.fork(0, s)
             for s in range(w.num_seqs):
                 bm.append_tokens(s, int(w.suffix_lens[s]))
-            self.copy_pairs = torch.from_numpy(bm.take_copies()).to(device)
+            copy_pairs = torch.from_numpy(bm.take_copies()).to(device)
             dw.block_tables = torch.from_numpy(bm.block_tables()).to(device)
         self.bt_host = dw.block_tables.cpu().numpy()
         self.ctx_host = w.context_lens.copy()
         self.max_ctx = int(self.ctx_host.max())
-        L = len(dw.layers)
-        self.outs = [torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=device)
-                     for _ in range(L)]
-        self.slots = torch.empty(dw.token_seq.numel(), dtype=torch.int64, device=device)
-        self.ws = pa.decode_workspace(w.num_seqs, w.num_heads, w.head_dim, self.max_ctx, device)
+        outs = [torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=device)
+                for _ in dw.layers]
+        self.step = DecodeStep(dw.key_caches, dw.value_caches, dw.queries, dw.keys_new, dw.values_new,
+                               outs, dw.block_tables, dw.context_lens, dw.token_seq, dw.token_pos,
+                               w.block_size, w.num_blocks, w.scale, self.max_ctx, copy_pairs)
+        self.outs = outs
+        self.copy_pairs = copy_pairs
         self.bytes_per_decode = decode_bytes(w, self.bt_host, self.ctx_host)
-        self.max_parts = -(-self.max_ctx // pa.pa_decode_partition_tokens(w.num_seqs, w.num_heads, self.max_ctx))
-        self.stream = torch.cuda.current_stream(device)
+        self.partition_tokens = pa.pa_decode_partition_tokens(w.num_seqs, w.num_heads, self.max_ctx)
+        self.max_parts = -(-self.max_ctx // self.partition_tokens)
 
     def launches_per_step(self) -> int:
+        """Library kernels per step: slot map; per layer the cache write, the
+        work-counter init, the partition pass and (with several partitions) the merge."""
         L = len(self.dw.layers)
-        per_layer = 1 + 1 + (1 if self.max_parts > 1 else 0)   # cache write, partition, merge
+        per_layer = 3 + (1 if self.max_parts > 1 else 0)
         return 1 + L * per_layer + (1 if self.copy_pairs is not None else 0)
 
-    def run(self, decode_events=None):
-        pa, w, dw = self.pa, self.w, self.dw
-        if self.copy_pairs is not None:
-            pa.pa_copy_blocks(dw.key_caches, dw.value_caches, self.copy_pairs, self.stream)
-        pa.pa_slot_mapping(self.slots, dw.block_tables, dw.token_seq, dw.token_pos, w.block_size,
-                           w.num_blocks, self.stream)
-        for i in range(len(dw.layers)):
-            pa.pa_reshape_and_cache(dw.keys_new[i], dw.values_new[i], dw.key_caches[i], dw.value_caches[i],
-                                    self.slots, self.stream)
-            if decode_events is not None:
-                decode_events[i][0].record(self.stream)
-            pa.pa_decode(self.outs[i], dw.queries[i], dw.key_caches[i], dw.value_caches[i], dw.block_tables,
-                         dw.context_lens, w.scale, self.max_ctx, self.ws, self.stream)
-            if decode_events is not None:
-                decode_events[i][1].record(self.stream)
+
+def timed(fn, K, device, world, stream):
+    """Device time of K calls of fn (CUDA events on the launching stream, barrier and
+    synchronize on both sides), max over ranks; ms for all K."""
+    import torch
+    barrier(world)
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(K):
+        fn(k)
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    return max_over_ranks(t0.elapsed_time(t1), world)
 
 
 def run_ours(args, rank, world, local):
@@ -260,63 +266,45 @@ def run_ours(args, rank, world, local):
     w = make_workload(args.workload, args.layers)
     st = Step(w, device)
     L = len(st.dw.layers)
+    stream = torch.cuda.current_stream(device)
     for _ in range(args.warmup):
-        st.run()
+        st.step.run(stream)
     torch.cuda.synchronize(device)
     status, bits = pa.pa_check_errors()
     if status != pa.PA_OK:
         raise RuntimeError(f"device error word after warm-up: {pa.pa_status_string(status)} 0x{bits:x}")
 
-    graph = None
-    if args.graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            st.stream = torch.cuda.current_stream(device)
-            st.run()
-        st.stream = torch.cuda.current_stream(device)
-        graph.replay()
-        torch.cuda.synchronize(device)
-
     K = args.steps
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
-          for _ in range(K)] if graph is None else None
-    uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
     except Exception:
         uuid = None
     clocks = ClockSampler(uuid)
-    barrier(world)
-    torch.cuda.synchronize(device)
     clocks.start()
     time.sleep(0.3)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(st.stream)
-    for k in range(K):
-        if graph is not None:
-            graph.replay()
-        else:
-            st.run(ev[k])
-    t1.record(st.stream)
-    torch.cuda.synchronize(device)
-    barrier(world)
+    # Eager pass: the step launched call by call, with CUDA events around every
+    # decode call (the dominant kernel's duration, for the roofline).
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+          for _ in range(K)]
+    ms_eager = timed(lambda k: st.step.run(stream, ev[k]), K, device, world, stream)
+    dec_ms = [a.elapsed_time(b) for row in ev for a, b in row]
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    # Graph pass: the same step captured once and replayed (the production configuration).
+    ms_graph = None
+    if not args.eager:
+        st.step.capture(warmup=2)
+        for _ in range(3):
+            st.step.replay()
+        ms_graph = timed(lambda k: st.step.replay(), K, device, world, stream)
     clk = clocks.stop()
-    ms_total = t0.elapsed_time(t1)
-    ms_total_max = max_over_ranks(ms_total, world)
     status, bits = pa.pa_check_errors()
     if status != pa.PA_OK:
         raise RuntimeError(f"device error word after timing: {pa.pa_status_string(status)} 0x{bits:x}")
 
-    ms_step = ms_total_max / K
+    ms_step = (ms_graph if ms_graph is not None else ms_eager) / K
     bytes_step = st.bytes_per_decode * L
     value = weak_scaling_value(bytes_step, world, ms_step)
     peak, peak_kind = measured_peak()
-    if ev is not None:
-        dec_ms = [a.elapsed_time(b) for row in ev for a, b in row]
-        dec_avg_ms = sum(dec_ms) / len(dec_ms)
-    else:
-        dec_avg_ms = ms_step / L
     achieved = st.bytes_per_decode / (dec_avg_ms * 1e-3) / 1e9
     ctx_tokens = int(st.ctx_host.sum())
 
@@ -342,10 +330,10 @@ def run_ours(args, rank, world, local):
             "layers": L, "num_seqs": w.num_seqs, "num_heads": w.num_heads, "head_dim": w.head_dim,
             "block_size": w.block_size, "num_blocks_per_layer": w.num_blocks,
             "context_tokens": ctx_tokens, "max_context_len": st.max_ctx,
-            "partition_tokens": pa.pa_decode_partition_tokens(w.num_seqs, w.num_heads, st.max_ctx),
+            "partition_tokens": st.partition_tokens,
             "l2": "inputs larger than L2: each layer's cache is read once per step",
             "kv_pool_gb": round(w.pool_bytes_all_layers() / 1e9, 3),
-            "cuda_graph": bool(args.graph),
+            "cuda_graph": ms_graph is not None,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
@@ -353,9 +341,12 @@ def run_ours(args, rank, world, local):
         "decode_tokens_per_s_per_layer": round(w.num_seqs / (ms_step * 1e-3 / L), 1),
         "context_tokens_per_s_per_layer": round(ctx_tokens / (ms_step * 1e-3 / L), 1),
         "decode_bytes_per_layer": st.bytes_per_decode,
+        "eager": {"value": round(weak_scaling_value(bytes_step, world, ms_eager / K), 2),
+                  "ms_per_step": round(ms_eager / K, 4)},
         "roofline": {
             "bound": "hbm",
-            "kernel": "pa_decode (partition + merge kernels; events bracket the call)",
+            "kernel": "pa_decode (work-counter init + partition + merge kernels; CUDA events "
+                      "bracket each call in the eager pass)",
             "achieved": round(achieved, 2),
             "peak": peak,
             "peak_kind": peak_kind,
@@ -365,7 +356,7 @@ def run_ours(args, rank, world, local):
             "traffic": committed_traffic(w.name),
         },
         "clocks": clk,
-        "gpu_launches": st.launches_per_step() * K,
+        "gpu_launches": st.launches_per_step() * K * (2 if ms_graph is not None else 1),
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -376,7 +367,7 @@ def run_ours(args, rank, world, local):
 def measure_e2e(st, args, world, device):
     """Same metric through the public API with the step's inputs in pinned host memory:
     every step copies q / new K,V / token ids / tables / lengths host->device, runs the
-    step and reads every layer's output back."""
+    step (graph replay unless --eager) and reads every layer's output back."""
     import torch
     dw = st.dw
     pin = lambda t: t.detach().cpu().pin_memory()  # noqa: E731
@@ -389,7 +380,7 @@ def measure_e2e(st, args, world, device):
     h2d = sum(t.numel() * t.element_size() for t in h_q + h_k + h_v + h_small)
     d2h = sum(t.numel() * t.element_size() for t in h_out)
     K = max(3, min(args.steps, 100))
-    s = st.stream
+    use_graph = st.step.graph is not None
 
     def one():
         for hs, ds in zip(h_small, d_small):
@@ -398,7 +389,10 @@ def measure_e2e(st, args, world, device):
             dw.queries[i].copy_(h_q[i], non_blocking=True)
             dw.keys_new[i].copy_(h_k[i], non_blocking=True)
             dw.values_new[i].copy_(h_v[i], non_blocking=True)
-        st.run()
+        if use_graph:
+            st.step.replay()
+        else:
+            st.step.run()
         for i in range(len(dw.layers)):
             h_out[i].copy_(st.outs[i], non_blocking=True)
 
@@ -413,7 +407,7 @@ def measure_e2e(st, args, world, device):
     dt = max_over_ranks(time.perf_counter() - t0, world) / K
     L = len(dw.layers)
     return {"value": round(st.bytes_per_decode * L * world / dt / 1e9, 2), "unit": "GB/s",
-            "ms_per_step": round(dt * 1e3, 4), "steps": K,
+            "ms_per_step": round(dt * 1e3, 4), "steps": K, "cuda_graph": use_graph,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 

@@ -1,0 +1,79 @@
+"""The decode step replayed as a CUDA graph gives the same bits as the same
+step launched eagerly, including after the inputs are updated in place
+between replays and with the copy-on-write block copies in the step."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_158_gb300 as pa
+from paged_kv_cache_158_gb300.pool import BlockManager
+from paged_kv_cache_158_gb300.step import DecodeStep
+from pa_testlib import u16
+from workloads import configs, gpu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def make_step(w, dw, copy_pairs=None):
+    outs = [torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=DEV)
+            for _ in dw.layers]
+    return DecodeStep(dw.key_caches, dw.value_caches, dw.queries, dw.keys_new, dw.values_new, outs,
+                      dw.block_tables, dw.context_lens, dw.token_seq, dw.token_pos, w.block_size,
+                      w.num_blocks, w.scale, int(w.context_lens.max()), copy_pairs)
+
+
+def clone_dw(dw):
+    import copy
+    c = copy.copy(dw)
+    c.key_caches = [t.clone() for t in dw.key_caches]
+    c.value_caches = [t.clone() for t in dw.value_caches]
+    c.queries = [t.clone() for t in dw.queries]
+    return c
+
+
+@pytest.mark.parametrize("cfg,layers", [(2, [0]), (1, [0, 1, 2]), (5, [0, 1])])
+def test_graph_replay_matches_eager(cfg, layers):
+    w = configs.ALL[cfg]() if cfg != 5 else configs.config5(num_layers=2)
+    dw = gpu.materialize(w, layers=layers, device=DEV)
+    dw_eager = clone_dw(dw)
+    eager = make_step(w, dw_eager)
+    graph = make_step(w, dw)
+    graph.capture()                       # runs the step twice eagerly, then captures it
+    for rep in range(2):
+        if rep == 1:                      # new queries, in place, before the second replay
+            for qe, qg in zip(dw_eager.queries, dw.queries):
+                qe.mul_(-1.0)
+                qg.mul_(-1.0)
+        eager.run()
+        graph.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(eager.outs, graph.outs):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for a, b in zip(dw_eager.key_caches + dw_eager.value_caches, dw.key_caches + dw.value_caches):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+def test_graph_step_with_copy_on_write():
+    w = configs.config4()
+    bm = BlockManager(w.num_blocks, w.block_size, w.num_seqs, w.max_blocks_per_seq, w.free_order)
+    bm.add_sequence(0)
+    bm.append_tokens(0, w.prefix_len)
+    for s in range(1, w.num_seqs):
+        bm.fork(0, s)
+    for s in range(w.num_seqs):
+        bm.append_tokens(s, int(w.suffix_lens[s]))
+    pairs = torch.from_numpy(bm.take_copies()).to(DEV)
+    dw = gpu.materialize(w, device=DEV)
+    dw.block_tables = torch.from_numpy(bm.block_tables()).to(DEV)
+    dw_eager = clone_dw(dw)
+    eager = make_step(w, dw_eager, pairs)
+    graph = make_step(w, dw, pairs)
+    eager.run()
+    graph.capture(warmup=1)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(eager.outs[0].view(torch.int16), graph.outs[0].view(torch.int16))
+    assert np.array_equal(u16(dw_eager.key_caches[0]), u16(dw.key_caches[0]))
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
