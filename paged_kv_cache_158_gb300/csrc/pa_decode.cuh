@@ -56,6 +56,8 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 #include "pa_launch.cuh"
@@ -250,7 +252,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
   cur_ptr += T::kP;
   float* merge = reinterpret_cast<float*>(cur_ptr);
   cur_ptr += T::kMerge;
-  // misc: [0..3] item ring, [4..7] warp sums, [8] failure flag
+  // misc: [1..3] item ring, [4..7] warp sums, [8] failure flag
   int* misc = reinterpret_cast<int*>(cur_ptr);
   cur_ptr += T::kMisc;
   const int bt_cap = a.part_tokens / B + 1;
@@ -271,10 +273,12 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
   }
   if (tid == 0) misc[8] = 0;
   fence_mbar_init();
-  // Everything below reads inputs or the workspace.
-  pdl_wait();
-  pdl_launch_dependents();
-  if (tid == 0) misc[0] = (int)atomicAdd(a.counter, 1u);
+  // The call's inputs (context lengths, block tables, queries, caches) were
+  // written before the call's first kernel, which lets this kernel launch
+  // only after its own wait: they are complete here, so the scan, the first
+  // item's block-table slice and its first copies start before pdl_wait.
+  // Only the work counter (zeroed by the kernel just before this one) and
+  // the workspace partials are touched after it.
 
   // ---- per-sequence item counts and their exclusive prefix sums ---------
   {
@@ -314,11 +318,11 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
       }
     }
   }
-  if (tid == 0) misc[1] = (int)atomicAdd(a.counter, 1u);
   __syncthreads();
   const int total = cum[nseq];
-  int cur = misc[0];
-  int nxt = misc[1];
+  // Item blockIdx.x is this CTA's first; later items come from the counter,
+  // numbered from gridDim.x on.
+  int cur = blockIdx.x;
   if (cur >= total) return;
 
   // First item's block-table slice (synchronous).
@@ -342,6 +346,25 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
   int buf = 0;
   int iter = 0;
 
+  // The first item's first copies, still before the wait.
+  {
+    const int n0 = warp_chunks<D, B>(it, warp);
+    if (lane == 0) {
+      for (; (int)iss < n0 && iss < (uint32_t)T::NST; ++iss) {
+        const int chunk = warp + (int)iss * T::NW;
+        const int phys = bt_s[(it.t_begin + chunk * T::TC) / B - it.blk0];
+        issue_chunk<D, B>(a, it, phys, chunk, my_stages + iss * 2 * T::CHUNK_ELEMS,
+                          smem_u32(&my_bars[iss]), policy);
+      }
+    }
+    iss = __shfl_sync(kFullMask, iss, 0);
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  if (tid == 0) misc[1] = (int)(gridDim.x + atomicAdd(a.counter, 1u));
+  __syncthreads();
+  int nxt = misc[1];
+
   while (true) {
     const bool has_next = nxt < total;
     ItemInfo nx;
@@ -353,7 +376,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
       for (int i = tid; i < nx.nblk; i += T::THREADS) cp_async_4(dst + i, row + nx.blk0 + i);
     }
     cp_async_commit();
-    if (tid == 0) misc[2 + (iter & 1)] = (int)atomicAdd(a.counter, 1u);
+    if (tid == 0) misc[2 + (iter & 1)] = (int)(gridDim.x + atomicAdd(a.counter, 1u));
 
     const int* bt = bt_s + buf * bt_cap;
     const size_t sh = (size_t)(a.seq_begin + it.s) * H + it.h;
@@ -494,32 +517,44 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
   }
 }
 
-// Merge the partitions of each (sequence, head): one warp per pair.  Lanes
-// load the partitions' (m, l) in parallel; the warp reduces max and sum by
-// shuffles, then accumulates the weighted partial outputs in partition
-// order, D/32 dimensions per lane.
+// Merge the partitions of each (sequence, head): one warp per pair.  The
+// context length (an input, complete before the call) is read before
+// pdl_wait; after it, the partitions' (m, l) and their first kPre partial
+// outputs are loaded together, then the warp reduces max and sum by shuffles
+// and accumulates the weighted partials in partition order, D/32 dimensions
+// per lane.
 template <int D, int B>
 __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams a, int total_seqs) {
   constexpr int DPL = D / 32;
+  constexpr int kPre = 8;
+  using Vec = typename std::conditional<DPL == 4, float4, float2>::type;
   const int lane = threadIdx.x & 31;
+  const long long pair = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const bool live = pair < (long long)total_seqs * a.num_heads;
+  int n = 0;
+  if (live) n = num_parts(effective_len(a.context_lens[pair / a.num_heads], a, B, false), a.part_tokens);
   pdl_wait();
   pdl_launch_dependents();
-  const long long pair = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (pair >= (long long)total_seqs * a.num_heads) return;
-  const int s = (int)(pair / a.num_heads);
-  const int c = effective_len(a.context_lens[s], a, B, false);
-  const int n = num_parts(c, a.part_tokens);
   if (n <= 1) return;
   const float* ml = a.ws_ml + (size_t)pair * a.max_parts * 2;
   const float* ob = a.ws_o + (size_t)pair * a.max_parts * D + lane * DPL;
-  float M = -INFINITY;
-  for (int p = lane; p < n; p += 32) M = fmaxf(M, ml[2 * p]);
+  float mp = -INFINITY, lp = 0.f;
+  if (lane < n) {
+    mp = ml[2 * lane];
+    lp = ml[2 * lane + 1];
+  }
+  Vec pre[kPre];
+#pragma unroll
+  for (int j = 0; j < kPre; ++j)
+    if (j < n) pre[j] = *reinterpret_cast<const Vec*>(ob + (size_t)j * D);
+  float M = mp;
+  for (int p = lane + 32; p < n; p += 32) M = fmaxf(M, ml[2 * p]);
 #pragma unroll
   for (int msk = 16; msk >= 1; msk >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, msk));
-  float L = 0.f;
-  for (int p = lane; p < n; p += 32) {
-    const float mp = ml[2 * p];
-    L += (mp == -INFINITY ? 0.f : exp2_approx(mp - M)) * ml[2 * p + 1];
+  float L = (mp == -INFINITY) ? 0.f : exp2_approx(mp - M) * lp;
+  for (int p = lane + 32; p < n; p += 32) {
+    const float m2 = ml[2 * p];
+    L += (m2 == -INFINITY ? 0.f : exp2_approx(m2 - M)) * ml[2 * p + 1];
   }
 #pragma unroll
   for (int msk = 16; msk >= 1; msk >>= 1) L += __shfl_xor_sync(kFullMask, L, msk);
@@ -528,22 +563,25 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams a
   for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
   for (int p0 = 0; p0 < n; p0 += 32) {
     const int pl = p0 + lane;
-    const float mp = pl < n ? ml[2 * pl] : -INFINITY;
-    const float wl = mp == -INFINITY ? 0.f : exp2_approx(mp - M);
+    const float m2 = pl < n ? (p0 == 0 ? mp : ml[2 * pl]) : -INFINITY;
+    const float wl = m2 == -INFINITY ? 0.f : exp2_approx(m2 - M);
     const int cnt = min(32, n - p0);
     for (int j = 0; j < cnt; ++j) {
       const float w = __shfl_sync(kFullMask, wl, j);
-      const float* op = ob + (size_t)(p0 + j) * D;
-      if constexpr (DPL == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(op);
-        acc[0] = fmaf(w, v.x, acc[0]);
-        acc[1] = fmaf(w, v.y, acc[1]);
-        acc[2] = fmaf(w, v.z, acc[2]);
-        acc[3] = fmaf(w, v.w, acc[3]);
+      const int p = p0 + j;
+      Vec v;
+      if (p < kPre) {
+#pragma unroll
+        for (int k = 0; k < kPre; ++k)
+          if (k == p) v = pre[k];
       } else {
-        const float2 v = *reinterpret_cast<const float2*>(op);
-        acc[0] = fmaf(w, v.x, acc[0]);
-        acc[1] = fmaf(w, v.y, acc[1]);
+        v = *reinterpret_cast<const Vec*>(ob + (size_t)p * D);
+      }
+      acc[0] = fmaf(w, v.x, acc[0]);
+      acc[1] = fmaf(w, v.y, acc[1]);
+      if constexpr (DPL == 4) {
+        acc[2] = fmaf(w, reinterpret_cast<const float4&>(v).z, acc[2]);
+        acc[3] = fmaf(w, reinterpret_cast<const float4&>(v).w, acc[3]);
       }
     }
   }
