@@ -46,6 +46,18 @@ def lib() -> ctypes.CDLL:
     L.oracle_copy_blocks.restype = i32
     L.oracle_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f64]
     L.oracle_decode.restype = i32
+    f32 = ctypes.c_float
+    L.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    L.oracle_e4m3_to_double.restype = f64
+    L.oracle_double_to_e4m3.argtypes = [f64]
+    L.oracle_double_to_e4m3.restype = ctypes.c_uint8
+    L.oracle_e4m3_to_double_array.argtypes = [vp, vp, ctypes.c_size_t]
+    L.oracle_double_to_e4m3_array.argtypes = [vp, vp, ctypes.c_size_t]
+    L.oracle_reshape_and_cache_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, f32]
+    L.oracle_reshape_and_cache_fp8.restype = i32
+    L.oracle_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f64,
+                                    f64, f64]
+    L.oracle_decode_fp8.restype = i32
     L.oracle_num_threads.argtypes = []
     L.oracle_num_threads.restype = i32
     _LIB = L
@@ -136,6 +148,59 @@ def decode(query, key_cache, value_cache, block_tables, context_lens, scale: flo
     rc = lib().oracle_decode(out16.ctypes.data, out64.ctypes.data if want64 else None, q.ctypes.data,
                              kc.ctypes.data, vc.ctypes.data, bt.ctypes.data, bt.shape[1],
                              cl.ctypes.data, S, H, D, B, NB, float(scale))
+    return out16, out64, rc
+
+
+def e4m3_to_double(codes: np.ndarray) -> np.ndarray:
+    c = _c(np.asarray(codes, dtype=np.uint8), np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    lib().oracle_e4m3_to_double_array(out.ctypes.data, c.ctypes.data, c.size)
+    return out
+
+
+def double_to_e4m3(x: np.ndarray) -> np.ndarray:
+    """Nearest E4M3 code (ties to even), saturating at +-448; uint8."""
+    x = _c(np.asarray(x, dtype=np.float64), np.float64)
+    out = np.empty(x.shape, dtype=np.uint8)
+    lib().oracle_double_to_e4m3_array(out.ctypes.data, x.ctypes.data, x.size)
+    return out
+
+
+def _inplace_u8(a: np.ndarray) -> np.ndarray:
+    if not (isinstance(a, np.ndarray) and a.flags.c_contiguous and a.dtype == np.uint8):
+        raise ValueError("FP8 caches must be C-contiguous uint8 arrays")
+    return a
+
+
+def reshape_and_cache_fp8(key_cache, value_cache, key, value, slot_mapping_arr, block_size: int,
+                          k_scale: float, v_scale: float) -> int:
+    """In place on the uint8 (E4M3) host caches [NB, H, B, D]."""
+    kc, vc = _inplace_u8(key_cache), _inplace_u8(value_cache)
+    k, v = _u16(key), _u16(value)
+    sm = _c(slot_mapping_arr, np.int64)
+    T, H, D = k.shape
+    return lib().oracle_reshape_and_cache_fp8(kc.ctypes.data, vc.ctypes.data, k.ctypes.data,
+                                              v.ctypes.data, sm.ctypes.data, T, H, D, block_size,
+                                              kc.shape[0], float(k_scale), float(v_scale))
+
+
+def decode_fp8(query, key_cache, value_cache, block_tables, context_lens, scale: float,
+               k_scale: float, v_scale: float, want64: bool = True):
+    """Decode over uint8 (E4M3) caches; returns (out16, out64 or None, status)."""
+    q = _u16(query)
+    kc = _c(key_cache, np.uint8)
+    vc = _c(value_cache, np.uint8)
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    S, H, D = q.shape
+    NB, H2, B, D2 = kc.shape
+    assert H2 == H and D2 == D
+    out16 = np.empty((S, H, D), dtype=np.uint16)
+    out64 = np.empty((S, H, D), dtype=np.float64) if want64 else None
+    rc = lib().oracle_decode_fp8(out16.ctypes.data, out64.ctypes.data if want64 else None,
+                                 q.ctypes.data, kc.ctypes.data, vc.ctypes.data, bt.ctypes.data,
+                                 bt.shape[1], cl.ctypes.data, S, H, D, B, NB, float(scale),
+                                 float(k_scale), float(v_scale))
     return out16, out64, rc
 
 

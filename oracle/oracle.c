@@ -219,6 +219,140 @@ int oracle_decode(uint16_t* out16, double* out64, const uint16_t* query,
   return bad ? -1 : 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* FP8 KV cache ["vLLM推理加速深度解读：PagedAttention如何提升10x吞吐量" §3.3 names */
+/* FP8 support; the format and scaling are not given there].  Reading taken:  */
+/* OCP FP8 E4M3 ("e4m3fn": 1 sign, 4 exponent bits with bias 7, 3 fraction    */
+/* bits, no infinities, S.1111.111 is NaN, largest finite 448), one scale per */
+/* cache tensor: stored = E4M3(x / scale) with x / scale evaluated in IEEE    */
+/* binary32 and rounded to nearest even, saturating to +-448; the value a     */
+/* code stands for is E4M3(code) * scale.                                     */
+
+double oracle_e4m3_to_double(uint8_t c) {
+  const int sign = (c >> 7) & 1;
+  const int e = (c >> 3) & 0xf;
+  const int f = c & 7;
+  double v;
+  if (e == 15 && f == 7) return NAN;
+  if (e == 0) v = ldexp((double)f, -9);           /* subnormal: f/8 * 2^-6 */
+  else v = ldexp((double)(8 + f), e - 10);         /* (1 + f/8) * 2^(e-7) */
+  return sign ? -v : v;
+}
+
+/* Nearest E4M3 code to x (ties to even), saturating at +-448; NaN -> 0x7f. */
+uint8_t oracle_double_to_e4m3(double x) {
+  const uint8_t sign = signbit(x) ? 0x80 : 0;
+  if (isnan(x)) return 0x7f;
+  const double a = fabs(x);
+  if (a >= 448.0) return (uint8_t)(sign | 0x7e);
+  if (a < 0x1p-6) {
+    const double r = nearbyint(a * 0x1p9);   /* subnormal step 2^-9 */
+    return (uint8_t)(sign | (uint8_t)r);      /* r == 8 is the smallest normal */
+  }
+  int e2;
+  frexp(a, &e2);
+  int E = e2 - 1;                             /* a in [2^E, 2^(E+1)) */
+  double r = nearbyint(ldexp(a, 3 - E));      /* significand in units of 2^(E-3) */
+  if (r == 16.0) { r = 8.0; E += 1; }
+  if (E + 7 > 15 || (E + 7 == 15 && r - 8 > 6)) return (uint8_t)(sign | 0x7e);
+  return (uint8_t)(sign | ((E + 7) << 3) | ((int)r - 8));
+}
+
+void oracle_e4m3_to_double_array(double* out, const uint8_t* in, size_t n) {
+  for (size_t i = 0; i < n; ++i) out[i] = oracle_e4m3_to_double(in[i]);
+}
+
+void oracle_double_to_e4m3_array(uint8_t* out, const double* in, size_t n) {
+  for (size_t i = 0; i < n; ++i) out[i] = oracle_double_to_e4m3(in[i]);
+}
+
+/* Quantised code of an fp16 value under a scale: E4M3(fl32(x / scale)). */
+static uint8_t quantize_e4m3(uint16_t h, float scale) {
+  const float x = (float)oracle_half_to_double(h);   /* exact */
+  const float y = x / scale;                          /* binary32 division, round to nearest */
+  return oracle_double_to_e4m3((double)y);
+}
+
+/* Cache write into FP8 caches (same slots as oracle_reshape_and_cache). */
+int oracle_reshape_and_cache_fp8(uint8_t* key_cache, uint8_t* value_cache, const uint16_t* key,
+                                 const uint16_t* value, const int64_t* slot_mapping,
+                                 int num_tokens, int num_heads, int head_dim, int block_size,
+                                 int num_blocks, float k_scale, float v_scale) {
+  int bad = 0;
+  for (int t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    const int64_t blk = slot / block_size;
+    const int64_t off = slot % block_size;
+    if (blk >= num_blocks) { bad = 1; continue; }
+    for (int h = 0; h < num_heads; ++h) {
+      for (int d = 0; d < head_dim; ++d) {
+        const size_t src = ((size_t)t * num_heads + h) * head_dim + d;
+        const size_t dst = (((size_t)blk * num_heads + h) * block_size + off) * head_dim + d;
+        key_cache[dst] = quantize_e4m3(key[src], k_scale);
+        value_cache[dst] = quantize_e4m3(value[src], v_scale);
+      }
+    }
+  }
+  return bad ? -1 : 0;
+}
+
+/* Decode over FP8 caches: the same attention on the dequantised values
+ * K_i = E4M3(code) * k_scale, V_i = E4M3(code) * v_scale (exact in binary64). */
+int oracle_decode_fp8(uint16_t* out16, double* out64, const uint16_t* query,
+                      const uint8_t* key_cache, const uint8_t* value_cache,
+                      const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                      int num_seqs, int num_heads, int head_dim, int block_size, int num_blocks,
+                      double scale, double k_scale, double v_scale) {
+  int bad = 0;
+  const long pairs = (long)num_seqs * num_heads;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (long sh = 0; sh < pairs; ++sh) {
+    const int s = (int)(sh / num_heads);
+    const int h = (int)(sh % num_heads);
+    const int c = context_lens[s];
+    double* acc = (double*)calloc((size_t)head_dim, sizeof(double));
+    double* x = (double*)malloc(sizeof(double) * (size_t)(c > 0 ? c : 1));
+    double* qd = (double*)malloc(sizeof(double) * (size_t)head_dim);
+    int ok = (c >= 0) && (c <= max_blocks * block_size);
+    for (int d = 0; d < head_dim; ++d)
+      qd[d] = oracle_half_to_double(query[((size_t)s * num_heads + h) * head_dim + d]);
+    for (int i = 0; ok && i < c; ++i) {
+      const int phys = block_tables[(size_t)s * max_blocks + i / block_size];
+      if (phys < 0 || phys >= num_blocks) { ok = 0; break; }
+      const uint8_t* k =
+          key_cache + (((size_t)phys * num_heads + h) * block_size + i % block_size) * head_dim;
+      double dot = 0.0;
+      for (int d = 0; d < head_dim; ++d) dot += qd[d] * (oracle_e4m3_to_double(k[d]) * k_scale);
+      x[i] = dot * scale;
+    }
+    double denom = 0.0;
+    if (ok && c > 0) {
+      double m = x[0];
+      for (int i = 1; i < c; ++i) if (x[i] > m) m = x[i];
+      for (int i = 0; i < c; ++i) {
+        const double w = exp(x[i] - m);
+        const int phys = block_tables[(size_t)s * max_blocks + i / block_size];
+        const uint8_t* v =
+            value_cache + (((size_t)phys * num_heads + h) * block_size + i % block_size) * head_dim;
+        denom += w;
+        for (int d = 0; d < head_dim; ++d) acc[d] += w * (oracle_e4m3_to_double(v[d]) * v_scale);
+      }
+    }
+    if (!ok) bad |= 1;
+    for (int d = 0; d < head_dim; ++d) {
+      const double o = (ok && c > 0) ? acc[d] / denom : 0.0;
+      const size_t idx = ((size_t)s * num_heads + h) * head_dim + d;
+      if (out64) out64[idx] = o;
+      if (out16) out16[idx] = oracle_double_to_half(o);
+    }
+    free(acc);
+    free(x);
+    free(qd);
+  }
+  return bad ? -1 : 0;
+}
+
 /* Threads the decode loop uses (OpenMP's maximum, 1 without OpenMP). */
 int oracle_num_threads(void) {
 #ifdef _OPENMP
