@@ -9,7 +9,11 @@ context lengths) over the step time; also reported as % of the measured HBM
 peak, attention tokens/s per layer and us per layer.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c3|c5|c2|c4|c1]
+                    [--kv-dtype fp16|fp8]
     python bench.py --impl reference ...   # the CPU oracle as the reference arm
+
+--kv-dtype fp8 runs the same step on FP8 (E4M3) caches: the bytes count one
+byte per cached K/V element, so compare it with fp16 on tokens/s as well.
 
 N > 1 runs under torch.distributed.run: every rank runs its own replica of
 the workload (sequences shard across GPUs with no exchange: weak scaling).
@@ -48,6 +52,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--eager", action="store_true", help="time eager launches only (no CUDA graph)")
+    ap.add_argument("--kv-dtype", choices=["fp16", "fp8"], default="fp16",
+                    help="KV-cache element type (fp8: E4M3 codes with per-tensor scales)")
     return ap.parse_args()
 
 
@@ -60,12 +66,13 @@ def make_workload(name: str, layers: int):
     return configs.ALL[cid]()
 
 
-def decode_bytes(w, bt, ctx) -> int:
+def decode_bytes(w, bt, ctx, kv_elem_bytes: int = 2) -> int:
     """Algorithmic bytes of one decode call: per (s, h): q (2D) + K and V of the c_s live
-    tokens (2 * c_s * D * 2) + out (2D); per s: ceil(c_s/B) table entries and one context length."""
+    tokens (2 * c_s * D * kv_elem_bytes) + out (2D); per s: ceil(c_s/B) table entries and
+    one context length."""
     S, H, D, B = w.num_seqs, w.num_heads, w.head_dim, w.block_size
     ctx = np.asarray(ctx, dtype=np.int64)
-    per_pair = 2 * D + 4 * ctx * D + 2 * D
+    per_pair = 2 * D + 2 * kv_elem_bytes * ctx * D + 2 * D
     return int(H * per_pair.sum() + 4 * (-(-ctx // B)).sum() + 4 * S)
 
 
@@ -194,7 +201,7 @@ def weak_scaling_value(bytes_per_rank_step: int, world: int, ms_per_step_max: fl
 class Step:
     """Device state of the workload and its decode step (the library's DecodeStep)."""
 
-    def __init__(self, w, device):
+    def __init__(self, w, device, fp8: bool = False):
         import torch
 
         import paged_kv_cache_158_gb300 as pa
@@ -203,7 +210,12 @@ class Step:
         from workloads import gpu
 
         self.pa, self.w, self.dev = pa, w, device
-        dw = gpu.materialize(w, device=device)
+        self.fp8_scales = configs.fp8_scales(w) if fp8 else None
+        if fp8:
+            dw = gpu.materialize(w, device=device, fp8_convert=pa.pa_convert_cache_fp8,
+                                 fp8_scales=self.fp8_scales)
+        else:
+            dw = gpu.materialize(w, device=device)
         self.dw = dw
         copy_pairs = None
         if w.block_tables is None:          # shared-prefix workload: the block manager plans
@@ -223,10 +235,11 @@ class Step:
                 for _ in dw.layers]
         self.step = DecodeStep(dw.key_caches, dw.value_caches, dw.queries, dw.keys_new, dw.values_new,
                                outs, dw.block_tables, dw.context_lens, dw.token_seq, dw.token_pos,
-                               w.block_size, w.num_blocks, w.scale, self.max_ctx, copy_pairs)
+                               w.block_size, w.num_blocks, w.scale, self.max_ctx, copy_pairs,
+                               self.fp8_scales)
         self.outs = outs
         self.copy_pairs = copy_pairs
-        self.bytes_per_decode = decode_bytes(w, self.bt_host, self.ctx_host)
+        self.bytes_per_decode = decode_bytes(w, self.bt_host, self.ctx_host, 1 if fp8 else 2)
         self.partition_tokens = pa.pa_decode_partition_tokens(w.num_seqs, w.num_heads, self.max_ctx)
         self.max_parts = -(-self.max_ctx // self.partition_tokens)
 
@@ -264,7 +277,8 @@ def run_ours(args, rank, world, local):
     if args.partition_tokens:
         pa.pa_decode_set_partition_tokens(args.partition_tokens)
     w = make_workload(args.workload, args.layers)
-    st = Step(w, device)
+    fp8 = args.kv_dtype == "fp8"
+    st = Step(w, device, fp8)
     L = len(st.dw.layers)
     stream = torch.cuda.current_stream(device)
     for _ in range(args.warmup):
@@ -323,16 +337,17 @@ def run_ours(args, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16 in, f32 accumulate",
+        "dtype": "e4m3 KV cache, f16 q/out, f32 accumulate" if fp8 else "f16 in, f32 accumulate",
         "data": "synthetic (seeded SplitMix64 / Box-Muller values, seeded block tables)",
         "config": {
             "workload": w.name,
+            "kv_dtype": args.kv_dtype,
             "layers": L, "num_seqs": w.num_seqs, "num_heads": w.num_heads, "head_dim": w.head_dim,
             "block_size": w.block_size, "num_blocks_per_layer": w.num_blocks,
             "context_tokens": ctx_tokens, "max_context_len": st.max_ctx,
             "partition_tokens": st.partition_tokens,
             "l2": "inputs larger than L2: each layer's cache is read once per step",
-            "kv_pool_gb": round(w.pool_bytes_all_layers() / 1e9, 3),
+            "kv_pool_gb": round(w.pool_bytes_all_layers() / (2 if fp8 else 1) / 1e9, 3),
             "cuda_graph": ms_graph is not None,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
@@ -345,7 +360,8 @@ def run_ours(args, rank, world, local):
                   "ms_per_step": round(ms_eager / K, 4)},
         "roofline": {
             "bound": "hbm",
-            "kernel": "pa_decode (work-counter init + partition + merge kernels; CUDA events "
+            "kernel": ("pa_decode_fp8" if fp8 else "pa_decode") +
+                      " (work-counter init + partition + merge kernels; CUDA events "
                       "bracket each call in the eager pass)",
             "achieved": round(achieved, 2),
             "peak": peak,
@@ -353,14 +369,14 @@ def run_ours(args, rank, world, local):
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "launch_us": round(dec_avg_ms * 1e3, 3),
-            "traffic": committed_traffic(w.name),
+            "traffic": committed_traffic(w.name + ("_fp8" if fp8 else "")),
         },
         "clocks": clk,
         "gpu_launches": st.launches_per_step() * K * (2 if ms_graph is not None else 1),
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, budget_s=12.0)
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=12.0, fp8=fp8)
     return line
 
 
@@ -413,24 +429,31 @@ def measure_e2e(st, args, world, device):
 
 # ------------------------------------------------------------ CPU oracle
 
-def oracle_sample(w):
-    """Host inputs of the bounded sample: layer 0 of the workload, every sequence and head."""
+def oracle_sample(w, fp8: bool = False):
+    """Host inputs of the bounded sample: layer 0 of the workload, every sequence and head,
+    and a call running the oracle's decode on them (FP8: the oracle quantises the pool)."""
     import oracle
     from workloads import gpu
     if w.block_tables is None:
         raise ValueError("the CPU baseline sample needs static block tables")
     kc, vc = gpu.host_pool(w, 0)
     q, _, _ = gpu.host_small(w, 0)
-    return oracle, q, kc, vc
+    if fp8:
+        ks, vs = configs.fp8_scales(w)
+        kc, vc = oracle.quantize_e4m3(kc, ks), oracle.quantize_e4m3(vc, vs)
+        return oracle, lambda: oracle.decode_fp8(q, kc, vc, w.block_tables, w.context_lens, w.scale,
+                                                 ks, vs, want64=False)
+    return oracle, lambda: oracle.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale,
+                                         want64=False)
 
 
-def cpu_baseline(w, budget_s: float):
-    oracle, q, kc, vc = oracle_sample(w)
-    nbytes = decode_bytes(w, w.block_tables, w.context_lens)
+def cpu_baseline(w, budget_s: float, fp8: bool = False):
+    oracle, run = oracle_sample(w, fp8)
+    nbytes = decode_bytes(w, w.block_tables, w.context_lens, 1 if fp8 else 2)
     reps, t_total = 0, 0.0
     while t_total < budget_s or reps < 1:
         t0 = time.perf_counter()
-        _, _, rc = oracle.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, want64=False)
+        _, _, rc = run()
         t_total += time.perf_counter() - t0
         reps += 1
         assert rc == 0
@@ -445,13 +468,14 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     w = make_workload(args.workload, 1)
-    oracle, q, kc, vc = oracle_sample(w)
-    nbytes = decode_bytes(w, w.block_tables, w.context_lens)
+    fp8 = args.kv_dtype == "fp8"
+    oracle, run = oracle_sample(w, fp8)
+    nbytes = decode_bytes(w, w.block_tables, w.context_lens, 1 if fp8 else 2)
     for _ in range(args.warmup):
-        oracle.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, want64=False)
+        run()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, want64=False)
+        run()
     dt = (time.perf_counter() - t0) / args.steps
     value = nbytes / dt / 1e9
     sample = f"{w.name} layer 0 decode per step (all {w.num_seqs} seqs x {w.num_heads} heads)"
@@ -461,7 +485,7 @@ def run_reference(args, rank, world):
         "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "layers": 1, "sample": sample},
+        "config": {"workload": w.name, "kv_dtype": args.kv_dtype, "layers": 1, "sample": sample},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -1,8 +1,8 @@
 /*
  * pa.h — C ABI of libpa.so, a GB300 (sm_103a) library for the PagedAttention
- * decode hot path: single-query attention over a paged fp16 KV cache, the
- * cache write that scatters new tokens into their slots, the copy-on-write
- * block copy, and the slot map.
+ * decode hot path: single-query attention over a paged fp16 (or FP8 E4M3)
+ * KV cache, the cache write that scatters new tokens into their slots, the
+ * copy-on-write block copy, and the slot map.
  *
  * Sources (page title, section):
  *   [P1] "深入解析LLM推理引擎：从PagedAttention到调度优化"
@@ -184,6 +184,73 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* key_cac
 pa_status pa_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
                          const int64_t* block_mapping, int num_pairs, int num_heads, int head_dim,
                          int block_size, int num_blocks, pa_stream_t stream);
+
+/* ---- FP8 KV cache ------------------------------------------------------
+ * [P2 §3.3 lists FP8 KV caches among the memory optimisations; the pages fix
+ * neither the format nor the scaling.]  The library's reading: OCP FP8 E4M3
+ * ("e4m3fn": 1 sign bit, 4 exponent bits of bias 7, 3 fraction bits, no
+ * infinities, codes 0x7F and 0xFF are NaN, largest finite value 448) with one
+ * fp32 scale per cache tensor.  An FP8 cache has the fp16 cache's layout
+ * with one-byte elements, uint8 [num_blocks][num_heads][block_size][head_dim],
+ * and code c stands for the value E4M3(c) * scale.  It holds a token in half
+ * the bytes, so decode reads half as much.  Scales must be finite and
+ * positive (PA_ERR_INVALID_ARG otherwise).
+ */
+
+/*
+ * Cache write into FP8 caches: the slots, padding and error rules of
+ * pa_reshape_and_cache, storing for each element x (fp16) the code
+ *
+ *   E4M3( fl32(x / scale) )   with scale = k_scale for keys, v_scale for values,
+ *
+ * where fl32 is IEEE binary32 division rounded to nearest and E4M3(.) rounds
+ * to the nearest code (ties to even), saturating to +-448.  Bit-exact.
+ *
+ *   key, value     fp16 [num_tokens][num_heads][head_dim]
+ *   key_cache,
+ *   value_cache    uint8 [num_blocks][num_heads][block_size][head_dim] (updated)
+ */
+pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,
+                                   void* value_cache, const int64_t* slot_mapping, int num_tokens,
+                                   int num_heads, int head_dim, int block_size, int num_blocks,
+                                   float k_scale, float v_scale, pa_stream_t stream);
+
+/*
+ * Decode attention over FP8 caches: pa_decode's formula, shapes, workspace
+ * (pa_decode_workspace_size) and error rules, on the dequantised cache
+ * K = E4M3(code) * k_scale, V = E4M3(code) * v_scale.
+ *
+ *   key_cache,
+ *   value_cache    uint8 [num_blocks][num_heads][block_size][head_dim]
+ *
+ * Arithmetic: the codes are widened to fp16 exactly; dot products, softmax
+ * and accumulation as in pa_decode with the logit multiplier
+ * fl32(scale * k_scale * log2 e) (base-2 exponentials); the merged output is
+ * multiplied by v_scale in fp32 and rounded once to fp16.
+ */
+pa_status pa_decode_fp8(void* out, const void* query, const void* key_cache,
+                        const void* value_cache, const int32_t* block_tables,
+                        int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                        int num_heads, int head_dim, int block_size, int num_blocks, float scale,
+                        float k_scale, float v_scale, int max_context_len, void* workspace,
+                        size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * Converts a whole fp16 buffer to E4M3 codes element by element with the
+ * rule of pa_reshape_and_cache_fp8 (code = E4M3(fl32(x / scale))), keeping
+ * the layout: turns an fp16 cache into the equivalent FP8 cache.
+ *
+ *   src            fp16 [num_elems]
+ *   dst            uint8 [num_elems] (written); must not overlap src
+ *   num_elems      a multiple of 16 (PA_ERR_INVALID_ARG otherwise)
+ */
+pa_status pa_convert_cache_fp8(const void* src, void* dst, size_t num_elems, float scale,
+                               pa_stream_t stream);
+
+/* Copy-on-write block copy for FP8 caches: pa_copy_blocks on uint8 caches. */
+pa_status pa_copy_blocks_fp8(void* const* key_caches, void* const* value_caches, int num_layers,
+                             const int64_t* block_mapping, int num_pairs, int num_heads,
+                             int head_dim, int block_size, int num_blocks, pa_stream_t stream);
 
 /*
  * Slot map [P2 §2.3 address map; P1 §3.2 worked block-table example]: for

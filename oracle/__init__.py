@@ -53,6 +53,7 @@ def lib() -> ctypes.CDLL:
     L.oracle_double_to_e4m3.restype = ctypes.c_uint8
     L.oracle_e4m3_to_double_array.argtypes = [vp, vp, ctypes.c_size_t]
     L.oracle_double_to_e4m3_array.argtypes = [vp, vp, ctypes.c_size_t]
+    L.oracle_quantize_e4m3_array.argtypes = [vp, vp, ctypes.c_size_t, f32]
     L.oracle_reshape_and_cache_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, f32]
     L.oracle_reshape_and_cache_fp8.restype = i32
     L.oracle_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f64,
@@ -163,6 +164,14 @@ def double_to_e4m3(x: np.ndarray) -> np.ndarray:
     x = _c(np.asarray(x, dtype=np.float64), np.float64)
     out = np.empty(x.shape, dtype=np.uint8)
     lib().oracle_double_to_e4m3_array(out.ctypes.data, x.ctypes.data, x.size)
+    return out
+
+
+def quantize_e4m3(x16, scale: float) -> np.ndarray:
+    """E4M3 codes of fp16 values (uint16 bits or float16): E4M3(fl32(x / scale))."""
+    x = _u16(x16)
+    out = np.empty(x.shape, dtype=np.uint8)
+    lib().oracle_quantize_e4m3_array(out.ctypes.data, x.ctypes.data, x.size, float(scale))
     return out
 
 

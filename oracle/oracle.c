@@ -273,6 +273,11 @@ static uint8_t quantize_e4m3(uint16_t h, float scale) {
   return oracle_double_to_e4m3((double)y);
 }
 
+/* Elementwise quantisation of n fp16 values (a whole cache, layout kept). */
+void oracle_quantize_e4m3_array(uint8_t* out, const uint16_t* in, size_t n, float scale) {
+  for (size_t i = 0; i < n; ++i) out[i] = quantize_e4m3(in[i], scale);
+}
+
 /* Cache write into FP8 caches (same slots as oracle_reshape_and_cache). */
 int oracle_reshape_and_cache_fp8(uint8_t* key_cache, uint8_t* value_cache, const uint16_t* key,
                                  const uint16_t* value, const int64_t* slot_mapping,

@@ -43,6 +43,17 @@ _lib.pa_decode_partition_tokens.argtypes = [_i32, _i32, _i32]
 _lib.pa_decode_partition_tokens.restype = _i32
 _lib.pa_decode_set_partition_tokens.argtypes = [_i32]
 _lib.pa_decode_set_partition_tokens.restype = None
+_f32 = ctypes.c_float
+_lib.pa_decode_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                               _f32, _f32, _f32, _i32, _vp, _sz, _vp]
+_lib.pa_decode_fp8.restype = _i32
+_lib.pa_reshape_and_cache_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                          _f32, _f32, _vp]
+_lib.pa_reshape_and_cache_fp8.restype = _i32
+_lib.pa_convert_cache_fp8.argtypes = [_vp, _vp, _sz, _f32, _vp]
+_lib.pa_convert_cache_fp8.restype = _i32
+_lib.pa_copy_blocks_fp8.argtypes = [_vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _vp]
+_lib.pa_copy_blocks_fp8.restype = _i32
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_OUT_OF_RANGE, PA_ERR_TIMEOUT = range(6)
 PA_ERRBIT_BLOCK_ID, PA_ERRBIT_CONTEXT, PA_ERRBIT_SLOT = 0x1, 0x2, 0x4
@@ -85,6 +96,16 @@ def _ptr(t: torch.Tensor, name: str, dtype: torch.dtype) -> int:
     return t.data_ptr()
 
 
+def _cache_ptr(t: torch.Tensor, name: str, fp8: bool) -> int:
+    """fp16 caches are torch.float16; FP8 (E4M3) caches are torch.uint8 holding
+    the codes (a torch.float8_e4m3fn tensor is accepted as the same bytes)."""
+    if not fp8:
+        return _ptr(t, name, torch.float16)
+    if isinstance(t, torch.Tensor) and t.dtype == torch.float8_e4m3fn:
+        t = t.view(torch.uint8)
+    return _ptr(t, name, torch.uint8)
+
+
 def pa_decode_workspace_size(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int) -> int:
     return int(_lib.pa_decode_workspace_size(num_seqs, num_heads, head_dim, max_context_len))
 
@@ -104,10 +125,7 @@ def decode_workspace(num_seqs: int, num_heads: int, head_dim: int, max_context_l
     return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
 
 
-def pa_decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
-              value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
-              scale: float, max_context_len: int, workspace: torch.Tensor, stream=None) -> None:
-    """out[S,H,D] = paged decode attention (see pa_decode in include/pa.h)."""
+def _decode_shapes(out, query, key_cache, value_cache, block_tables, context_lens):
     S, H, D = query.shape
     NB, H2, B, D2 = key_cache.shape
     if (H2, D2) != (H, D) or tuple(value_cache.shape) != tuple(key_cache.shape):
@@ -116,6 +134,14 @@ def pa_decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
         raise ValueError("out / block_tables shape")
     if context_lens.shape != (S,):
         raise ValueError("context_lens shape")
+    return S, H, D, B, NB
+
+
+def pa_decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+              value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+              scale: float, max_context_len: int, workspace: torch.Tensor, stream=None) -> None:
+    """out[S,H,D] = paged decode attention (see pa_decode in include/pa.h)."""
+    S, H, D, B, NB = _decode_shapes(out, query, key_cache, value_cache, block_tables, context_lens)
     st = _lib.pa_decode(_ptr(out, "out", torch.float16), _ptr(query, "query", torch.float16),
                         _ptr(key_cache, "key_cache", torch.float16),
                         _ptr(value_cache, "value_cache", torch.float16),
@@ -124,6 +150,23 @@ def pa_decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
                         float(scale), int(max_context_len), _ptr(workspace, "workspace", torch.uint8),
                         workspace.numel(), _stream(stream))
     _check(st, "pa_decode")
+
+
+def pa_decode_fp8(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                  value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                  scale: float, k_scale: float, v_scale: float, max_context_len: int,
+                  workspace: torch.Tensor, stream=None) -> None:
+    """pa_decode over FP8 (E4M3, uint8) caches with per-tensor scales."""
+    S, H, D, B, NB = _decode_shapes(out, query, key_cache, value_cache, block_tables, context_lens)
+    st = _lib.pa_decode_fp8(_ptr(out, "out", torch.float16), _ptr(query, "query", torch.float16),
+                            _cache_ptr(key_cache, "key_cache", True),
+                            _cache_ptr(value_cache, "value_cache", True),
+                            _ptr(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+                            _ptr(context_lens, "context_lens", torch.int32), S, H, D, B, NB,
+                            float(scale), float(k_scale), float(v_scale), int(max_context_len),
+                            _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
+                            _stream(stream))
+    _check(st, "pa_decode_fp8")
 
 
 def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
@@ -141,8 +184,43 @@ def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torc
     _check(st, "pa_reshape_and_cache")
 
 
+def pa_reshape_and_cache_fp8(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
+                             value_cache: torch.Tensor, slot_mapping: torch.Tensor, k_scale: float,
+                             v_scale: float, stream=None) -> None:
+    """Quantise key/value [T,H,D] (fp16) to E4M3 codes into their slots of uint8 caches."""
+    T, H, D = key.shape
+    NB, H2, B, D2 = key_cache.shape
+    if (H2, D2) != (H, D) or tuple(value.shape) != (T, H, D) or slot_mapping.shape != (T,):
+        raise ValueError("shape mismatch")
+    st = _lib.pa_reshape_and_cache_fp8(_ptr(key, "key", torch.float16),
+                                       _ptr(value, "value", torch.float16),
+                                       _cache_ptr(key_cache, "key_cache", True),
+                                       _cache_ptr(value_cache, "value_cache", True),
+                                       _ptr(slot_mapping, "slot_mapping", torch.int64), T, H, D, B,
+                                       NB, float(k_scale), float(v_scale), _stream(stream))
+    _check(st, "pa_reshape_and_cache_fp8")
+
+
+def pa_convert_cache_fp8(src: torch.Tensor, dst: torch.Tensor, scale: float, stream=None) -> None:
+    """dst (uint8, same shape) := E4M3 codes of src (fp16) under `scale`, element by element."""
+    if tuple(src.shape) != tuple(dst.shape):
+        raise ValueError("src and dst must have the same shape")
+    st = _lib.pa_convert_cache_fp8(_ptr(src, "src", torch.float16), _cache_ptr(dst, "dst", True),
+                                   src.numel(), float(scale), _stream(stream))
+    _check(st, "pa_convert_cache_fp8")
+
+
 def pa_copy_blocks(key_caches, value_caches, block_mapping: torch.Tensor, stream=None) -> None:
     """Copy-on-write block copy across all layers; block_mapping is int64 [P, 2] (src, dst)."""
+    _copy_blocks(key_caches, value_caches, block_mapping, stream, False)
+
+
+def pa_copy_blocks_fp8(key_caches, value_caches, block_mapping: torch.Tensor, stream=None) -> None:
+    """pa_copy_blocks for FP8 (uint8) caches."""
+    _copy_blocks(key_caches, value_caches, block_mapping, stream, True)
+
+
+def _copy_blocks(key_caches, value_caches, block_mapping, stream, fp8: bool) -> None:
     L = len(key_caches)
     if len(value_caches) != L or L == 0:
         raise ValueError("need one value cache per key cache")
@@ -150,13 +228,14 @@ def pa_copy_blocks(key_caches, value_caches, block_mapping: torch.Tensor, stream
     for t in list(key_caches) + list(value_caches):
         if tuple(t.shape) != (NB, H, B, D):
             raise ValueError("all caches must share one shape")
-    kp = (ctypes.c_void_p * L)(*[_ptr(t, "key_caches[i]", torch.float16) for t in key_caches])
-    vp = (ctypes.c_void_p * L)(*[_ptr(t, "value_caches[i]", torch.float16) for t in value_caches])
+    kp = (ctypes.c_void_p * L)(*[_cache_ptr(t, "key_caches[i]", fp8) for t in key_caches])
+    vp = (ctypes.c_void_p * L)(*[_cache_ptr(t, "value_caches[i]", fp8) for t in value_caches])
     if block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
         raise ValueError("block_mapping must be [P, 2]")
-    st = _lib.pa_copy_blocks(kp, vp, L, _ptr(block_mapping, "block_mapping", torch.int64),
-                             block_mapping.shape[0], H, D, B, NB, _stream(stream))
-    _check(st, "pa_copy_blocks")
+    fn = _lib.pa_copy_blocks_fp8 if fp8 else _lib.pa_copy_blocks
+    st = fn(kp, vp, L, _ptr(block_mapping, "block_mapping", torch.int64), block_mapping.shape[0],
+            H, D, B, NB, _stream(stream))
+    _check(st, "pa_copy_blocks_fp8" if fp8 else "pa_copy_blocks")
 
 
 def pa_slot_mapping(slot_mapping: torch.Tensor, block_tables: torch.Tensor, token_seq: torch.Tensor,
@@ -188,6 +267,7 @@ def raise_on_device_errors(stream=None) -> None:
 
 __all__ = [
     "pa_decode", "pa_reshape_and_cache", "pa_copy_blocks", "pa_slot_mapping", "pa_check_errors",
+    "pa_decode_fp8", "pa_reshape_and_cache_fp8", "pa_copy_blocks_fp8", "pa_convert_cache_fp8",
     "pa_status_string", "pa_decode_workspace_size", "pa_decode_partition_tokens",
     "pa_decode_set_partition_tokens", "decode_workspace", "raise_on_device_errors", "PAError",
 ]

@@ -7,19 +7,25 @@
 #include "pa_internal.h"
 
 namespace pa {
-cudaError_t launch_decode_partition_d64(const DecodeParams&, int, int, size_t, cudaStream_t);
-cudaError_t launch_decode_partition_d128(const DecodeParams&, int, int, size_t, cudaStream_t);
+#define PA_DECLARE_DECODE(sfx)                                                           \
+  cudaError_t launch_decode_partition_##sfx(const DecodeParams&, int, int, size_t,      \
+                                            cudaStream_t);                              \
+  int decode_ctas_per_sm_##sfx(int, size_t);                                            \
+  size_t decode_fixed_smem_##sfx(int);                                                  \
+  cudaError_t decode_prepare_##sfx();
+PA_DECLARE_DECODE(d64)
+PA_DECLARE_DECODE(d128)
+PA_DECLARE_DECODE(f8_d64)
+PA_DECLARE_DECODE(f8_d128)
+#undef PA_DECLARE_DECODE
 cudaError_t launch_decode_reduce_d64(const DecodeParams&, int, int, cudaStream_t);
 cudaError_t launch_decode_reduce_d128(const DecodeParams&, int, int, cudaStream_t);
-int decode_ctas_per_sm_d64(int, size_t);
-int decode_ctas_per_sm_d128(int, size_t);
-size_t decode_fixed_smem_d64(int);
-size_t decode_fixed_smem_d128(int);
-cudaError_t decode_prepare_d64();
-cudaError_t decode_prepare_d128();
 
-cudaError_t launch_decode_partition(const DecodeParams& p, int head_dim, int block_size, int grid,
-                                    size_t smem, cudaStream_t st) {
+cudaError_t launch_decode_partition(const DecodeParams& p, bool fp8, int head_dim, int block_size,
+                                    int grid, size_t smem, cudaStream_t st) {
+  if (fp8)
+    return head_dim == 64 ? launch_decode_partition_f8_d64(p, block_size, grid, smem, st)
+                          : launch_decode_partition_f8_d128(p, block_size, grid, smem, st);
   return head_dim == 64 ? launch_decode_partition_d64(p, block_size, grid, smem, st)
                         : launch_decode_partition_d128(p, block_size, grid, smem, st);
 }
@@ -30,23 +36,31 @@ cudaError_t launch_decode_reduce(const DecodeParams& p, int head_dim, int block_
                         : launch_decode_reduce_d128(p, block_size, total_seqs, st);
 }
 
-size_t decode_smem_bytes(int head_dim, int block_size, int part_tokens, int seqs_in_launch) {
+size_t decode_smem_bytes(bool fp8, int head_dim, int block_size, int part_tokens,
+                         int seqs_in_launch) {
   const size_t fixed =
-      head_dim == 64 ? decode_fixed_smem_d64(block_size) : decode_fixed_smem_d128(block_size);
+      fp8 ? (head_dim == 64 ? decode_fixed_smem_f8_d64(block_size)
+                            : decode_fixed_smem_f8_d128(block_size))
+          : (head_dim == 64 ? decode_fixed_smem_d64(block_size) : decode_fixed_smem_d128(block_size));
   const size_t bt = 2 * (size_t)(part_tokens / block_size + 1) * 4;
   const size_t seq = (2 * (size_t)seqs_in_launch + 1) * 4;
   return (fixed + bt + seq + 15) & ~size_t(15);
 }
 
-int decode_ctas_per_sm(int head_dim, int block_size, size_t smem) {
+int decode_ctas_per_sm(bool fp8, int head_dim, int block_size, size_t smem) {
+  if (fp8)
+    return head_dim == 64 ? decode_ctas_per_sm_f8_d64(block_size, smem)
+                          : decode_ctas_per_sm_f8_d128(block_size, smem);
   return head_dim == 64 ? decode_ctas_per_sm_d64(block_size, smem)
                         : decode_ctas_per_sm_d128(block_size, smem);
 }
 
 cudaError_t decode_prepare_device(int) {
-  cudaError_t e = decode_prepare_d64();
-  if (e != cudaSuccess) return e;
-  return decode_prepare_d128();
+  cudaError_t e;
+  if ((e = decode_prepare_d64()) != cudaSuccess) return e;
+  if ((e = decode_prepare_d128()) != cudaSuccess) return e;
+  if ((e = decode_prepare_f8_d64()) != cudaSuccess) return e;
+  return decode_prepare_f8_d128();
 }
 
 }  // namespace pa
@@ -97,6 +111,7 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0;
 bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7) == 0; }
 bool head_dim_ok(int d) { return d == 64 || d == 128; }
 bool block_size_ok(int b) { return b == 4 || b == 8 || b == 16 || b == 32; }
+bool scale_ok(float s) { return s > 0.f && s <= 3.4028234663852886e38f; }  // finite, positive
 
 // Tokens per partition.  512 measured best on the 7B-, 13B-shaped and
 // long-context batches (256 / 512 / 1024 swept): large enough that the
@@ -143,41 +158,14 @@ WsLayout ws_layout(int S, int H, int D, int max_context_len) {
   return w;
 }
 
-}  // namespace
-
-extern "C" {
-
-const char* pa_status_string(pa_status status) {
-  switch (status) {
-    case PA_OK: return "PA_OK";
-    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
-    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
-    case PA_ERR_CUDA: return "PA_ERR_CUDA";
-    case PA_ERR_OUT_OF_RANGE: return "PA_ERR_OUT_OF_RANGE";
-    case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
-  }
-  return "PA_ERR_UNKNOWN";
-}
-
-int pa_decode_partition_tokens(int num_seqs, int num_heads, int max_context_len) {
-  if (num_seqs < 0 || num_heads <= 0 || max_context_len < 0) return 0;
-  return part_tokens_for(num_seqs, num_heads, max_context_len);
-}
-
-void pa_decode_set_partition_tokens(int tokens) {
-  g_part_override.store(tokens > 0 ? tokens : 0, std::memory_order_relaxed);
-}
-
-size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len) {
-  if (num_seqs < 0 || num_heads <= 0 || !head_dim_ok(head_dim) || max_context_len < 0) return 0;
-  return ws_layout(num_seqs, num_heads, head_dim, max_context_len).total;
-}
-
-pa_status pa_decode(void* out, const void* query, const void* key_cache, const void* value_cache,
-                    const int32_t* block_tables, int max_blocks_per_seq,
-                    const int32_t* context_lens, int num_seqs, int num_heads, int head_dim,
-                    int block_size, int num_blocks, float scale, int max_context_len,
-                    void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+// The decode call for both cache element types (fp8: E4M3 caches with
+// per-tensor scales; k_scale and v_scale are 1 for fp16).
+pa_status decode_impl(bool fp8, void* out, const void* query, const void* key_cache,
+                      const void* value_cache, const int32_t* block_tables,
+                      int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                      int num_heads, int head_dim, int block_size, int num_blocks, float scale,
+                      float k_scale, float v_scale, int max_context_len, void* workspace,
+                      size_t workspace_bytes, pa_stream_t stream) {
   if (!head_dim_ok(head_dim) || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
   if (num_seqs < 0 || num_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 ||
       max_context_len < 0)
@@ -214,7 +202,8 @@ pa_status pa_decode(void* out, const void* query, const void* key_cache, const v
   p.max_context_len = max_context_len;
   p.part_tokens = w.part_tokens;
   p.max_parts = w.max_parts;
-  p.scale_log2 = (float)((double)scale * 1.4426950408889634073599246810019);
+  p.scale_log2 = (float)((double)scale * (double)k_scale * 1.4426950408889634073599246810019);
+  p.v_scale = v_scale;
 
   unsigned int* counters = reinterpret_cast<unsigned int*>(ws + w.counters_off);
   if (pa::launch_zero_words(counters, (int)(w.zero_bytes / 4), cs) != cudaSuccess) return PA_ERR_CUDA;
@@ -223,12 +212,12 @@ pa_status pa_decode(void* out, const void* query, const void* key_cache, const v
     p.num_seqs = num_seqs - p.seq_begin < pa::kMaxSeqsPerLaunch ? num_seqs - p.seq_begin
                                                                  : pa::kMaxSeqsPerLaunch;
     p.counter = counters + b;
-    const size_t smem = pa::decode_smem_bytes(head_dim, block_size, w.part_tokens, p.num_seqs);
-    const int per_sm = pa::decode_ctas_per_sm(head_dim, block_size, smem);
+    const size_t smem = pa::decode_smem_bytes(fp8, head_dim, block_size, w.part_tokens, p.num_seqs);
+    const int per_sm = pa::decode_ctas_per_sm(fp8, head_dim, block_size, smem);
     long long grid = (long long)per_sm * ds.sms;
     const long long items_ub = (long long)p.num_seqs * num_heads * w.max_parts;
     if (grid > items_ub) grid = items_ub;
-    if (pa::launch_decode_partition(p, head_dim, block_size, (int)grid, smem, cs) != cudaSuccess)
+    if (pa::launch_decode_partition(p, fp8, head_dim, block_size, (int)grid, smem, cs) != cudaSuccess)
       return PA_ERR_CUDA;
   }
   if (w.max_parts > 1) {
@@ -238,6 +227,83 @@ pa_status pa_decode(void* out, const void* query, const void* key_cache, const v
       return PA_ERR_CUDA;
   }
   return PA_OK;
+}
+
+pa_status copy_blocks_impl(int elem_bytes, void* const* key_caches, void* const* value_caches,
+                           int num_layers, const int64_t* block_mapping, int num_pairs,
+                           int num_heads, int head_dim, int block_size, int num_blocks,
+                           pa_stream_t stream) {
+  if (!head_dim_ok(head_dim) || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+  if (num_layers < 0 || num_pairs < 0 || num_heads <= 0 || num_blocks <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_layers == 0 || num_pairs == 0) return PA_OK;
+  if (!key_caches || !value_caches || !block_mapping || !aligned8(block_mapping))
+    return PA_ERR_INVALID_ARG;
+  for (int l = 0; l < num_layers; ++l) {
+    if (!key_caches[l] || !value_caches[l] || !aligned16(key_caches[l]) ||
+        !aligned16(value_caches[l]))
+      return PA_ERR_INVALID_ARG;
+  }
+  DeviceState ds;
+  pa_status st = device_state(&ds, false);
+  if (st != PA_OK) return st;
+  return pa::launch_copy_blocks(key_caches, value_caches, num_layers, block_mapping, num_pairs,
+                                num_heads, head_dim, block_size, elem_bytes, num_blocks, ds.err,
+                                reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_status_string(pa_status status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_OUT_OF_RANGE: return "PA_ERR_OUT_OF_RANGE";
+    case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
+  }
+  return "PA_ERR_UNKNOWN";
+}
+
+int pa_decode_partition_tokens(int num_seqs, int num_heads, int max_context_len) {
+  if (num_seqs < 0 || num_heads <= 0 || max_context_len < 0) return 0;
+  return part_tokens_for(num_seqs, num_heads, max_context_len);
+}
+
+void pa_decode_set_partition_tokens(int tokens) {
+  g_part_override.store(tokens > 0 ? tokens : 0, std::memory_order_relaxed);
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len) {
+  if (num_seqs < 0 || num_heads <= 0 || !head_dim_ok(head_dim) || max_context_len < 0) return 0;
+  return ws_layout(num_seqs, num_heads, head_dim, max_context_len).total;
+}
+
+pa_status pa_decode(void* out, const void* query, const void* key_cache, const void* value_cache,
+                    const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* context_lens, int num_seqs, int num_heads, int head_dim,
+                    int block_size, int num_blocks, float scale, int max_context_len,
+                    void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  return decode_impl(false, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_heads, head_dim, block_size, num_blocks, scale,
+                     1.f, 1.f, max_context_len, workspace, workspace_bytes, stream);
+}
+
+pa_status pa_decode_fp8(void* out, const void* query, const void* key_cache,
+                        const void* value_cache, const int32_t* block_tables,
+                        int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                        int num_heads, int head_dim, int block_size, int num_blocks, float scale,
+                        float k_scale, float v_scale, int max_context_len, void* workspace,
+                        size_t workspace_bytes, pa_stream_t stream) {
+  if (!scale_ok(k_scale) || !scale_ok(v_scale)) return PA_ERR_INVALID_ARG;
+  return decode_impl(true, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_heads, head_dim, block_size, num_blocks, scale,
+                     k_scale, v_scale, max_context_len, workspace, workspace_bytes, stream);
 }
 
 pa_status pa_reshape_and_cache(const void* key, const void* value, void* key_cache,
@@ -264,23 +330,50 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* key_cac
 pa_status pa_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
                          const int64_t* block_mapping, int num_pairs, int num_heads, int head_dim,
                          int block_size, int num_blocks, pa_stream_t stream) {
+  return copy_blocks_impl(2, key_caches, value_caches, num_layers, block_mapping, num_pairs,
+                          num_heads, head_dim, block_size, num_blocks, stream);
+}
+
+pa_status pa_copy_blocks_fp8(void* const* key_caches, void* const* value_caches, int num_layers,
+                             const int64_t* block_mapping, int num_pairs, int num_heads,
+                             int head_dim, int block_size, int num_blocks, pa_stream_t stream) {
+  return copy_blocks_impl(1, key_caches, value_caches, num_layers, block_mapping, num_pairs,
+                          num_heads, head_dim, block_size, num_blocks, stream);
+}
+
+pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,
+                                   void* value_cache, const int64_t* slot_mapping, int num_tokens,
+                                   int num_heads, int head_dim, int block_size, int num_blocks,
+                                   float k_scale, float v_scale, pa_stream_t stream) {
   if (!head_dim_ok(head_dim) || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
-  if (num_layers < 0 || num_pairs < 0 || num_heads <= 0 || num_blocks <= 0)
+  if (num_tokens < 0 || num_heads <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+  if (!scale_ok(k_scale) || !scale_ok(v_scale)) return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache) ||
+      !aligned8(slot_mapping))
     return PA_ERR_INVALID_ARG;
-  if (num_layers == 0 || num_pairs == 0) return PA_OK;
-  if (!key_caches || !value_caches || !block_mapping || !aligned8(block_mapping))
-    return PA_ERR_INVALID_ARG;
-  for (int l = 0; l < num_layers; ++l) {
-    if (!key_caches[l] || !value_caches[l] || !aligned16(key_caches[l]) ||
-        !aligned16(value_caches[l]))
-      return PA_ERR_INVALID_ARG;
-  }
   DeviceState ds;
   pa_status st = device_state(&ds, false);
   if (st != PA_OK) return st;
-  return pa::launch_copy_blocks(key_caches, value_caches, num_layers, block_mapping, num_pairs,
-                                num_heads, head_dim, block_size, num_blocks, ds.err,
-                                reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+  return pa::launch_reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping,
+                                          num_tokens, num_heads, head_dim, block_size, num_blocks,
+                                          k_scale, v_scale, ds.err,
+                                          reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+pa_status pa_convert_cache_fp8(const void* src, void* dst, size_t num_elems, float scale,
+                               pa_stream_t stream) {
+  if (!scale_ok(scale) || (num_elems & 15) != 0) return PA_ERR_INVALID_ARG;
+  if (num_elems == 0) return PA_OK;
+  if (!src || !dst || !aligned16(src) || !aligned16(dst)) return PA_ERR_INVALID_ARG;
+  DeviceState ds;
+  pa_status st = device_state(&ds, false);
+  if (st != PA_OK) return st;
+  return pa::launch_convert_cache_fp8(src, dst, (long long)num_elems, scale,
+                                      reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
 }

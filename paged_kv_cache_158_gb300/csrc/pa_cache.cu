@@ -48,6 +48,68 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// ---- cache write into an FP8 (E4M3) cache
+// ("vLLM推理加速深度解读：PagedAttention如何提升10x吞吐量" §3.3 names FP8 KV
+// caches; format and scaling as stated in the public header).  Thread i makes
+// 16-byte output vector i (16 codes) of the [T][H][D] inputs: it reads the
+// 16 fp16 values (32 bytes), divides each by the tensor's scale in IEEE
+// binary32 (round to nearest) and rounds the quotient to the nearest E4M3
+// code, saturating to +-448.
+__device__ __forceinline__ uint4 quantize16(const uint4& lo, const uint4& hi, float scale) {
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  uint32_t c[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float2 f = half2_bits_to_float2(w[j]);
+    c[j] = f32x2_to_e4m3x2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
+  }
+  return make_uint4(c[0] | c[1] << 16, c[2] | c[3] << 16, c[4] | c[5] << 16, c[6] | c[7] << 16);
+}
+
+template <int D>
+__global__ void __launch_bounds__(256)
+    reshape_and_cache_fp8_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                                 uint4* __restrict__ key_cache, uint4* __restrict__ value_cache,
+                                 const int64_t* __restrict__ slot_mapping, int num_tokens,
+                                 int num_heads, int log2_block, long long num_slots,
+                                 float k_scale, float v_scale, unsigned int* err) {
+  constexpr int V = D / 16;  // 16-byte code vectors per head row
+  pdl_wait();
+  pdl_launch_dependents();
+  const long long per_token = (long long)num_heads * V;
+  const long long total = (long long)num_tokens * per_token;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const long long t = i / per_token;
+    const int rem = (int)(i - t * per_token);
+    const long long slot = slot_mapping[t];
+    if (slot < 0) continue;  // padding token
+    if (slot >= num_slots) {
+      if (rem == 0) atomicOr(err, PA_ERRBIT_SLOT);
+      continue;
+    }
+    const int h = rem / V;
+    const int v = rem - h * V;
+    const long long blk = slot >> log2_block;
+    const long long off = slot & ((1 << log2_block) - 1);
+    const long long dst = ((blk * num_heads + h) << log2_block | off) * V + v;
+    key_cache[dst] = quantize16(key[2 * i], key[2 * i + 1], k_scale);
+    value_cache[dst] = quantize16(value[2 * i], value[2 * i + 1], v_scale);
+  }
+}
+
+// Elementwise quantisation of a whole fp16 buffer (a cache, layout kept):
+// vector i of 16 codes from fp16 vectors 2i and 2i+1.
+__global__ void __launch_bounds__(256)
+    convert_cache_fp8_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                             long long vecs, float scale) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < vecs; i += stride)
+    dst[i] = quantize16(src[2 * i], src[2 * i + 1], scale);
+}
+
 // ---- copy-on-write block copy
 // ("vLLM基础架构：核心组件、PagedAttention原理、KV Cache管理与连续批处理机制" §2.3)
 // blockIdx.y = pair, blockIdx.z = layer * 2 + (0 key | 1 value); blockIdx.x
@@ -154,12 +216,50 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k
                     k, v, kc, vc, slot_mapping, num_tokens, num_heads, lb, slots, err);
 }
 
+cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,
+                                         void* value_cache, const int64_t* slot_mapping,
+                                         int num_tokens, int num_heads, int head_dim,
+                                         int block_size, int num_blocks, float k_scale,
+                                         float v_scale, unsigned int* err, cudaStream_t stream) {
+  const long long vecs = (long long)num_tokens * num_heads * (head_dim / 16);
+  if (vecs == 0) return cudaSuccess;
+  const int threads = 256;
+  long long blocks = (vecs + threads - 1) / threads;
+  const long long cap = (long long)sm_count() * 16;
+  if (blocks > cap) blocks = cap;
+  const int lb = log2_exact(block_size);
+  const long long slots = (long long)num_blocks * block_size;
+  auto k = static_cast<const uint4*>(key);
+  auto v = static_cast<const uint4*>(value);
+  auto kc = static_cast<uint4*>(key_cache);
+  auto vc = static_cast<uint4*>(value_cache);
+  if (head_dim == 64)
+    return launch_pdl(reshape_and_cache_fp8_kernel<64>, dim3((unsigned)blocks), dim3(threads), 0,
+                      stream, k, v, kc, vc, slot_mapping, num_tokens, num_heads, lb, slots,
+                      k_scale, v_scale, err);
+  return launch_pdl(reshape_and_cache_fp8_kernel<128>, dim3((unsigned)blocks), dim3(threads), 0,
+                    stream, k, v, kc, vc, slot_mapping, num_tokens, num_heads, lb, slots, k_scale,
+                    v_scale, err);
+}
+
+cudaError_t launch_convert_cache_fp8(const void* src, void* dst, long long num_elems, float scale,
+                                     cudaStream_t stream) {
+  const long long vecs = num_elems / 16;
+  if (vecs == 0) return cudaSuccess;
+  const int threads = 256;
+  long long blocks = (vecs + threads - 1) / threads;
+  const long long cap = (long long)sm_count() * 16;
+  if (blocks > cap) blocks = cap;
+  return launch_pdl(convert_cache_fp8_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream,
+                    static_cast<const uint4*>(src), static_cast<uint4*>(dst), vecs, scale);
+}
+
 cudaError_t launch_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
                                const int64_t* block_mapping, int num_pairs, int num_heads,
-                               int head_dim, int block_size, int num_blocks, unsigned int* err,
-                               cudaStream_t stream) {
+                               int head_dim, int block_size, int elem_bytes, int num_blocks,
+                               unsigned int* err, cudaStream_t stream) {
   if (num_pairs == 0 || num_layers == 0) return cudaSuccess;
-  const long long block_vecs = (long long)num_heads * block_size * head_dim / 8;
+  const long long block_vecs = (long long)num_heads * block_size * head_dim * elem_bytes / 16;
   const int threads = 256;
   long long xblocks = (block_vecs + threads - 1) / threads;
   if (xblocks > 64) xblocks = 64;

@@ -51,6 +51,12 @@
 //    (the pending merges form a serial latency chain in the kernel's tail).
 //  * The summation order depends only on logical token positions, so the
 //    result is bit-identical under any relabelling of physical blocks.
+//  * FP8 caches (F8: one E4M3 byte per element, one scale per cache tensor)
+//    use the same lane layout: a lane loads its 8 codes (8 bytes) of a row,
+//    widens them to fp16 pairs in registers (E4M3 values are exact in fp16),
+//    and runs the fp16 arithmetic above.  The key scale is folded into the
+//    logit scale and the value scale multiplies the CTA's merged output, so
+//    the cache is read once at one byte per element.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -64,7 +70,7 @@
 
 namespace pa {
 
-template <int D, int B>
+template <int D, int B, bool F8 = false>
 struct DecodeTraits {
   static constexpr int NW = 4;                // warps per CTA
   static constexpr int NST = 3;               // stages per warp
@@ -74,8 +80,10 @@ struct DecodeTraits {
   static constexpr int RI = 32 / LR;          // token rows per warp-wide load
   static constexpr int TPL = TC / RI;         // token rows per lane
   static constexpr int DUP = LR / TPL;        // lanes sharing a logit after the reduction
+  static constexpr int ELEM = F8 ? 1 : 2;    // bytes per cache element
   static constexpr int CHUNK_ELEMS = TC * D;
-  static constexpr int STAGE_BYTES = 2 * CHUNK_ELEMS * 2;  // K rows then V rows
+  static constexpr int CHUNK_BYTES = CHUNK_ELEMS * ELEM;
+  static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;  // K rows then V rows
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(TPL >= 1 && TPL <= LR && (TPL & (TPL - 1)) == 0, "lane layout");
   static_assert(NST == 3, "next-item block ids are kept in three registers");
@@ -141,17 +149,17 @@ __device__ __forceinline__ ItemInfo locate_item(int item, const int* cum, const 
 // Chunks of an item that warp `warp` processes (chunks warp, warp+NW, ...).
 template <int D, int B>
 __device__ __forceinline__ int warp_chunks(const ItemInfo& it, int warp) {
-  using T = DecodeTraits<D, B>;
+  using T = DecodeTraits<D, B>;  // chunking does not depend on the element type
   const int n = (it.t_end - it.t_begin + T::TC - 1) / T::TC;
   return warp < n ? (n - 1 - warp) / T::NW + 1 : 0;
 }
 
 // Issues the bulk copies of one chunk (K rows and V rows) into a stage.
-template <int D, int B>
+template <int D, int B, bool F8>
 __device__ __forceinline__ void issue_chunk(const DecodeParams& a, const ItemInfo& it, int phys,
-                                            int chunk, __half* stage, uint32_t bar,
+                                            int chunk, unsigned char* stage, uint32_t bar,
                                             uint64_t policy) {
-  using T = DecodeTraits<D, B>;
+  using T = DecodeTraits<D, B, F8>;
   const int t0 = it.t_begin + chunk * T::TC;
   const int rows = min(T::TC, it.t_end - t0);
   if (phys < 0 || phys >= a.num_blocks) {
@@ -159,20 +167,32 @@ __device__ __forceinline__ void issue_chunk(const DecodeParams& a, const ItemInf
     mbar_arrive(bar);  // completes the phase with no data; the chunk is skipped
     return;
   }
-  const size_t off = (((size_t)phys * a.num_heads + it.h) * B + (t0 % B)) * D;
-  const uint32_t bytes = (uint32_t)rows * D * 2;
+  const size_t off = (((size_t)phys * a.num_heads + it.h) * B + (t0 % B)) * D * T::ELEM;
+  const uint32_t bytes = (uint32_t)rows * D * T::ELEM;
   mbar_arrive_expect_tx(bar, 2 * bytes);
-  bulk_g2s_hint(smem_u32(stage), static_cast<const __half*>(a.key_cache) + off, bytes, bar, policy);
-  bulk_g2s_hint(smem_u32(stage + T::CHUNK_ELEMS), static_cast<const __half*>(a.value_cache) + off,
-                bytes, bar, policy);
+  bulk_g2s_hint(smem_u32(stage), static_cast<const unsigned char*>(a.key_cache) + off, bytes, bar,
+                policy);
+  bulk_g2s_hint(smem_u32(stage + T::CHUNK_BYTES),
+                static_cast<const unsigned char*>(a.value_cache) + off, bytes, bar, policy);
+}
+
+// A lane's 8 elements of cache row t in a stage, as 4 packed fp16 pairs.
+template <int D, bool F8>
+__device__ __forceinline__ uint4 load_row8(const unsigned char* rows, int t, int cidx) {
+  if constexpr (F8) {
+    return e4m3x8_to_f16x8(lds64(rows + t * D + 8 * cidx));
+  } else {
+    return lds128(rows + (t * D + 8 * cidx) * 2);
+  }
 }
 
 // One chunk for one warp: logits, online-softmax update, p.V accumulation.
-template <int D, int B, bool FULL>
-__device__ __forceinline__ void process_chunk(const __half* Ks, const __half* Vs, int rows,
-                                              const uint4& q, float scale_log2, float* p_w,
-                                              int lane, float& m, float& l, float (&o)[8]) {
-  using T = DecodeTraits<D, B>;
+template <int D, int B, bool F8, bool FULL>
+__device__ __forceinline__ void process_chunk(const unsigned char* Ks, const unsigned char* Vs,
+                                              int rows, const uint4& q, float scale_log2,
+                                              float* p_w, int lane, float& m, float& l,
+                                              float (&o)[8]) {
+  using T = DecodeTraits<D, B, F8>;
   const int cidx = lane % T::LR;  // which 8 dimensions
   const int r = lane / T::LR;     // which row group
 
@@ -181,7 +201,7 @@ __device__ __forceinline__ void process_chunk(const __half* Ks, const __half* Vs
 #pragma unroll
   for (int k = 0; k < T::TPL; ++k) {
     const int t = r + T::RI * k;
-    v[k] = dot8_f16(q, lds128(Ks + t * D + 8 * cidx));
+    v[k] = dot8_f16(q, load_row8<D, F8>(Ks, t, cidx));
   }
   // Reduce-scatter over the LR lanes of the row group: at each halving step a
   // lane keeps one half of its values and adds its partner's copy of it.
@@ -226,7 +246,7 @@ __device__ __forceinline__ void process_chunk(const __half* Ks, const __half* Vs
   for (int k = 0; k < T::TPL; ++k) {
     const int t = r + T::RI * k;
     if (FULL || t < rows) {
-      const uint4 vv = lds128(Vs + t * D + 8 * cidx);
+      const uint4 vv = load_row8<D, F8>(Vs, t, cidx);
       const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -238,13 +258,13 @@ __device__ __forceinline__ void process_chunk(const __half* Ks, const __half* Vs
   }
 }
 
-template <int D, int B>
-__global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
+template <int D, int B, bool F8>
+__global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS)
     decode_partition_kernel(const DecodeParams a) {
-  using T = DecodeTraits<D, B>;
+  using T = DecodeTraits<D, B, F8>;
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* cur_ptr = smem;
-  __half* stages = reinterpret_cast<__half*>(cur_ptr);
+  unsigned char* stages = cur_ptr;
   cur_ptr += T::kStages;
   uint64_t* bars = reinterpret_cast<uint64_t*>(cur_ptr);
   cur_ptr += T::kBars;
@@ -334,7 +354,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
   __syncthreads();
 
   const uint64_t policy = policy_evict_first();
-  __half* my_stages = stages + (size_t)warp * T::NST * (2 * T::CHUNK_ELEMS);
+  unsigned char* my_stages = stages + (size_t)warp * T::NST * T::STAGE_BYTES;
   uint64_t* my_bars = bars + warp * T::NST;
   float* my_p = p_s + warp * T::TC;
   const int cidx = lane % T::LR;
@@ -353,8 +373,8 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
       for (; (int)iss < n0 && iss < (uint32_t)T::NST; ++iss) {
         const int chunk = warp + (int)iss * T::NW;
         const int phys = bt_s[(it.t_begin + chunk * T::TC) / B - it.blk0];
-        issue_chunk<D, B>(a, it, phys, chunk, my_stages + iss * 2 * T::CHUNK_ELEMS,
-                          smem_u32(&my_bars[iss]), policy);
+        issue_chunk<D, B, F8>(a, it, phys, chunk, my_stages + iss * T::STAGE_BYTES,
+                              smem_u32(&my_bars[iss]), policy);
       }
     }
     iss = __shfl_sync(kFullMask, iss, 0);
@@ -398,16 +418,16 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
         while (iss < u + T::NST) {
           const int k = (int)(iss - base);
           const int st = iss % T::NST;
-          __half* stage = my_stages + st * 2 * T::CHUNK_ELEMS;
+          unsigned char* stage = my_stages + st * T::STAGE_BYTES;
           const uint32_t bar = smem_u32(&my_bars[st]);
           if (k < n_my) {
             const int chunk = warp + k * T::NW;
             const int phys = bt[(it.t_begin + chunk * T::TC) / B - it.blk0];
-            issue_chunk<D, B>(a, it, phys, chunk, stage, bar, policy);
+            issue_chunk<D, B, F8>(a, it, phys, chunk, stage, bar, policy);
           } else if (k - n_my < n_nx) {
             const int j = k - n_my;
             const int phys = j == 0 ? nxp0 : (j == 1 ? nxp1 : nxp2);
-            issue_chunk<D, B>(a, nx, phys, warp + j * T::NW, stage, bar, policy);
+            issue_chunk<D, B, F8>(a, nx, phys, warp + j * T::NW, stage, bar, policy);
           } else {
             break;
           }
@@ -446,13 +466,13 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
       const int rows = min(T::TC, it.t_end - t0);
       const int phys = bt[t0 / B - it.blk0];
       if (phys >= 0 && phys < a.num_blocks) {
-        const __half* Ks = my_stages + st * 2 * T::CHUNK_ELEMS;
+        const unsigned char* Ks = my_stages + st * T::STAGE_BYTES;
         if (rows == T::TC)
-          process_chunk<D, B, true>(Ks, Ks + T::CHUNK_ELEMS, rows, q, a.scale_log2, my_p, lane, m,
-                                    l, o);
+          process_chunk<D, B, F8, true>(Ks, Ks + T::CHUNK_BYTES, rows, q, a.scale_log2, my_p, lane,
+                                        m, l, o);
         else
-          process_chunk<D, B, false>(Ks, Ks + T::CHUNK_ELEMS, rows, q, a.scale_log2, my_p, lane,
-                                     m, l, o);
+          process_chunk<D, B, F8, false>(Ks, Ks + T::CHUNK_BYTES, rows, q, a.scale_log2, my_p,
+                                         lane, m, l, o);
       }
       __syncwarp();
       ++u;
@@ -491,6 +511,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, B>::THREADS)
         L = fmaf(sc, mb[w * T::MS + D + 1], L);
         O = fmaf(sc, mb[w * T::MS + d], O);
       }
+      if constexpr (F8) O *= a.v_scale;
       if (it.n_parts == 1) {
         const float r = (it.c > 0 && L > 0.f) ? O / L : 0.f;
         static_cast<__half*>(a.out)[sh * D + d] = __float2half_rn(r);
@@ -597,25 +618,25 @@ cudaError_t launch_reduce_t(const DecodeParams& p, int total_seqs, cudaStream_t 
   return launch_pdl(decode_reduce_kernel<D, B>, dim3(blocks), dim3(128), 0, st, p, total_seqs);
 }
 
-template <int D, int B>
+template <int D, int B, bool F8>
 cudaError_t launch_partition_t(const DecodeParams& p, int grid, size_t smem, cudaStream_t st) {
-  return launch_pdl(decode_partition_kernel<D, B>, dim3(grid), dim3(DecodeTraits<D, B>::THREADS),
-                    smem, st, p);
+  return launch_pdl(decode_partition_kernel<D, B, F8>, dim3(grid),
+                    dim3(DecodeTraits<D, B, F8>::THREADS), smem, st, p);
 }
 
-template <int D, int B>
+template <int D, int B, bool F8>
 int ctas_per_sm_t(size_t smem) {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_partition_kernel<D, B>,
-                                                    DecodeTraits<D, B>::THREADS, smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_partition_kernel<D, B, F8>,
+                                                    DecodeTraits<D, B, F8>::THREADS, smem) !=
       cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }
 
-template <int D, int B>
+template <int D, int B, bool F8>
 cudaError_t prepare_t() {
-  return cudaFuncSetAttribute(decode_partition_kernel<D, B>,
+  return cudaFuncSetAttribute(decode_partition_kernel<D, B, F8>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
 }
 

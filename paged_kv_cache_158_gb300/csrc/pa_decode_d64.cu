@@ -1,2 +1,3 @@
 #define PA_D 64
+#define PA_F8 0
 #include "pa_decode_inst.inc"

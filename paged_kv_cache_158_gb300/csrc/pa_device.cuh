@@ -170,4 +170,36 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
 
+__device__ __forceinline__ uint2 lds64(const void* p) {
+  return *reinterpret_cast<const uint2*>(p);
+}
+
+// ---- FP8 E4M3 ------------------------------------------------------------
+
+// Two E4M3 codes (low byte = first element) -> packed fp16 pair (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
+  uint32_t r;
+  const unsigned short c = (unsigned short)codes16;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
+  return r;
+}
+
+// Eight E4M3 codes (element order in memory) -> 4 packed fp16 pairs.
+__device__ __forceinline__ uint4 e4m3x8_to_f16x8(const uint2& c) {
+  uint4 r;
+  r.x = e4m3x2_to_f16x2(c.x & 0xffffu);
+  r.y = e4m3x2_to_f16x2(c.x >> 16);
+  r.z = e4m3x2_to_f16x2(c.y & 0xffffu);
+  r.w = e4m3x2_to_f16x2(c.y >> 16);
+  return r;
+}
+
+// Nearest E4M3 codes of two floats (ties to even, saturating to +-448);
+// `first` goes to the low byte, matching element order in memory.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float first, float second) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(second), "f"(first));
+  return r;
+}
+
 }  // namespace pa

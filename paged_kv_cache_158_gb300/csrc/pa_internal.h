@@ -20,8 +20,8 @@ constexpr int kCopyMaxLayers = 32;
 struct DecodeParams {
   void* out;                  // fp16 [S][H][D]
   const void* query;          // fp16 [S][H][D]
-  const void* key_cache;      // fp16 [NB][H][B][D]
-  const void* value_cache;    // fp16 [NB][H][B][D]
+  const void* key_cache;      // fp16 or E4M3 [NB][H][B][D]
+  const void* value_cache;    // fp16 or E4M3 [NB][H][B][D]
   const int32_t* block_tables;  // [S][max_blocks]
   const int32_t* context_lens;  // [S]
   float* ws_ml;               // [S][H][max_parts][2]: running max (base-2 units) and sum
@@ -36,19 +36,22 @@ struct DecodeParams {
   int max_context_len;        // host bound; larger lengths are clipped and flagged
   int part_tokens;            // tokens per partition (multiple of 32)
   int max_parts;              // ceil(max_context_len / part_tokens)
-  float scale_log2;           // scale * log2(e): logits are kept in base-2 units
+  float scale_log2;           // scale * log2(e) (* k_scale for E4M3 caches): base-2 logits
+  float v_scale;              // E4M3 caches: multiplies the output (unused for fp16)
 };
 
-// Partition-kernel launch: picks the instantiation for (head_dim, block_size).
-cudaError_t launch_decode_partition(const DecodeParams& p, int head_dim, int block_size,
+// Partition-kernel launch: picks the instantiation for (cache element type,
+// head_dim, block_size); fp8 selects E4M3 caches.
+cudaError_t launch_decode_partition(const DecodeParams& p, bool fp8, int head_dim, int block_size,
                                     int grid, size_t smem_bytes, cudaStream_t stream);
 // LSE-merge launch over all (seq, head) pairs of the batch.
 cudaError_t launch_decode_reduce(const DecodeParams& p, int head_dim, int block_size,
                                  int total_seqs, cudaStream_t stream);
 // Dynamic shared memory of the partition kernel.
-size_t decode_smem_bytes(int head_dim, int block_size, int part_tokens, int seqs_in_launch);
+size_t decode_smem_bytes(bool fp8, int head_dim, int block_size, int part_tokens,
+                         int seqs_in_launch);
 // Resident CTAs per SM of the partition kernel for that shared-memory size.
-int decode_ctas_per_sm(int head_dim, int block_size, size_t smem_bytes);
+int decode_ctas_per_sm(bool fp8, int head_dim, int block_size, size_t smem_bytes);
 // One-time per-device kernel attributes (dynamic shared memory opt-in).
 cudaError_t decode_prepare_device(int device);
 
@@ -60,10 +63,21 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k
                                      int num_tokens, int num_heads, int head_dim, int block_size,
                                      int num_blocks, unsigned int* err, cudaStream_t stream);
 
+cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,
+                                         void* value_cache, const int64_t* slot_mapping,
+                                         int num_tokens, int num_heads, int head_dim,
+                                         int block_size, int num_blocks, float k_scale,
+                                         float v_scale, unsigned int* err, cudaStream_t stream);
+
+// num_elems: a multiple of 16.
+cudaError_t launch_convert_cache_fp8(const void* src, void* dst, long long num_elems, float scale,
+                                     cudaStream_t stream);
+
+// elem_bytes: 2 for fp16 caches, 1 for E4M3 caches.
 cudaError_t launch_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
                                const int64_t* block_mapping, int num_pairs, int num_heads,
-                               int head_dim, int block_size, int num_blocks, unsigned int* err,
-                               cudaStream_t stream);
+                               int head_dim, int block_size, int elem_bytes, int num_blocks,
+                               unsigned int* err, cudaStream_t stream);
 
 cudaError_t launch_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,
                                 int max_blocks, const int32_t* token_seq,

@@ -53,11 +53,13 @@ def poison_dead_slots_device(kc: torch.Tensor, vc: torch.Tensor, mask: np.ndarra
         t.permute(0, 2, 1, 3)[dead] = nan
 
 
-def sampled_oracle(w, layer: int, seqs, new_tokens: bool = True):
+def sampled_oracle(w, layer: int, seqs, new_tokens: bool = True, fp8_scales=None):
     """Oracle outputs for a subset of sequences of a full-size workload, on a
     mini-pool holding only their blocks (relabelled 0..n-1; relabelling does
     not change the result).  Applies the decode step's cache write of each
-    sampled sequence's new token.  Returns ref64 [len(seqs), H, D]."""
+    sampled sequence's new token.  With fp8_scales = (k_scale, v_scale) the
+    pool is the FP8 cache (the oracle quantises the generated fp16 pool, the
+    cache write quantises, the decode dequantises).  Returns ref64 [len(seqs), H, D]."""
     seqs = np.asarray(seqs)
     B = w.block_size
     nbs = [-(-int(w.context_lens[s]) // B) for s in seqs]
@@ -75,7 +77,46 @@ def sampled_oracle(w, layer: int, seqs, new_tokens: bool = True):
         slots, rc = oracle.slot_mapping(bt, np.arange(len(seqs), dtype=np.int32),
                                         tok_pos[idx].astype(np.int32), B, len(used))
         assert rc == 0
+    if fp8_scales is not None:
+        ks, vs = fp8_scales
+        kc, vc = oracle.quantize_e4m3(kc, ks), oracle.quantize_e4m3(vc, vs)
+        if new_tokens:
+            assert oracle.reshape_and_cache_fp8(kc, vc, kn[idx], vn[idx], slots, B, ks, vs) == 0
+        _, ref64, rc = oracle.decode_fp8(q[seqs], kc, vc, bt, ctx, w.scale, ks, vs)
+        assert rc == 0
+        return ref64
+    if new_tokens:
         assert oracle.reshape_and_cache(kc, vc, kn[idx], vn[idx], slots, B) == 0
     _, ref64, rc = oracle.decode(q[seqs], kc, vc, bt, ctx, w.scale)
     assert rc == 0
     return ref64
+
+
+# ---- FP8 caches
+
+NAN8 = 0x7F   # an E4M3 NaN code
+
+
+def materialize_fp8(w, layers=None, device="cuda"):
+    """Device workload with uint8 FP8 caches: each layer's generated fp16 pool
+    converted by the library's pa_convert_cache_fp8 under configs.fp8_scales."""
+    import paged_kv_cache_158_gb300 as pa
+    from workloads import configs
+    return gpu.materialize(w, layers=layers, device=device, fp8_convert=pa.pa_convert_cache_fp8,
+                           fp8_scales=configs.fp8_scales(w))
+
+
+def poison_dead_slots_host_fp8(kc: np.ndarray, vc: np.ndarray, mask: np.ndarray) -> None:
+    dead = ~mask
+    kc.transpose(0, 2, 1, 3)[dead] = NAN8
+    vc.transpose(0, 2, 1, 3)[dead] = NAN8
+
+
+def poison_dead_slots_device_fp8(kc: torch.Tensor, vc: torch.Tensor, mask: np.ndarray) -> None:
+    dead = torch.from_numpy(~mask).to(kc.device)
+    for t in (kc, vc):
+        t.permute(0, 2, 1, 3)[dead] = NAN8
+
+
+def u8(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().numpy().view(np.uint8)

@@ -88,3 +88,37 @@ def test_python_binding_refuses_to_run_without_library(tmp_path, monkeypatch):
     mod = importlib.util.module_from_spec(spec)
     with pytest.raises(ImportError):
         spec.loader.exec_module(mod)
+
+
+def test_fp8_calls_reject_bad_arguments_before_any_launch():
+    lib = ctypes.CDLL(LIB)
+    vp, i, fl = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    good = 0x10000
+    d = lib.pa_decode_fp8
+    d.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, fl, fl, fl, i, vp, ctypes.c_size_t, vp]
+    for ks, vs in [(0.0, 1.0), (1.0, -1.0), (float("inf"), 1.0), (1.0, float("nan"))]:
+        assert d(good, good, good, good, good, 4, good, 2, 2, 128, 16, 8, 0.1, ks, vs, 64, good,
+                 1 << 20, None) == 1
+    assert d(good, good, good, good, good, 4, good, 2, 2, 96, 16, 8, 0.1, 1.0, 1.0, 64, good,
+             1 << 20, None) == 2
+    assert d(good, good + 8, good, good, good, 4, good, 2, 2, 128, 16, 8, 0.1, 1.0, 1.0, 64, good,
+             1 << 20, None) == 1
+    assert d(None, None, None, None, None, 4, None, 0, 2, 128, 16, 8, 0.1, 1.0, 1.0, 64, None, 0,
+             None) == 0
+    r = lib.pa_reshape_and_cache_fp8
+    r.argtypes = [vp, vp, vp, vp, vp] + [i] * 5 + [fl, fl, vp]
+    assert r(good, good, good, good, good, 3, 2, 128, 16, 8, 0.0, 1.0, None) == 1
+    assert r(good, good, good, good, good, 3, 2, 64, 12, 8, 1.0, 1.0, None) == 2
+    assert r(good, good, good + 8, good, good, 3, 2, 64, 16, 8, 1.0, 1.0, None) == 1
+    assert r(None, None, None, None, None, 0, 2, 128, 16, 8, 1.0, 1.0, None) == 0
+    c = lib.pa_copy_blocks_fp8
+    c.argtypes = [vp, vp, i, vp, i, i, i, i, i, vp]
+    ptrs = (ctypes.c_void_p * 1)(good + 8)
+    assert c(ptrs, ptrs, 1, good, 2, 2, 128, 16, 8, None) == 1
+    assert c(None, None, 0, None, 0, 2, 128, 16, 8, None) == 0
+    v = lib.pa_convert_cache_fp8
+    v.argtypes = [vp, vp, ctypes.c_size_t, fl, vp]
+    assert v(good, good, 24, 1.0, None) == 1                           # not a multiple of 16
+    assert v(good, good, 32, -1.0, None) == 1
+    assert v(good + 8, good, 32, 1.0, None) == 1
+    assert v(None, None, 0, 1.0, None) == 0

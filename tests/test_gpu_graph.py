@@ -15,12 +15,12 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def make_step(w, dw, copy_pairs=None):
+def make_step(w, dw, copy_pairs=None, fp8_scales=None):
     outs = [torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=DEV)
             for _ in dw.layers]
     return DecodeStep(dw.key_caches, dw.value_caches, dw.queries, dw.keys_new, dw.values_new, outs,
                       dw.block_tables, dw.context_lens, dw.token_seq, dw.token_pos, w.block_size,
-                      w.num_blocks, w.scale, int(w.context_lens.max()), copy_pairs)
+                      w.num_blocks, w.scale, int(w.context_lens.max()), copy_pairs, fp8_scales)
 
 
 def clone_dw(dw):
@@ -52,6 +52,25 @@ def test_graph_replay_matches_eager(cfg, layers):
             assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     for a, b in zip(dw_eager.key_caches + dw_eager.value_caches, dw.key_caches + dw.value_caches):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+def test_graph_replay_matches_eager_fp8():
+    from pa_testlib import materialize_fp8
+    w = configs.config5(num_layers=2)
+    sc = configs.fp8_scales(w)
+    dw = materialize_fp8(w, layers=[0, 1])
+    dw_eager = clone_dw(dw)
+    eager = make_step(w, dw_eager, fp8_scales=sc)
+    graph = make_step(w, dw, fp8_scales=sc)
+    graph.capture()
+    eager.run()
+    graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager.outs, graph.outs):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for a, b in zip(dw_eager.key_caches + dw_eager.value_caches, dw.key_caches + dw.value_caches):
+        assert torch.equal(a, b)
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
 
 

@@ -140,3 +140,19 @@ def test_fp8_decode_empty_context_and_bad_block():
     bt[1, 0] = 5
     _, _, rc = oracle.decode_fp8(q, kc, kc, bt, np.array([0, 3], np.int32), 0.1, 1.0, 1.0)
     assert rc != 0
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.37, 0.0625, 3.0])
+def test_quantize_every_fp16_pattern_matches_torch(scale):
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    x16 = bits.view(np.float16)
+    finite = np.isfinite(x16)
+    ours = oracle.quantize_e4m3(bits[finite], scale)
+    q32 = x16[finite].astype(np.float32) / np.float32(scale)      # IEEE binary32 division
+    inrange = np.abs(q32) < 464.0
+    assert np.array_equal(ours[inrange], torch_e4m3_encode_f32(q32[inrange]))
+    # beyond the finite range: +-448 with the value's sign
+    big = ~inrange
+    assert np.all(ours[big] == np.where(q32[big] > 0, 0x7E, 0xFE))
+    inf = oracle.quantize_e4m3(np.array([0x7C00, 0xFC00], dtype=np.uint16), scale)
+    assert list(inf) == [0x7E, 0xFE]

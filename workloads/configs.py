@@ -220,4 +220,15 @@ def small_random(seed: int, num_seqs: int, num_heads: int, head_dim: int, block_
                     q_sigma=q_sigma)
 
 
+def fp8_scales(w: Workload) -> tuple[float, float]:
+    """Per-tensor scales (k_scale, v_scale) of a workload's FP8 caches: about
+    1/70 and 1/84 of the values' standard deviation, so that values up to
+    about 6 and 5.3 sigma lie inside E4M3's finite range (448) and the rare
+    larger ones saturate.  Two different, non-power-of-two values, rounded to
+    binary32 (the type the library takes)."""
+    k = float(np.float32(w.kv_sigma * 0.0137))
+    v = float(np.float32(w.kv_sigma * 0.0119))
+    return k, v
+
+
 ALL = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}

@@ -52,21 +52,39 @@ class DeviceWorkload:
     layers: list = field(default_factory=list)
 
 
-def materialize(w: Workload, layers=None, device="cuda", fill_caches: bool = True) -> DeviceWorkload:
+def materialize(w: Workload, layers=None, device="cuda", fill_caches: bool = True,
+                fp8_convert=None, fp8_scales=None) -> DeviceWorkload:
     """Allocate and fill the caches of the given layers (default: all) and upload the
-    per-layer query and new-token tensors."""
+    per-layer query and new-token tensors.
+
+    With fp8_convert (a callable (src_fp16, dst_uint8, scale) supplied by the
+    caller) the caches are uint8 FP8 caches: each layer's fp16 pool is
+    generated into a scratch buffer and handed to fp8_convert with
+    fp8_scales = (k_scale, v_scale)."""
     layers = list(range(w.num_layers)) if layers is None else list(layers)
     kv_bank = device_bank(w.seed, w.kv_sigma, device)
     shape = (w.num_blocks, w.num_heads, w.block_size, w.head_dim)
     kcs, vcs, qs, kn, vn = [], [], [], [], []
     tok_seq, tok_pos = w.new_tokens()
     T = len(tok_seq)
+    scratch = None
+    if fp8_convert is not None and fill_caches:
+        scratch = torch.empty(shape, dtype=torch.float16, device=device)
     for l in layers:
-        kc = torch.empty(shape, dtype=torch.float16, device=device)
-        vc = torch.empty(shape, dtype=torch.float16, device=device)
-        if fill_caches:
-            fill(kc, w.seed, w.key_pool_stream(l), kv_bank)
-            fill(vc, w.seed, w.value_pool_stream(l), kv_bank)
+        if fp8_convert is not None:
+            kc = torch.empty(shape, dtype=torch.uint8, device=device)
+            vc = torch.empty(shape, dtype=torch.uint8, device=device)
+            if fill_caches:
+                for dst, stream, sc in ((kc, w.key_pool_stream(l), fp8_scales[0]),
+                                        (vc, w.value_pool_stream(l), fp8_scales[1])):
+                    fill(scratch, w.seed, stream, kv_bank)
+                    fp8_convert(scratch, dst, sc)
+        else:
+            kc = torch.empty(shape, dtype=torch.float16, device=device)
+            vc = torch.empty(shape, dtype=torch.float16, device=device)
+            if fill_caches:
+                fill(kc, w.seed, w.key_pool_stream(l), kv_bank)
+                fill(vc, w.seed, w.value_pool_stream(l), kv_bank)
         kcs.append(kc)
         vcs.append(vc)
         qs.append(upload_u16(synth.host_tensor(w.seed, w.query_stream(l),
@@ -75,6 +93,7 @@ def materialize(w: Workload, layers=None, device="cuda", fill_caches: bool = Tru
                                                w.kv_bank()), device))
         vn.append(upload_u16(synth.host_tensor(w.seed, w.value_new_stream(l), (T, w.num_heads, w.head_dim),
                                                w.kv_bank()), device))
+    del scratch
     bt = None if w.block_tables is None else torch.from_numpy(w.block_tables).to(device)
     return DeviceWorkload(w, kcs, vcs, qs, kn, vn, bt, torch.from_numpy(w.context_lens).to(device),
                           torch.from_numpy(tok_seq).to(device), torch.from_numpy(tok_pos).to(device),
