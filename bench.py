@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--eager", action="store_true", help="time eager launches only (no CUDA graph)")
+    ap.add_argument("--op", choices=["step", "swap"], default="step",
+                    help="swap: time block swap-out/in of whole sequences to pinned host memory")
     ap.add_argument("--kv-dtype", choices=["fp16", "fp8"], default="fp16",
                     help="KV-cache element type (fp8: E4M3 codes with per-tensor scales)")
     return ap.parse_args()
@@ -427,6 +429,72 @@ def measure_e2e(st, args, world, device):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
+def run_swap(args):
+    """Swap-out and swap-in of whole sequences' blocks (every layer's K and V) between the
+    device pool and pinned host memory through pa_swap_blocks, against one contiguous
+    copy-engine transfer of the same bytes (torch copy_ between a device buffer and a
+    pinned buffer) as the link's reference rate."""
+    import torch
+
+    import paged_kv_cache_158_gb300 as pa
+    w = make_workload(args.workload, args.layers)
+    dev = torch.device("cuda", 0)
+    fp8 = args.kv_dtype == "fp8"
+    dt = torch.uint8 if fp8 else torch.float16
+    shape = (w.num_blocks, w.num_heads, w.block_size, w.head_dim)
+    L = w.num_layers
+    caches = [torch.empty(shape, dtype=dt, device=dev) for _ in range(2 * L)]
+    for c in caches:
+        c.view(torch.uint8).random_(0, 256)
+    nswap = max(1, w.num_seqs // 16)
+    blocks = np.concatenate([w.block_tables[s, :-(-int(w.context_lens[s]) // w.block_size)]
+                             for s in range(nswap)]).astype(np.int64)
+    nb = len(blocks)
+    host = [torch.empty((nb,) + shape[1:], dtype=dt).pin_memory() for _ in range(2 * L)]
+    out_map = torch.from_numpy(np.stack([blocks, np.arange(nb)], 1).copy()).to(dev)
+    in_map = torch.from_numpy(np.stack([np.arange(nb), blocks], 1).copy()).to(dev)
+    nbytes = nb * host[0][0].numel() * host[0].element_size() * 2 * L
+    stream = torch.cuda.current_stream(dev)
+    K, W = max(3, min(args.steps, 30)), max(3, args.warmup)
+
+    def t_of(fn):
+        for _ in range(W):
+            fn()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(K):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / K * 1e-3
+
+    t_out = t_of(lambda: pa.pa_swap_blocks(host, caches, out_map))
+    t_in = t_of(lambda: pa.pa_swap_blocks(caches, host, in_map))
+    status, bits = pa.pa_check_errors()
+    if status != pa.PA_OK:
+        raise RuntimeError(f"device error word: {pa.pa_status_string(status)} 0x{bits:x}")
+    flat_d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    flat_h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    t_d2h = t_of(lambda: flat_h.copy_(flat_d, non_blocking=True))
+    t_h2d = t_of(lambda: flat_d.copy_(flat_h, non_blocking=True))
+    gbs = lambda t: round(nbytes / t / 1e9, 2)  # noqa: E731
+    return {
+        "metric": "block swap GB/s (bytes of the swapped blocks over the call's device time)",
+        "value": gbs(t_out), "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": W,
+        "higher_is_better": True, "dtype": "e4m3" if fp8 else "f16", "data": "synthetic",
+        "config": {"workload": w.name, "kv_dtype": args.kv_dtype, "layers": L,
+                   "sequences_swapped": nswap, "blocks": nb, "caches": 2 * L,
+                   "bytes_per_direction": nbytes},
+        "swap_out_gbs": gbs(t_out), "swap_in_gbs": gbs(t_in),
+        "swap_out_ms": round(t_out * 1e3, 3), "swap_in_ms": round(t_in * 1e3, 3),
+        "copy_engine_reference": {"d2h_gbs": gbs(t_d2h), "h2d_gbs": gbs(t_h2d),
+                                  "what": "one contiguous transfer of the same bytes"},
+        "frac_of_copy_engine": {"out": round(t_d2h / t_out, 3), "in": round(t_h2d / t_in, 3)},
+        "gpu_launches": 2 * (K + W),
+    }
+
+
 # ------------------------------------------------------------ CPU oracle
 
 def oracle_sample(w, fp8: bool = False):
@@ -499,6 +567,11 @@ def main():
         line = run_reference(args, int(os.environ.get("RANK", "0")), world_env)
         if line is not None:
             print(json.dumps(line), flush=True)
+        return
+    if args.op == "swap":
+        import torch
+        torch.cuda.set_device(0)
+        print(json.dumps(run_swap(args)), flush=True)
         return
     rank, world, local = dist_setup(args.gpus)
     line = run_ours(args, rank, world, local)

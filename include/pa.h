@@ -185,6 +185,42 @@ pa_status pa_copy_blocks(void* const* key_caches, void* const* value_caches, int
                          const int64_t* block_mapping, int num_pairs, int num_heads, int head_dim,
                          int block_size, int num_blocks, pa_stream_t stream);
 
+/*
+ * Block swap between the device cache and a host copy [P4 §三: when GPU
+ * memory runs short the scheduler moves some blocks to CPU memory and brings
+ * them back when needed (blocks_to_swap_out / blocks_to_swap_in); P2 §4.3:
+ * preemption pauses requests when memory runs short]: for every pair p and
+ * every cache c,
+ *
+ *   dst_caches[c] block dst_p  :=  src_caches[c] block src_p   (block_bytes bytes)
+ *
+ * with (src_p, dst_p) = (block_mapping[2p], block_mapping[2p+1]) and block k
+ * of a cache being bytes [k * block_bytes, (k+1) * block_bytes).  Pass every
+ * layer's key and value caches (2 * num_layers caches; block_bytes =
+ * num_heads * block_size * head_dim * element size).  Swap-out: sources on
+ * the device, destinations in host memory; swap-in: the reverse.  One launch
+ * moves all pairs of all caches.
+ *
+ *   dst_caches,
+ *   src_caches     HOST arrays of num_caches pointers.  Each pointer is device
+ *                  memory of the current device or pinned (page-locked:
+ *                  cudaHostAlloc / cudaHostRegister) host memory; the kernel
+ *                  reaches host memory directly over the CPU-GPU link.
+ *                  Pageable host memory or another device's memory returns
+ *                  PA_ERR_INVALID_ARG.  16-byte aligned.
+ *   block_mapping  int64 [num_pairs][2], device memory or pinned host memory
+ *   block_bytes    a multiple of 16
+ *   src_num_blocks, dst_num_blocks  pool sizes; an id outside [0, n) skips
+ *                  the pair and sets PA_ERRBIT_COPY
+ * Preconditions as pa_copy_blocks: destination blocks distinct; no overlap
+ * between the source and destination ranges of one call.  Bit-exact.  The
+ * host side must stay allocated and unchanged until the stream reaches the
+ * copy.
+ */
+pa_status pa_swap_blocks(void* const* dst_caches, const void* const* src_caches, int num_caches,
+                         const int64_t* block_mapping, int num_pairs, size_t block_bytes,
+                         int64_t src_num_blocks, int64_t dst_num_blocks, pa_stream_t stream);
+
 /* ---- FP8 KV cache ------------------------------------------------------
  * [P2 §3.3 lists FP8 KV caches among the memory optimisations; the pages fix
  * neither the format nor the scaling.]  The library's reading: OCP FP8 E4M3

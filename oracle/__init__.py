@@ -59,6 +59,9 @@ def lib() -> ctypes.CDLL:
     L.oracle_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, f64,
                                     f64, f64]
     L.oracle_decode_fp8.restype = i32
+    L.oracle_swap_blocks.argtypes = [vp, vp, i32, vp, i32, ctypes.c_size_t, ctypes.c_int64,
+                                     ctypes.c_int64]
+    L.oracle_swap_blocks.restype = i32
     L.oracle_num_threads.argtypes = []
     L.oracle_num_threads.restype = i32
     _LIB = L
@@ -211,6 +214,26 @@ def decode_fp8(query, key_cache, value_cache, block_tables, context_lens, scale:
                                  bt.shape[1], cl.ctypes.data, S, H, D, B, NB, float(scale),
                                  float(k_scale), float(v_scale))
     return out16, out64, rc
+
+
+def swap_blocks(dst_pools, src_pools, block_mapping) -> int:
+    """In place: block dst of every dst_pools[c] := block src of src_pools[c] for each
+    (src, dst) row of block_mapping.  Pools are C-contiguous arrays whose first axis is
+    the block id (any element type; the copy is bytewise)."""
+    if len(dst_pools) != len(src_pools):
+        raise ValueError("one destination pool per source pool")
+    n = len(src_pools)
+    for a in list(dst_pools) + list(src_pools):
+        if not (isinstance(a, np.ndarray) and a.flags.c_contiguous):
+            raise ValueError("pools must be C-contiguous numpy arrays")
+    bb = src_pools[0].nbytes // src_pools[0].shape[0]
+    if any(a.nbytes // a.shape[0] != bb for a in list(dst_pools) + list(src_pools)):
+        raise ValueError("all pools must have the same block size in bytes")
+    m = _c(block_mapping, np.int64)
+    dp = (ctypes.c_void_p * n)(*[a.ctypes.data for a in dst_pools])
+    sp = (ctypes.c_void_p * n)(*[a.ctypes.data for a in src_pools])
+    return lib().oracle_swap_blocks(dp, sp, n, m.ctypes.data, m.shape[0], bb,
+                                    src_pools[0].shape[0], dst_pools[0].shape[0])
 
 
 def num_threads() -> int:

@@ -154,6 +154,30 @@ int oracle_copy_blocks(uint16_t** key_caches, uint16_t** value_caches, int num_l
 }
 
 /* ------------------------------------------------------------------------ */
+/* Block swap between two pools ["【硬核】啃透vLLM源码" §三: when GPU memory   */
+/* runs short the scheduler moves blocks to CPU memory and back              */
+/* (blocks_to_swap_out / blocks_to_swap_in); "vLLM推理加速深度解读" §4.3     */
+/* preemption]: for each pair (src, dst) and each of num_caches caches,      */
+/* block dst of the destination pool receives block src of the source pool,  */
+/* byte for byte (block_bytes bytes: all heads of one block of one layer's   */
+/* keys or values).  Either pool may be the host's or the device's.          */
+
+int oracle_swap_blocks(uint8_t** dst_caches, uint8_t** src_caches, int num_caches,
+                       const int64_t* block_mapping, int num_pairs, size_t block_bytes,
+                       int64_t src_num_blocks, int64_t dst_num_blocks) {
+  int bad = 0;
+  for (int p = 0; p < num_pairs; ++p) {
+    const int64_t src = block_mapping[2 * p];
+    const int64_t dst = block_mapping[2 * p + 1];
+    if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks) { bad = 1; continue; }
+    for (int c = 0; c < num_caches; ++c)
+      for (size_t e = 0; e < block_bytes; ++e)
+        dst_caches[c][(size_t)dst * block_bytes + e] = src_caches[c][(size_t)src * block_bytes + e];
+  }
+  return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Decode attention over the paged cache [P2 §2.1, §2.3]:                   */
 /*   out[s,h] = softmax(q[s,h] . K_paged^T * scale) V_paged                  */
 /* with K_paged[i] = key_cache[bt[s][i div B]][h][i mod B] for i < c_s.      */

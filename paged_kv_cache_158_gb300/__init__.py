@@ -52,6 +52,8 @@ _lib.pa_reshape_and_cache_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _
 _lib.pa_reshape_and_cache_fp8.restype = _i32
 _lib.pa_convert_cache_fp8.argtypes = [_vp, _vp, _sz, _f32, _vp]
 _lib.pa_convert_cache_fp8.restype = _i32
+_lib.pa_swap_blocks.argtypes = [_vp, _vp, _i32, _vp, _i32, _sz, ctypes.c_int64, ctypes.c_int64, _vp]
+_lib.pa_swap_blocks.restype = _i32
 _lib.pa_copy_blocks_fp8.argtypes = [_vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _vp]
 _lib.pa_copy_blocks_fp8.restype = _i32
 
@@ -238,6 +240,40 @@ def _copy_blocks(key_caches, value_caches, block_mapping, stream, fp8: bool) -> 
     _check(st, "pa_copy_blocks_fp8" if fp8 else "pa_copy_blocks")
 
 
+def _swap_ptr(t: torch.Tensor, name: str) -> int:
+    """A CUDA tensor or a pinned CPU tensor (the kernel reaches pinned host memory directly)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def pa_swap_blocks(dst_caches, src_caches, block_mapping: torch.Tensor, stream=None) -> None:
+    """Block dst of every dst_caches[c] := block src of src_caches[c] for each (src, dst) row of
+    block_mapping (int64 [P, 2], CUDA or pinned).  One side is the device pool, the other a
+    pinned host pool; dim 0 of every cache is the block id.  Pass all layers' K and V caches."""
+    n = len(src_caches)
+    if len(dst_caches) != n or n == 0:
+        raise ValueError("one destination cache per source cache")
+    bb = src_caches[0].numel() // src_caches[0].shape[0] * src_caches[0].element_size()
+    for t in list(src_caches) + list(dst_caches):
+        if t.numel() // t.shape[0] * t.element_size() != bb:
+            raise ValueError("all caches must have the same block size in bytes")
+        if tuple(t.shape[1:]) != tuple(src_caches[0].shape[1:]) or t.dtype != src_caches[0].dtype:
+            raise ValueError("all caches must share block shape and dtype")
+    if block_mapping.dtype != torch.int64 or block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
+        raise ValueError("block_mapping must be int64 [P, 2]")
+    dp = (ctypes.c_void_p * n)(*[_swap_ptr(t, "dst_caches[i]") for t in dst_caches])
+    sp = (ctypes.c_void_p * n)(*[_swap_ptr(t, "src_caches[i]") for t in src_caches])
+    st = _lib.pa_swap_blocks(dp, sp, n, _swap_ptr(block_mapping, "block_mapping"),
+                             block_mapping.shape[0], bb, src_caches[0].shape[0],
+                             dst_caches[0].shape[0], _stream(stream))
+    _check(st, "pa_swap_blocks")
+
+
 def pa_slot_mapping(slot_mapping: torch.Tensor, block_tables: torch.Tensor, token_seq: torch.Tensor,
                     token_pos: torch.Tensor, block_size: int, num_blocks: int, stream=None) -> None:
     """slot_mapping[t] = block_tables[seq][pos // B] * B + pos % B for each new token."""
@@ -268,6 +304,7 @@ def raise_on_device_errors(stream=None) -> None:
 __all__ = [
     "pa_decode", "pa_reshape_and_cache", "pa_copy_blocks", "pa_slot_mapping", "pa_check_errors",
     "pa_decode_fp8", "pa_reshape_and_cache_fp8", "pa_copy_blocks_fp8", "pa_convert_cache_fp8",
+    "pa_swap_blocks",
     "pa_status_string", "pa_decode_workspace_size", "pa_decode_partition_tokens",
     "pa_decode_set_partition_tokens", "decode_workspace", "raise_on_device_errors", "PAError",
 ]

@@ -3,6 +3,7 @@
 // units; this file only validates, sizes and launches.
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "pa_internal.h"
 
@@ -111,6 +112,23 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0;
 bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7) == 0; }
 bool head_dim_ok(int d) { return d == 64 || d == 128; }
 bool block_size_ok(int b) { return b == 4 || b == 8 || b == 16 || b == 32; }
+// The address under which the device reaches p: device memory as is,
+// pinned (page-locked) host memory through its mapping; nullptr when the
+// device cannot reach it (pageable host memory, another device's memory).
+const void* device_address(const void* p, int dev) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  switch (at.type) {
+    case cudaMemoryTypeDevice: return at.device == dev ? p : nullptr;
+    case cudaMemoryTypeManaged: return p;
+    case cudaMemoryTypeHost: return at.devicePointer;
+    default: return nullptr;
+  }
+}
+
 bool scale_ok(float s) { return s > 0.f && s <= 3.4028234663852886e38f; }  // finite, positive
 
 // Tokens per partition.  512 measured best on the 7B-, 13B-shaped and
@@ -374,6 +392,40 @@ pa_status pa_convert_cache_fp8(const void* src, void* dst, size_t num_elems, flo
   if (st != PA_OK) return st;
   return pa::launch_convert_cache_fp8(src, dst, (long long)num_elems, scale,
                                       reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+pa_status pa_swap_blocks(void* const* dst_caches, const void* const* src_caches, int num_caches,
+                         const int64_t* block_mapping, int num_pairs, size_t block_bytes,
+                         int64_t src_num_blocks, int64_t dst_num_blocks, pa_stream_t stream) {
+  if (num_caches < 0 || num_pairs < 0 || src_num_blocks <= 0 || dst_num_blocks <= 0 ||
+      block_bytes == 0 || (block_bytes & 15) != 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_caches == 0 || num_pairs == 0) return PA_OK;
+  if (!dst_caches || !src_caches || !block_mapping || !aligned8(block_mapping))
+    return PA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  const void* map_dev = device_address(block_mapping, dev);
+  if (!map_dev) return PA_ERR_INVALID_ARG;
+  std::vector<void*> dst(num_caches);
+  std::vector<const void*> src(num_caches);
+  for (int c = 0; c < num_caches; ++c) {
+    if (!dst_caches[c] || !src_caches[c] || !aligned16(dst_caches[c]) || !aligned16(src_caches[c]))
+      return PA_ERR_INVALID_ARG;
+    dst[c] = const_cast<void*>(device_address(dst_caches[c], dev));
+    src[c] = device_address(src_caches[c], dev);
+    if (!dst[c] || !src[c] || !aligned16(dst[c]) || !aligned16(src[c])) return PA_ERR_INVALID_ARG;
+  }
+  DeviceState ds;
+  pa_status st = device_state(&ds, false);
+  if (st != PA_OK) return st;
+  return pa::launch_swap_blocks(dst.data(), src.data(), num_caches,
+                                static_cast<const int64_t*>(map_dev), num_pairs,
+                                (long long)block_bytes, (long long)src_num_blocks,
+                                (long long)dst_num_blocks, ds.err,
+                                reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
 }

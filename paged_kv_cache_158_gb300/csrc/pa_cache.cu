@@ -140,6 +140,48 @@ __global__ void __launch_bounds__(256)
     d[i] = s[i];
 }
 
+// ---- block swap between device and host pools
+// ("【硬核】啃透vLLM源码：从PagedAttention到连续批处理，大模型推理加速24倍的秘密" §三:
+// blocks_to_swap_out / blocks_to_swap_in).  One launch moves every (pair,
+// cache): blockIdx.y = pair, blockIdx.z = cache; blockIdx.x and the threads
+// stride over the block's 16-byte vectors.  One side is host memory reached
+// over the CPU-GPU link (pinned, mapped into the device's address space),
+// so each thread keeps kSwapUnroll independent loads in flight before it
+// stores.
+struct SwapPtrs {
+  const uint4* src[kSwapMaxCaches];
+  uint4* dst[kSwapMaxCaches];
+};
+
+constexpr int kSwapUnroll = 4;
+
+__global__ void __launch_bounds__(256)
+    swap_blocks_kernel(SwapPtrs ptrs, const int64_t* __restrict__ block_mapping, int pair_base,
+                       long long block_vecs, long long src_num_blocks, long long dst_num_blocks,
+                       unsigned int* err) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int pair = pair_base + blockIdx.y;
+  const long long src = block_mapping[2 * pair];
+  const long long dst = block_mapping[2 * pair + 1];
+  if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks) {
+    if (blockIdx.x == 0 && blockIdx.z == 0 && threadIdx.x == 0) atomicOr(err, PA_ERRBIT_COPY);
+    return;
+  }
+  const uint4* s = ptrs.src[blockIdx.z] + src * block_vecs;
+  uint4* d = ptrs.dst[blockIdx.z] + dst * block_vecs;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + (kSwapUnroll - 1) * stride < block_vecs; i += kSwapUnroll * stride) {
+    uint4 t[kSwapUnroll];
+#pragma unroll
+    for (int u = 0; u < kSwapUnroll; ++u) t[u] = s[i + u * stride];
+#pragma unroll
+    for (int u = 0; u < kSwapUnroll; ++u) d[i + u * stride] = t[u];
+  }
+  for (; i < block_vecs; i += stride) d[i] = s[i];
+}
+
 // ---- slot map ("vLLM推理加速深度解读：PagedAttention如何提升10x吞吐量" §2.3)
 __global__ void __launch_bounds__(256)
     slot_mapping_kernel(int64_t* __restrict__ slot_mapping, const int32_t* __restrict__ block_tables,
@@ -275,6 +317,34 @@ cudaError_t launch_copy_blocks(void* const* key_caches, void* const* value_cache
       dim3 grid((unsigned)xblocks, (unsigned)np, (unsigned)(2 * nl));
       const cudaError_t e = launch_pdl(copy_blocks_kernel, grid, dim3(threads), 0, stream, ptrs,
                                        block_mapping, p0, block_vecs, (long long)num_blocks, err);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_swap_blocks(void* const* dst_caches, const void* const* src_caches,
+                               int num_caches, const int64_t* block_mapping, int num_pairs,
+                               long long block_bytes, long long src_num_blocks,
+                               long long dst_num_blocks, unsigned int* err, cudaStream_t stream) {
+  if (num_pairs == 0 || num_caches == 0) return cudaSuccess;
+  const long long block_vecs = block_bytes / 16;
+  const int threads = 256;
+  long long xblocks = (block_vecs + threads * kSwapUnroll - 1) / (threads * kSwapUnroll);
+  if (xblocks > 64) xblocks = 64;
+  for (int c0 = 0; c0 < num_caches; c0 += kSwapMaxCaches) {
+    const int nc = num_caches - c0 < kSwapMaxCaches ? num_caches - c0 : kSwapMaxCaches;
+    SwapPtrs ptrs{};
+    for (int i = 0; i < nc; ++i) {
+      ptrs.src[i] = static_cast<const uint4*>(src_caches[c0 + i]);
+      ptrs.dst[i] = static_cast<uint4*>(dst_caches[c0 + i]);
+    }
+    for (int p0 = 0; p0 < num_pairs; p0 += 65535) {
+      const int np = num_pairs - p0 < 65535 ? num_pairs - p0 : 65535;
+      dim3 grid((unsigned)xblocks, (unsigned)np, (unsigned)nc);
+      const cudaError_t e = launch_pdl(swap_blocks_kernel, grid, dim3(threads), 0, stream, ptrs,
+                                       block_mapping, p0, block_vecs, src_num_blocks,
+                                       dst_num_blocks, err);
       if (e != cudaSuccess) return e;
     }
   }

@@ -16,6 +16,8 @@ constexpr int kMaxSeqsPerLaunch = 1024;
 // Layers handled by one launch of the block-copy kernel (pointer table passed
 // by value as a kernel parameter).
 constexpr int kCopyMaxLayers = 32;
+// Caches handled by one launch of the block-swap kernel.
+constexpr int kSwapMaxCaches = 64;
 
 struct DecodeParams {
   void* out;                  // fp16 [S][H][D]
@@ -78,6 +80,13 @@ cudaError_t launch_copy_blocks(void* const* key_caches, void* const* value_cache
                                const int64_t* block_mapping, int num_pairs, int num_heads,
                                int head_dim, int block_size, int elem_bytes, int num_blocks,
                                unsigned int* err, cudaStream_t stream);
+
+// block_bytes: a multiple of 16; pointers are device addresses (device
+// memory or mapped pinned host memory).
+cudaError_t launch_swap_blocks(void* const* dst_caches, const void* const* src_caches,
+                               int num_caches, const int64_t* block_mapping, int num_pairs,
+                               long long block_bytes, long long src_num_blocks,
+                               long long dst_num_blocks, unsigned int* err, cudaStream_t stream);
 
 cudaError_t launch_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,
                                 int max_blocks, const int32_t* token_seq,

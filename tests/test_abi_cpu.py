@@ -122,3 +122,18 @@ def test_fp8_calls_reject_bad_arguments_before_any_launch():
     assert v(good, good, 32, -1.0, None) == 1
     assert v(good + 8, good, 32, 1.0, None) == 1
     assert v(None, None, 0, 1.0, None) == 0
+
+
+def test_swap_rejects_bad_arguments_before_any_launch():
+    lib = ctypes.CDLL(LIB)
+    vp = ctypes.c_void_p
+    f = lib.pa_swap_blocks
+    f.argtypes = [vp, vp, ctypes.c_int, vp, ctypes.c_int, ctypes.c_size_t, ctypes.c_int64,
+                  ctypes.c_int64, vp]
+    good = 0x10000
+    ptrs = (ctypes.c_void_p * 1)(good)
+    assert f(ptrs, ptrs, 1, good, 2, 24, 8, 8, None) == 1            # block bytes not a multiple of 16
+    assert f(ptrs, ptrs, 1, good, 2, 0, 8, 8, None) == 1
+    assert f(ptrs, ptrs, 1, good, 2, 64, 0, 8, None) == 1           # empty pool
+    assert f(ptrs, ptrs, 1, good + 4, 2, 64, 8, 8, None) == 1       # misaligned mapping
+    assert f(None, None, 0, None, 0, 64, 8, 8, None) == 0           # nothing to do

@@ -1,0 +1,101 @@
+"""GPU parity of the block swap between the device pool and a pinned host
+pool: swap-out and swap-in bit-exact against the oracle, for fp16 and FP8
+caches, with the block mapping in device or pinned host memory; bad ids are
+flagged and skipped; host memory the device cannot reach is refused."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_158_gb300 as pa
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def _clean():
+    pa.pa_check_errors()
+    yield
+    torch.cuda.synchronize()
+
+
+def host_view(t: torch.Tensor) -> np.ndarray:
+    a = t.detach().cpu().contiguous()
+    return a.view(torch.uint8).numpy().reshape(a.shape[0], -1).copy()
+
+
+def pools(rng, layers, nb_dev, nb_host, shape, dtype):
+    dev = []
+    for _ in range(2 * layers):
+        raw = rng.integers(0, 1 << 16, (nb_dev,) + shape, dtype=np.uint16)
+        t = torch.from_numpy(raw.view(np.int16)).to(DEV)
+        dev.append(t.view(torch.float16) if dtype == torch.float16 else t.view(torch.uint8)
+                   .view((nb_dev,) + shape[:-1] + (2 * shape[-1],)))
+    host = [torch.zeros((nb_host,) + tuple(dev[0].shape[1:]), dtype=dev[0].dtype).pin_memory()
+            for _ in range(2 * layers)]
+    return dev, host
+
+
+@pytest.mark.parametrize("dtype,map_on_device", [(torch.float16, True), (torch.uint8, False)])
+def test_swap_out_and_in_bit_exact(dtype, map_on_device):
+    rng = np.random.default_rng(7 if map_on_device else 8)
+    layers, nb_dev, nb_host = 3, 40, 25
+    shape = (4, 16, 64)                      # H, B, D (uint8 caches: D doubles)
+    dev, host = pools(rng, layers, nb_dev, nb_host, shape, dtype)
+    ref_dev = [host_view(t) for t in dev]
+    ref_host = [host_view(t) for t in host]
+
+    out_map = np.stack([rng.choice(nb_dev, 12, replace=False), rng.choice(nb_host, 12, replace=False)],
+                       axis=1).astype(np.int64)
+    m = torch.from_numpy(out_map)
+    m = m.to(DEV) if map_on_device else m.pin_memory()
+    pa.pa_swap_blocks(host, dev, m)
+    torch.cuda.synchronize()
+    assert oracle.swap_blocks(ref_host, ref_dev, out_map) == 0
+    for t, r in zip(host, ref_host):
+        assert np.array_equal(host_view(t), r)
+
+    # swap in to other device blocks (the ones not swapped out)
+    free = np.setdiff1d(np.arange(nb_dev), out_map[:, 0])
+    in_map = np.stack([out_map[:, 1], rng.choice(free, 12, replace=False)], axis=1).astype(np.int64)
+    m = torch.from_numpy(in_map)
+    m = m.to(DEV) if map_on_device else m.pin_memory()
+    pa.pa_swap_blocks(dev, host, m)
+    torch.cuda.synchronize()
+    assert oracle.swap_blocks(ref_dev, ref_host, in_map) == 0
+    for t, r in zip(dev, ref_dev):
+        assert np.array_equal(host_view(t), r)
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+def test_swap_bad_id_is_flagged_and_skipped():
+    rng = np.random.default_rng(9)
+    dev, host = pools(rng, 1, 10, 6, (2, 8, 64), torch.float16)
+    ref_dev = [host_view(t) for t in dev]
+    ref_host = [host_view(t) for t in host]
+    mapping = np.array([[1, 0], [10, 1], [2, 6], [3, 5]], dtype=np.int64)
+    pa.pa_swap_blocks(host, dev, torch.from_numpy(mapping).to(DEV))
+    st, bits = pa.pa_check_errors()
+    assert st == pa.PA_ERR_OUT_OF_RANGE and bits == pa.PA_ERRBIT_COPY
+    assert oracle.swap_blocks(ref_host, ref_dev, mapping) == -1
+    for t, r in zip(host, ref_host):
+        assert np.array_equal(host_view(t), r)
+
+
+def test_swap_refuses_pageable_host_memory():
+    dev = torch.zeros((4, 2, 8, 64), dtype=torch.float16, device=DEV)
+    pageable = np.zeros((4, 2, 8, 64), dtype=np.float16)
+    mapping = torch.tensor([[0, 1]], dtype=torch.int64, device=DEV)
+    lib = ctypes.CDLL(pa.LIB_PATH)
+    vp = ctypes.c_void_p
+    lib.pa_swap_blocks.argtypes = [vp, vp, ctypes.c_int, vp, ctypes.c_int, ctypes.c_size_t,
+                                   ctypes.c_int64, ctypes.c_int64, vp]
+    dst = (ctypes.c_void_p * 1)(pageable.ctypes.data)
+    src = (ctypes.c_void_p * 1)(dev.data_ptr())
+    assert lib.pa_swap_blocks(dst, src, 1, mapping.data_ptr(), 1, 2 * 8 * 64 * 2, 4, 4, None) == \
+        pa.PA_ERR_INVALID_ARG
+    with pytest.raises(ValueError):
+        pa.pa_swap_blocks([torch.zeros_like(dev).cpu()], [dev], mapping)

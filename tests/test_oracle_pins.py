@@ -408,3 +408,26 @@ def test_generator_matches_splitmix64_definition():
     assert np.array_equal(vals, np.array(expect, dtype=np.uint16))
     z = synth.normal_bank(7)
     assert abs(z.mean()) < 2e-3 and abs(z.std() - 1) < 2e-3
+
+
+def test_swap_blocks_matches_numpy():
+    """Swap out then in between pools of different sizes (block-id spaces) and
+    element types: each destination block equals its source block byte for byte."""
+    rng = np.random.default_rng(11)
+    dev = [rng.integers(0, 1 << 16, (12, 2, 4, 8), dtype=np.uint16) for _ in range(3)]
+    host = [np.zeros((7, 2, 4, 8), dtype=np.uint16) for _ in range(3)]
+    out_map = np.array([[3, 0], [11, 6], [0, 2]], dtype=np.int64)
+    assert oracle.swap_blocks(host, dev, out_map) == 0
+    for c in range(3):
+        assert np.array_equal(host[c][[0, 6, 2]], dev[c][[3, 11, 0]])
+        assert not host[c][[1, 3, 4, 5]].any()
+    dev2 = [np.zeros_like(d) for d in dev]
+    in_map = np.array([[6, 1], [0, 9]], dtype=np.int64)
+    assert oracle.swap_blocks(dev2, host, in_map) == 0
+    for c in range(3):
+        assert np.array_equal(dev2[c][1], dev[c][11]) and np.array_equal(dev2[c][9], dev[c][3])
+    # byte pools (FP8 caches) and out-of-range ids
+    a = rng.integers(0, 256, (5, 64), dtype=np.uint8)
+    b = np.zeros((4, 64), dtype=np.uint8)
+    assert oracle.swap_blocks([b], [a], np.array([[4, 3], [5, 0], [1, 4]], np.int64)) == -1
+    assert np.array_equal(b[3], a[4]) and not b[0].any()
