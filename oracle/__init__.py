@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
     L.oracle_swap_blocks.argtypes = [vp, vp, i32, vp, i32, ctypes.c_size_t, ctypes.c_int64,
                                      ctypes.c_int64]
     L.oracle_swap_blocks.restype = i32
+    L.oracle_prefill.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, f64]
+    L.oracle_prefill.restype = i32
     L.oracle_num_threads.argtypes = []
     L.oracle_num_threads.restype = i32
     _LIB = L
@@ -234,6 +236,27 @@ def swap_blocks(dst_pools, src_pools, block_mapping) -> int:
     sp = (ctypes.c_void_p * n)(*[a.ctypes.data for a in src_pools])
     return lib().oracle_swap_blocks(dp, sp, n, m.ctypes.data, m.shape[0], bb,
                                     src_pools[0].shape[0], dst_pools[0].shape[0])
+
+
+def prefill(query, key_cache, value_cache, block_tables, context_lens, query_start, scale: float,
+            want64: bool = True):
+    """Multi-query paged attention: query / out [total_q, H, D]; query_start int32 [S+1].
+    Returns (out16, out64 or None, status)."""
+    q = _u16(query)
+    kc, vc = _u16(key_cache), _u16(value_cache)
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    qs = _c(query_start, np.int32)
+    TQ, H, D = q.shape
+    NB, H2, B, D2 = kc.shape
+    assert H2 == H and D2 == D and qs.shape[0] == cl.shape[0] + 1 and qs[-1] == TQ
+    out16 = np.zeros((TQ, H, D), dtype=np.uint16)
+    out64 = np.zeros((TQ, H, D), dtype=np.float64) if want64 else None
+    rc = lib().oracle_prefill(out16.ctypes.data, out64.ctypes.data if want64 else None,
+                              q.ctypes.data, kc.ctypes.data, vc.ctypes.data, bt.ctypes.data,
+                              bt.shape[1], cl.ctypes.data, qs.ctypes.data, cl.shape[0], H, D, B,
+                              NB, float(scale))
+    return out16, out64, rc
 
 
 def num_threads() -> int:

@@ -244,6 +244,77 @@ int oracle_decode(uint16_t* out16, double* out64, const uint16_t* query,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Multi-query paged attention: a chunk of new query tokens per sequence    */
+/* (chunked prefill; decode is the one-token case; prefill and decode        */
+/* sequences share one batch) ["vLLM推理加速深度解读：PagedAttention如何提升10x吞吐量" */
+/* §4.3: prefill and decode in the same batch; "深入解析LLM推理引擎：从PagedAttention  */
+/* 到调度优化" §3.3: attention reads K/V through the block table].           */
+/* Sequence s has q_len = query_start[s+1] - query_start[s] new tokens, the  */
+/* last q_len of its context_lens[s] tokens (their K/V already written);     */
+/* new token j sits at position p = c_s - q_len + j and attends causally to  */
+/* positions 0..p:                                                            */
+/*   out[query_start[s]+j, h] = softmax_i<=p(scale q.K_i) V.                 */
+/* query / out: [total_query_tokens][num_heads][head_dim].                    */
+
+int oracle_prefill(uint16_t* out16, double* out64, const uint16_t* query,
+                   const uint16_t* key_cache, const uint16_t* value_cache,
+                   const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                   const int32_t* query_start, int num_seqs, int num_heads, int head_dim,
+                   int block_size, int num_blocks, double scale) {
+  int bad = 0;
+  const long pairs = (long)num_seqs * num_heads;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (long sh = 0; sh < pairs; ++sh) {
+    const int s = (int)(sh / num_heads);
+    const int h = (int)(sh % num_heads);
+    const int c = context_lens[s];
+    const int q0 = query_start[s];
+    const int q_len = query_start[s + 1] - q0;
+    int ok = (c >= 0) && (c <= max_blocks * block_size) && (q_len >= 0) && (q_len <= c);
+    double* x = (double*)malloc(sizeof(double) * (size_t)(c > 0 ? c : 1));
+    double* qd = (double*)malloc(sizeof(double) * (size_t)head_dim);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)head_dim);
+    for (int j = 0; ok && j < q_len; ++j) {
+      const int p = c - q_len + j;
+      const size_t row = ((size_t)(q0 + j) * num_heads + h) * head_dim;
+      for (int d = 0; d < head_dim; ++d) qd[d] = oracle_half_to_double(query[row + d]);
+      for (int i = 0; ok && i <= p; ++i) {
+        const int phys = block_tables[(size_t)s * max_blocks + i / block_size];
+        if (phys < 0 || phys >= num_blocks) { ok = 0; break; }
+        const uint16_t* k =
+            key_cache + (((size_t)phys * num_heads + h) * block_size + i % block_size) * head_dim;
+        double dot = 0.0;
+        for (int d = 0; d < head_dim; ++d) dot += qd[d] * oracle_half_to_double(k[d]);
+        x[i] = dot * scale;
+      }
+      if (!ok) break;
+      double m = x[0];
+      for (int i = 1; i <= p; ++i) if (x[i] > m) m = x[i];
+      double denom = 0.0;
+      for (int d = 0; d < head_dim; ++d) acc[d] = 0.0;
+      for (int i = 0; i <= p; ++i) {
+        const double w = exp(x[i] - m);
+        const int phys = block_tables[(size_t)s * max_blocks + i / block_size];
+        const uint16_t* v =
+            value_cache + (((size_t)phys * num_heads + h) * block_size + i % block_size) * head_dim;
+        denom += w;
+        for (int d = 0; d < head_dim; ++d) acc[d] += w * oracle_half_to_double(v[d]);
+      }
+      for (int d = 0; d < head_dim; ++d) {
+        const double o = acc[d] / denom;
+        if (out64) out64[row + d] = o;
+        if (out16) out16[row + d] = oracle_double_to_half(o);
+      }
+    }
+    if (!ok) bad |= 1;
+    free(x);
+    free(qd);
+    free(acc);
+  }
+  return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* FP8 KV cache ["vLLM推理加速深度解读：PagedAttention如何提升10x吞吐量" §3.3 names */
 /* FP8 support; the format and scaling are not given there].  Reading taken:  */
 /* OCP FP8 E4M3 ("e4m3fn": 1 sign, 4 exponent bits with bias 7, 3 fraction    */
