@@ -52,11 +52,17 @@
 //  * The summation order depends only on logical token positions, so the
 //    result is bit-identical under any relabelling of physical blocks.
 //  * FP8 caches (F8: one E4M3 byte per element, one scale per cache tensor)
-//    use the same lane layout: a lane loads its 8 codes (8 bytes) of a row,
-//    widens them to fp16 pairs in registers (E4M3 values are exact in fp16),
-//    and runs the fp16 arithmetic above.  The key scale is folded into the
-//    logit scale and the value scale multiplies the CTA's merged output, so
-//    the cache is read once at one byte per element.
+//    read a token's row in half the bytes, so per byte of HBM the kernel
+//    does twice the arithmetic; the fp16 layout above is then bound by
+//    instruction issue, not by HBM.  The FP8 layout cuts the instructions
+//    per token: a lane owns 16 dimensions (16 codes = 16 bytes), a chunk is
+//    32 tokens (it spans 32/B physical blocks, one bulk copy per block for K
+//    and for V), codes are widened to fp16 pairs in registers (exact), and
+//    p.V runs as fp16 x fp16 -> fp32 fused multiply-adds with the softmax
+//    weights rounded to fp16 (relative error <= 2^-11 per weight; the
+//    denominator sums the same rounded weights).  The key scale is folded
+//    into the logit scale and the value scale multiplies the CTA's merged
+//    output.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -75,8 +81,13 @@ struct DecodeTraits {
   static constexpr int NW = 4;                // warps per CTA
   static constexpr int NST = 3;               // stages per warp
   static constexpr int THREADS = NW * 32;
-  static constexpr int TC = B < 16 ? B : 16;  // tokens per chunk (inside one block)
-  static constexpr int LR = D / 8;            // lanes per token row (16 bytes each)
+  // Tokens per chunk: fp16 chunks lie inside one block; FP8 chunks are 16
+  // tokens and span BPC = 16 / B blocks when B < 16 (partitions are
+  // multiples of 32 tokens, so a chunk never straddles a partition).
+  static constexpr int TC = F8 ? 16 : (B < 16 ? B : 16);
+  static constexpr int BPC = TC > B ? TC / B : 1;  // blocks per chunk
+  static constexpr int DPL = F8 ? 16 : 8;     // dimensions per lane (16 bytes either way)
+  static constexpr int LR = D / DPL;          // lanes per token row
   static constexpr int RI = 32 / LR;          // token rows per warp-wide load
   static constexpr int TPL = TC / RI;         // token rows per lane
   static constexpr int DUP = LR / TPL;        // lanes sharing a logit after the reduction
@@ -91,7 +102,7 @@ struct DecodeTraits {
   // Fixed part of the dynamic shared memory (bytes), in layout order.
   static constexpr size_t kStages = size_t(NW) * NST * STAGE_BYTES;
   static constexpr size_t kBars = size_t(NW) * NST * 8;
-  static constexpr size_t kP = size_t(NW) * TC * 4;
+  static constexpr size_t kP = size_t(NW) * TC * 4;  // softmax weights (fp32, or fp16 for F8)
   static constexpr int MS = D + 4;            // merge stride (floats): o[D], m, l, pad
   static constexpr size_t kMerge = 2 * size_t(NW) * MS * 4;
   static constexpr size_t kMisc = 16 * 4;     // item ring, warp sums, flags
@@ -147,62 +158,103 @@ __device__ __forceinline__ ItemInfo locate_item(int item, const int* cum, const 
 }
 
 // Chunks of an item that warp `warp` processes (chunks warp, warp+NW, ...).
-template <int D, int B>
+template <int D, int B, bool F8>
 __device__ __forceinline__ int warp_chunks(const ItemInfo& it, int warp) {
-  using T = DecodeTraits<D, B>;  // chunking does not depend on the element type
+  using T = DecodeTraits<D, B, F8>;
   const int n = (it.t_end - it.t_begin + T::TC - 1) / T::TC;
   return warp < n ? (n - 1 - warp) / T::NW + 1 : 0;
 }
 
-// Issues the bulk copies of one chunk (K rows and V rows) into a stage.
+// Physical ids of the blocks of chunk `chunk` of an item, from the item's
+// block-table slice in shared memory (-1 for blocks past the live rows).
 template <int D, int B, bool F8>
-__device__ __forceinline__ void issue_chunk(const DecodeParams& a, const ItemInfo& it, int phys,
+__device__ __forceinline__ void chunk_ids(int (&phys)[DecodeTraits<D, B, F8>::BPC], const int* bt,
+                                          const ItemInfo& it, int chunk) {
+  using T = DecodeTraits<D, B, F8>;
+  const int t0 = it.t_begin + chunk * T::TC;
+#pragma unroll
+  for (int b = 0; b < T::BPC; ++b) phys[b] = t0 + b * B < it.t_end ? bt[t0 / B + b - it.blk0] : -1;
+}
+
+// True when every block of the chunk that holds live rows has a valid id.
+template <int D, int B, bool F8>
+__device__ __forceinline__ bool chunk_ids_ok(const DecodeParams& a, const int (&phys)[DecodeTraits<D, B, F8>::BPC],
+                                             int rows) {
+  bool ok = true;
+#pragma unroll
+  for (int b = 0; b < DecodeTraits<D, B, F8>::BPC; ++b)
+    if (b * B < rows && (phys[b] < 0 || phys[b] >= a.num_blocks)) ok = false;
+  return ok;
+}
+
+// Issues the bulk copies of one chunk into a stage: for each block of the
+// chunk with live rows, its K rows and its V rows (contiguous in the
+// [NB][H][B][D] layout); only live rows are copied.
+template <int D, int B, bool F8>
+__device__ __forceinline__ void issue_chunk(const DecodeParams& a, const ItemInfo& it,
+                                            const int (&phys)[DecodeTraits<D, B, F8>::BPC],
                                             int chunk, unsigned char* stage, uint32_t bar,
                                             uint64_t policy) {
   using T = DecodeTraits<D, B, F8>;
   const int t0 = it.t_begin + chunk * T::TC;
   const int rows = min(T::TC, it.t_end - t0);
-  if (phys < 0 || phys >= a.num_blocks) {
+  if (rows <= 0) {  // not a chunk of this item (cannot happen): complete the phase empty
+    mbar_arrive(bar);
+    return;
+  }
+  if (!chunk_ids_ok<D, B, F8>(a, phys, rows)) {
     atomicOr(a.err, PA_ERRBIT_BLOCK_ID);
     mbar_arrive(bar);  // completes the phase with no data; the chunk is skipped
     return;
   }
-  const size_t off = (((size_t)phys * a.num_heads + it.h) * B + (t0 % B)) * D * T::ELEM;
-  const uint32_t bytes = (uint32_t)rows * D * T::ELEM;
-  mbar_arrive_expect_tx(bar, 2 * bytes);
-  bulk_g2s_hint(smem_u32(stage), static_cast<const unsigned char*>(a.key_cache) + off, bytes, bar,
-                policy);
-  bulk_g2s_hint(smem_u32(stage + T::CHUNK_BYTES),
-                static_cast<const unsigned char*>(a.value_cache) + off, bytes, bar, policy);
+  mbar_arrive_expect_tx(bar, 2u * (uint32_t)rows * D * T::ELEM);
+#pragma unroll
+  for (int b = 0; b < T::BPC; ++b) {
+    const int r = min(B, rows - b * B);
+    if (r <= 0) break;
+    const size_t off = (((size_t)phys[b] * a.num_heads + it.h) * B + (t0 % B)) * D * T::ELEM;
+    const uint32_t bytes = (uint32_t)r * D * T::ELEM;
+    const int soff = b * B * D * T::ELEM;
+    bulk_g2s_hint(smem_u32(stage + soff), static_cast<const unsigned char*>(a.key_cache) + off,
+                  bytes, bar, policy);
+    bulk_g2s_hint(smem_u32(stage + T::CHUNK_BYTES + soff),
+                  static_cast<const unsigned char*>(a.value_cache) + off, bytes, bar, policy);
+  }
 }
 
-// A lane's 8 elements of cache row t in a stage, as 4 packed fp16 pairs.
+// A lane's query slice: DPL fp16 values (16 or 32 bytes).
+template <int DPL>
+struct QSlice {
+  uint4 v[DPL / 8];
+};
+
+// Partial dot of the lane's query slice with its slice of cache row t.
 template <int D, bool F8>
-__device__ __forceinline__ uint4 load_row8(const unsigned char* rows, int t, int cidx) {
+__device__ __forceinline__ float row_dot(const QSlice<F8 ? 16 : 8>& q, const unsigned char* rows,
+                                         int t, int cidx) {
   if constexpr (F8) {
-    return e4m3x8_to_f16x8(lds64(rows + t * D + 8 * cidx));
+    const uint4 c = lds128(rows + t * D + 16 * cidx);
+    const float a = dot8_f16(q.v[0], e4m3x8_to_f16x8(make_uint2(c.x, c.y)));
+    return a + dot8_f16(q.v[1], e4m3x8_to_f16x8(make_uint2(c.z, c.w)));
   } else {
-    return lds128(rows + (t * D + 8 * cidx) * 2);
+    return dot8_f16(q.v[0], lds128(rows + (t * D + 8 * cidx) * 2));
   }
 }
 
 // One chunk for one warp: logits, online-softmax update, p.V accumulation.
 template <int D, int B, bool F8, bool FULL>
 __device__ __forceinline__ void process_chunk(const unsigned char* Ks, const unsigned char* Vs,
-                                              int rows, const uint4& q, float scale_log2,
-                                              float* p_w, int lane, float& m, float& l,
-                                              float (&o)[8]) {
+                                              int rows, const QSlice<DecodeTraits<D, B, F8>::DPL>& q,
+                                              float scale_log2, float* p_w, int lane, float& m,
+                                              float& l, float (&o)[DecodeTraits<D, B, F8>::DPL]) {
   using T = DecodeTraits<D, B, F8>;
-  const int cidx = lane % T::LR;  // which 8 dimensions
+  const int cidx = lane % T::LR;  // which DPL dimensions
   const int r = lane / T::LR;     // which row group
 
-  // Partial dots over this lane's 8 dimensions for its TPL rows.
+  // Partial dots over this lane's dimensions for its TPL rows.
   float v[T::TPL];
 #pragma unroll
-  for (int k = 0; k < T::TPL; ++k) {
-    const int t = r + T::RI * k;
-    v[k] = dot8_f16(q, load_row8<D, F8>(Ks, t, cidx));
-  }
+  for (int k = 0; k < T::TPL; ++k) v[k] = row_dot<D, F8>(q, Ks, r + T::RI * k, cidx);
   // Reduce-scatter over the LR lanes of the row group: at each halving step a
   // lane keeps one half of its values and adds its partner's copy of it.
 #pragma unroll
@@ -217,7 +269,6 @@ __device__ __forceinline__ void process_chunk(const unsigned char* Ks, const uns
   }
 #pragma unroll
   for (int msk = T::DUP / 2; msk >= 1; msk >>= 1) v[0] += __shfl_xor_sync(kFullMask, v[0], msk);
-
   const int kl = cidx / T::DUP;          // this lane's logit: row r + RI*kl
   const int tl = r + T::RI * kl;
   float x = v[0] * scale_log2;
@@ -228,31 +279,74 @@ __device__ __forceinline__ void process_chunk(const unsigned char* Ks, const uns
   for (int msk = T::DUP; msk < 32; msk <<= 1) cm = fmaxf(cm, __shfl_xor_sync(kFullMask, cm, msk));
   const float m_new = fmaxf(m, cm);
   const float alpha = exp2_approx(m - m_new);  // 0 on the first chunk (m = -inf)
-  const float pv = exp2_approx(x - m_new);     // 0 for masked rows
+  float pv = exp2_approx(x - m_new);           // 0 for masked rows
+  if constexpr (F8) {
+    // The weight p.V uses, rounded to fp16; the denominator sums the same value.
+    const __half ph = __float2half_rn(pv);
+    pv = __half2float(ph);
+    if ((cidx % T::DUP) == 0)
+      reinterpret_cast<__half*>(p_w)[r * T::TPL + kl] = ph;
+  } else {
+    if ((cidx % T::DUP) == 0) p_w[r * T::TPL + kl] = pv;
+  }
   float ps = pv;
 #pragma unroll
   for (int msk = T::DUP; msk < 32; msk <<= 1) ps += __shfl_xor_sync(kFullMask, ps, msk);
   l = l * alpha + ps;
   m = m_new;
-
-  if ((cidx % T::DUP) == 0) p_w[r * T::TPL + kl] = pv;
   __syncwarp();
-  float pk[T::TPL];
+  if (alpha != 1.f) {  // warp-uniform; skipping a multiply by 1 changes no bit
 #pragma unroll
-  for (int k = 0; k < T::TPL; ++k) pk[k] = p_w[r * T::TPL + k];
+    for (int i = 0; i < T::DPL; ++i) o[i] *= alpha;
+  }
+
+  if constexpr (F8) {
+    // The row group's TPL fp16 weights, contiguous in shared memory.
+    static_assert(T::TPL == 2 || T::TPL == 4 || T::TPL == 8, "FP8 weight load");
+    uint32_t pk[T::TPL / 2];
+    const __half* pw = reinterpret_cast<const __half*>(p_w) + r * T::TPL;
+    if constexpr (T::TPL == 8) {
+      const uint4 w4 = lds128(pw);
+      pk[0] = w4.x;
+      pk[1] = w4.y;
+      pk[2] = w4.z;
+      pk[3] = w4.w;
+    } else if constexpr (T::TPL == 4) {
+      const uint2 w2 = lds64(pw);
+      pk[0] = w2.x;
+      pk[1] = w2.y;
+    } else {
+      pk[0] = *reinterpret_cast<const uint32_t*>(pw);
+    }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) o[i] *= alpha;
+    for (int k = 0; k < T::TPL; ++k) {
+      const int t = r + T::RI * k;
+      if (FULL || t < rows) {
+        const uint16_t p16 = (uint16_t)(pk[k / 2] >> (16 * (k & 1)));
+        const uint4 c = lds128(Vs + t * D + 16 * cidx);
+        const uint4 h0 = e4m3x8_to_f16x8(make_uint2(c.x, c.y));
+        const uint4 h1 = e4m3x8_to_f16x8(make_uint2(c.z, c.w));
+        const uint32_t w[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
 #pragma unroll
-  for (int k = 0; k < T::TPL; ++k) {
-    const int t = r + T::RI * k;
-    if (FULL || t < rows) {
-      const uint4 vv = load_row8<D, F8>(Vs, t, cidx);
-      const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+        for (int j = 0; j < 8; ++j) fma2_f16_f32(p16, w[j], o[2 * j], o[2 * j + 1]);
+      }
+    }
+  } else {
+    float pk[T::TPL];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f = half2_bits_to_float2(w[j]);
-        o[2 * j] = fmaf(pk[k], f.x, o[2 * j]);
-        o[2 * j + 1] = fmaf(pk[k], f.y, o[2 * j + 1]);
+    for (int k = 0; k < T::TPL; ++k) pk[k] = p_w[r * T::TPL + k];
+#pragma unroll
+    for (int k = 0; k < T::TPL; ++k) {
+      const int t = r + T::RI * k;
+      if (FULL || t < rows) {
+        const uint4 vv = lds128(Vs + (t * D + 8 * cidx) * 2);
+        const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = half2_bits_to_float2(w[j]);
+          o[2 * j] = fmaf(pk[k], f.x, o[2 * j]);
+          o[2 * j + 1] = fmaf(pk[k], f.y, o[2 * j + 1]);
+        }
       }
     }
   }
@@ -368,12 +462,13 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS)
 
   // The first item's first copies, still before the wait.
   {
-    const int n0 = warp_chunks<D, B>(it, warp);
+    const int n0 = warp_chunks<D, B, F8>(it, warp);
     if (lane == 0) {
       for (; (int)iss < n0 && iss < (uint32_t)T::NST; ++iss) {
         const int chunk = warp + (int)iss * T::NW;
-        const int phys = bt_s[(it.t_begin + chunk * T::TC) / B - it.blk0];
-        issue_chunk<D, B, F8>(a, it, phys, chunk, my_stages + iss * T::STAGE_BYTES,
+        int ph[T::BPC];
+        chunk_ids<D, B, F8>(ph, bt_s, it, chunk);
+        issue_chunk<D, B, F8>(a, it, ph, chunk, my_stages + iss * T::STAGE_BYTES,
                               smem_u32(&my_bars[iss]), policy);
       }
     }
@@ -400,17 +495,25 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS)
 
     const int* bt = bt_s + buf * bt_cap;
     const size_t sh = (size_t)(a.seq_begin + it.s) * H + it.h;
-    const int n_my = warp_chunks<D, B>(it, warp);
-    const int n_nx = has_next ? warp_chunks<D, B>(nx, warp) : 0;
+    const int n_my = warp_chunks<D, B, F8>(it, warp);
+    const int n_nx = has_next ? warp_chunks<D, B, F8>(nx, warp) : 0;
     const uint32_t base = u;
 
-    // Block ids of this warp's first chunks of the next item (lane 0 only).
-    int nxp0 = -1, nxp1 = -1, nxp2 = -1;
+    // Block ids of this warp's first NST chunks of the next item (lane 0 only).
+    int nxp[T::NST][T::BPC];
+#pragma unroll
+    for (int j = 0; j < T::NST; ++j)
+#pragma unroll
+      for (int b = 0; b < T::BPC; ++b) nxp[j][b] = -1;
     if (lane == 0 && n_nx > 0) {
       const int32_t* row = a.block_tables + (size_t)(a.seq_begin + nx.s) * a.max_blocks;
-      nxp0 = row[(nx.t_begin + warp * T::TC) / B];
-      if (n_nx > 1) nxp1 = row[(nx.t_begin + (warp + T::NW) * T::TC) / B];
-      if (n_nx > 2) nxp2 = row[(nx.t_begin + (warp + 2 * T::NW) * T::TC) / B];
+#pragma unroll
+      for (int j = 0; j < T::NST; ++j) {
+        const int t0 = nx.t_begin + (warp + j * T::NW) * T::TC;
+#pragma unroll
+        for (int b = 0; b < T::BPC; ++b)
+          if (j < n_nx && t0 + b * B < nx.t_end) nxp[j][b] = row[t0 / B + b];
+      }
     }
     // Fill free stages: the rest of this item's chunks, then the next item's.
     auto issue_upto = [&]() {
@@ -422,12 +525,16 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS)
           const uint32_t bar = smem_u32(&my_bars[st]);
           if (k < n_my) {
             const int chunk = warp + k * T::NW;
-            const int phys = bt[(it.t_begin + chunk * T::TC) / B - it.blk0];
-            issue_chunk<D, B, F8>(a, it, phys, chunk, stage, bar, policy);
+            int ph[T::BPC];
+            chunk_ids<D, B, F8>(ph, bt, it, chunk);
+            issue_chunk<D, B, F8>(a, it, ph, chunk, stage, bar, policy);
           } else if (k - n_my < n_nx) {
             const int j = k - n_my;
-            const int phys = j == 0 ? nxp0 : (j == 1 ? nxp1 : nxp2);
-            issue_chunk<D, B, F8>(a, nx, phys, warp + j * T::NW, stage, bar, policy);
+            int ph[T::BPC];
+#pragma unroll
+            for (int b = 0; b < T::BPC; ++b)
+              ph[b] = j == 0 ? nxp[0][b] : (j == 1 ? nxp[1][b] : nxp[2][b]);
+            issue_chunk<D, B, F8>(a, nx, ph, warp + j * T::NW, stage, bar, policy);
           } else {
             break;
           }
@@ -438,12 +545,15 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS)
     };
     issue_upto();
 
-    const uint4 q = *reinterpret_cast<const uint4*>(static_cast<const __half*>(a.query) +
-                                                    sh * D + 8 * cidx);
-    float m = -INFINITY, l = 0.f;
-    float o[8];
+    QSlice<T::DPL> q;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = 0.f;
+    for (int j = 0; j < T::DPL / 8; ++j)
+      q.v[j] = *reinterpret_cast<const uint4*>(static_cast<const __half*>(a.query) + sh * D +
+                                               T::DPL * cidx + 8 * j);
+    float m = -INFINITY, l = 0.f;
+    float o[T::DPL];
+#pragma unroll
+    for (int i = 0; i < T::DPL; ++i) o[i] = 0.f;
 
     for (int i = 0; i < n_my; ++i) {
       const int st = u % T::NST;
@@ -464,8 +574,9 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS)
       const int chunk = warp + i * T::NW;
       const int t0 = it.t_begin + chunk * T::TC;
       const int rows = min(T::TC, it.t_end - t0);
-      const int phys = bt[t0 / B - it.blk0];
-      if (phys >= 0 && phys < a.num_blocks) {
+      int ph[T::BPC];
+      chunk_ids<D, B, F8>(ph, bt, it, chunk);
+      if (rows > 0 && chunk_ids_ok<D, B, F8>(a, ph, rows)) {
         const unsigned char* Ks = my_stages + st * T::STAGE_BYTES;
         if (rows == T::TC)
           process_chunk<D, B, F8, true>(Ks, Ks + T::CHUNK_BYTES, rows, q, a.scale_log2, my_p, lane,
@@ -483,12 +594,14 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS)
 #pragma unroll
     for (int msk = T::LR; msk < 32; msk <<= 1) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] += __shfl_xor_sync(kFullMask, o[i], msk);
+      for (int i = 0; i < T::DPL; ++i) o[i] += __shfl_xor_sync(kFullMask, o[i], msk);
     }
     float* mw = merge + (iter & 1) * T::NW * T::MS + warp * T::MS;
     if (rgrp == 0) {
-      reinterpret_cast<float4*>(mw + 8 * cidx)[0] = make_float4(o[0], o[1], o[2], o[3]);
-      reinterpret_cast<float4*>(mw + 8 * cidx)[1] = make_float4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+      for (int i = 0; i < T::DPL / 4; ++i)
+        reinterpret_cast<float4*>(mw + T::DPL * cidx)[i] =
+            make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
     }
     if (lane == 0) {
       mw[D] = m;

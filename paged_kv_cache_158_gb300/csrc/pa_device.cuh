@@ -160,6 +160,19 @@ __device__ __forceinline__ float dot8_f16(const uint4& a, const uint4& b) {
   return acc;
 }
 
+// o0 += p * lo(v), o1 += p * hi(v): fp16 x fp16 products added in fp32 with
+// one rounding each (the products are exact in fp32).  p: fp16 bits.
+__device__ __forceinline__ void fma2_f16_f32(uint16_t p, uint32_t v, float& o0, float& o1) {
+  asm("{\n"
+      "  .reg .f16 v0, v1;\n"
+      "  mov.b32 {v0, v1}, %2;\n"
+      "  fma.rn.f32.f16 %0, %3, v0, %0;\n"
+      "  fma.rn.f32.f16 %1, %3, v1, %1;\n"
+      "}\n"
+      : "+f"(o0), "+f"(o1)
+      : "r"(v), "h"(p));
+}
+
 __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t u) {
   __half2 h;
   *reinterpret_cast<uint32_t*>(&h) = u;
