@@ -52,8 +52,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--eager", action="store_true", help="time eager launches only (no CUDA graph)")
-    ap.add_argument("--op", choices=["step", "swap"], default="step",
-                    help="swap: time block swap-out/in of whole sequences to pinned host memory")
+    ap.add_argument("--op", choices=["step", "swap", "prefill"], default="step",
+                    help="swap: time block swap-out/in of whole sequences to pinned host memory; "
+                         "prefill: time multi-query paged attention on the 7B-shaped chunked prefill")
     ap.add_argument("--kv-dtype", choices=["fp16", "fp8"], default="fp16",
                     help="KV-cache element type (fp8: E4M3 codes with per-tensor scales)")
     return ap.parse_args()
@@ -495,6 +496,78 @@ def run_swap(args):
     }
 
 
+def prefill_flops(w) -> int:
+    """Algorithmic FLOPs of a chunked-prefill call: a new token at position p costs
+    4*D*(p+1) FLOPs per head (2*D for each of its p+1 dot products q.K_i and 2*D for each
+    of the p+1 accumulations p_i V_i); masked work is not counted."""
+    tot = 0
+    for ql, c in zip(w.extra["q_lens"], w.context_lens):
+        ql, c = int(ql), int(c)
+        pos = np.arange(c - ql, c, dtype=np.int64)
+        tot += int((pos + 1).sum())
+    return 4 * w.head_dim * w.num_heads * tot
+
+
+def run_prefill_bench(args):
+    import torch
+
+    import paged_kv_cache_158_gb300 as pa
+    from workloads import gpu
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = configs.prefill_7b()
+    dv = gpu.materialize_prefill(w, dev)
+    tq = int(np.sum(w.extra["q_lens"]))
+    out = torch.empty((tq, w.num_heads, w.head_dim), dtype=torch.float16, device=dev)
+    max_q = int(max(w.extra["q_lens"]))
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        pa.pa_prefill(out, dv["query"], dv["key_cache"], dv["value_cache"], dv["block_tables"],
+                      dv["context_lens"], dv["query_start"], w.scale, max_q)
+
+    K, W = max(3, min(args.steps, 200)), max(3, args.warmup)
+    for _ in range(W):
+        call()
+    torch.cuda.synchronize(dev)
+    status, bits = pa.pa_check_errors()
+    if status != pa.PA_OK:
+        raise RuntimeError(f"device error word: {pa.pa_status_string(status)} 0x{bits:x}")
+    clocks = ClockSampler(None)
+    clocks.start()
+    time.sleep(0.3)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    sec = a.elapsed_time(b) / K * 1e-3
+    flops = prefill_flops(w)
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, kind = float(json.load(f)["bf16_tflops"]), "measured (bf16 burst; fp16 runs at the bf16 rate)"
+    except (OSError, KeyError, ValueError):
+        peak, kind = 1900.0, "fallback"
+    kv_bytes = int(np.sum(w.context_lens)) * w.num_heads * w.head_dim * 2 * 2
+    tflops = flops / sec / 1e12
+    return {
+        "metric": "multi-query paged attention TFLOP/s (causal algorithmic FLOPs over call time)",
+        "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": W,
+        "ms_per_call": round(sec * 1e3, 4), "higher_is_better": True, "dtype": "f16 in, f32 accumulate",
+        "data": "synthetic", "config": {"workload": w.name, "num_seqs": w.num_seqs,
+                                        "num_heads": w.num_heads, "head_dim": w.head_dim,
+                                        "block_size": w.block_size, "query_tokens": tq,
+                                        "context_tokens": int(np.sum(w.context_lens))},
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak, "peak_kind": kind,
+                     "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "flops_per_call": flops,
+                     "kv_bytes_per_call": kv_bytes,
+                     "kv_gbs": round(kv_bytes / sec / 1e9, 1)},
+        "clocks": clk, "gpu_launches": K + W,
+    }
+
+
 # ------------------------------------------------------------ CPU oracle
 
 def oracle_sample(w, fp8: bool = False):
@@ -567,6 +640,9 @@ def main():
         line = run_reference(args, int(os.environ.get("RANK", "0")), world_env)
         if line is not None:
             print(json.dumps(line), flush=True)
+        return
+    if args.op == "prefill":
+        print(json.dumps(run_prefill_bench(args)), flush=True)
         return
     if args.op == "swap":
         import torch

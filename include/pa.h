@@ -186,6 +186,46 @@ pa_status pa_copy_blocks(void* const* key_caches, void* const* value_caches, int
                          int block_size, int num_blocks, pa_stream_t stream);
 
 /*
+ * Multi-query paged attention: chunked prefill and mixed prefill + decode
+ * batches [P2 §4.3: prefill (the prompt) and decode (generated tokens) can
+ * share one batch; P2 §2.1 and §2.3: attention over K/V gathered through the
+ * block table; P1 §3.3].  Sequence s brings
+ * q_len_s = query_start[s+1] - query_start[s] new tokens, which are the last
+ * q_len_s of its c_s = context_lens[s] cached tokens (written before this
+ * call by pa_reshape_and_cache).  New token j of sequence s sits at position
+ * p = c_s - q_len_s + j and attends causally:
+ *
+ *   out[query_start[s]+j, h, :] = softmax( scale * q . K_paged[s,h,i,:] for i <= p ) . V_paged[s,h,:,:]
+ *
+ * A one-token chunk is decode; q_len_s == 0 contributes nothing.
+ *
+ *   out            fp16 [num_query_tokens][num_heads][head_dim]   (written for
+ *                  the rows of valid sequences)
+ *   query          fp16 [num_query_tokens][num_heads][head_dim]
+ *   key_cache,
+ *   value_cache    fp16 [num_blocks][num_heads][block_size][head_dim]
+ *   block_tables   int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens   int32 [num_seqs]
+ *   query_start    int32 [num_seqs + 1], non-decreasing, query_start[0] = 0,
+ *                  query_start[num_seqs] = num_query_tokens
+ *   max_query_len  host-side upper bound of q_len (sizes the launch)
+ * A sequence with q_len < 0, q_len > c_s, c_s past its table or q_len >
+ * max_query_len is skipped and flagged PA_ERRBIT_CONTEXT; a block id outside
+ * [0, num_blocks) reads zeros and is flagged PA_ERRBIT_BLOCK_ID.
+ *
+ * Supported: head_dim in {64, 128}, block_size in {8, 16, 32}, num_blocks *
+ * num_heads * block_size < 2^31.  Runs on the tensor cores (tcgen05.mma,
+ * fp16 operands, fp32 accumulation in tensor memory); the softmax weights
+ * are rounded once to fp16 for the second product (the denominator sums the
+ * same rounded weights); the result is rounded once to fp16.
+ */
+pa_status pa_prefill(void* out, const void* query, const void* key_cache, const void* value_cache,
+                     const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* context_lens, const int32_t* query_start, int num_seqs,
+                     int num_query_tokens, int num_heads, int head_dim, int block_size,
+                     int num_blocks, float scale, int max_query_len, pa_stream_t stream);
+
+/*
  * Block swap between the device cache and a host copy [P4 §三: when GPU
  * memory runs short the scheduler moves some blocks to CPU memory and brings
  * them back when needed (blocks_to_swap_out / blocks_to_swap_in); P2 §4.3:

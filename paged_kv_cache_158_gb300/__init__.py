@@ -52,6 +52,9 @@ _lib.pa_reshape_and_cache_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _
 _lib.pa_reshape_and_cache_fp8.restype = _i32
 _lib.pa_convert_cache_fp8.argtypes = [_vp, _vp, _sz, _f32, _vp]
 _lib.pa_convert_cache_fp8.restype = _i32
+_lib.pa_prefill.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                            _i32, _f32, _i32, _vp]
+_lib.pa_prefill.restype = _i32
 _lib.pa_swap_blocks.argtypes = [_vp, _vp, _i32, _vp, _i32, _sz, ctypes.c_int64, ctypes.c_int64, _vp]
 _lib.pa_swap_blocks.restype = _i32
 _lib.pa_copy_blocks_fp8.argtypes = [_vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _vp]
@@ -240,6 +243,30 @@ def _copy_blocks(key_caches, value_caches, block_mapping, stream, fp8: bool) -> 
     _check(st, "pa_copy_blocks_fp8" if fp8 else "pa_copy_blocks")
 
 
+def pa_prefill(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+               value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+               query_start: torch.Tensor, scale: float, max_query_len: int, stream=None) -> None:
+    """Multi-query paged attention (chunked prefill / mixed batches): out[TQ,H,D] for the new
+    tokens query[TQ,H,D]; query_start int32 [S+1] (see pa_prefill in include/pa.h)."""
+    TQ, H, D = query.shape
+    NB, H2, B, D2 = key_cache.shape
+    S = context_lens.shape[0]
+    if (H2, D2) != (H, D) or tuple(value_cache.shape) != tuple(key_cache.shape):
+        raise ValueError("cache shape does not match query")
+    if tuple(out.shape) != (TQ, H, D) or block_tables.dim() != 2 or block_tables.shape[0] != S:
+        raise ValueError("out / block_tables shape")
+    if query_start.shape != (S + 1,):
+        raise ValueError("query_start must be [num_seqs + 1]")
+    st = _lib.pa_prefill(_ptr(out, "out", torch.float16), _ptr(query, "query", torch.float16),
+                         _ptr(key_cache, "key_cache", torch.float16),
+                         _ptr(value_cache, "value_cache", torch.float16),
+                         _ptr(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+                         _ptr(context_lens, "context_lens", torch.int32),
+                         _ptr(query_start, "query_start", torch.int32), S, TQ, H, D, B, NB,
+                         float(scale), int(max_query_len), _stream(stream))
+    _check(st, "pa_prefill")
+
+
 def _swap_ptr(t: torch.Tensor, name: str) -> int:
     """A CUDA tensor or a pinned CPU tensor (the kernel reaches pinned host memory directly)."""
     if not isinstance(t, torch.Tensor):
@@ -304,7 +331,7 @@ def raise_on_device_errors(stream=None) -> None:
 __all__ = [
     "pa_decode", "pa_reshape_and_cache", "pa_copy_blocks", "pa_slot_mapping", "pa_check_errors",
     "pa_decode_fp8", "pa_reshape_and_cache_fp8", "pa_copy_blocks_fp8", "pa_convert_cache_fp8",
-    "pa_swap_blocks",
+    "pa_swap_blocks", "pa_prefill",
     "pa_status_string", "pa_decode_workspace_size", "pa_decode_partition_tokens",
     "pa_decode_set_partition_tokens", "decode_workspace", "raise_on_device_errors", "PAError",
 ]

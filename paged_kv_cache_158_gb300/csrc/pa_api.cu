@@ -430,6 +430,52 @@ pa_status pa_swap_blocks(void* const* dst_caches, const void* const* src_caches,
              : PA_ERR_CUDA;
 }
 
+pa_status pa_prefill(void* out, const void* query, const void* key_cache, const void* value_cache,
+                     const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* context_lens, const int32_t* query_start, int num_seqs,
+                     int num_query_tokens, int num_heads, int head_dim, int block_size,
+                     int num_blocks, float scale, int max_query_len, pa_stream_t stream) {
+  if (!head_dim_ok(head_dim) || !(block_size == 8 || block_size == 16 || block_size == 32))
+    return PA_ERR_UNSUPPORTED;
+  if (num_seqs < 0 || num_query_tokens < 0 || num_heads <= 0 || num_blocks <= 0 ||
+      max_blocks_per_seq <= 0 || max_query_len < 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0 || num_query_tokens == 0 || max_query_len == 0) return PA_OK;
+  if (!pa::prefill_rows_fit(num_blocks, num_heads, block_size)) return PA_ERR_UNSUPPORTED;
+  if ((long long)num_seqs * ((max_query_len + 127) / 128) * num_heads >= (1LL << 31))
+    return PA_ERR_UNSUPPORTED;
+  if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens ||
+      !query_start)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache) ||
+      !aligned4(block_tables) || !aligned4(context_lens) || !aligned4(query_start))
+    return PA_ERR_INVALID_ARG;
+  DeviceState ds;
+  pa_status st = device_state(&ds, false);
+  if (st != PA_OK) return st;
+  pa::PrefillArgs g{};
+  g.out = out;
+  g.query = query;
+  g.key_cache = key_cache;
+  g.value_cache = value_cache;
+  g.block_tables = block_tables;
+  g.context_lens = context_lens;
+  g.query_start = query_start;
+  g.err = ds.err;
+  g.num_seqs = num_seqs;
+  g.num_query_tokens = num_query_tokens;
+  g.num_heads = num_heads;
+  g.head_dim = head_dim;
+  g.block_size = block_size;
+  g.num_blocks = num_blocks;
+  g.max_blocks = max_blocks_per_seq;
+  g.max_query_len = max_query_len;
+  g.scale_log2 = (float)((double)scale * 1.4426950408889634073599246810019);
+  return pa::launch_prefill(g, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
 pa_status pa_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,
                           int max_blocks_per_seq, const int32_t* token_seq,
                           const int32_t* token_pos, int num_tokens, int num_seqs, int block_size,

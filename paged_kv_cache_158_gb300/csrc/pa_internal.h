@@ -88,6 +88,24 @@ cudaError_t launch_swap_blocks(void* const* dst_caches, const void* const* src_c
                                long long block_bytes, long long src_num_blocks,
                                long long dst_num_blocks, unsigned int* err, cudaStream_t stream);
 
+// Multi-query paged attention (tensor cores): arguments as in pa_prefill.
+struct PrefillArgs {
+  void* out;
+  const void* query;
+  const void* key_cache;
+  const void* value_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* query_start;
+  unsigned int* err;
+  int num_seqs, num_query_tokens, num_heads, head_dim, block_size, num_blocks, max_blocks;
+  int max_query_len;
+  float scale_log2;
+};
+cudaError_t launch_prefill(const PrefillArgs& args, cudaStream_t stream);
+// The cache's rows (num_blocks * num_heads * block_size) fit the kernel's int coordinates.
+bool prefill_rows_fit(int num_blocks, int num_heads, int block_size);
+
 cudaError_t launch_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,
                                 int max_blocks, const int32_t* token_seq,
                                 const int32_t* token_pos, int num_tokens, int num_seqs,

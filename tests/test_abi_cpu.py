@@ -137,3 +137,18 @@ def test_swap_rejects_bad_arguments_before_any_launch():
     assert f(ptrs, ptrs, 1, good, 2, 64, 0, 8, None) == 1           # empty pool
     assert f(ptrs, ptrs, 1, good + 4, 2, 64, 8, 8, None) == 1       # misaligned mapping
     assert f(None, None, 0, None, 0, 64, 8, 8, None) == 0           # nothing to do
+
+
+def test_prefill_rejects_bad_arguments_before_any_launch():
+    lib = ctypes.CDLL(LIB)
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    f = lib.pa_prefill
+    f.argtypes = [vp, vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, ctypes.c_float, i, vp]
+    g = 0x10000
+    assert f(g, g, g, g, g, 4, g, g, 2, 10, 2, 96, 16, 8, 0.1, 8, None) == 2    # head_dim
+    assert f(g, g, g, g, g, 4, g, g, 2, 10, 2, 128, 4, 8, 0.1, 8, None) == 2    # block_size 4
+    assert f(g + 8, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, 8, None) == 1
+    assert f(g, g, g, g, g, 4, g, g + 2, 2, 10, 2, 128, 16, 8, 0.1, 8, None) == 1
+    assert f(g, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, -1, None) == 1
+    assert f(None, None, None, None, None, 4, None, None, 0, 0, 2, 128, 16, 8, 0.1, 8, None) == 0
+    assert f(g, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 1 << 27, 0.1, 8, None) == 2   # rows >= 2^31

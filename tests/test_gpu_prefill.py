@@ -1,0 +1,132 @@
+"""GPU parity of multi-query paged attention (chunked prefill and mixed
+prefill + decode batches, tensor cores) against the oracle: every output of
+small ragged batches (chunks crossing tile boundaries, one-token chunks,
+empty chunks, whole-context chunks, NaN in every dead slot), sampled rows of
+the 7B-shaped chunked prefill at full size, and the error reporting."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_158_gb300 as pa
+from pa_testlib import decode_gate, live_slot_mask, poison_dead_slots_device, poison_dead_slots_host
+from workloads import configs, gpu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def _clean():
+    pa.pa_check_errors()
+    yield
+    torch.cuda.synchronize()
+
+
+def run_prefill(w, dv, max_q=None):
+    tq = int(np.sum(w.extra["q_lens"]))
+    out = torch.full((tq, w.num_heads, w.head_dim), float("nan"), dtype=torch.float16, device=DEV)
+    pa.pa_prefill(out, dv["query"], dv["key_cache"], dv["value_cache"], dv["block_tables"],
+                  dv["context_lens"], dv["query_start"], w.scale,
+                  int(max(w.extra["q_lens"])) if max_q is None else max_q)
+    return out
+
+
+def oracle_prefill(w, poison_mask=None):
+    kc, vc = gpu.host_pool(w, 0)
+    if poison_mask is not None:
+        poison_dead_slots_host(kc, vc, poison_mask)
+    _, ref64, rc = oracle.prefill(gpu.host_queries(w), kc, vc, w.block_tables, w.context_lens,
+                                  configs.query_start(w), w.scale)
+    assert rc == 0
+    return ref64
+
+
+MIXED = ([130, 1, 0, 77, 300, 1], [130, 500, 40, 77, 700, 1])
+
+
+@pytest.mark.parametrize("D,B", [(64, 8), (64, 16), (128, 16), (128, 32), (128, 8), (64, 32)])
+def test_prefill_mixed_batch_all_outputs(D, B):
+    """Whole-context chunk crossing a tile boundary, decode rows, an empty
+    chunk, a short whole-context chunk, a chunk after a 400-token prefix, a
+    one-token context; NaN in every slot no live token uses."""
+    w = configs.prefill_workload(f"mixed_D{D}_B{B}", 4000 + D + B, *MIXED, 3, D, B)
+    dv = gpu.materialize_prefill(w, DEV)
+    mask = live_slot_mask(w.block_tables, w.context_lens, w.num_blocks, B)
+    poison_dead_slots_device(dv["key_cache"], dv["value_cache"], mask)
+    out = run_prefill(w, dv)
+    ref64 = oracle_prefill(w, mask)
+    decode_gate(out, ref64, f"prefill D{D} B{B}")
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+@pytest.mark.parametrize("q_len,ctx", [(128, 128), (129, 1000), (256, 256), (383, 2047), (1, 3000)])
+def test_prefill_tile_edges(q_len, ctx):
+    w = configs.prefill_workload(f"edge_{q_len}_{ctx}", 4100 + q_len, [q_len, 5], [ctx, 9], 2, 128, 16)
+    dv = gpu.materialize_prefill(w, DEV)
+    out = run_prefill(w, dv)
+    decode_gate(out, oracle_prefill(w), f"prefill q{q_len} c{ctx}")
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+def test_prefill_deterministic_and_decode_rows_match_decode():
+    w = configs.prefill_workload("det", 4200, [200, 1, 1, 1], [900, 333, 64, 1000], 4, 128, 16)
+    dv = gpu.materialize_prefill(w, DEV)
+    a = run_prefill(w, dv).clone()
+    b = run_prefill(w, dv)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    ref64 = oracle_prefill(w)
+    decode_gate(a, ref64, "prefill det")
+    # the one-token chunks against the decode kernel on the same cache
+    qs = configs.query_start(w)
+    rows = torch.from_numpy(qs[1:4].astype(np.int64)).to(DEV)
+    q = dv["query"][rows].contiguous()
+    bt = dv["block_tables"][1:4].contiguous()
+    cl = dv["context_lens"][1:4].contiguous()
+    outd = torch.empty_like(q)
+    ws = pa.decode_workspace(3, w.num_heads, w.head_dim, 1000)
+    pa.pa_decode(outd, q, dv["key_cache"], dv["value_cache"], bt, cl, w.scale, 1000, ws)
+    decode_gate(outd, ref64[qs[1:4]], "decode rows")
+
+
+def test_prefill_7b_full_size_sampled_rows():
+    """The 7B-shaped chunked prefill at full size; sampled 16-row windows of
+    every sequence checked against the oracle on the causally truncated
+    problem (rows j0..j0+15 only see positions up to their own)."""
+    w = configs.prefill_7b()
+    dv = gpu.materialize_prefill(w, DEV)
+    out = run_prefill(w, dv)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    kc, vc = gpu.host_pool(w, 0)
+    q = gpu.host_queries(w)
+    qs = configs.query_start(w)
+    rng = np.random.default_rng(61)
+    for s in range(w.num_seqs):
+        ql, c = int(w.extra["q_lens"][s]), int(w.context_lens[s])
+        for j0 in (0, int(rng.integers(1, ql - 16)), ql - 16):
+            p_last = c - ql + j0 + 15
+            bt = w.block_tables[s:s + 1]
+            _, ref64, rc = oracle.prefill(q[qs[s] + j0:qs[s] + j0 + 16], kc, vc, bt,
+                                          np.array([p_last + 1], np.int32),
+                                          np.array([0, 16], np.int32), w.scale)
+            assert rc == 0
+            decode_gate(out[qs[s] + j0:qs[s] + j0 + 16], ref64, f"{w.name} s{s} rows {j0}..")
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+def test_prefill_bad_inputs_flagged():
+    w = configs.prefill_workload("bad", 4300, [40, 30], [100, 60], 2, 64, 16)
+    dv = gpu.materialize_prefill(w, DEV)
+    run_prefill(w, dv, max_q=32)                   # max_query_len below the real chunk lengths
+    st, bits = pa.pa_check_errors()
+    assert st == pa.PA_ERR_OUT_OF_RANGE and bits & pa.PA_ERRBIT_CONTEXT
+    w.block_tables[1, 0] = w.num_blocks + 7
+    dv["block_tables"] = torch.from_numpy(w.block_tables).to(DEV)
+    out = run_prefill(w, dv)
+    st, bits = pa.pa_check_errors()
+    assert st == pa.PA_ERR_OUT_OF_RANGE and bits & pa.PA_ERRBIT_BLOCK_ID
+    # the other sequence is unaffected
+    w.block_tables[1, 0] = 0
+    ref64 = oracle_prefill(w)
+    decode_gate(out[:40], ref64[:40], "unaffected sequence")

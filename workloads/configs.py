@@ -220,6 +220,37 @@ def small_random(seed: int, num_seqs: int, num_heads: int, head_dim: int, block_
                     q_sigma=q_sigma)
 
 
+def prefill_workload(name: str, seed: int, q_lens, ctx, num_heads: int, head_dim: int,
+                     block_size: int, spare_blocks: int = 3, kv_sigma: float = 1.0,
+                     q_sigma: float = 1.0, cid: int = 0) -> Workload:
+    """A chunked-prefill / mixed batch on one layer: sequence s has ctx[s] cached tokens,
+    the last q_lens[s] of which are its new query tokens (q_lens[s] == 1: decode).
+    Blocks come from a seeded permutation of a pool with a few spare blocks."""
+    d = synth.Draws(seed)
+    ctx = np.asarray(ctx, dtype=np.int32)
+    q_lens = np.asarray(q_lens, dtype=np.int32)
+    need = int(sum(-(-int(c) // block_size) for c in ctx))
+    NB = need + spare_blocks
+    perm = d.permutation(NB)
+    mb = max(1, -(-int(ctx.max()) // block_size))
+    return Workload(name, cid, seed, 1, len(ctx), num_heads, head_dim, block_size, NB, mb, ctx,
+                    _tables_from_permutation(perm, ctx, block_size, mb), kv_sigma=kv_sigma,
+                    q_sigma=q_sigma, description="chunked prefill / mixed batch",
+                    extra={"q_lens": q_lens})
+
+
+def query_start(w: Workload) -> np.ndarray:
+    """int32 [S + 1]: prefix sums of the prefill workload's chunk lengths."""
+    return np.concatenate([[0], np.cumsum(w.extra["q_lens"])]).astype(np.int32)
+
+
+def prefill_7b() -> Workload:
+    """LLaMA-7B-shaped chunked prefill: 4 sequences x a 512-token chunk after a 1536-token
+    cached prefix (context 2048), H32 D128 B16."""
+    return prefill_workload("p1_chunked_prefill_S4_H32_D128_B16_q512_c2048", SEED_BASE + 6,
+                            [512] * 4, [2048] * 4, 32, 128, 16, spare_blocks=0, cid=6)
+
+
 def fp8_scales(w: Workload) -> tuple[float, float]:
     """Per-tensor scales (k_scale, v_scale) of a workload's FP8 caches: about
     1/70 and 1/84 of the values' standard deviation, so that values up to

@@ -131,3 +131,28 @@ def host_small(w: Workload, layer: int):
     k = synth.host_tensor(w.seed, w.key_new_stream(layer), (T, w.num_heads, w.head_dim), w.kv_bank())
     v = synth.host_tensor(w.seed, w.value_new_stream(layer), (T, w.num_heads, w.head_dim), w.kv_bank())
     return q, k, v
+
+
+def host_queries(w: Workload) -> np.ndarray:
+    """A prefill workload's new-token queries [sum(q_lens), H, D] (uint16)."""
+    tq = int(np.sum(w.extra["q_lens"]))
+    return synth.host_tensor(w.seed, w.query_stream(0), (tq, w.num_heads, w.head_dim), w.q_bank())
+
+
+def materialize_prefill(w: Workload, device="cuda") -> dict:
+    """Device tensors of a prefill workload: layer-0 caches (generator fill), the
+    queries, block tables, context lengths and query_start."""
+    from .configs import query_start
+    kv_bank = device_bank(w.seed, w.kv_sigma, device)
+    shape = (w.num_blocks, w.num_heads, w.block_size, w.head_dim)
+    kc = torch.empty(shape, dtype=torch.float16, device=device)
+    vc = torch.empty(shape, dtype=torch.float16, device=device)
+    fill(kc, w.seed, w.key_pool_stream(0), kv_bank)
+    fill(vc, w.seed, w.value_pool_stream(0), kv_bank)
+    return {
+        "key_cache": kc, "value_cache": vc,
+        "query": upload_u16(host_queries(w), device),
+        "block_tables": torch.from_numpy(w.block_tables).to(device),
+        "context_lens": torch.from_numpy(w.context_lens).to(device),
+        "query_start": torch.from_numpy(query_start(w)).to(device),
+    }
