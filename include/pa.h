@@ -216,8 +216,8 @@ pa_status pa_copy_blocks(void* const* key_caches, void* const* value_caches, int
  * Supported: head_dim in {64, 128}, block_size in {8, 16, 32}, num_blocks *
  * num_heads * block_size < 2^31.  Runs on the tensor cores (tcgen05.mma,
  * fp16 operands, fp32 accumulation in tensor memory); the softmax weights
- * are rounded once to fp16 for the second product (the denominator sums the
- * same rounded weights); the result is rounded once to fp16.
+ * are rounded once to fp16 for the second product (the denominator sums them
+ * in fp32 before rounding); the result is rounded once to fp16.
  */
 pa_status pa_prefill(void* out, const void* query, const void* key_cache, const void* value_cache,
                      const int32_t* block_tables, int max_blocks_per_seq,

@@ -134,6 +134,13 @@ __device__ __forceinline__ float exp2_approx(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // acc + a.lo*b.lo + a.hi*b.hi for two packed fp16 pairs, each product added
 // with one fp32 rounding (fp16 x fp16 products are exact in fp32).
 __device__ __forceinline__ float dot2_f16_f32(uint32_t a, uint32_t b, float acc) {

@@ -20,10 +20,12 @@
 //    an mbarrier.
 //  * Each thread owns one query row (TMEM lane = row): it reads its S row
 //    with tcgen05.ld, applies the causal and context masks, keeps the online
-//    softmax (m, l) in fp32 base-2 units, rounds P to fp16 (l sums the same
-//    rounded weights) and writes it to shared memory in the swizzled K-major
-//    layout the second MMA reads, and rescales its O row in TMEM when the
-//    running maximum grows.  V rows past the context are zeroed in shared
+//    softmax (m in raw logit units, l in fp32, exponentials in base 2 with
+//    the scale folded into one fused multiply-add), rounds P to fp16 for the
+//    second MMA and writes it to shared memory in the swizzled K-major
+//    layout that MMA reads, and rescales its O row in TMEM when the running
+//    maximum grows.  Masks are applied only on tiles that reach the
+//    diagonal or the context end.  V rows past the context are zeroed in shared
 //    memory (0 * NaN in stale slots would poison the sum).
 //  * Work per KV tile: the TMA of the next tile overlaps the softmax and
 //    both MMAs of the current one; the softmax and the MMAs of one CTA run
@@ -218,7 +220,8 @@ __global__ void __launch_bounds__(128, 1)
           ++kv_issued;
         }
 
-        // Online softmax on this thread's row.
+        // Online softmax on this thread's row, in raw logit units for the
+        // maximum (scale > 0) and base 2 for the exponentials.
         float x[kKT];
 #pragma unroll
         for (int cb = 0; cb < kKT / 32; ++cb) {
@@ -229,15 +232,17 @@ __global__ void __launch_bounds__(128, 1)
           for (int j = 0; j < 32; ++j) x[cb * 32 + j] = __uint_as_float(r[j]);
         }
         const int kv0 = t * kKT;
+        if (kv0 + kKT - 1 > pos_min) {  // tile reaches the diagonal (or the context end)
+          const int lim = min(qpos, c - 1) - kv0;   // last visible column of this row
+#pragma unroll
+          for (int j = 0; j < kKT; ++j)
+            if (j > lim) x[j] = -INFINITY;
+        }
         float mx = m;
 #pragma unroll
-        for (int j = 0; j < kKT; ++j) {
-          const int kv = kv0 + j;
-          x[j] = (kv <= qpos && kv < c) ? x[j] * a.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, x[j]);
-        }
-        const float alpha = (mx == -INFINITY) ? 1.f : exp2_approx(m - mx);
-        const float mref = (mx == -INFINITY) ? 0.f : mx;
+        for (int j = 0; j < kKT; j += 2) mx = fmax3(mx, x[j], x[j + 1]);
+        const float alpha = (mx == -INFINITY) ? 1.f : exp2_approx((m - mx) * a.scale_log2);
+        const float neg = (mx == -INFINITY) ? 0.f : -mx * a.scale_log2;
         float ps = 0.f;
         unsigned char* prow = sm + T::OFF_P;
 #pragma unroll
@@ -245,10 +250,10 @@ __global__ void __launch_bounds__(128, 1)
           uint32_t w[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const __half2 hp = __floats2half2_rn(exp2_approx(x[8 * j8 + 2 * u] - mref),
-                                                 exp2_approx(x[8 * j8 + 2 * u + 1] - mref));
-            const float2 back = __half22float2(hp);
-            ps += back.x + back.y;
+            const float p0 = exp2_approx(fmaf(x[8 * j8 + 2 * u], a.scale_log2, neg));
+            const float p1 = exp2_approx(fmaf(x[8 * j8 + 2 * u + 1], a.scale_log2, neg));
+            ps += p0 + p1;
+            const __half2 hp = __floats2half2_rn(p0, p1);
             w[u] = *reinterpret_cast<const uint32_t*>(&hp);
           }
           const int at = j8 / 8, ch = j8 % 8;
