@@ -53,13 +53,16 @@ struct PrefillTraits {
   static constexpr int ATOM = 128 * 128;            // bytes of one [128 rows][64 fp16] atom array
   static constexpr int QB = kQT * D * 2;
   static constexpr int KB = kKT * D * 2;
-  static constexpr int PB = kQT * kKT * 2;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K0 = QB;                 // stage s: K at OFF_K0 + s*2*KB, V after it
-  static constexpr int OFF_P = QB + 4 * KB;
-  static constexpr int OFF_BAR = OFF_P + PB;        // q, kv[2], s, o barriers; TMEM slot; flags
-  static constexpr int SMEM = OFF_BAR + 128 + 1024;  // + alignment slack
-  static constexpr uint32_t TMEM_COLS = 256;        // S: 128 columns, O: D columns
+  static constexpr int OFF_Q = 0;                   // Q tile x at OFF_Q + x*QB
+  static constexpr int OFF_K0 = 2 * QB;             // stage s: K at OFF_K0 + s*2*KB, V after it
+  static constexpr int OFF_BAR = OFF_K0 + 4 * KB;
+  // Barriers, TMEM slot and alignment slack; at least 120 KB so that one CTA
+  // holds an SM (each CTA allocates all 512 TMEM columns).
+  static constexpr int SMEM_USED = OFF_BAR + 256 + 1024;
+  static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+  static constexpr int THREADS = 288;               // two softmax warpgroups + one MMA/TMA warp
+  static constexpr uint32_t TMEM_COLS = 512;        // S_x: 128 columns each, O_x: D columns each
+  static constexpr uint32_t COL_O = 256;
   static_assert(D == 64 || D == 128, "head_dim");
 };
 
@@ -74,18 +77,34 @@ struct PrefillParams {
   int max_blocks;
   int num_blocks;
   int block_size;
-  int qtiles;                    // query tiles per sequence covered by the grid
+  int qpairs;                    // pairs of query tiles per sequence covered by the grid
   int max_query_len;             // host bound of the chunk lengths
   int oob_row;                   // a row coordinate past the cache (zero-filled loads)
   float scale_log2;
 };
 
-__device__ __forceinline__ uint32_t swz128(int row, int chunk16) {
-  return (uint32_t)(row * 128 + ((chunk16 ^ (row & 7)) << 4));
-}
+// Per-CTA geometry of one query tile (x = 0, 1 of the pair).
+struct QTile {
+  int rows;      // valid rows (<= 0: inactive)
+  int pos_min;   // position of row 0
+  int n_kv;      // KV tiles it needs
+};
+
+// A waiting thread's view of an mbarrier: the next phase it expects.  Used
+// only where at most one phase can complete between two waits (a parity
+// wait cannot tell phase k from phase k + 2).
+struct Waiter {
+  uint32_t bar;
+  uint32_t phase = 0;
+  __device__ bool wait() {
+    const bool ok = mbar_wait_bounded(bar, phase & 1);
+    ++phase;
+    return ok;
+  }
+};
 
 template <int D>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const PrefillParams a) {
   using T = PrefillTraits<D>;
@@ -94,26 +113,31 @@ __global__ void __launch_bounds__(128, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(sm);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + T::OFF_BAR);
-  const uint32_t q_bar = smem_u32(&bars[0]);
-  const uint32_t kv_bar0 = smem_u32(&bars[1]);
-  const uint32_t s_bar = smem_u32(&bars[3]);
-  const uint32_t o_bar = smem_u32(&bars[4]);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + T::OFF_BAR + 64);
+  // barriers: 0 q_full; 1,2 kv_full[st]; 3,4 s_full[x]; 5,6 p_full[x]; 7,8 o_full[x]
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + T::OFF_BAR + 128);
+  int* fail = reinterpret_cast<int*>(sm + T::OFF_BAR + 132);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
+  const int lane = tid & 31;
   const int H = a.num_heads;
   const int h = blockIdx.x % H;
   const int rest = blockIdx.x / H;
   const int s = rest % a.num_seqs;
-  const int qt = a.qtiles - 1 - rest / a.num_seqs;  // heaviest tiles first
+  const int pq = a.qpairs - 1 - rest / a.num_seqs;  // heaviest pairs first
 
   if (tid == 0) {
-    mbar_init(q_bar, 1);
-    mbar_init(kv_bar0, 1);
-    mbar_init(kv_bar0 + 8, 1);
-    mbar_init(s_bar, 1);
-    mbar_init(o_bar, 1);
+    mbar_init(bar(0), 1);
+    mbar_init(bar(1), 1);
+    mbar_init(bar(2), 1);
+    mbar_init(bar(3), 1);
+    mbar_init(bar(4), 1);
+    mbar_init(bar(5), 128);
+    mbar_init(bar(6), 128);
+    mbar_init(bar(7), 1);
+    mbar_init(bar(8), 1);
+    *fail = 0;
     fence_mbar_init();
     prefetch_tensormap(&tq);
     prefetch_tensormap(&tk);
@@ -127,9 +151,6 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_s = tmem;
-  const uint32_t tmem_o = tmem + 128;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
 
   pdl_wait();
   pdl_launch_dependents();
@@ -139,21 +160,27 @@ __global__ void __launch_bounds__(128, 1)
   const int c = a.context_lens[s];
   const bool bad = q_len < 0 || q_len > c || c > a.max_blocks * a.block_size ||
                    q_len > a.max_query_len;
-  if (bad && qt == a.qtiles - 1 && h == 0 && tid == 0) atomicOr(a.err, PA_ERRBIT_CONTEXT);
-  const int rows_valid = bad ? 0 : min(kQT, q_len - qt * kQT);
+  if (bad && pq == a.qpairs - 1 && h == 0 && tid == 0) atomicOr(a.err, PA_ERRBIT_CONTEXT);
+  QTile qx[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    const int qt = 2 * pq + x;
+    qx[x].rows = bad ? 0 : min(kQT, q_len - qt * kQT);
+    qx[x].pos_min = c - q_len + qt * kQT;
+    qx[x].n_kv = qx[x].rows > 0 ? (qx[x].pos_min + qx[x].rows - 1) / kKT + 1 : 0;
+  }
+  const int n_kv = max(qx[0].n_kv, qx[1].n_kv);
 
-  if (rows_valid > 0) {
-    const int pos_min = c - q_len + qt * kQT;          // position of this tile's row 0
-    const int n_t = (pos_min + rows_valid - 1) / kKT + 1;
+  if (warp == 8 && n_kv > 0) {
+    // ---------------- TMA producer and MMA issuer (lane 0; the warp zeroes V rows)
     const int32_t* bt = a.block_tables + (size_t)s * a.max_blocks;
-    const int bpt = kKT / a.block_size;                // blocks per KV tile
-
-    // Thread 0: K and V tile t into stage st (one box per block and atom).
-    auto issue_kv = [&](int t, int st) {
-      const uint32_t bar = kv_bar0 + 8 * st;
+    const int bpt = kKT / a.block_size;
+    int kv_issued = 0, qk[2] = {0, 0}, pv[2] = {0, 0};
+    auto issue_kv = [&](int t) {
+      const int st = t & 1;
       const uint32_t kdst = s_base + T::OFF_K0 + st * 2 * T::KB;
       const uint32_t vdst = kdst + T::KB;
-      mbar_arrive_expect_tx(bar, 2 * T::KB);
+      mbar_arrive_expect_tx(bar(1 + st), 2 * T::KB);
       for (int b = 0; b < bpt; ++b) {
         const int lb = t * bpt + b;
         int row = a.oob_row;
@@ -167,175 +194,230 @@ __global__ void __launch_bounds__(128, 1)
         const uint32_t roff = (uint32_t)(b * a.block_size * 128);
 #pragma unroll
         for (int at = 0; at < T::NA; ++at) {
-          tma_load_2d(kdst + at * T::ATOM + roff, &tk, at * 64, row, bar);
-          tma_load_2d(vdst + at * T::ATOM + roff, &tv, at * 64, row, bar);
+          tma_load_2d(kdst + at * T::ATOM + roff, &tk, at * 64, row, bar(1 + st));
+          tma_load_2d(vdst + at * T::ATOM + roff, &tv, at * 64, row, bar(1 + st));
         }
       }
+      ++kv_issued;
     };
-
-    if (tid == 0) {
-      mbar_arrive_expect_tx(q_bar, T::QB);
-#pragma unroll
-      for (int at = 0; at < T::NA; ++at)
-        tma_load_3d(s_base + T::OFF_Q + at * T::ATOM, &tq, at * 64, h, q0 + qt * kQT, q_bar);
-      issue_kv(0, 0);
-    }
-
     constexpr uint32_t kIdQK = umma_idesc_f16(kQT, kKT, false, false);
     constexpr uint32_t kIdPV = umma_idesc_f16(kQT, D, false, true);
-    const int qpos = pos_min + tid;                    // this thread's query position
-    float m = -INFINITY, l = 0.f;
-    // Thread 0's record of what it started, for a clean exit after a timeout.
-    int kv_issued = 1, qk_done = 0, pv_done = 0;
-    bool good = true;
-    int t = 0;
-    for (; t < n_t; ++t) {
-      const int st = t & 1;
-      const uint32_t kaddr = s_base + T::OFF_K0 + st * 2 * T::KB;
-      const uint32_t vaddr = kaddr + T::KB;
-      // Every wait is bounded; a thread that gives up skips the work but still
-      // reaches the block-wide vote below, so all threads leave together.
-      good = mbar_wait_bounded(kv_bar0 + 8 * st, (t >> 1) & 1);
-      if (t == 0) good = good && mbar_wait_bounded(q_bar, 0);
-
-      // S = Q K^T
-      if (tid == 0 && good) {
-        tc_fence_after();
+    auto qk_mma = [&](int x, int t) {
+      const uint32_t kaddr = s_base + T::OFF_K0 + (t & 1) * 2 * T::KB;
+      tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const int at = k / 4, kk = k % 4;
-          const uint64_t da = umma_desc_sw128(s_base + T::OFF_Q + at * T::ATOM + kk * 32, 16, 1024);
-          const uint64_t db = umma_desc_sw128(kaddr + at * T::ATOM + kk * 32, 16, 1024);
-          umma_f16(tmem_s, da, db, kIdQK, k > 0);
-        }
-        umma_commit(s_bar);
-        ++qk_done;
+      for (int k = 0; k < D / 16; ++k) {
+        const int at = k / 4, kk = k % 4;
+        const uint64_t da = umma_desc_sw128(s_base + T::OFF_Q + x * T::QB + at * T::ATOM + kk * 32, 16, 1024);
+        const uint64_t db = umma_desc_sw128(kaddr + at * T::ATOM + kk * 32, 16, 1024);
+        umma_f16(tmem + 128 * x, da, db, kIdQK, k > 0);
       }
-      good = good && mbar_wait_bounded(s_bar, t & 1);
-      if (t > 0) good = good && mbar_wait_bounded(o_bar, (t - 1) & 1);  // P.V of t-1 done
-      if (good) {
-        tc_fence_after();
-        if (tid == 0 && t + 1 < n_t) {
-          issue_kv(t + 1, st ^ 1);
-          ++kv_issued;
-        }
-
-        // Online softmax on this thread's row, in raw logit units for the
-        // maximum (scale > 0) and base 2 for the exponentials.
-        float x[kKT];
+      umma_commit(bar(3 + x));
+      ++qk[x];
+    };
+    auto pv_mma = [&](int x, int t) {
+      const uint32_t vaddr = s_base + T::OFF_K0 + (t & 1) * 2 * T::KB + T::KB;
+      tc_fence_after();
 #pragma unroll
-        for (int cb = 0; cb < kKT / 32; ++cb) {
-          uint32_t r[32];
-          tmem_ld32(tmem_s + lane_off + cb * 32, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) x[cb * 32 + j] = __uint_as_float(r[j]);
-        }
-        const int kv0 = t * kKT;
-        if (kv0 + kKT - 1 > pos_min) {  // tile reaches the diagonal (or the context end)
-          const int lim = min(qpos, c - 1) - kv0;   // last visible column of this row
-#pragma unroll
-          for (int j = 0; j < kKT; ++j)
-            if (j > lim) x[j] = -INFINITY;
-        }
-        float mx = m;
-#pragma unroll
-        for (int j = 0; j < kKT; j += 2) mx = fmax3(mx, x[j], x[j + 1]);
-        const float alpha = (mx == -INFINITY) ? 1.f : exp2_approx((m - mx) * a.scale_log2);
-        const float neg = (mx == -INFINITY) ? 0.f : -mx * a.scale_log2;
-        float ps = 0.f;
-        unsigned char* prow = sm + T::OFF_P;
-#pragma unroll
-        for (int j8 = 0; j8 < kKT / 8; ++j8) {
-          uint32_t w[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float p0 = exp2_approx(fmaf(x[8 * j8 + 2 * u], a.scale_log2, neg));
-            const float p1 = exp2_approx(fmaf(x[8 * j8 + 2 * u + 1], a.scale_log2, neg));
-            ps += p0 + p1;
-            const __half2 hp = __floats2half2_rn(p0, p1);
-            w[u] = *reinterpret_cast<const uint32_t*>(&hp);
-          }
-          const int at = j8 / 8, ch = j8 % 8;
-          *reinterpret_cast<uint4*>(prow + at * T::ATOM + swz128(tid, ch)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        l = l * alpha + ps;
-        m = mx;
-        // Rescale this row of O when the maximum grew (warp-collective access).
-        if (t > 0 && __any_sync(kFullMask, alpha != 1.f)) {
-#pragma unroll
-          for (int cb = 0; cb < D / 32; ++cb) {
-            uint32_t r[32];
-            tmem_ld32(tmem_o + lane_off + cb * 32, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-            tmem_st32(tmem_o + lane_off + cb * 32, r);
-          }
-          tmem_wait_st();
-        }
-        // Zero V rows past the context (stale slots may hold anything).
-        if (kv0 + tid >= c) {
-          unsigned char* vrow = sm + (vaddr - s_base) + tid * 128;
-#pragma unroll
-          for (int at = 0; at < T::NA; ++at)
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-              *reinterpret_cast<uint4*>(vrow + at * T::ATOM + ch * 16) = make_uint4(0, 0, 0, 0);
-        }
+      for (int k = 0; k < kKT / 16; ++k) {
+        const uint64_t db = umma_desc_sw128(vaddr + k * 16 * 128, T::ATOM, 1024);
+        umma_f16_tmem_a(tmem + T::COL_O + D * x, tmem + 128 * x + 8 * k, db, kIdPV, t > 0 || k > 0);
+      }
+      umma_commit(bar(7 + x));
+      ++pv[x];
+    };
+    // V rows of tile t past the context: zeroed by the whole warp after the
+    // tile has landed (stale slots may hold anything; 0 * NaN would poison O).
+    auto zero_v_tail = [&](int t) {
+      const int first = c - t * kKT;
+      if (first >= kKT) return;
+      unsigned char* v = sm + T::OFF_K0 + (t & 1) * 2 * T::KB + T::KB;
+      const int nchunks = (kKT - max(first, 0)) * 8;
+      for (int i = lane; i < nchunks * T::NA; i += 32) {
+        const int at = i / nchunks, r = max(first, 0) + (i % nchunks) / 8, ch = i % 8;
+        *reinterpret_cast<uint4*>(v + at * T::ATOM + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
       }
       fence_proxy_async_smem();
-      tc_fence_before();
-      good = __syncthreads_and(good) != 0;
-      tc_fence_after();
-      if (!good) break;
-
-      // O += P V
-      if (tid == 0) {
+      __syncwarp();
+    };
+    // kv_full of tile t: barrier 1 + (t & 1), parity (t >> 1) & 1.
+    auto wait_kv = [&](int t) { return mbar_wait_bounded(bar(1 + (t & 1)), (t >> 1) & 1); };
+    Waiter p_w[2] = {{bar(5)}, {bar(6)}}, o_w[2] = {{bar(7)}, {bar(8)}};
+    bool ok = true;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(0), (qx[1].rows > 0 ? 2 : 1) * T::QB);
 #pragma unroll
-        for (int k = 0; k < kKT / 16; ++k) {
-          const int at = k / 4, kk = k % 4;
-          const uint64_t da = umma_desc_sw128(s_base + T::OFF_P + at * T::ATOM + kk * 32, 16, 1024);
-          const uint64_t db = umma_desc_sw128(vaddr + k * 16 * 128, T::ATOM, 1024);
-          umma_f16(tmem_o, da, db, kIdPV, t > 0 || k > 0);
-        }
-        umma_commit(o_bar);
-        ++pv_done;
+      for (int x = 0; x < 2; ++x)
+        if (qx[x].rows > 0)
+#pragma unroll
+          for (int at = 0; at < T::NA; ++at)
+            tma_load_3d(s_base + T::OFF_Q + x * T::QB + at * T::ATOM, &tq, at * 64, h,
+                        q0 + (2 * pq + x) * kQT, bar(0));
+      issue_kv(0);
+      if (n_kv > 1) issue_kv(1);
+    }
+    ok = mbar_wait_bounded(bar(0), 0) && wait_kv(0);
+    ok = __all_sync(kFullMask, ok);
+    if (ok) {
+      zero_v_tail(0);
+      if (lane == 0) {
+        qk_mma(0, 0);
+        if (qx[1].n_kv > 0) qk_mma(1, 0);
       }
     }
-    if (good) good = mbar_wait_bounded(o_bar, (n_t - 1) & 1);
-    good = __syncthreads_and(good) != 0;
-    if (!good) {
-      if (tid == 0) {
-        atomicOr(a.err, PA_ERRBIT_TIMEOUT);
-        // Let every copy and MMA this CTA started finish (bounded) before
-        // its TMEM and shared memory are released.
-        for (int u = t; u < kv_issued; ++u) mbar_wait_bounded(kv_bar0 + 8 * (u & 1), (u >> 1) & 1);
-        if (qk_done > 0) mbar_wait_bounded(s_bar, (qk_done - 1) & 1);
-        if (pv_done > 0) mbar_wait_bounded(o_bar, (pv_done - 1) & 1);
+    // O(x, t - 1) must be complete before S(x, t) overwrites P(x, t - 1), so each
+    // QK waits for the previous P.V of its own tile; the other tile's work
+    // keeps the tensor pipe busy meanwhile.
+    uint32_t o_seen[2] = {0, 0};  // completed P.V phases observed, per tile
+    auto wait_o = [&](int x, int upto) {  // until P.V(x, upto) is observed complete
+      bool r = true;
+      while ((int)o_seen[x] <= upto && r) {
+        r = o_w[x].wait();
+        ++o_seen[x];
       }
-    } else {
+      return r;
+    };
+    for (int t = 0; t < n_kv && ok; ++t) {
+      const bool a0 = t < qx[0].n_kv, a1 = t < qx[1].n_kv;
+      const bool n0 = t + 1 < qx[0].n_kv, n1 = t + 1 < qx[1].n_kv;
+      if (a0) ok = ok && p_w[0].wait();
+      if (ok && lane == 0 && a0) pv_mma(0, t);
+      if (ok && t + 1 < n_kv) {
+        ok = wait_kv(t + 1);
+        ok = __all_sync(kFullMask, ok);
+        if (ok) zero_v_tail(t + 1);
+      }
+      if (ok && n0) {
+        ok = wait_o(0, t);
+        if (ok && lane == 0) qk_mma(0, t + 1);
+      }
+      if (ok && a1) ok = p_w[1].wait();
+      if (ok && lane == 0 && a1) pv_mma(1, t);
+      if (ok && n1) {
+        ok = wait_o(1, t);
+        if (ok && lane == 0) qk_mma(1, t + 1);
+      }
+      if (ok && t + 2 < n_kv) {  // stage (t & 1) is free once both P.V of tile t are done
+        if (a0) ok = ok && wait_o(0, t);
+        if (a1) ok = ok && wait_o(1, t);
+        if (ok && lane == 0) issue_kv(t + 2);
+      }
+      ok = __all_sync(kFullMask, ok);
+    }
+    if (!ok) {
+      if (lane == 0) {
+        atomicOr(a.err, PA_ERRBIT_TIMEOUT);
+        *fail = 1;
+        // Let every copy and MMA this CTA started finish (bounded) before the
+        // TMEM and shared memory are released.
+        for (int i = 0; i < 2; ++i) {
+          if (kv_issued > i) mbar_wait_bounded(bar(1 + i), ((kv_issued - 1 - ((kv_issued - 1 - i) & 1)) >> 1) & 1);
+          if (qk[i] > 0) mbar_wait_bounded(bar(3 + i), (qk[i] - 1) & 1);
+          if (pv[i] > 0) mbar_wait_bounded(bar(7 + i), (pv[i] - 1) & 1);
+        }
+      }
+    }
+  } else if (warp < 8) {
+    // ---------------- softmax warpgroup x: one query row per thread
+    const int x = warp >> 2;
+    const int row = tid & 127;
+    const QTile qt = qx[x];
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + 128 * x + lane_off;
+    const uint32_t t_o = tmem + T::COL_O + D * x + lane_off;
+    const int qpos = qt.pos_min + row;
+    float m = -INFINITY, l = 0.f;
+    Waiter s_w{bar(3 + x)};
+    bool ok = true;
+    for (int t = 0; t < qt.n_kv; ++t) {
+      ok = s_w.wait();
+      if (!ok || *fail) { ok = false; break; }
       tc_fence_after();
-      // Epilogue: O / l -> fp16 rows of the output.
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      __half* orow = static_cast<__half*>(a.out) + ((size_t)(q0 + qt * kQT + tid) * H + h) * D;
+      float xv[kKT];
 #pragma unroll
-      for (int cb = 0; cb < D / 32; ++cb) {
+      for (int cb = 0; cb < kKT / 32; ++cb) {
         uint32_t r[32];
-        tmem_ld32(tmem_o + lane_off + cb * 32, r);
+        tmem_ld32(t_s + cb * 32, r);
         tmem_wait_ld();
-        if (tid < rows_valid) {
 #pragma unroll
-          for (int j8 = 0; j8 < 4; ++j8) {
-            uint32_t w[4];
+        for (int j = 0; j < 32; ++j) xv[cb * 32 + j] = __uint_as_float(r[j]);
+      }
+      const int kv0 = t * kKT;
+      if (kv0 + kKT - 1 > qt.pos_min) {  // tile reaches the diagonal (or the context end)
+        const int lim = min(qpos, c - 1) - kv0;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const __half2 hv = __floats2half2_rn(__uint_as_float(r[8 * j8 + 2 * u]) * inv,
-                                                   __uint_as_float(r[8 * j8 + 2 * u + 1]) * inv);
-              w[u] = *reinterpret_cast<const uint32_t*>(&hv);
+        for (int j = 0; j < kKT; ++j)
+          if (j > lim) xv[j] = -INFINITY;
+      }
+      float mx = m;
+#pragma unroll
+      for (int j = 0; j < kKT; j += 2) mx = fmax3(mx, xv[j], xv[j + 1]);
+      const float alpha = (mx == -INFINITY) ? 1.f : exp2_approx((m - mx) * a.scale_log2);
+      const float neg = (mx == -INFINITY) ? 0.f : -mx * a.scale_log2;
+      float ps = 0.f;
+      uint32_t pk[kKT / 2];
+#pragma unroll
+      for (int j = 0; j < kKT / 2; ++j) {
+        const float p0 = exp2_approx(fmaf(xv[2 * j], a.scale_log2, neg));
+        const float p1 = exp2_approx(fmaf(xv[2 * j + 1], a.scale_log2, neg));
+        ps += p0 + p1;
+        const __half2 hp = __floats2half2_rn(p0, p1);
+        pk[j] = *reinterpret_cast<const uint32_t*>(&hp);
+      }
+      l = l * alpha + ps;
+      m = mx;
+      // O(x, t - 1) is complete here: S(x, t) was computed after it.
+      if (t > 0 && __any_sync(kFullMask, alpha != 1.f)) {
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t r[32];
+          tmem_ld32(t_o + cb * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+          tmem_st32(t_o + cb * 32, r);
+        }
+      }
+      // P (fp16 pairs) over the first 64 columns of this tile's S.
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = pk[j];
+        tmem_st32(t_s, r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = pk[32 + j];
+        tmem_st32(t_s + 32, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(5 + x));
+    }
+    if (ok && qt.n_kv > 0) {
+      // The last P.V of this tile (phase n_kv - 1; the earlier ones completed
+      // before S of the last tile was computed, so the parity is unambiguous).
+      const bool done = mbar_wait_bounded(bar(7 + x), (qt.n_kv - 1) & 1);
+      if (done && !*fail) {
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        __half* orow = static_cast<__half*>(a.out) +
+                       ((size_t)(q0 + (2 * pq + x) * kQT + row) * H + h) * D;
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t r[32];
+          tmem_ld32(t_o + cb * 32, r);
+          tmem_wait_ld();
+          if (row < qt.rows) {
+#pragma unroll
+            for (int j8 = 0; j8 < 4; ++j8) {
+              uint32_t w[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const __half2 hv = __floats2half2_rn(__uint_as_float(r[8 * j8 + 2 * u]) * inv,
+                                                     __uint_as_float(r[8 * j8 + 2 * u + 1]) * inv);
+                w[u] = *reinterpret_cast<const uint32_t*>(&hv);
+              }
+              *reinterpret_cast<uint4*>(orow + cb * 32 + j8 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            *reinterpret_cast<uint4*>(orow + cb * 32 + j8 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
       }
@@ -405,13 +487,13 @@ cudaError_t launch_prefill_t(const PrefillArgs& g, cudaStream_t stream) {
   p.max_blocks = g.max_blocks;
   p.num_blocks = g.num_blocks;
   p.block_size = g.block_size;
-  p.qtiles = (g.max_query_len + kQT - 1) / kQT;
+  p.qpairs = (g.max_query_len + 2 * kQT - 1) / (2 * kQT);
   p.max_query_len = g.max_query_len;
   p.oob_row = (int)rows;
   p.scale_log2 = g.scale_log2;
-  const long long grid = (long long)g.num_seqs * p.qtiles * g.num_heads;
-  return launch_pdl(prefill_kernel<D>, dim3((unsigned)grid), dim3(128), (size_t)T::SMEM, stream, tq,
-                    tk, tv, p);
+  const long long grid = (long long)g.num_seqs * p.qpairs * g.num_heads;
+  return launch_pdl(prefill_kernel<D>, dim3((unsigned)grid), dim3(T::THREADS), (size_t)T::SMEM,
+                    stream, tq, tk, tv, p);
 }
 
 }  // namespace
