@@ -60,11 +60,24 @@ struct PrefillTraits {
   // holds an SM (each CTA allocates all 512 TMEM columns).
   static constexpr int SMEM_USED = OFF_BAR + 256 + 1024;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
-  static constexpr int THREADS = 288;               // two softmax warpgroups + one MMA/TMA warp
+  // Two softmax warpgroups and one producer warpgroup (its first warp issues
+  // the TMA copies and the MMAs).  Registers: the kernel is compiled for 384
+  // threads at kRegsLaunch each; the producer warpgroup gives registers back
+  // and the softmax warpgroups take them (the split never exceeds the launch
+  // allocation: kRegsSplit <= 384 * registers per thread at launch).
+  static constexpr int THREADS = 384;
   static constexpr uint32_t TMEM_COLS = 512;        // S_x: 128 columns each, O_x: D columns each
   static constexpr uint32_t COL_O = 256;
   static_assert(D == 64 || D == 128, "head_dim");
 };
+
+constexpr int kRegsSoftmax = 200;
+constexpr int kRegsProducer = 96;
+// Registers the split needs at launch (per block); the launcher checks the
+// compiled kernel's count against it before the first launch, since a
+// setmaxnreg.inc beyond the block's allocation would wait forever.
+constexpr int kRegsSplit = 2 * 128 * kRegsSoftmax + 128 * kRegsProducer;
+static_assert(kRegsSplit <= 65536, "register split exceeds the register file");
 
 struct PrefillParams {
   void* out;                     // fp16 [TQ][H][D]
@@ -113,7 +126,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(sm);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + T::OFF_BAR);
-  // barriers: 0 q_full; 1,2 kv_full[st]; 3,4 s_full[x]; 5,6 p_full[x]; 7,8 o_full[x]
+  // barriers: 0 q_full; 1,2 kv_full[st]; 3,4 s_full[x]; 5,6 p_full[x]; 7,8 o_full[x]; 9 done
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + T::OFF_BAR + 128);
   int* fail = reinterpret_cast<int*>(sm + T::OFF_BAR + 132);
@@ -137,6 +150,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
     mbar_init(bar(6), 128);
     mbar_init(bar(7), 1);
     mbar_init(bar(8), 1);
+    mbar_init(bar(9), T::THREADS);
     *fail = 0;
     fence_mbar_init();
     prefetch_tensormap(&tq);
@@ -171,27 +185,38 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
   }
   const int n_kv = max(qx[0].n_kv, qx[1].n_kv);
 
-  if (warp == 8 && n_kv > 0) {
+  // The roles never meet again: each ends by arriving on the done barrier,
+  // after which warp 0 frees the tensor memory.
+  if (warp >= 8) {
+    setmaxnreg_dec<kRegsProducer>();
+    if (warp == 8 && n_kv > 0) {
     // ---------------- TMA producer and MMA issuer (lane 0; the warp zeroes V rows)
     const int32_t* bt = a.block_tables + (size_t)s * a.max_blocks;
     const int bpt = kKT / a.block_size;
     int kv_issued = 0, qk[2] = {0, 0}, pv[2] = {0, 0};
-    auto issue_kv = [&](int t) {
+    // Cache row of block `lane` of KV tile t (lanes < bpt; one load per lane,
+    // fetched a tile ahead so no copy waits on the block table).
+    auto tile_row = [&](int t) {
+      const int lb = t * bpt + lane;
+      int row = a.oob_row;
+      if (lane < bpt && t < n_kv && lb * a.block_size < c) {
+        const int phys = bt[lb];
+        if (phys >= 0 && phys < a.num_blocks)
+          row = (phys * H + h) * a.block_size;
+        else
+          atomicOr(a.err, PA_ERRBIT_BLOCK_ID);
+      }
+      return row;
+    };
+    // Warp-wide: K and V tile t into stage t & 1, lane b issuing block b's boxes.
+    auto issue_kv = [&](int t, int row) {
       const int st = t & 1;
       const uint32_t kdst = s_base + T::OFF_K0 + st * 2 * T::KB;
       const uint32_t vdst = kdst + T::KB;
-      mbar_arrive_expect_tx(bar(1 + st), 2 * T::KB);
-      for (int b = 0; b < bpt; ++b) {
-        const int lb = t * bpt + b;
-        int row = a.oob_row;
-        if (lb * a.block_size < c) {
-          const int phys = bt[lb];
-          if (phys >= 0 && phys < a.num_blocks)
-            row = (phys * H + h) * a.block_size;
-          else
-            atomicOr(a.err, PA_ERRBIT_BLOCK_ID);
-        }
-        const uint32_t roff = (uint32_t)(b * a.block_size * 128);
+      if (lane == 0) mbar_arrive_expect_tx(bar(1 + st), 2 * T::KB);
+      __syncwarp();
+      if (lane < bpt) {
+        const uint32_t roff = (uint32_t)(lane * a.block_size * 128);
 #pragma unroll
         for (int at = 0; at < T::NA; ++at) {
           tma_load_2d(kdst + at * T::ATOM + roff, &tk, at * 64, row, bar(1 + st));
@@ -253,11 +278,16 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
           for (int at = 0; at < T::NA; ++at)
             tma_load_3d(s_base + T::OFF_Q + x * T::QB + at * T::ATOM, &tq, at * 64, h,
                         q0 + (2 * pq + x) * kQT, bar(0));
-      issue_kv(0);
-      if (n_kv > 1) issue_kv(1);
     }
-    ok = mbar_wait_bounded(bar(0), 0) && wait_kv(0);
-    ok = __all_sync(kFullMask, ok);
+    int row_next;  // this lane's block row of the next tile to issue
+    {
+      const int r0 = tile_row(0);
+      const int r1 = tile_row(1);
+      issue_kv(0, r0);
+      if (n_kv > 1) issue_kv(1, r1);
+      row_next = tile_row(2);
+    }
+    ok = __all_sync(kFullMask, mbar_wait_bounded(bar(0), 0) && wait_kv(0));
     if (ok) {
       zero_v_tail(0);
       if (lane == 0) {
@@ -277,32 +307,36 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       }
       return r;
     };
+    // Every wait result is made warp-uniform at once, so all branches below
+    // (including the warp-wide TMA issue) are taken by the whole warp.
+    auto uni = [&](bool v) { return __all_sync(kFullMask, v); };
     for (int t = 0; t < n_kv && ok; ++t) {
       const bool a0 = t < qx[0].n_kv, a1 = t < qx[1].n_kv;
       const bool n0 = t + 1 < qx[0].n_kv, n1 = t + 1 < qx[1].n_kv;
-      if (a0) ok = ok && p_w[0].wait();
+      if (a0) ok = uni(p_w[0].wait());
       if (ok && lane == 0 && a0) pv_mma(0, t);
       if (ok && t + 1 < n_kv) {
-        ok = wait_kv(t + 1);
-        ok = __all_sync(kFullMask, ok);
+        ok = uni(wait_kv(t + 1));
         if (ok) zero_v_tail(t + 1);
       }
       if (ok && n0) {
-        ok = wait_o(0, t);
+        ok = uni(wait_o(0, t));
         if (ok && lane == 0) qk_mma(0, t + 1);
       }
-      if (ok && a1) ok = p_w[1].wait();
+      if (ok && a1) ok = uni(p_w[1].wait());
       if (ok && lane == 0 && a1) pv_mma(1, t);
       if (ok && n1) {
-        ok = wait_o(1, t);
+        ok = uni(wait_o(1, t));
         if (ok && lane == 0) qk_mma(1, t + 1);
       }
       if (ok && t + 2 < n_kv) {  // stage (t & 1) is free once both P.V of tile t are done
-        if (a0) ok = ok && wait_o(0, t);
-        if (a1) ok = ok && wait_o(1, t);
-        if (ok && lane == 0) issue_kv(t + 2);
+        if (a0) ok = uni(wait_o(0, t));
+        if (ok && a1) ok = uni(wait_o(1, t));
+        if (ok) {
+          issue_kv(t + 2, row_next);
+          row_next = tile_row(t + 3);
+        }
       }
-      ok = __all_sync(kFullMask, ok);
     }
     if (!ok) {
       if (lane == 0) {
@@ -317,7 +351,13 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
         }
       }
     }
-  } else if (warp < 8) {
+    }
+    tc_fence_before();
+    mbar_arrive(bar(9));
+    return;
+  }
+  setmaxnreg_inc<kRegsSoftmax>();
+  {
     // ---------------- softmax warpgroup x: one query row per thread
     const int x = warp >> 2;
     const int row = tid & 127;
@@ -333,15 +373,14 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       ok = s_w.wait();
       if (!ok || *fail) { ok = false; break; }
       tc_fence_after();
+      uint32_t sr[kKT];
+#pragma unroll
+      for (int cb = 0; cb < kKT / 32; ++cb)
+        tmem_ld32(t_s + cb * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cb * 32]));
+      tmem_wait_ld();  // one wait for all four loads
       float xv[kKT];
 #pragma unroll
-      for (int cb = 0; cb < kKT / 32; ++cb) {
-        uint32_t r[32];
-        tmem_ld32(t_s + cb * 32, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) xv[cb * 32 + j] = __uint_as_float(r[j]);
-      }
+      for (int j = 0; j < kKT; ++j) xv[j] = __uint_as_float(sr[j]);
       const int kv0 = t * kKT;
       if (kv0 + kKT - 1 > qt.pos_min) {  // tile reaches the diagonal (or the context end)
         const int lim = min(qpos, c - 1) - kv0;
@@ -349,33 +388,42 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
         for (int j = 0; j < kKT; ++j)
           if (j > lim) xv[j] = -INFINITY;
       }
-      float mx = m;
+      // Independent partial maxima and sums keep the dependency chains short
+      // (one warp per scheduler runs this code).
+      float mq[4] = {m, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int j = 0; j < kKT; j += 2) mx = fmax3(mx, xv[j], xv[j + 1]);
+      for (int j = 0; j < kKT; j += 8)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) mq[u] = fmax3(mq[u], xv[j + 2 * u], xv[j + 2 * u + 1]);
+      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       const float alpha = (mx == -INFINITY) ? 1.f : exp2_approx((m - mx) * a.scale_log2);
       const float neg = (mx == -INFINITY) ? 0.f : -mx * a.scale_log2;
-      float ps = 0.f;
+      float sq[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[kKT / 2];
 #pragma unroll
       for (int j = 0; j < kKT / 2; ++j) {
         const float p0 = exp2_approx(fmaf(xv[2 * j], a.scale_log2, neg));
         const float p1 = exp2_approx(fmaf(xv[2 * j + 1], a.scale_log2, neg));
-        ps += p0 + p1;
+        sq[j & 3] += p0 + p1;
         const __half2 hp = __floats2half2_rn(p0, p1);
         pk[j] = *reinterpret_cast<const uint32_t*>(&hp);
       }
-      l = l * alpha + ps;
+      l = l * alpha + ((sq[0] + sq[1]) + (sq[2] + sq[3]));
       m = mx;
       // O(x, t - 1) is complete here: S(x, t) was computed after it.
       if (t > 0 && __any_sync(kFullMask, alpha != 1.f)) {
 #pragma unroll
-        for (int cb = 0; cb < D / 32; ++cb) {
-          uint32_t r[32];
-          tmem_ld32(t_o + cb * 32, r);
+        for (int cb = 0; cb < D / 32; cb += 2) {
+          uint32_t r[2][32];
+          tmem_ld32(t_o + cb * 32, r[0]);
+          tmem_ld32(t_o + cb * 32 + 32, r[1]);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-          tmem_st32(t_o + cb * 32, r);
+          for (int u = 0; u < 2; ++u) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[u][j] = __float_as_uint(__uint_as_float(r[u][j]) * alpha);
+            tmem_st32(t_o + (cb + u) * 32, r[u]);
+          }
         }
       }
       // P (fp16 pairs) over the first 64 columns of this tile's S.
@@ -424,8 +472,9 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
     }
   }
   tc_fence_before();
-  __syncthreads();
+  mbar_arrive(bar(9));
   if (warp == 0) {
+    if (!mbar_wait_bounded(bar(9), 0) && lane == 0) atomicOr(a.err, PA_ERRBIT_TIMEOUT);
     tc_fence_after();
     tmem_dealloc(tmem, T::TMEM_COLS);
   }
@@ -461,8 +510,13 @@ cudaError_t launch_prefill_t(const PrefillArgs& g, cudaStream_t stream) {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    T::SMEM);
+    cudaFuncAttributes fa{};
+    attr_err = cudaFuncGetAttributes(&fa, prefill_kernel<D>);
+    if (attr_err == cudaSuccess && fa.numRegs * T::THREADS < kRegsSplit)
+      attr_err = cudaErrorInvalidConfiguration;  // never launch a split that could not be granted
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(prefill_kernel<D>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap tq, tk, tv;

@@ -102,6 +102,20 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ---- per-warpgroup register budgets -----------------------------------------
+// Executed by every warp of a warpgroup.  The budgets of all warpgroups must
+// not exceed the block's launch allocation (threads x registers at launch).
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---- tcgen05.mma (kind::f16, one CTA) --------------------------------------
 
 // Shared-memory matrix descriptor, 128-byte swizzle: start address, leading
