@@ -126,7 +126,8 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(sm);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + T::OFF_BAR);
-  // barriers: 0 q_full; 1,2 kv_full[st]; 3,4 s_full[x]; 5,6 p_full[x]; 7,8 o_full[x]; 9 done
+  // barriers: 0 q_full; 1,2 kv_full[st]; 3,4 s_full[x]; 5,6 p_full[x]; 7,8 o_full[x]; 9 done;
+  // 10,11 kv_empty[st]
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + T::OFF_BAR + 128);
   int* fail = reinterpret_cast<int*>(sm + T::OFF_BAR + 132);
@@ -151,6 +152,8 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
     mbar_init(bar(7), 1);
     mbar_init(bar(8), 1);
     mbar_init(bar(9), T::THREADS);
+    mbar_init(bar(10), 1);
+    mbar_init(bar(11), 1);
     *fail = 0;
     fence_mbar_init();
     prefetch_tensormap(&tq);
@@ -189,42 +192,70 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
   // after which warp 0 frees the tensor memory.
   if (warp >= 8) {
     setmaxnreg_dec<kRegsProducer>();
-    if (warp == 8 && n_kv > 0) {
-    // ---------------- TMA producer and MMA issuer (lane 0; the warp zeroes V rows)
-    const int32_t* bt = a.block_tables + (size_t)s * a.max_blocks;
-    const int bpt = kKT / a.block_size;
-    int kv_issued = 0, qk[2] = {0, 0}, pv[2] = {0, 0};
-    // Cache row of block `lane` of KV tile t (lanes < bpt; one load per lane,
-    // fetched a tile ahead so no copy waits on the block table).
-    auto tile_row = [&](int t) {
-      const int lb = t * bpt + lane;
-      int row = a.oob_row;
-      if (lane < bpt && t < n_kv && lb * a.block_size < c) {
-        const int phys = bt[lb];
-        if (phys >= 0 && phys < a.num_blocks)
-          row = (phys * H + h) * a.block_size;
-        else
-          atomicOr(a.err, PA_ERRBIT_BLOCK_ID);
-      }
-      return row;
-    };
-    // Warp-wide: K and V tile t into stage t & 1, lane b issuing block b's boxes.
-    auto issue_kv = [&](int t, int row) {
-      const int st = t & 1;
-      const uint32_t kdst = s_base + T::OFF_K0 + st * 2 * T::KB;
-      const uint32_t vdst = kdst + T::KB;
-      if (lane == 0) mbar_arrive_expect_tx(bar(1 + st), 2 * T::KB);
-      __syncwarp();
-      if (lane < bpt) {
-        const uint32_t roff = (uint32_t)(lane * a.block_size * 128);
-#pragma unroll
-        for (int at = 0; at < T::NA; ++at) {
-          tma_load_2d(kdst + at * T::ATOM + roff, &tk, at * 64, row, bar(1 + st));
-          tma_load_2d(vdst + at * T::ATOM + roff, &tv, at * 64, row, bar(1 + st));
+    // kv_full of tile t: barrier 1 + (t & 1), parity (t >> 1) & 1; kv_empty of
+    // stage st (barrier 10 + st) completes once per tile that used it.
+    auto wait_kv = [&](int t) { return mbar_wait_bounded(bar(1 + (t & 1)), (t >> 1) & 1); };
+    if (warp == 9 && n_kv > 0) {
+      // ---------------- TMA warp: Q tiles, then K/V tiles into a two-stage ring
+      const int32_t* bt = a.block_tables + (size_t)s * a.max_blocks;
+      const int bpt = kKT / a.block_size;
+      // Cache row of block `lane` of KV tile t (lanes < bpt; one load per lane,
+      // fetched a tile ahead so no copy waits on the block table).
+      auto tile_row = [&](int t) {
+        const int lb = t * bpt + lane;
+        int row = a.oob_row;
+        if (lane < bpt && t < n_kv && lb * a.block_size < c) {
+          const int phys = bt[lb];
+          if (phys >= 0 && phys < a.num_blocks)
+            row = (phys * H + h) * a.block_size;
+          else
+            atomicOr(a.err, PA_ERRBIT_BLOCK_ID);
         }
+        return row;
+      };
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(0), (qx[1].rows > 0 ? 2 : 1) * T::QB);
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+          if (qx[x].rows > 0)
+#pragma unroll
+            for (int at = 0; at < T::NA; ++at)
+              tma_load_3d(s_base + T::OFF_Q + x * T::QB + at * T::ATOM, &tq, at * 64, h,
+                          q0 + (2 * pq + x) * kQT, bar(0));
       }
-      ++kv_issued;
-    };
+      int row = tile_row(0);
+      int issued = 0;
+      bool ok = true;
+      for (int t = 0; t < n_kv; ++t) {
+        const int st = t & 1;
+        if (t >= 2) {  // the P.V of tile t - 2 released this stage
+          ok = __all_sync(kFullMask, mbar_wait_bounded(bar(10 + st), ((t >> 1) - 1) & 1));
+          if (!ok) break;
+        }
+        const uint32_t kdst = s_base + T::OFF_K0 + st * 2 * T::KB;
+        const uint32_t vdst = kdst + T::KB;
+        if (lane == 0) mbar_arrive_expect_tx(bar(1 + st), 2 * T::KB);
+        __syncwarp();
+        if (lane < bpt) {  // lane b issues block b's boxes
+          const uint32_t roff = (uint32_t)(lane * a.block_size * 128);
+#pragma unroll
+          for (int at = 0; at < T::NA; ++at) {
+            tma_load_2d(kdst + at * T::ATOM + roff, &tk, at * 64, row, bar(1 + st));
+            tma_load_2d(vdst + at * T::ATOM + roff, &tv, at * 64, row, bar(1 + st));
+          }
+        }
+        ++issued;
+        row = tile_row(t + 1);
+      }
+      if (!ok && lane == 0) {
+        *fail = 1;
+        // Let the copies this warp started land (bounded) before the shared
+        // memory is released.
+        for (int u = max(0, issued - 2); u < issued; ++u) wait_kv(u);
+      }
+    } else if (warp == 8 && n_kv > 0) {
+    // ---------------- MMA issuer (lane 0; the warp zeroes V rows past the context)
+    int qk[2] = {0, 0}, pv[2] = {0, 0}, rel = 0;
     constexpr uint32_t kIdQK = umma_idesc_f16(kQT, kKT, false, false);
     constexpr uint32_t kIdPV = umma_idesc_f16(kQT, D, false, true);
     auto qk_mma = [&](int x, int t) {
@@ -240,7 +271,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       umma_commit(bar(3 + x));
       ++qk[x];
     };
-    auto pv_mma = [&](int x, int t) {
+    auto pv_mma = [&](int x, int t, bool release) {
       const uint32_t vaddr = s_base + T::OFF_K0 + (t & 1) * 2 * T::KB + T::KB;
       tc_fence_after();
 #pragma unroll
@@ -250,6 +281,10 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       }
       umma_commit(bar(7 + x));
       ++pv[x];
+      if (release) {  // the last reader of stage t & 1: hand it back to the TMA warp
+        umma_commit(bar(10 + (t & 1)));
+        ++rel;
+      }
     };
     // V rows of tile t past the context: zeroed by the whole warp after the
     // tile has landed (stale slots may hold anything; 0 * NaN would poison O).
@@ -265,29 +300,8 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       fence_proxy_async_smem();
       __syncwarp();
     };
-    // kv_full of tile t: barrier 1 + (t & 1), parity (t >> 1) & 1.
-    auto wait_kv = [&](int t) { return mbar_wait_bounded(bar(1 + (t & 1)), (t >> 1) & 1); };
     Waiter p_w[2] = {{bar(5)}, {bar(6)}}, o_w[2] = {{bar(7)}, {bar(8)}};
-    bool ok = true;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar(0), (qx[1].rows > 0 ? 2 : 1) * T::QB);
-#pragma unroll
-      for (int x = 0; x < 2; ++x)
-        if (qx[x].rows > 0)
-#pragma unroll
-          for (int at = 0; at < T::NA; ++at)
-            tma_load_3d(s_base + T::OFF_Q + x * T::QB + at * T::ATOM, &tq, at * 64, h,
-                        q0 + (2 * pq + x) * kQT, bar(0));
-    }
-    int row_next;  // this lane's block row of the next tile to issue
-    {
-      const int r0 = tile_row(0);
-      const int r1 = tile_row(1);
-      issue_kv(0, r0);
-      if (n_kv > 1) issue_kv(1, r1);
-      row_next = tile_row(2);
-    }
-    ok = __all_sync(kFullMask, mbar_wait_bounded(bar(0), 0) && wait_kv(0));
+    bool ok = __all_sync(kFullMask, mbar_wait_bounded(bar(0), 0) && wait_kv(0));
     if (ok) {
       zero_v_tail(0);
       if (lane == 0) {
@@ -308,13 +322,13 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       return r;
     };
     // Every wait result is made warp-uniform at once, so all branches below
-    // (including the warp-wide TMA issue) are taken by the whole warp.
+    // are taken by the whole warp.
     auto uni = [&](bool v) { return __all_sync(kFullMask, v); };
     for (int t = 0; t < n_kv && ok; ++t) {
       const bool a0 = t < qx[0].n_kv, a1 = t < qx[1].n_kv;
       const bool n0 = t + 1 < qx[0].n_kv, n1 = t + 1 < qx[1].n_kv;
       if (a0) ok = uni(p_w[0].wait());
-      if (ok && lane == 0 && a0) pv_mma(0, t);
+      if (ok && lane == 0 && a0) pv_mma(0, t, !a1);
       if (ok && t + 1 < n_kv) {
         ok = uni(wait_kv(t + 1));
         if (ok) zero_v_tail(t + 1);
@@ -324,31 +338,23 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
         if (ok && lane == 0) qk_mma(0, t + 1);
       }
       if (ok && a1) ok = uni(p_w[1].wait());
-      if (ok && lane == 0 && a1) pv_mma(1, t);
+      if (ok && lane == 0 && a1) pv_mma(1, t, true);
       if (ok && n1) {
         ok = uni(wait_o(1, t));
         if (ok && lane == 0) qk_mma(1, t + 1);
-      }
-      if (ok && t + 2 < n_kv) {  // stage (t & 1) is free once both P.V of tile t are done
-        if (a0) ok = uni(wait_o(0, t));
-        if (ok && a1) ok = uni(wait_o(1, t));
-        if (ok) {
-          issue_kv(t + 2, row_next);
-          row_next = tile_row(t + 3);
-        }
       }
     }
     if (!ok) {
       if (lane == 0) {
         atomicOr(a.err, PA_ERRBIT_TIMEOUT);
         *fail = 1;
-        // Let every copy and MMA this CTA started finish (bounded) before the
-        // TMEM and shared memory are released.
+        // Let every MMA this warp started finish (bounded) before the TMEM and
+        // shared memory are released.
         for (int i = 0; i < 2; ++i) {
-          if (kv_issued > i) mbar_wait_bounded(bar(1 + i), ((kv_issued - 1 - ((kv_issued - 1 - i) & 1)) >> 1) & 1);
           if (qk[i] > 0) mbar_wait_bounded(bar(3 + i), (qk[i] - 1) & 1);
           if (pv[i] > 0) mbar_wait_bounded(bar(7 + i), (pv[i] - 1) & 1);
         }
+        if (rel > 0) mbar_wait_bounded(bar(10 + ((rel - 1) & 1)), (((rel - 1) >> 1)) & 1);
       }
     }
     }
