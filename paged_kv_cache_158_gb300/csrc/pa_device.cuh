@@ -134,6 +134,34 @@ __device__ __forceinline__ float exp2_approx(float x) {
   return y;
 }
 
+// (2^a, 2^b) as a packed fp16 pair (low half = 2^a): the arguments are
+// rounded to fp16 and one ex2.approx.f16x2 computes both.
+__device__ __forceinline__ uint32_t exp2_f16x2(float a, float b) {
+  uint32_t r;
+  asm("{\n"
+      "  .reg .b32 x;\n"
+      "  cvt.rn.f16x2.f32 x, %2, %1;\n"
+      "  ex2.approx.f16x2 %0, x;\n"
+      "}\n"
+      : "=r"(r)
+      : "f"(a), "f"(b));
+  return r;
+}
+
+// acc + lo(h) + hi(h) for a packed fp16 pair, in fp32 (each add rounded once).
+__device__ __forceinline__ float add_f16x2_f32(uint32_t h, float acc) {
+  asm("{\n"
+      "  .reg .f16 h0, h1, one;\n"
+      "  mov.b32 {h0, h1}, %1;\n"
+      "  mov.b16 one, 0x3C00;\n"
+      "  fma.rn.f32.f16 %0, h0, one, %0;\n"
+      "  fma.rn.f32.f16 %0, h1, one, %0;\n"
+      "}\n"
+      : "+f"(acc)
+      : "r"(h));
+  return acc;
+}
+
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;

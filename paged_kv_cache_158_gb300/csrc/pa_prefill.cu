@@ -21,10 +21,12 @@
 //  * Each thread owns one query row (TMEM lane = row): it reads its S row
 //    with tcgen05.ld, applies the causal and context masks, keeps the online
 //    softmax (m in raw logit units, l in fp32, exponentials in base 2 with
-//    the scale folded into one fused multiply-add), rounds P to fp16 for the
-//    second MMA and writes it to shared memory in the swizzled K-major
-//    layout that MMA reads, and rescales its O row in TMEM when the running
-//    maximum grows.  Masks are applied only on tiles that reach the
+//    the scale folded into one fused multiply-add; the exponentials of a
+//    pair of arguments run as one packed fp16 ex2, whose fp16 results are
+//    the P operand of the second MMA and are summed in fp32 for l), and
+//    rescales its O row in TMEM when its reference maximum moves, which it
+//    does only when the row's maximum exceeds it by more than 2^8 (weights
+//    stay <= 256, exact in fp16 range and summed in fp32).  Masks are applied only on tiles that reach the
 //    diagonal or the context end.  V rows past the context are zeroed in shared
 //    memory (0 * NaN in stale slots would poison the sum).
 //  * Work per KV tile: the TMA of the next tile overlaps the softmax and
@@ -126,20 +128,22 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(sm);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + T::OFF_BAR);
-  // barriers: 0 q_full; 1,2 kv_full[st]; 3,4 s_full[x]; 5,6 p_full[x]; 7,8 o_full[x]; 9 done;
-  // 10,11 kv_empty[st]
+  // barriers: 0 q_full; 1,2 k_full[st]; 3,4 s_full[x]; 5,6 p_full[x]; 7,8 o_full[x]; 9 done;
+  // 10,11 k_empty[st]; 12,13 v_full[st]; 14,15 v_empty[st]
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + T::OFF_BAR + 128);
-  int* fail = reinterpret_cast<int*>(sm + T::OFF_BAR + 132);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + T::OFF_BAR + 192);
+  int* fail = reinterpret_cast<int*>(sm + T::OFF_BAR + 196);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int H = a.num_heads;
-  const int h = blockIdx.x % H;
-  const int rest = blockIdx.x / H;
-  const int s = rest % a.num_seqs;
-  const int pq = a.qpairs - 1 - rest / a.num_seqs;  // heaviest pairs first
+  // Pairs of one (sequence, head) are adjacent in the grid, heaviest first:
+  // they run together and read the same K/V tiles, the second from L2.
+  const int pq = a.qpairs - 1 - (int)(blockIdx.x % a.qpairs);
+  const int rest = blockIdx.x / a.qpairs;
+  const int h = rest % H;
+  const int s = rest / H;
 
   if (tid == 0) {
     mbar_init(bar(0), 1);
@@ -152,8 +156,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
     mbar_init(bar(7), 1);
     mbar_init(bar(8), 1);
     mbar_init(bar(9), T::THREADS);
-    mbar_init(bar(10), 1);
-    mbar_init(bar(11), 1);
+    for (int i = 10; i < 16; ++i) mbar_init(bar(i), 1);
     *fail = 0;
     fence_mbar_init();
     prefetch_tensormap(&tq);
@@ -192,9 +195,12 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
   // after which warp 0 frees the tensor memory.
   if (warp >= 8) {
     setmaxnreg_dec<kRegsProducer>();
-    // kv_full of tile t: barrier 1 + (t & 1), parity (t >> 1) & 1; kv_empty of
-    // stage st (barrier 10 + st) completes once per tile that used it.
-    auto wait_kv = [&](int t) { return mbar_wait_bounded(bar(1 + (t & 1)), (t >> 1) & 1); };
+    // K and V of tile t sit in stage t & 1 of two separate rings: k_full / v_full
+    // (barriers 1 + st / 12 + st) complete once per tile, parity (t >> 1) & 1;
+    // k_empty / v_empty (10 + st / 14 + st) once per tile that used the stage.
+    // K is released after the tile's QK products, V after its P.V products.
+    auto wait_k = [&](int t) { return mbar_wait_bounded(bar(1 + (t & 1)), (t >> 1) & 1); };
+    auto wait_v = [&](int t) { return mbar_wait_bounded(bar(12 + (t & 1)), (t >> 1) & 1); };
     if (warp == 9 && n_kv > 0) {
       // ---------------- TMA warp: Q tiles, then K/V tiles into a two-stage ring
       const int32_t* bt = a.block_tables + (size_t)s * a.max_blocks;
@@ -223,42 +229,50 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
               tma_load_3d(s_base + T::OFF_Q + x * T::QB + at * T::ATOM, &tq, at * 64, h,
                           q0 + (2 * pq + x) * kQT, bar(0));
       }
-      int row = tile_row(0);
-      int issued = 0;
-      bool ok = true;
-      for (int t = 0; t < n_kv; ++t) {
+      // Program order per tile: K(t) then V(t); K(t + 1) needs the QK of
+      // tile t - 1, which the MMA warp issues after the P.V of tile t - 2 that
+      // frees V(t)'s stage, so this order never waits on a later release.
+      auto issue = [&](int t, int row, bool is_v) {
         const int st = t & 1;
-        if (t >= 2) {  // the P.V of tile t - 2 released this stage
-          ok = __all_sync(kFullMask, mbar_wait_bounded(bar(10 + st), ((t >> 1) - 1) & 1));
-          if (!ok) break;
-        }
-        const uint32_t kdst = s_base + T::OFF_K0 + st * 2 * T::KB;
-        const uint32_t vdst = kdst + T::KB;
-        if (lane == 0) mbar_arrive_expect_tx(bar(1 + st), 2 * T::KB);
+        const uint32_t dst = s_base + T::OFF_K0 + st * 2 * T::KB + (is_v ? T::KB : 0);
+        const uint32_t fb = bar((is_v ? 12 : 1) + st);
+        if (lane == 0) mbar_arrive_expect_tx(fb, T::KB);
         __syncwarp();
         if (lane < bpt) {  // lane b issues block b's boxes
           const uint32_t roff = (uint32_t)(lane * a.block_size * 128);
 #pragma unroll
-          for (int at = 0; at < T::NA; ++at) {
-            tma_load_2d(kdst + at * T::ATOM + roff, &tk, at * 64, row, bar(1 + st));
-            tma_load_2d(vdst + at * T::ATOM + roff, &tv, at * 64, row, bar(1 + st));
-          }
+          for (int at = 0; at < T::NA; ++at)
+            tma_load_2d(dst + at * T::ATOM + roff, is_v ? &tv : &tk, at * 64, row, fb);
         }
-        ++issued;
+      };
+      int row = tile_row(0);
+      int k_issued = 0, v_issued = 0;
+      bool ok = true;
+      for (int t = 0; t < n_kv && ok; ++t) {
+        const int st = t & 1;
+        if (t >= 2) ok = __all_sync(kFullMask, mbar_wait_bounded(bar(10 + st), ((t >> 1) - 1) & 1));
+        if (!ok) break;
+        issue(t, row, false);
+        ++k_issued;
+        if (t >= 2) ok = __all_sync(kFullMask, mbar_wait_bounded(bar(14 + st), ((t >> 1) - 1) & 1));
+        if (!ok) break;
+        issue(t, row, true);
+        ++v_issued;
         row = tile_row(t + 1);
       }
       if (!ok && lane == 0) {
         *fail = 1;
         // Let the copies this warp started land (bounded) before the shared
         // memory is released.
-        for (int u = max(0, issued - 2); u < issued; ++u) wait_kv(u);
+        for (int u = max(0, k_issued - 2); u < k_issued; ++u) wait_k(u);
+        for (int u = max(0, v_issued - 2); u < v_issued; ++u) wait_v(u);
       }
     } else if (warp == 8 && n_kv > 0) {
     // ---------------- MMA issuer (lane 0; the warp zeroes V rows past the context)
-    int qk[2] = {0, 0}, pv[2] = {0, 0}, rel = 0;
+    int qk[2] = {0, 0}, pv[2] = {0, 0}, krel = 0, vrel = 0;
     constexpr uint32_t kIdQK = umma_idesc_f16(kQT, kKT, false, false);
     constexpr uint32_t kIdPV = umma_idesc_f16(kQT, D, false, true);
-    auto qk_mma = [&](int x, int t) {
+    auto qk_mma = [&](int x, int t, bool release) {
       const uint32_t kaddr = s_base + T::OFF_K0 + (t & 1) * 2 * T::KB;
       tc_fence_after();
 #pragma unroll
@@ -270,6 +284,10 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       }
       umma_commit(bar(3 + x));
       ++qk[x];
+      if (release) {  // the last reader of K stage t & 1
+        umma_commit(bar(10 + (t & 1)));
+        ++krel;
+      }
     };
     auto pv_mma = [&](int x, int t, bool release) {
       const uint32_t vaddr = s_base + T::OFF_K0 + (t & 1) * 2 * T::KB + T::KB;
@@ -281,9 +299,9 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       }
       umma_commit(bar(7 + x));
       ++pv[x];
-      if (release) {  // the last reader of stage t & 1: hand it back to the TMA warp
-        umma_commit(bar(10 + (t & 1)));
-        ++rel;
+      if (release) {  // the last reader of V stage t & 1
+        umma_commit(bar(14 + (t & 1)));
+        ++vrel;
       }
     };
     // V rows of tile t past the context: zeroed by the whole warp after the
@@ -301,13 +319,10 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       __syncwarp();
     };
     Waiter p_w[2] = {{bar(5)}, {bar(6)}}, o_w[2] = {{bar(7)}, {bar(8)}};
-    bool ok = __all_sync(kFullMask, mbar_wait_bounded(bar(0), 0) && wait_kv(0));
-    if (ok) {
-      zero_v_tail(0);
-      if (lane == 0) {
-        qk_mma(0, 0);
-        if (qx[1].n_kv > 0) qk_mma(1, 0);
-      }
+    bool ok = __all_sync(kFullMask, mbar_wait_bounded(bar(0), 0) && wait_k(0));
+    if (ok && lane == 0) {
+      qk_mma(0, 0, qx[1].n_kv == 0);
+      if (qx[1].n_kv > 0) qk_mma(1, 0, true);
     }
     // O(x, t - 1) must be complete before S(x, t) overwrites P(x, t - 1), so each
     // QK waits for the previous P.V of its own tile; the other tile's work
@@ -327,21 +342,20 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
     for (int t = 0; t < n_kv && ok; ++t) {
       const bool a0 = t < qx[0].n_kv, a1 = t < qx[1].n_kv;
       const bool n0 = t + 1 < qx[0].n_kv, n1 = t + 1 < qx[1].n_kv;
-      if (a0) ok = uni(p_w[0].wait());
+      ok = uni(wait_v(t));
+      if (ok) zero_v_tail(t);
+      if (ok && a0) ok = uni(p_w[0].wait());
       if (ok && lane == 0 && a0) pv_mma(0, t, !a1);
-      if (ok && t + 1 < n_kv) {
-        ok = uni(wait_kv(t + 1));
-        if (ok) zero_v_tail(t + 1);
-      }
+      if (ok && t + 1 < n_kv) ok = uni(wait_k(t + 1));
       if (ok && n0) {
         ok = uni(wait_o(0, t));
-        if (ok && lane == 0) qk_mma(0, t + 1);
+        if (ok && lane == 0) qk_mma(0, t + 1, !n1);
       }
       if (ok && a1) ok = uni(p_w[1].wait());
       if (ok && lane == 0 && a1) pv_mma(1, t, true);
       if (ok && n1) {
         ok = uni(wait_o(1, t));
-        if (ok && lane == 0) qk_mma(1, t + 1);
+        if (ok && lane == 0) qk_mma(1, t + 1, true);
       }
     }
     if (!ok) {
@@ -354,7 +368,8 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
           if (qk[i] > 0) mbar_wait_bounded(bar(3 + i), (qk[i] - 1) & 1);
           if (pv[i] > 0) mbar_wait_bounded(bar(7 + i), (pv[i] - 1) & 1);
         }
-        if (rel > 0) mbar_wait_bounded(bar(10 + ((rel - 1) & 1)), (((rel - 1) >> 1)) & 1);
+        if (krel > 0) mbar_wait_bounded(bar(10 + ((krel - 1) & 1)), ((krel - 1) >> 1) & 1);
+        if (vrel > 0) mbar_wait_bounded(bar(14 + ((vrel - 1) & 1)), ((vrel - 1) >> 1) & 1);
       }
     }
     }
@@ -372,6 +387,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
     const uint32_t t_s = tmem + 128 * x + lane_off;
     const uint32_t t_o = tmem + T::COL_O + D * x + lane_off;
     const int qpos = qt.pos_min + row;
+    const float lazy_raw = 8.f / a.scale_log2;  // 8 in base-2 units, as a raw logit difference
     float m = -INFINITY, l = 0.f;
     Waiter s_w{bar(3 + x)};
     bool ok = true;
@@ -401,18 +417,22 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       for (int j = 0; j < kKT; j += 8)
 #pragma unroll
         for (int u = 0; u < 4; ++u) mq[u] = fmax3(mq[u], xv[j + 2 * u], xv[j + 2 * u + 1]);
-      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-      const float alpha = (mx == -INFINITY) ? 1.f : exp2_approx((m - mx) * a.scale_log2);
+      const float tile_max = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      // Lazy reference: m moves only when the row's maximum exceeds it by more
+      // than 8 in base-2 units, so weights stay <= 2^8 and O is rarely rescaled
+      // (the final division by l uses the same reference).
+      const float mx = tile_max > m + lazy_raw ? tile_max : m;
+      const float alpha = (mx == -INFINITY || mx == m) ? 1.f : exp2_approx((m - mx) * a.scale_log2);
       const float neg = (mx == -INFINITY) ? 0.f : -mx * a.scale_log2;
+      // Weights as fp16 pairs straight from the packed exponential (they feed
+      // the fp16 P.V product); the row sum adds those exact fp16 values in fp32.
       float sq[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[kKT / 2];
 #pragma unroll
       for (int j = 0; j < kKT / 2; ++j) {
-        const float p0 = exp2_approx(fmaf(xv[2 * j], a.scale_log2, neg));
-        const float p1 = exp2_approx(fmaf(xv[2 * j + 1], a.scale_log2, neg));
-        sq[j & 3] += p0 + p1;
-        const __half2 hp = __floats2half2_rn(p0, p1);
-        pk[j] = *reinterpret_cast<const uint32_t*>(&hp);
+        pk[j] = exp2_f16x2(fmaf(xv[2 * j], a.scale_log2, neg),
+                           fmaf(xv[2 * j + 1], a.scale_log2, neg));
+        sq[j & 3] = add_f16x2_f32(pk[j], sq[j & 3]);
       }
       l = l * alpha + ((sq[0] + sq[1]) + (sq[2] + sq[3]));
       m = mx;
