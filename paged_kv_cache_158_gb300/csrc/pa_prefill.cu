@@ -318,24 +318,15 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       fence_proxy_async_smem();
       __syncwarp();
     };
-    Waiter p_w[2] = {{bar(5)}, {bar(6)}}, o_w[2] = {{bar(7)}, {bar(8)}};
+    Waiter p_w[2] = {{bar(5)}, {bar(6)}};
     bool ok = __all_sync(kFullMask, mbar_wait_bounded(bar(0), 0) && wait_k(0));
     if (ok && lane == 0) {
       qk_mma(0, 0, qx[1].n_kv == 0);
       if (qx[1].n_kv > 0) qk_mma(1, 0, true);
     }
-    // O(x, t - 1) must be complete before S(x, t) overwrites P(x, t - 1), so each
-    // QK waits for the previous P.V of its own tile; the other tile's work
-    // keeps the tensor pipe busy meanwhile.
-    uint32_t o_seen[2] = {0, 0};  // completed P.V phases observed, per tile
-    auto wait_o = [&](int x, int upto) {  // until P.V(x, upto) is observed complete
-      bool r = true;
-      while ((int)o_seen[x] <= upto && r) {
-        r = o_w[x].wait();
-        ++o_seen[x];
-      }
-      return r;
-    };
+    // S(x, t + 1) overwrites the columns P(x, t) occupies; tcgen05.mma issued
+    // by one thread execute in issue order, so QK(x, t + 1) is issued right
+    // after P.V(x, t) without waiting for it.
     // Every wait result is made warp-uniform at once, so all branches below
     // are taken by the whole warp.
     auto uni = [&](bool v) { return __all_sync(kFullMask, v); };
@@ -347,16 +338,10 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       if (ok && a0) ok = uni(p_w[0].wait());
       if (ok && lane == 0 && a0) pv_mma(0, t, !a1);
       if (ok && t + 1 < n_kv) ok = uni(wait_k(t + 1));
-      if (ok && n0) {
-        ok = uni(wait_o(0, t));
-        if (ok && lane == 0) qk_mma(0, t + 1, !n1);
-      }
+      if (ok && n0 && lane == 0) qk_mma(0, t + 1, !n1);
       if (ok && a1) ok = uni(p_w[1].wait());
       if (ok && lane == 0 && a1) pv_mma(1, t, true);
-      if (ok && n1) {
-        ok = uni(wait_o(1, t));
-        if (ok && lane == 0) qk_mma(1, t + 1, true);
-      }
+      if (ok && n1 && lane == 0) qk_mma(1, t + 1, true);
     }
     if (!ok) {
       if (lane == 0) {
