@@ -272,6 +272,9 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
     int qk[2] = {0, 0}, pv[2] = {0, 0}, krel = 0, vrel = 0;
     constexpr uint32_t kIdQK = umma_idesc_f16(kQT, kKT, false, false);
     constexpr uint32_t kIdPV = umma_idesc_f16(kQT, D, false, true);
+    // The whole warp runs the issue code (warp-uniform operands); lane 0
+    // alone issues each instruction.
+    const bool leader = lane == 0;
     auto qk_mma = [&](int x, int t, bool release) {
       const uint32_t kaddr = s_base + T::OFF_K0 + (t & 1) * 2 * T::KB;
       tc_fence_after();
@@ -280,12 +283,12 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
         const int at = k / 4, kk = k % 4;
         const uint64_t da = umma_desc_sw128(s_base + T::OFF_Q + x * T::QB + at * T::ATOM + kk * 32, 16, 1024);
         const uint64_t db = umma_desc_sw128(kaddr + at * T::ATOM + kk * 32, 16, 1024);
-        umma_f16(tmem + 128 * x, da, db, kIdQK, k > 0);
+        umma_f16_if(leader, tmem + 128 * x, da, db, kIdQK, k > 0);
       }
-      umma_commit(bar(3 + x));
+      umma_commit_if(leader, bar(3 + x));
       ++qk[x];
       if (release) {  // the last reader of K stage t & 1
-        umma_commit(bar(10 + (t & 1)));
+        umma_commit_if(leader, bar(10 + (t & 1)));
         ++krel;
       }
     };
@@ -295,12 +298,13 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
 #pragma unroll
       for (int k = 0; k < kKT / 16; ++k) {
         const uint64_t db = umma_desc_sw128(vaddr + k * 16 * 128, T::ATOM, 1024);
-        umma_f16_tmem_a(tmem + T::COL_O + D * x, tmem + 128 * x + 8 * k, db, kIdPV, t > 0 || k > 0);
+        umma_f16_tmem_a_if(leader, tmem + T::COL_O + D * x, tmem + 128 * x + 8 * k, db, kIdPV,
+                           t > 0 || k > 0);
       }
-      umma_commit(bar(7 + x));
+      umma_commit_if(leader, bar(7 + x));
       ++pv[x];
       if (release) {  // the last reader of V stage t & 1
-        umma_commit(bar(14 + (t & 1)));
+        umma_commit_if(leader, bar(14 + (t & 1)));
         ++vrel;
       }
     };
@@ -320,7 +324,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
     };
     Waiter p_w[2] = {{bar(5)}, {bar(6)}};
     bool ok = __all_sync(kFullMask, mbar_wait_bounded(bar(0), 0) && wait_k(0));
-    if (ok && lane == 0) {
+    if (ok) {
       qk_mma(0, 0, qx[1].n_kv == 0);
       if (qx[1].n_kv > 0) qk_mma(1, 0, true);
     }
@@ -336,12 +340,12 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       ok = uni(wait_v(t));
       if (ok) zero_v_tail(t);
       if (ok && a0) ok = uni(p_w[0].wait());
-      if (ok && lane == 0 && a0) pv_mma(0, t, !a1);
+      if (ok && a0) pv_mma(0, t, !a1);
       if (ok && t + 1 < n_kv) ok = uni(wait_k(t + 1));
-      if (ok && n0 && lane == 0) qk_mma(0, t + 1, !n1);
+      if (ok && n0) qk_mma(0, t + 1, !n1);
       if (ok && a1) ok = uni(p_w[1].wait());
-      if (ok && lane == 0 && a1) pv_mma(1, t, true);
-      if (ok && n1 && lane == 0) qk_mma(1, t + 1, true);
+      if (ok && a1) pv_mma(1, t, true);
+      if (ok && n1) qk_mma(1, t + 1, true);
     }
     if (!ok) {
       if (lane == 0) {

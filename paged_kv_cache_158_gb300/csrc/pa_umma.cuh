@@ -165,6 +165,47 @@ __device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
       : "memory");
 }
 
+// Predicated forms: every lane of the warp executes them with the same
+// operands (warp-uniform control flow, so the operands can stay in uniform
+// registers) and only the lane with `leader` set issues the instruction.
+__device__ __forceinline__ void umma_f16_if(bool leader, uint32_t d_tmem, uint64_t a_desc,
+                                            uint64_t b_desc, uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred p, e;\n"
+      "  setp.ne.b32 p, %4, 0;\n"
+      "  setp.ne.b32 e, %5, 0;\n"
+      "  @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u), "r"(leader ? 1u : 0u)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_f16_tmem_a_if(bool leader, uint32_t d_tmem, uint32_t a_tmem,
+                                                   uint64_t b_desc, uint32_t idesc,
+                                                   bool accumulate) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred p, e;\n"
+      "  setp.ne.b32 p, %4, 0;\n"
+      "  setp.ne.b32 e, %5, 0;\n"
+      "  @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u), "r"(leader ? 1u : 0u)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_if(bool leader, uint32_t bar) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred e;\n"
+      "  setp.ne.b32 e, %1, 0;\n"
+      "  @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+      "}\n" ::"r"(bar),
+      "r"(leader ? 1u : 0u)
+      : "memory");
+}
+
 // Arrives once on the mbarrier when every tcgen05.mma this thread issued
 // before has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
