@@ -21,7 +21,6 @@ the workload (sequences shard across GPUs with no exchange: weak scaling).
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import os
@@ -79,9 +78,17 @@ def decode_bytes(w, bt, ctx, kv_elem_bytes: int = 2) -> int:
     return int(H * per_pair.sum() + 4 * (-(-ctx // B)).sum() + 4 * S)
 
 
+# Sources that define the decode kernels (the ncu traffic is tied to these).
+DECODE_SOURCES = ("pa_decode.cuh", "pa_decode_inst.inc", "pa_decode_d64.cu", "pa_decode_d128.cu",
+                  "pa_decode_f8_d64.cu", "pa_decode_f8_d128.cu", "pa_device.cuh", "pa_launch.cuh",
+                  "pa_internal.h")
+
+
 def source_hash() -> str:
+    """Hash of the decode kernels' sources."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "paged_kv_cache_158_gb300", "csrc", "*"))):
+    csrc = os.path.join(ROOT, "paged_kv_cache_158_gb300", "csrc")
+    for p in sorted(os.path.join(csrc, f) for f in DECODE_SOURCES):
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode())
             h.update(f.read())

@@ -176,10 +176,13 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* key_cac
  *   value_caches   HOST arrays of num_layers device pointers, each to an fp16
  *                  [num_blocks][num_heads][block_size][head_dim] cache
  *   block_mapping  device int64 [num_pairs][2]
- * Preconditions (not checked: the mapping lives on the device): destination
- * ids are distinct and no destination is also a source in the same call;
- * otherwise copies race.  An id outside [0, num_blocks) skips that pair and
- * sets PA_ERRBIT_COPY.  num_pairs == 0 is a no-op.  Bit-exact.
+ * Preconditions: destination ids are distinct and no destination is also a
+ * source in the same call.  For num_pairs <= 1024 the kernel checks them:
+ * a pair whose destination is another pair's destination or source is
+ * skipped (not copied) and sets PA_ERRBIT_COPY, so nothing races; larger
+ * mappings are not checked and violating them races.  An id outside
+ * [0, num_blocks) skips that pair and sets PA_ERRBIT_COPY.  num_pairs == 0
+ * is a no-op.  Bit-exact.
  */
 pa_status pa_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
                          const int64_t* block_mapping, int num_pairs, int num_heads, int head_dim,
@@ -252,8 +255,10 @@ pa_status pa_prefill(void* out, const void* query, const void* key_cache, const 
  *   block_bytes    a multiple of 16
  *   src_num_blocks, dst_num_blocks  pool sizes; an id outside [0, n) skips
  *                  the pair and sets PA_ERRBIT_COPY
- * Preconditions as pa_copy_blocks: destination blocks distinct; no overlap
- * between the source and destination ranges of one call.  Bit-exact.  The
+ * Destination blocks must be distinct: for num_pairs <= 1024 a pair whose
+ * destination repeats another's is skipped and sets PA_ERRBIT_COPY (larger
+ * mappings are not checked).  Source and destination pools must not
+ * overlap.  Bit-exact.  The
  * host side must stay allocated and unchanged until the stream reaches the
  * copy.
  */

@@ -119,16 +119,43 @@ struct LayerPtrs {
   uint4* v[kCopyMaxLayers];
 };
 
+// Block copies and swaps check their mapping for conflicting pairs on the
+// device when it has at most this many pairs.
+constexpr int kMappingCheckMaxPairs = 1024;
+
+// True when another pair of the mapping writes `dst` or reads it (with
+// `dst_also_src`), i.e. copying this pair would race.  Checked by the whole
+// CTA for mappings of at most kMappingCheckMaxPairs pairs.
+__device__ __forceinline__ bool mapping_conflict(const int64_t* __restrict__ block_mapping,
+                                                 int num_pairs, int pair, long long dst,
+                                                 bool dst_also_src) {
+  __shared__ int conflict;
+  if (threadIdx.x == 0) conflict = 0;
+  __syncthreads();
+  if (num_pairs <= kMappingCheckMaxPairs) {
+    for (int q = threadIdx.x; q < num_pairs; q += blockDim.x) {
+      if (q == pair) continue;
+      if (block_mapping[2 * q + 1] == dst || (dst_also_src && block_mapping[2 * q] == dst))
+        conflict = 1;
+    }
+  }
+  __syncthreads();
+  return conflict != 0;
+}
+
 __global__ void __launch_bounds__(256)
     copy_blocks_kernel(LayerPtrs ptrs, const int64_t* __restrict__ block_mapping, int pair_base,
-                       long long block_vecs, long long num_blocks, unsigned int* err) {
+                       int num_pairs, long long block_vecs, long long num_blocks,
+                       unsigned int* err) {
   pdl_wait();
   pdl_launch_dependents();
   const int pair = pair_base + blockIdx.y;
   const int layer = blockIdx.z >> 1;
   const long long src = block_mapping[2 * pair];
   const long long dst = block_mapping[2 * pair + 1];
-  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+  // every thread of the CTA reaches the check's barriers
+  const bool conflict = mapping_conflict(block_mapping, num_pairs, pair, dst, true);
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks || conflict) {
     if (blockIdx.x == 0 && blockIdx.z == 0 && threadIdx.x == 0) atomicOr(err, PA_ERRBIT_COPY);
     return;
   }
@@ -157,14 +184,16 @@ constexpr int kSwapUnroll = 4;
 
 __global__ void __launch_bounds__(256)
     swap_blocks_kernel(SwapPtrs ptrs, const int64_t* __restrict__ block_mapping, int pair_base,
-                       long long block_vecs, long long src_num_blocks, long long dst_num_blocks,
-                       unsigned int* err) {
+                       int num_pairs, long long block_vecs, long long src_num_blocks,
+                       long long dst_num_blocks, unsigned int* err) {
   pdl_wait();
   pdl_launch_dependents();
   const int pair = pair_base + blockIdx.y;
   const long long src = block_mapping[2 * pair];
   const long long dst = block_mapping[2 * pair + 1];
-  if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks) {
+  // every thread of the CTA reaches the check's barriers
+  const bool conflict = mapping_conflict(block_mapping, num_pairs, pair, dst, false);
+  if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks || conflict) {
     if (blockIdx.x == 0 && blockIdx.z == 0 && threadIdx.x == 0) atomicOr(err, PA_ERRBIT_COPY);
     return;
   }
@@ -316,7 +345,8 @@ cudaError_t launch_copy_blocks(void* const* key_caches, void* const* value_cache
       const int np = num_pairs - p0 < 65535 ? num_pairs - p0 : 65535;
       dim3 grid((unsigned)xblocks, (unsigned)np, (unsigned)(2 * nl));
       const cudaError_t e = launch_pdl(copy_blocks_kernel, grid, dim3(threads), 0, stream, ptrs,
-                                       block_mapping, p0, block_vecs, (long long)num_blocks, err);
+                                       block_mapping, p0, num_pairs, block_vecs,
+                                       (long long)num_blocks, err);
       if (e != cudaSuccess) return e;
     }
   }
@@ -343,7 +373,7 @@ cudaError_t launch_swap_blocks(void* const* dst_caches, const void* const* src_c
       const int np = num_pairs - p0 < 65535 ? num_pairs - p0 : 65535;
       dim3 grid((unsigned)xblocks, (unsigned)np, (unsigned)nc);
       const cudaError_t e = launch_pdl(swap_blocks_kernel, grid, dim3(threads), 0, stream, ptrs,
-                                       block_mapping, p0, block_vecs, src_num_blocks,
+                                       block_mapping, p0, num_pairs, block_vecs, src_num_blocks,
                                        dst_num_blocks, err);
       if (e != cudaSuccess) return e;
     }

@@ -97,3 +97,24 @@ def test_shared_prefix_identity_bit_exact():
                  w.scale, int(ctx.max()), ws)
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
     assert torch.equal(shared.view(torch.int16), out.view(torch.int16))
+
+
+def test_copy_blocks_conflicting_pairs_are_skipped_and_flagged():
+    """A pair whose destination is another pair's destination or source is not
+    copied (nothing races) and the copy error bit is set; other pairs copy."""
+    rng = np.random.default_rng(12)
+    NB, H, B, D = 12, 2, 16, 64
+    kc = torch.from_numpy(rng.integers(0, 1 << 16, (NB, H, B, D), dtype=np.uint16).view(np.int16)).cuda()
+    vc = torch.from_numpy(rng.integers(0, 1 << 16, (NB, H, B, D), dtype=np.uint16).view(np.int16)).cuda()
+    kc, vc = kc.view(torch.float16), vc.view(torch.float16)
+    before_k, before_v = u16(kc).copy(), u16(vc).copy()
+    # pairs 0 and 1 share destination 5; pair 2 writes 3, which pair 3 reads; pair 4 is clean
+    mapping = np.array([[0, 5], [1, 5], [2, 3], [3, 7], [8, 9]], dtype=np.int64)
+    pa.pa_check_errors()
+    pa.pa_copy_blocks([kc], [vc], torch.from_numpy(mapping).cuda())
+    st, bits = pa.pa_check_errors()
+    assert st == pa.PA_ERR_OUT_OF_RANGE and bits == pa.PA_ERRBIT_COPY
+    ek, ev = before_k.copy(), before_v.copy()
+    for src, dst in ([3, 7], [8, 9]):          # the pairs without a conflict
+        ek[dst], ev[dst] = before_k[src], before_v[src]
+    assert np.array_equal(u16(kc), ek) and np.array_equal(u16(vc), ev)

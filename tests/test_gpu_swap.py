@@ -99,3 +99,18 @@ def test_swap_refuses_pageable_host_memory():
         pa.PA_ERR_INVALID_ARG
     with pytest.raises(ValueError):
         pa.pa_swap_blocks([torch.zeros_like(dev).cpu()], [dev], mapping)
+
+
+def test_swap_duplicate_destinations_are_skipped_and_flagged():
+    rng = np.random.default_rng(10)
+    dev, host = pools(rng, 1, 10, 6, (2, 8, 64), torch.float16)
+    ref_host = [host_view(t) for t in host]
+    ref_dev = [host_view(t) for t in dev]
+    mapping = np.array([[1, 2], [4, 2], [5, 0]], dtype=np.int64)   # pairs 0 and 1 share destination 2
+    pa.pa_swap_blocks(host, dev, torch.from_numpy(mapping).to(DEV))
+    st, bits = pa.pa_check_errors()
+    assert st == pa.PA_ERR_OUT_OF_RANGE and bits == pa.PA_ERRBIT_COPY
+    for t, r, d in zip(host, ref_host, ref_dev):
+        expect = r.copy()
+        expect[0] = d[5]
+        assert np.array_equal(host_view(t), expect)
