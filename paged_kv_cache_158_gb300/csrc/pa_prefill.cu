@@ -275,15 +275,21 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
     // The whole warp runs the issue code (warp-uniform operands); lane 0
     // alone issues each instruction.
     const bool leader = lane == 0;
+    // Base descriptors, computed once; the descriptor of a K step or stage
+    // differs only in its start address field (16-byte units), so each MMA
+    // adds a compile-time offset.
+    const uint64_t q_desc0 = umma_desc_sw128(s_base + T::OFF_Q, 16, 1024);
+    const uint64_t k_desc0 = umma_desc_sw128(s_base + T::OFF_K0, 16, 1024);
+    const uint64_t v_desc0 = umma_desc_sw128(s_base + T::OFF_K0 + T::KB, T::ATOM, 1024);
+    constexpr uint64_t kStageStep = (uint64_t)(2 * T::KB) >> 4;
     auto qk_mma = [&](int x, int t, bool release) {
-      const uint32_t kaddr = s_base + T::OFF_K0 + (t & 1) * 2 * T::KB;
+      const uint64_t qd = q_desc0 + (uint64_t)((x * T::QB) >> 4);
+      const uint64_t kd = k_desc0 + (t & 1) * kStageStep;
       tc_fence_after();
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
-        const int at = k / 4, kk = k % 4;
-        const uint64_t da = umma_desc_sw128(s_base + T::OFF_Q + x * T::QB + at * T::ATOM + kk * 32, 16, 1024);
-        const uint64_t db = umma_desc_sw128(kaddr + at * T::ATOM + kk * 32, 16, 1024);
-        umma_f16_if(leader, tmem + 128 * x, da, db, kIdQK, k > 0);
+        const uint64_t off = (uint64_t)(((k / 4) * T::ATOM + (k % 4) * 32) >> 4);
+        umma_f16_if(leader, tmem + 128 * x, qd + off, kd + off, kIdQK, k > 0);
       }
       umma_commit_if(leader, bar(3 + x));
       ++qk[x];
@@ -293,14 +299,12 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       }
     };
     auto pv_mma = [&](int x, int t, bool release) {
-      const uint32_t vaddr = s_base + T::OFF_K0 + (t & 1) * 2 * T::KB + T::KB;
+      const uint64_t vd = v_desc0 + (t & 1) * kStageStep;
       tc_fence_after();
 #pragma unroll
-      for (int k = 0; k < kKT / 16; ++k) {
-        const uint64_t db = umma_desc_sw128(vaddr + k * 16 * 128, T::ATOM, 1024);
-        umma_f16_tmem_a_if(leader, tmem + T::COL_O + D * x, tmem + 128 * x + 8 * k, db, kIdPV,
-                           t > 0 || k > 0);
-      }
+      for (int k = 0; k < kKT / 16; ++k)
+        umma_f16_tmem_a_if(leader, tmem + T::COL_O + D * x, tmem + 128 * x + 8 * k,
+                           vd + (uint64_t)((k * 16 * 128) >> 4), kIdPV, t > 0 || k > 0);
       umma_commit_if(leader, bar(7 + x));
       ++pv[x];
       if (release) {  // the last reader of V stage t & 1
