@@ -500,7 +500,27 @@ def run_swap(args):
                                   "what": "one contiguous transfer of the same bytes"},
         "frac_of_copy_engine": {"out": round(t_d2h / t_out, 3), "in": round(t_h2d / t_in, 3)},
         "gpu_launches": 2 * (K + W),
+        "cpu_baseline": None if args.no_cpu_baseline else swap_cpu_baseline(host, nb, budget_s=5.0),
     }
+
+
+def swap_cpu_baseline(host_caches, nb: int, budget_s: float):
+    """The oracle's block swap between two host pools with the blocks, caches and block size of
+    the timed swap (the same bytes per call)."""
+    import oracle
+    src = [t.numpy().view(np.uint8).reshape(nb, -1) for t in host_caches]
+    dst = [np.empty_like(a) for a in src]
+    mapping = np.stack([np.arange(nb), np.arange(nb)[::-1]], 1).astype(np.int64)
+    nbytes = sum(a.nbytes for a in src)
+    reps, t_total = 0, 0.0
+    while t_total < budget_s or reps < 1:
+        t0 = time.perf_counter()
+        assert oracle.swap_blocks(dst, src, mapping) == 0
+        t_total += time.perf_counter() - t0
+        reps += 1
+    return {"value": round(nbytes * reps / t_total / 1e9, 3), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "sample": f"{nb} blocks x {len(src)} caches host to host, {reps} repetitions, "
+                                        f"{t_total:.1f} s", "host_cpus": os.cpu_count()}
 
 
 def prefill_flops(w) -> int:
@@ -572,7 +592,36 @@ def run_prefill_bench(args):
                      "kv_bytes_per_call": kv_bytes,
                      "kv_gbs": round(kv_bytes / sec / 1e9, 1)},
         "clocks": clk, "gpu_launches": K + W,
+        "cpu_baseline": None if args.no_cpu_baseline else prefill_cpu_baseline(w, budget_s=10.0),
     }
+
+
+def prefill_cpu_baseline(w, budget_s: float):
+    """The oracle's multi-query attention on a bounded sample of the same workload: the last
+    32 new tokens of sequence 0 over its whole context, every head (the causally truncated
+    problem that gives exactly those rows)."""
+    import oracle
+    from workloads import gpu
+    kc, vc = gpu.host_pool(w, 0)
+    q = gpu.host_queries(w)
+    qs = configs.query_start(w)
+    ql, c, n = int(w.extra["q_lens"][0]), int(w.context_lens[0]), 32
+    rows = q[qs[0] + ql - n:qs[0] + ql]
+    bt = w.block_tables[0:1]
+    flops = 4 * w.head_dim * w.num_heads * sum(range(c - n + 1, c + 1))
+    reps, t_total = 0, 0.0
+    while t_total < budget_s or reps < 1:
+        t0 = time.perf_counter()
+        _, _, rc = oracle.prefill(rows, kc, vc, bt, np.array([c], np.int32), np.array([0, n], np.int32),
+                                  w.scale, want64=False)
+        t_total += time.perf_counter() - t0
+        reps += 1
+        assert rc == 0
+    return {"value": round(flops * reps / t_total / 1e12, 6), "unit": "TFLOP/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{w.name}: last {n} new tokens of sequence 0 over its {c}-token context, "
+                      f"all {w.num_heads} heads, {reps} repetitions, {t_total:.1f} s",
+            "host_cpus": os.cpu_count()}
 
 
 # ------------------------------------------------------------ CPU oracle
