@@ -189,36 +189,40 @@ __device__ __forceinline__ bool chunk_ids_ok(const DecodeParams& a, const int (&
 
 // Issues the bulk copies of one chunk into a stage: for each block of the
 // chunk with live rows, its K rows and its V rows (contiguous in the
-// [NB][H][B][D] layout); only live rows are copied.
+// [NB][H][B][D] layout); only live rows are copied.  Warp-uniform: every
+// lane executes it with the same operands and only `leader` issues.
 template <int D, int B, bool F8>
 __device__ __forceinline__ void issue_chunk(const DecodeParams& a, const ItemInfo& it,
                                             const int (&phys)[DecodeTraits<D, B, F8>::BPC],
-                                            int chunk, unsigned char* stage, uint32_t bar,
-                                            uint64_t policy) {
+                                            int chunk, uint32_t stage, uint32_t bar,
+                                            uint64_t policy, bool leader) {
   using T = DecodeTraits<D, B, F8>;
   const int t0 = it.t_begin + chunk * T::TC;
   const int rows = min(T::TC, it.t_end - t0);
   if (rows <= 0) {  // not a chunk of this item (cannot happen): complete the phase empty
-    mbar_arrive(bar);
+    mbar_arrive_if(leader, bar);
     return;
   }
   if (!chunk_ids_ok<D, B, F8>(a, phys, rows)) {
-    atomicOr(a.err, PA_ERRBIT_BLOCK_ID);
-    mbar_arrive(bar);  // completes the phase with no data; the chunk is skipped
+    if (leader) atomicOr(a.err, PA_ERRBIT_BLOCK_ID);
+    mbar_arrive_if(leader, bar);  // completes the phase with no data; the chunk is skipped
     return;
   }
-  mbar_arrive_expect_tx(bar, 2u * (uint32_t)rows * D * T::ELEM);
+  mbar_arrive_expect_tx_if(leader, bar, 2u * (uint32_t)rows * D * T::ELEM);
+  // Byte offset of (block 0, head h, row t0 % B) and the stride between blocks.
+  const size_t head_off = ((size_t)it.h * B + (t0 % B)) * D * T::ELEM;
+  const size_t blk_stride = (size_t)a.num_heads * B * D * T::ELEM;
 #pragma unroll
   for (int b = 0; b < T::BPC; ++b) {
     const int r = min(B, rows - b * B);
     if (r <= 0) break;
-    const size_t off = (((size_t)phys[b] * a.num_heads + it.h) * B + (t0 % B)) * D * T::ELEM;
+    const size_t off = (size_t)phys[b] * blk_stride + head_off;
     const uint32_t bytes = (uint32_t)r * D * T::ELEM;
-    const int soff = b * B * D * T::ELEM;
-    bulk_g2s_hint(smem_u32(stage + soff), static_cast<const unsigned char*>(a.key_cache) + off,
-                  bytes, bar, policy);
-    bulk_g2s_hint(smem_u32(stage + T::CHUNK_BYTES + soff),
-                  static_cast<const unsigned char*>(a.value_cache) + off, bytes, bar, policy);
+    const uint32_t soff = b * B * D * T::ELEM;
+    bulk_g2s_hint_if(leader, stage + soff, static_cast<const unsigned char*>(a.key_cache) + off,
+                     bytes, bar, policy);
+    bulk_g2s_hint_if(leader, stage + T::CHUNK_BYTES + soff,
+                     static_cast<const unsigned char*>(a.value_cache) + off, bytes, bar, policy);
   }
 }
 
@@ -460,20 +464,24 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS)
   int buf = 0;
   int iter = 0;
 
-  // The first item's first copies, still before the wait.
+  const bool leader = lane == 0;
+  const uint32_t my_stages_s = smem_u32(my_stages);
+  const uint32_t my_bars_s = smem_u32(my_bars);
+  // The first item's first copies, still before the wait (warp-uniform; the
+  // leader issues).
   {
     const int n0 = warp_chunks<D, B, F8>(it, warp);
-    if (lane == 0) {
-      for (; (int)iss < n0 && iss < (uint32_t)T::NST; ++iss) {
-        const int chunk = warp + (int)iss * T::NW;
-        int ph[T::BPC];
-        chunk_ids<D, B, F8>(ph, bt_s, it, chunk);
-        issue_chunk<D, B, F8>(a, it, ph, chunk, my_stages + iss * T::STAGE_BYTES,
-                              smem_u32(&my_bars[iss]), policy);
-      }
+    for (; (int)iss < n0 && iss < (uint32_t)T::NST; ++iss) {
+      const int chunk = warp + (int)iss * T::NW;
+      int ph[T::BPC];
+      chunk_ids<D, B, F8>(ph, bt_s, it, chunk);
+      issue_chunk<D, B, F8>(a, it, ph, chunk, my_stages_s + iss * T::STAGE_BYTES,
+                            my_bars_s + 8 * iss, policy, leader);
     }
-    iss = __shfl_sync(kFullMask, iss, 0);
   }
+  // Stage of the next issue and of the next consumption (with its phase).
+  int st_i = (int)iss % T::NST, st_c = 0;
+  uint32_t ph_c = 0;
   pdl_wait();
   pdl_launch_dependents();
   if (tid == 0) misc[1] = (int)(gridDim.x + atomicAdd(a.counter, 1u));
@@ -499,13 +507,14 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS)
     const int n_nx = has_next ? warp_chunks<D, B, F8>(nx, warp) : 0;
     const uint32_t base = u;
 
-    // Block ids of this warp's first NST chunks of the next item (lane 0 only).
+    // Block ids of this warp's first NST chunks of the next item (every lane
+    // loads the same ids: the issue code is warp-uniform).
     int nxp[T::NST][T::BPC];
 #pragma unroll
     for (int j = 0; j < T::NST; ++j)
 #pragma unroll
       for (int b = 0; b < T::BPC; ++b) nxp[j][b] = -1;
-    if (lane == 0 && n_nx > 0) {
+    if (n_nx > 0) {
       const int32_t* row = a.block_tables + (size_t)(a.seq_begin + nx.s) * a.max_blocks;
 #pragma unroll
       for (int j = 0; j < T::NST; ++j) {
@@ -515,33 +524,31 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS)
           if (j < n_nx && t0 + b * B < nx.t_end) nxp[j][b] = row[t0 / B + b];
       }
     }
-    // Fill free stages: the rest of this item's chunks, then the next item's.
+    // Fill free stages: the rest of this item's chunks, then the next item's
+    // (warp-uniform; the leader issues).
     auto issue_upto = [&]() {
-      if (lane == 0) {
-        while (iss < u + T::NST) {
-          const int k = (int)(iss - base);
-          const int st = iss % T::NST;
-          unsigned char* stage = my_stages + st * T::STAGE_BYTES;
-          const uint32_t bar = smem_u32(&my_bars[st]);
-          if (k < n_my) {
-            const int chunk = warp + k * T::NW;
-            int ph[T::BPC];
-            chunk_ids<D, B, F8>(ph, bt, it, chunk);
-            issue_chunk<D, B, F8>(a, it, ph, chunk, stage, bar, policy);
-          } else if (k - n_my < n_nx) {
-            const int j = k - n_my;
-            int ph[T::BPC];
+      while (iss < u + T::NST) {
+        const int k = (int)(iss - base);
+        const uint32_t stage = my_stages_s + st_i * T::STAGE_BYTES;
+        const uint32_t bar = my_bars_s + 8 * st_i;
+        if (k < n_my) {
+          const int chunk = warp + k * T::NW;
+          int ph[T::BPC];
+          chunk_ids<D, B, F8>(ph, bt, it, chunk);
+          issue_chunk<D, B, F8>(a, it, ph, chunk, stage, bar, policy, leader);
+        } else if (k - n_my < n_nx) {
+          const int j = k - n_my;
+          int ph[T::BPC];
 #pragma unroll
-            for (int b = 0; b < T::BPC; ++b)
-              ph[b] = j == 0 ? nxp[0][b] : (j == 1 ? nxp[1][b] : nxp[2][b]);
-            issue_chunk<D, B, F8>(a, nx, ph, warp + j * T::NW, stage, bar, policy);
-          } else {
-            break;
-          }
-          ++iss;
+          for (int b = 0; b < T::BPC; ++b)
+            ph[b] = j == 0 ? nxp[0][b] : (j == 1 ? nxp[1][b] : nxp[2][b]);
+          issue_chunk<D, B, F8>(a, nx, ph, warp + j * T::NW, stage, bar, policy, leader);
+        } else {
+          break;
         }
+        ++iss;
+        st_i = st_i + 1 == T::NST ? 0 : st_i + 1;
       }
-      iss = __shfl_sync(kFullMask, iss, 0);
     };
     issue_upto();
 
@@ -556,9 +563,9 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS)
     for (int i = 0; i < T::DPL; ++i) o[i] = 0.f;
 
     for (int i = 0; i < n_my; ++i) {
-      const int st = u % T::NST;
-      const uint32_t bar = smem_u32(&my_bars[st]);
-      bool ok = mbar_wait_bounded(bar, (u / T::NST) & 1);
+      const int st = st_c;
+      const uint32_t bar = my_bars_s + 8 * st;
+      bool ok = mbar_wait_bounded(bar, ph_c);
       ok = __all_sync(kFullMask, ok);
       if (!ok) {
         // Drain this warp's copies still in flight (bounded), then give up.
@@ -587,6 +594,10 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS)
       }
       __syncwarp();
       ++u;
+      if (++st_c == T::NST) {
+        st_c = 0;
+        ph_c ^= 1;
+      }
       issue_upto();
     }
 

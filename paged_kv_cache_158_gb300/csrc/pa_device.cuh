@@ -106,6 +106,43 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst_smem, const void* src
       : "memory");
 }
 
+// Predicated forms for warp-uniform code: every lane executes them with the
+// same operands and only the lane with `leader` set performs the operation.
+__device__ __forceinline__ void mbar_arrive_expect_tx_if(bool leader, uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred e;\n"
+      "  setp.ne.b32 e, %2, 0;\n"
+      "  @e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
+      "}\n" ::"r"(bar),
+      "r"(bytes), "r"(leader ? 1u : 0u)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_if(bool leader, uint32_t bar) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred e;\n"
+      "  setp.ne.b32 e, %1, 0;\n"
+      "  @e mbarrier.arrive.shared::cta.b64 _, [%0];\n"
+      "}\n" ::"r"(bar),
+      "r"(leader ? 1u : 0u)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s_hint_if(bool leader, uint32_t dst_smem, const void* src,
+                                                 uint32_t bytes, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred e;\n"
+      "  setp.ne.b32 e, %5, 0;\n"
+      "  @e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+      "[%1], %2, [%3], %4;\n"
+      "}\n" ::"r"(dst_smem),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy), "r"(leader ? 1u : 0u)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
