@@ -19,7 +19,14 @@ Semantics ("深入解析LLM推理引擎：从PagedAttention到调度优化" §3.
     fresh one (copy-on-write) and repoints the table; the last holder writes
     in place;
   * freeing a sequence drops its references; blocks reaching zero return to
-    the free list.
+    the free list;
+  * swapping ("【硬核】啃透vLLM源码：从PagedAttention到连续批处理，大模型推理加速24倍的秘密"
+    §三: when GPU memory runs short, blocks go to CPU memory and come back
+    when needed): swap-out gives each of the sequence's blocks a host block
+    and drops the sequence's reference to the GPU block (a block still held
+    by another sequence stays; the host gets a copy); swap-in gives each host
+    block a fresh GPU block and frees the host block.  The (src, dst) pairs
+    returned are what pa_swap_blocks moves.
 This implementation is array based and appends tokens in bulk per sequence.
 """
 from __future__ import annotations
@@ -40,7 +47,7 @@ class OutOfBlocksError(RuntimeError):
 
 class BlockManager:
     def __init__(self, num_blocks: int, block_size: int, max_seqs: int, max_blocks_per_seq: int,
-                 free_order=None):
+                 free_order=None, num_host_blocks: int = 0):
         self.num_blocks = int(num_blocks)
         self.block_size = int(block_size)
         order = np.arange(self.num_blocks) if free_order is None else np.asarray(free_order)
@@ -53,6 +60,11 @@ class BlockManager:
         self.lengths = np.zeros(int(max_seqs), dtype=np.int64)
         self.live = np.zeros(int(max_seqs), dtype=bool)
         self.pending_copies: list[tuple[int, int]] = []
+        # host (CPU) blocks for swapped-out sequences: a stack like the GPU list
+        self.num_host_blocks = int(num_host_blocks)
+        self._hfree = np.arange(self.num_host_blocks, dtype=np.int64)[::-1].copy()
+        self._htop = self.num_host_blocks
+        self.swapped = np.zeros(int(max_seqs), dtype=bool)
 
     # -- free list ---------------------------------------------------------
     def num_free(self) -> int:
@@ -82,6 +94,8 @@ class BlockManager:
 
     def fork(self, src: int, dst: int) -> None:
         """dst starts with src's contents, sharing every block."""
+        if self.swapped[src]:
+            raise ValueError(f"sequence {src} is swapped out")
         self.add_sequence(dst)
         n = int(self.nblocks[src])
         blocks = self.tables[src, :n]
@@ -94,6 +108,8 @@ class BlockManager:
         """Reserve slots for n more tokens of seq; returns their logical positions.
         Copy-on-write pairs (src, dst) accumulate in pending_copies."""
         B = self.block_size
+        if self.swapped[seq]:
+            raise ValueError(f"sequence {seq} is swapped out")
         pos0 = int(self.lengths[seq])
         if n <= 0:
             return np.empty(0, dtype=np.int32)
@@ -115,9 +131,54 @@ class BlockManager:
         self.lengths[seq] = pos0 + n
         return np.arange(pos0, pos0 + n, dtype=np.int32)
 
+    def num_free_host(self) -> int:
+        return self._htop
+
+    def swap_out(self, seq: int) -> np.ndarray:
+        """Move seq's blocks to host blocks; returns (gpu_block, host_block) pairs, int64 [n, 2]."""
+        if not self.live[seq] or self.swapped[seq]:
+            raise ValueError(f"sequence {seq} is not resident")
+        n = int(self.nblocks[seq])
+        if n > self._htop:
+            raise OutOfBlocksError("no free host blocks")
+        pairs = np.empty((n, 2), dtype=np.int64)
+        for j in range(n):
+            b = int(self.tables[seq, j])
+            self._htop -= 1
+            hb = int(self._hfree[self._htop])
+            pairs[j] = (b, hb)
+            self._drop(b)
+            self.tables[seq, j] = hb
+        self.swapped[seq] = True
+        return pairs
+
+    def swap_in(self, seq: int) -> np.ndarray:
+        """Bring seq's blocks back into fresh GPU blocks; returns (host_block, gpu_block) pairs."""
+        if not self.live[seq] or not self.swapped[seq]:
+            raise ValueError(f"sequence {seq} is not swapped out")
+        n = int(self.nblocks[seq])
+        if n > self._top:
+            raise OutOfBlocksError("no free blocks")
+        pairs = np.empty((n, 2), dtype=np.int64)
+        for j in range(n):
+            hb = int(self.tables[seq, j])
+            g = self._take()
+            pairs[j] = (hb, g)
+            self._hfree[self._htop] = hb
+            self._htop += 1
+            self.tables[seq, j] = g
+        self.swapped[seq] = False
+        return pairs
+
     def free_sequence(self, seq: int) -> None:
-        for b in self.tables[seq, :int(self.nblocks[seq])]:
-            self._drop(int(b))
+        if self.swapped[seq]:
+            for hb in self.tables[seq, :int(self.nblocks[seq])]:
+                self._hfree[self._htop] = int(hb)
+                self._htop += 1
+            self.swapped[seq] = False
+        else:
+            for b in self.tables[seq, :int(self.nblocks[seq])]:
+                self._drop(int(b))
         self.tables[seq, :] = -1
         self.nblocks[seq] = 0
         self.lengths[seq] = 0

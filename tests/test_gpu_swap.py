@@ -114,3 +114,53 @@ def test_swap_duplicate_destinations_are_skipped_and_flagged():
         expect = r.copy()
         expect[0] = d[5]
         assert np.array_equal(host_view(t), expect)
+
+
+def test_block_manager_swap_round_trip_keeps_decode_bits():
+    """Decode, swap a sequence out with the block manager's pairs, let another
+    sequence overwrite the freed GPU blocks, swap it back into different
+    blocks, decode again: every output is bit-identical (decode depends only
+    on logical positions)."""
+    from paged_kv_cache_158_gb300.pool import BlockManager
+    from workloads import configs as cfgs, gpu as wgpu
+    rng = np.random.default_rng(21)
+    S, H, D, B, NB, NH = 4, 4, 128, 16, 64, 32
+    bm = BlockManager(NB, B, S + 1, 16, free_order=rng.permutation(NB), num_host_blocks=NH)
+    lens = [100, 130, 37, 200]
+    for s, n in enumerate(lens):
+        bm.add_sequence(s)
+        bm.append_tokens(s, n)
+    w = cfgs.small_random(2500, S, H, D, B, 8)   # only for its value streams and bank
+    bank = wgpu.device_bank(w.seed, w.kv_sigma, DEV)
+    kc = torch.empty((NB, H, B, D), dtype=torch.float16, device=DEV)
+    vc = torch.empty_like(kc)
+    wgpu.fill(kc, w.seed, 0, bank)
+    wgpu.fill(vc, w.seed, 1, bank)
+    torch.manual_seed(21)
+    q = torch.randn((S, H, D), device=DEV).half()
+    ctx = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    ws = pa.decode_workspace(S, H, D, max(lens))
+
+    def decode():
+        out = torch.empty((S, H, D), dtype=torch.float16, device=DEV)
+        bt = torch.from_numpy(bm.block_tables(np.arange(S))).to(DEV)
+        pa.pa_decode(out, q, kc, vc, bt, ctx, 0.088, max(lens), ws)
+        return out
+
+    before = decode().clone()
+    host_k = torch.zeros((NH, H, B, D), dtype=torch.float16).pin_memory()
+    host_v = torch.zeros_like(host_k).pin_memory()
+    out_pairs = bm.swap_out(1)
+    pa.pa_swap_blocks([host_k, host_v], [kc, vc], torch.from_numpy(out_pairs).to(DEV))
+    bm.add_sequence(S)                                  # reuses the freed blocks
+    bm.append_tokens(S, B * min(bm.num_free() // 2, 16))
+    reused = torch.from_numpy(bm.tables[S, :int(bm.nblocks[S])].astype(np.int64)).to(DEV)
+    kc[reused] = float("nan")
+    vc[reused] = float("nan")
+    in_pairs = bm.swap_in(1)
+    assert not np.array_equal(np.sort(in_pairs[:, 1]), np.sort(out_pairs[:, 0]))  # new blocks
+    pa.pa_swap_blocks([kc, vc], [host_k, host_v], torch.from_numpy(in_pairs).to(DEV))
+    after = decode()
+    torch.cuda.synchronize()
+    assert torch.equal(before.view(torch.int16), after.view(torch.int16))
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)

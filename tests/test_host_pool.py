@@ -100,3 +100,76 @@ def test_random_operations_match_model(seed):
         assert [tuple(p) for p in bm.take_copies()] == model.copies
         model.copies = []
         assert bm.num_free() == len(model.free)
+
+
+def gather(pool: np.ndarray, table: np.ndarray, n: int) -> np.ndarray:
+    """A sequence's blocks in logical order (pool: [NB, ...])."""
+    return pool[table[:n]].copy()
+
+
+def test_swap_out_and_in_round_trip_restores_every_sequence():
+    """Swap a shared-prefix sequence out and back in with the pairs the manager
+    returns, moving block contents with the oracle's swap: every sequence's
+    logical contents are unchanged, the other sequences' blocks untouched, and
+    the free counts come back."""
+    import oracle
+    rng = np.random.default_rng(4)
+    B, NB, NH = 4, 40, 16
+    bm = BlockManager(NB, B, 4, 12, num_host_blocks=NH)
+    dev = rng.integers(0, 1 << 16, (NB, 2, B, 8), dtype=np.uint16)
+    host = np.zeros((NH, 2, B, 8), dtype=np.uint16)
+    bm.add_sequence(0)
+    bm.append_tokens(0, 10)            # 3 blocks, the last partial
+    bm.fork(0, 1)                      # seq 1 shares all three
+    bm.append_tokens(1, 5)             # copy-on-write of the partial block + 1 new
+    cow = bm.take_copies()
+    for src, dst in cow:
+        dev[dst] = dev[src]
+    bm.add_sequence(2)
+    bm.append_tokens(2, 7)
+    before = {s: gather(dev, bm.tables[s], int(bm.nblocks[s])) for s in (0, 1, 2)}
+    free0, hfree0 = bm.num_free(), bm.num_free_host()
+
+    out = bm.swap_out(1)
+    assert out.shape == (int(bm.nblocks[1]), 2) and bm.swapped[1]
+    assert oracle.swap_blocks([host], [dev], out) == 0
+    assert bm.num_free_host() == hfree0 - len(out)
+    # blocks still shared with sequence 0 stay allocated; the rest are free
+    shared = set(bm.tables[0, :int(bm.nblocks[0])].tolist())
+    assert bm.num_free() == free0 + sum(1 for g, _ in out if int(g) not in shared)
+    # the freed GPU blocks are reused (and overwritten) by a new sequence
+    bm.add_sequence(3)
+    bm.append_tokens(3, B * min(bm.num_free(), 12))
+    dev[bm.tables[3, :int(bm.nblocks[3])]] = 0xDEAD
+    bm.free_sequence(3)
+
+    back = bm.swap_in(1)
+    assert not bm.swapped[1] and bm.num_free_host() == hfree0
+    assert oracle.swap_blocks([dev], [host], back) == 0
+    for s in (0, 1, 2):
+        assert np.array_equal(gather(dev, bm.tables[s], int(bm.nblocks[s])), before[s])
+    # blocks sequence 1 shared with sequence 0 came back as private copies
+    n_shared = sum(1 for g, _ in out if int(g) in shared)
+    assert n_shared == 2 and bm.num_free() == free0 - n_shared
+
+
+def test_swap_errors_leave_state_unchanged():
+    bm = BlockManager(8, 4, 2, 4, num_host_blocks=1)
+    bm.add_sequence(0)
+    bm.append_tokens(0, 9)             # 3 blocks, more than the one host block
+    tables, free = bm.tables.copy(), bm.num_free()
+    with pytest.raises(OutOfBlocksError):
+        bm.swap_out(0)
+    assert np.array_equal(bm.tables, tables) and bm.num_free() == free and not bm.swapped[0]
+    with pytest.raises(ValueError):
+        bm.swap_in(0)                  # not swapped out
+    bm2 = BlockManager(8, 4, 2, 4, num_host_blocks=4)
+    bm2.add_sequence(0)
+    bm2.append_tokens(0, 8)
+    bm2.swap_out(0)
+    with pytest.raises(ValueError):
+        bm2.append_tokens(0, 1)        # a swapped-out sequence takes no tokens
+    with pytest.raises(ValueError):
+        bm2.fork(0, 1)
+    bm2.free_sequence(0)               # freeing returns its host blocks
+    assert bm2.num_free_host() == 4 and bm2.num_free() == 8
