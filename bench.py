@@ -379,6 +379,7 @@ def run_ours(args, rank, world, local):
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "launch_us": round(dec_avg_ms * 1e3, 3),
+            "launch_us_p10_p50_p90": [round(float(np.percentile(dec_ms, q)) * 1e3, 3) for q in (10, 50, 90)],
             "traffic": committed_traffic(w.name + ("_fp8" if fp8 else "")),
         },
         "clocks": clk,
