@@ -56,11 +56,11 @@
 //    does twice the arithmetic; the fp16 layout above is then bound by
 //    instruction issue, not by HBM.  The FP8 layout cuts the instructions
 //    per token: a lane owns 16 dimensions (16 codes = 16 bytes), a chunk is
-//    32 tokens (it spans 32/B physical blocks, one bulk copy per block for K
-//    and for V), codes are widened to fp16 pairs in registers (exact), and
-//    p.V runs as fp16 x fp16 -> fp32 fused multiply-adds with the softmax
-//    weights rounded to fp16 (relative error <= 2^-11 per weight; the
-//    denominator sums the same rounded weights).  The key scale is folded
+//    16 tokens (it spans 16/B physical blocks when B < 16, one bulk copy per
+//    block for K and for V), codes are widened to fp16 pairs in registers
+//    (exact), and p.V runs as fp16 x fp16 -> fp32 fused multiply-adds with
+//    the softmax weights rounded to fp16 (relative error <= 2^-11 per
+//    weight; the denominator sums the same rounded weights).  The key scale is folded
 //    into the logit scale and the value scale multiplies the CTA's merged
 //    output.
 #pragma once
