@@ -393,39 +393,34 @@ def run_ours(args, rank, world, local):
 
 def measure_e2e(st, args, world, device):
     """Same metric through the public API with the step's inputs in pinned host memory:
-    every step copies q / new K,V / token ids / tables / lengths host->device, runs the
-    step (graph replay unless --eager) and reads every layer's output back."""
+    every step copies q / new K,V / token ids / tables / lengths host->device and reads every
+    layer's output back (DecodeStep.bind_host: the uploads run ahead of the compute on a copy
+    stream, the outputs go back on a second one right behind the decodes), as a graph replay
+    unless --eager."""
     import torch
     dw = st.dw
     pin = lambda t: t.detach().cpu().pin_memory()  # noqa: E731
     h_q = [pin(t) for t in dw.queries]
     h_k = [pin(t) for t in dw.keys_new]
     h_v = [pin(t) for t in dw.values_new]
-    h_small = [pin(t) for t in (dw.token_seq, dw.token_pos, dw.block_tables, dw.context_lens)]
-    d_small = [dw.token_seq, dw.token_pos, dw.block_tables, dw.context_lens]
+    h_small = [pin(t) for t in (dw.block_tables, dw.context_lens, dw.token_seq, dw.token_pos)]
     h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in st.outs]
     h2d = sum(t.numel() * t.element_size() for t in h_q + h_k + h_v + h_small)
     d2h = sum(t.numel() * t.element_size() for t in h_out)
+    st.step.bind_host(h_q, h_k, h_v, h_out, *h_small)
     K = max(3, min(args.steps, 100))
-    use_graph = st.step.graph is not None
-
-    def one():
-        for hs, ds in zip(h_small, d_small):
-            ds.copy_(hs, non_blocking=True)
-        for i in range(len(dw.layers)):
-            dw.queries[i].copy_(h_q[i], non_blocking=True)
-            dw.keys_new[i].copy_(h_k[i], non_blocking=True)
-            dw.values_new[i].copy_(h_v[i], non_blocking=True)
-        if use_graph:
-            st.step.replay()
-        else:
-            st.step.run()
-        for i in range(len(dw.layers)):
-            h_out[i].copy_(st.outs[i], non_blocking=True)
-
+    use_graph = not args.eager
+    if use_graph:
+        st.step.capture(warmup=2, host=True)
+        one = lambda: st.step.replay(host=True)  # noqa: E731
+    else:
+        one = st.step.run_host
     for _ in range(3):
         one()
     torch.cuda.synchronize(device)
+    for i, o in enumerate(st.outs):  # the host copies are the device results
+        if not torch.equal(h_out[i].view(torch.int16), o.cpu().view(torch.int16)):
+            raise RuntimeError(f"host output of layer {i} differs from the device output")
     barrier(world)
     t0 = time.perf_counter()
     for _ in range(K):
@@ -435,6 +430,8 @@ def measure_e2e(st, args, world, device):
     L = len(dw.layers)
     return {"value": round(st.bytes_per_decode * L * world / dt / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(dt * 1e3, 4), "steps": K, "cuda_graph": use_graph,
+            "copies": "uploads on a copy stream ahead of the compute (waits at layers 0, 1, 2, 4, "
+                      "...); outputs read back on a second copy stream right behind the decodes",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 

@@ -19,6 +19,21 @@ before capturing (``capture`` does this).
 With ``fp8_scales=(k_scale, v_scale)`` the caches are FP8 (E4M3 codes in
 uint8 tensors) and the step uses the library's FP8 cache write, block copy
 and decode.
+
+Host-resident inputs (``bind_host``): every step copies the step's inputs
+from pinned host buffers and its outputs back.  A layer needs only its own
+query and new key/value rows, so the uploads run on a copy stream ahead of
+the compute stream, and each layer's output goes back on a second copy
+stream after its decode: only the first layer's upload and the last layer's
+download are not hidden behind the decode kernels.  The compute stream waits
+for the uploads only at layers 0, 1, 2, 4, 8, ... (each wait covers the next
+power-of-two group of layers, which the copy stream, several times faster
+than the decode, has finished by then), and hands outputs to the download
+stream in the mirror-image groups (..., 4, 2, 1, 1 layers at the end), so
+most consecutive kernels keep their programmatic launch chaining.  The small
+per-step inputs (token ids and positions, block tables, context lengths) are
+copied first, on the compute stream.  The whole fork/join captures into one
+CUDA graph like the device-resident step.
 """
 from __future__ import annotations
 
@@ -26,6 +41,16 @@ import torch
 
 from . import (decode_workspace, pa_copy_blocks, pa_copy_blocks_fp8, pa_decode, pa_decode_fp8,
                pa_reshape_and_cache, pa_reshape_and_cache_fp8, pa_slot_mapping)
+
+
+def _pow2_groups(n: int) -> list[tuple[int, int]]:
+    """Layer ranges [0, 1), [1, 2), [2, 4), [4, 8), ... covering n layers."""
+    out, a = [], 0
+    while a < n:
+        b = min(n, max(1, 2 * a))
+        out.append((a, b))
+        a = b
+    return out
 
 
 class DecodeStep:
@@ -50,7 +75,9 @@ class DecodeStep:
         S, H, D = queries[0].shape
         self.slots = torch.empty(token_seq.numel(), dtype=torch.int64, device=dev)
         self.workspace = decode_workspace(S, H, D, self.max_context_len, dev)
-        self.graph: torch.cuda.CUDAGraph | None = None
+        self.graph: torch.cuda.CUDAGraph | None = None        # device-resident step
+        self.host_graph: torch.cuda.CUDAGraph | None = None   # step from / to the host buffers
+        self.host = None
 
     @property
     def num_layers(self) -> int:
@@ -68,40 +95,129 @@ class DecodeStep:
         pa_slot_mapping(self.slots, self.block_tables, self.token_seq, self.token_pos, self.block_size,
                         self.num_blocks, s)
         for i in range(self.num_layers):
-            if f8:
-                pa_reshape_and_cache_fp8(self.keys_new[i], self.values_new[i], self.key_caches[i],
-                                         self.value_caches[i], self.slots, f8[0], f8[1], s)
-            else:
-                pa_reshape_and_cache(self.keys_new[i], self.values_new[i], self.key_caches[i],
-                                     self.value_caches[i], self.slots, s)
+            self._write(i, s)
             if decode_events is not None:
                 decode_events[i][0].record(s)
-            if f8:
-                pa_decode_fp8(self.outs[i], self.queries[i], self.key_caches[i], self.value_caches[i],
-                              self.block_tables, self.context_lens, self.scale, f8[0], f8[1],
-                              self.max_context_len, self.workspace, s)
-            else:
-                pa_decode(self.outs[i], self.queries[i], self.key_caches[i], self.value_caches[i],
-                          self.block_tables, self.context_lens, self.scale, self.max_context_len,
-                          self.workspace, s)
+            self._decode(i, s)
             if decode_events is not None:
                 decode_events[i][1].record(s)
 
-    def capture(self, warmup: int = 2) -> None:
-        """Warm up (eager runs), then capture one step into a CUDA graph."""
+    def bind_host(self, queries, keys_new, values_new, outs, block_tables, context_lens, token_seq,
+                  token_pos) -> None:
+        """Pinned host buffers the step reads its inputs from and writes its outputs to (one
+        query / new key / new value / output tensor per layer, shaped like the device ones)."""
+        n = self.num_layers
+        if not (len(queries) == len(keys_new) == len(values_new) == len(outs) == n):
+            raise ValueError("one host query, new key/value and output per layer")
+        pairs = list(zip(queries, self.queries)) + list(zip(keys_new, self.keys_new)) + \
+            list(zip(values_new, self.values_new)) + list(zip(outs, self.outs)) + \
+            [(block_tables, self.block_tables), (context_lens, self.context_lens),
+             (token_seq, self.token_seq), (token_pos, self.token_pos)]
+        for h, d in pairs:
+            if h.is_cuda or not h.is_pinned():
+                raise ValueError("host buffers must be pinned host memory")
+            if h.shape != d.shape or h.dtype != d.dtype or not h.is_contiguous():
+                raise ValueError("a host buffer does not match its device buffer")
+        dev = self.queries[0].device
+        self.host = {
+            "q": list(queries), "k": list(keys_new), "v": list(values_new), "out": list(outs),
+            "small": [(block_tables, self.block_tables), (context_lens, self.context_lens),
+                      (token_seq, self.token_seq), (token_pos, self.token_pos)],
+            "up": torch.cuda.Stream(dev), "down": torch.cuda.Stream(dev),
+            "ev_in": [torch.cuda.Event() for _ in range(n)],
+            "ev_out": [torch.cuda.Event() for _ in range(n)],
+        }
+
+    def run_host(self, stream=None) -> None:
+        """One step from the bound host buffers to the bound host outputs (see bind_host),
+        launched eagerly on `stream` with the copies overlapped layer by layer."""
+        if self.host is None:
+            raise RuntimeError("bind_host() first")
+        hb = self.host
+        s = stream if stream is not None else torch.cuda.current_stream()
+        up, down = hb["up"], hb["down"]
+        # The copy streams start after everything queued before this step.
+        up.wait_stream(s)
+        down.wait_stream(s)
+        groups = _pow2_groups(self.num_layers)
+        with torch.cuda.stream(up):
+            for g0, g1 in groups:
+                for i in range(g0, g1):
+                    self.queries[i].copy_(hb["q"][i], non_blocking=True)
+                    self.keys_new[i].copy_(hb["k"][i], non_blocking=True)
+                    self.values_new[i].copy_(hb["v"][i], non_blocking=True)
+                hb["ev_in"][g0].record(up)
+        with torch.cuda.stream(s):
+            for h, d in hb["small"]:
+                d.copy_(h, non_blocking=True)
+        f8 = self.fp8_scales
+        if self.copy_pairs is not None and self.copy_pairs.numel():
+            (pa_copy_blocks_fp8 if f8 else pa_copy_blocks)(self.key_caches, self.value_caches,
+                                                           self.copy_pairs, s)
+        pa_slot_mapping(self.slots, self.block_tables, self.token_seq, self.token_pos, self.block_size,
+                        self.num_blocks, s)
+        starts = {g0 for g0, _ in groups}
+        # Downloads in the mirror-image groups: ..., 4, 2, 1, 1 layers at the end.
+        L = self.num_layers
+        ends = {L - g0: L - g1 for g0, g1 in groups}   # group end (exclusive) -> group start
+        for i in range(L):
+            if i in starts:
+                s.wait_event(hb["ev_in"][i])
+            self._write(i, s)
+            self._decode(i, s)
+            if i + 1 in ends:
+                hb["ev_out"][i].record(s)
+                down.wait_event(hb["ev_out"][i])
+                with torch.cuda.stream(down):
+                    for j in range(ends[i + 1], i + 1):
+                        hb["out"][j].copy_(self.outs[j], non_blocking=True)
+        # The step ends when its last output is on the host.
+        s.wait_stream(down)
+        s.wait_stream(up)
+
+    def _write(self, i: int, s) -> None:
+        """Layer i's cache write of the new tokens."""
+        f8 = self.fp8_scales
+        if f8:
+            pa_reshape_and_cache_fp8(self.keys_new[i], self.values_new[i], self.key_caches[i],
+                                     self.value_caches[i], self.slots, f8[0], f8[1], s)
+        else:
+            pa_reshape_and_cache(self.keys_new[i], self.values_new[i], self.key_caches[i],
+                                 self.value_caches[i], self.slots, s)
+
+    def _decode(self, i: int, s) -> None:
+        """Layer i's paged decode."""
+        f8 = self.fp8_scales
+        if f8:
+            pa_decode_fp8(self.outs[i], self.queries[i], self.key_caches[i], self.value_caches[i],
+                          self.block_tables, self.context_lens, self.scale, f8[0], f8[1],
+                          self.max_context_len, self.workspace, s)
+        else:
+            pa_decode(self.outs[i], self.queries[i], self.key_caches[i], self.value_caches[i],
+                      self.block_tables, self.context_lens, self.scale, self.max_context_len,
+                      self.workspace, s)
+
+    def capture(self, warmup: int = 2, host: bool = False) -> None:
+        """Warm up (eager runs), then capture one step into a CUDA graph; with host=True the
+        captured step is run_host (copies from / to the bound host buffers included)."""
+        fn = self.run_host if host else self.run
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
             for _ in range(max(1, warmup)):
-                self.run(side)
+                fn(side)
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.run(torch.cuda.current_stream())
-        self.graph = g
+            fn(torch.cuda.current_stream())
+        if host:
+            self.host_graph = g
+        else:
+            self.graph = g
 
-    def replay(self) -> None:
-        if self.graph is None:
+    def replay(self, host: bool = False) -> None:
+        g = self.host_graph if host else self.graph
+        if g is None:
             raise RuntimeError("capture() first")
-        self.graph.replay()
+        g.replay()

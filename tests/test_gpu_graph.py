@@ -96,3 +96,65 @@ def test_graph_step_with_copy_on_write():
     assert torch.equal(eager.outs[0].view(torch.int16), graph.outs[0].view(torch.int16))
     assert np.array_equal(u16(dw_eager.key_caches[0]), u16(dw.key_caches[0]))
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+@pytest.mark.parametrize("cfg,layers,use_graph", [(2, [0], False), (5, [0, 1], True), (1, [0, 1, 2], True)])
+def test_host_staged_step_matches_device_step(cfg, layers, use_graph):
+    """Inputs uploaded from pinned host buffers and outputs read back, overlapped layer by
+    layer (eager or as one graph): the host outputs and the caches are bit-identical to the
+    device-resident step's, also after the host inputs change in place; the device input
+    buffers are poisoned before each run, so every input must come through the copies."""
+    w = configs.ALL[cfg]() if cfg != 5 else configs.config5(num_layers=2)
+    dw_ref = gpu.materialize(w, layers=layers, device=DEV)
+    ref = make_step(w, dw_ref)
+    dw = gpu.materialize(w, layers=layers, device=DEV)
+    st = make_step(w, dw)
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    h_q, h_k, h_v = ([pin(t) for t in ts] for ts in (dw.queries, dw.keys_new, dw.values_new))
+    h_small = [pin(t) for t in (dw.block_tables, dw.context_lens, dw.token_seq, dw.token_pos)]
+    h_out = [torch.full(o.shape, float("nan"), dtype=o.dtype).pin_memory() for o in st.outs]
+    st.bind_host(h_q, h_k, h_v, h_out, *h_small)
+
+    def poison():
+        for t in dw.queries + dw.keys_new + dw.values_new:
+            t.fill_(float("nan"))
+        dw.context_lens.zero_()
+        dw.token_pos.zero_()
+
+    if use_graph:
+        st.capture(host=True)
+    for rep in range(2):
+        if rep == 1:                      # new queries, in place, on both sides
+            for qr, qh in zip(dw_ref.queries, h_q):
+                qr.mul_(-1.0)
+                qh.mul_(-1.0)
+        poison()
+        ref.run()
+        st.replay(host=True) if use_graph else st.run_host()
+        torch.cuda.synchronize()
+        for a, b in zip(ref.outs, h_out):
+            assert torch.equal(a.cpu().view(torch.int16), b.view(torch.int16))
+    for a, b in zip(dw_ref.key_caches + dw_ref.value_caches, dw.key_caches + dw.value_caches):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+def test_bind_host_refuses_pageable_or_mismatched_buffers():
+    w = configs.config1()
+    dw = gpu.materialize(w, layers=[0], device=DEV)
+    st = make_step(w, dw)
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    args = [[pin(dw.queries[0])], [pin(dw.keys_new[0])], [pin(dw.values_new[0])],
+            [torch.empty(st.outs[0].shape, dtype=torch.float16).pin_memory()]] + \
+        [pin(t) for t in (dw.block_tables, dw.context_lens, dw.token_seq, dw.token_pos)]
+    st.bind_host(*args)
+    bad = list(args)
+    bad[0] = [dw.queries[0].cpu()]                       # pageable
+    with pytest.raises(ValueError):
+        st.bind_host(*bad)
+    bad = list(args)
+    bad[4] = pin(dw.block_tables[:, :1].contiguous())    # wrong shape
+    with pytest.raises(ValueError):
+        st.bind_host(*bad)
+    with pytest.raises(RuntimeError):
+        make_step(w, dw).run_host()
