@@ -8,11 +8,13 @@
 //   out = softmax_{i <= p}(scale * q . K_i) V.
 //
 // Design (GB300):
-//  * One CTA of four warps per (sequence, head, tile of 128 new tokens).
-//    Q (128 x D) and the paged K/V tiles (128 tokens = 128/B blocks) arrive
-//    by TMA tensor copies with 128-byte swizzle, one box per physical block,
-//    into a two-stage ring; a block past the context is fetched from an
-//    out-of-range coordinate (zero fill).
+//  * One CTA per (sequence, head, pair of 128-row query tiles), 12 warps:
+//    two softmax warpgroups (one query row per thread) and a producer
+//    warpgroup whose first warp issues the MMAs and second the TMA copies.
+//    Q (128 x D per tile) and the paged K/V tiles (128 tokens = 128/B
+//    blocks) arrive by TMA tensor copies with 128-byte swizzle, one box per
+//    physical block, into two-stage rings; a block past the context is
+//    fetched from an out-of-range coordinate (zero fill).
 //  * One thread issues tcgen05.mma: S = Q K^T (M = 128 queries, N = 128
 //    tokens, fp32 in TMEM columns [0, 128)), then O += P V (N = D, TMEM
 //    columns [128, 128 + D)), each as D/16 or 8 instructions of K = 16 with
