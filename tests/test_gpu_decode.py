@@ -198,3 +198,33 @@ def test_decode_context_beyond_max_is_clipped_and_flagged():
     kc, vc = gpu.host_pool(w, 0)
     _, ref64, _ = oracle.decode(q, kc, vc, w.block_tables, np.full(2, 48, np.int32), w.scale)
     decode_gate(out, ref64, "clipped to max_context_len")
+
+
+@pytest.mark.parametrize("part", [0, 32])
+def test_decode_more_sequences_than_one_launch(part):
+    """1100 sequences (the call splits them over two launches of at most 1024, each with its own
+    item numbering and the shared workspace), ragged and empty contexts, every output."""
+    pa.pa_decode_set_partition_tokens(part)
+    w = configs.small_random(5100 + part, 1100, 2, 64, 16, 100, min_context=0)
+    dw = gpu.materialize(w, device=DEV)
+    mask = live_slot_mask(w.block_tables, w.context_lens, w.num_blocks, 16)
+    poison_dead_slots_device(dw.key_caches[0], dw.value_caches[0], mask)
+    out = run_decode(dw)
+    _, ref64, rc = full_oracle(w, write_new=False)
+    assert rc == 0
+    decode_gate(out, ref64, f"S1100 part{part}")
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+@pytest.mark.parametrize("part", [0, 32])
+def test_decode_long_contexts_many_partitions(part):
+    """Contexts up to 20 000 tokens: 40 partitions of 512, or 625 of 32 (the merge walks its
+    partials in rounds of 32), every output."""
+    pa.pa_decode_set_partition_tokens(part)
+    w = configs.small_random(5200 + part, 3, 2, 128, 32, 20000, min_context=15000)
+    dw = gpu.materialize(w, device=DEV)
+    out = run_decode(dw)
+    _, ref64, rc = full_oracle(w, poison=False, write_new=False)
+    assert rc == 0
+    decode_gate(out, ref64, f"long contexts part{part}")
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)

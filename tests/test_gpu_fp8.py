@@ -236,3 +236,18 @@ def test_decode_fp8_out_of_range_block_id_is_flagged():
     st, bits = pa.pa_check_errors()
     assert st == pa.PA_ERR_OUT_OF_RANGE and bits & pa.PA_ERRBIT_BLOCK_ID
     assert NAN8 == 0x7F
+
+
+def test_decode_fp8_more_sequences_than_one_launch():
+    """1100 sequences over two launches, forced 32-token partitions, every output."""
+    pa.pa_decode_set_partition_tokens(32)
+    w = configs.small_random(5300, 1100, 2, 128, 16, 100, min_context=0)
+    dw = materialize_fp8(w)
+    out = run_decode_fp8(dw)
+    kc8, vc8 = oracle_fp8_pool(w)
+    q = gpu.host_small(w, 0)[0]
+    ks, vs = configs.fp8_scales(w)
+    _, ref64, rc = oracle.decode_fp8(q, kc8, vc8, w.block_tables, w.context_lens, w.scale, ks, vs)
+    assert rc == 0
+    decode_gate(out, ref64, "fp8 S1100")
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
