@@ -130,3 +130,15 @@ def test_prefill_bad_inputs_flagged():
     w.block_tables[1, 0] = 0
     ref64 = oracle_prefill(w)
     decode_gate(out[:40], ref64[:40], "unaffected sequence")
+
+
+def test_prefill_long_chunk_and_many_decode_rows():
+    """A 1000-token chunk over a 5000-token context (four query-tile pairs), a 700-token
+    whole-context chunk and 150 one-token rows in one batch; every output."""
+    q_lens = [1000] + [1] * 150 + [700]
+    ctx = [5000] + [100 + 13 * i for i in range(150)] + [700]
+    w = configs.prefill_workload("long_many", 4600, q_lens, ctx, 2, 128, 16)
+    dv = gpu.materialize_prefill(w, DEV)
+    out = run_prefill(w, dv)
+    decode_gate(out, oracle_prefill(w), "long chunk + 150 decode rows")
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)

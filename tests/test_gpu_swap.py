@@ -164,3 +164,32 @@ def test_block_manager_swap_round_trip_keeps_decode_bits():
     torch.cuda.synchronize()
     assert torch.equal(before.view(torch.int16), after.view(torch.int16))
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+def test_swap_more_caches_and_pairs_than_one_launch():
+    """70 caches (the kernel takes 64 per launch) and, on one cache, 70 000 pairs (at most
+    65 535 per launch): every block lands where the oracle puts it."""
+    rng = np.random.default_rng(31)
+    dev, host = pools(rng, 35, 12, 8, (1, 4, 64), torch.float16)
+    ref_dev = [host_view(t) for t in dev]
+    ref_host = [host_view(t) for t in host]
+    mapping = np.stack([rng.choice(12, 8, replace=False), rng.permutation(8)], 1).astype(np.int64)
+    pa.pa_swap_blocks(host, dev, torch.from_numpy(mapping).to(DEV))
+    torch.cuda.synchronize()
+    assert oracle.swap_blocks(ref_host, ref_dev, mapping) == 0
+    for t, r in zip(host, ref_host):
+        assert np.array_equal(host_view(t), r)
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+    n = 70_000
+    d_pool = torch.from_numpy(rng.integers(0, 1 << 16, (n, 1, 4, 64), dtype=np.uint16)
+                              .view(np.int16)).to(DEV).view(torch.float16)
+    h_pool = torch.zeros((n, 1, 4, 64), dtype=torch.float16).pin_memory()
+    big = np.stack([rng.permutation(n), rng.permutation(n)], 1).astype(np.int64)
+    pa.pa_swap_blocks([h_pool], [d_pool], torch.from_numpy(big).to(DEV))
+    torch.cuda.synchronize()
+    ref = [host_view(h_pool)]
+    expect = np.zeros_like(ref[0])
+    expect[big[:, 1]] = host_view(d_pool)[big[:, 0]]
+    assert np.array_equal(ref[0], expect)
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
