@@ -64,6 +64,9 @@ def lib() -> ctypes.CDLL:
     L.oracle_swap_blocks.restype = i32
     L.oracle_prefill.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, f64]
     L.oracle_prefill.restype = i32
+    L.oracle_prefill_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
+                                     f64, f64, f64]
+    L.oracle_prefill_fp8.restype = i32
     L.oracle_num_threads.argtypes = []
     L.oracle_num_threads.restype = i32
     _LIB = L
@@ -256,6 +259,28 @@ def prefill(query, key_cache, value_cache, block_tables, context_lens, query_sta
                               q.ctypes.data, kc.ctypes.data, vc.ctypes.data, bt.ctypes.data,
                               bt.shape[1], cl.ctypes.data, qs.ctypes.data, cl.shape[0], H, D, B,
                               NB, float(scale))
+    return out16, out64, rc
+
+
+def prefill_fp8(query, key_cache, value_cache, block_tables, context_lens, query_start,
+                scale: float, k_scale: float, v_scale: float, want64: bool = True):
+    """Multi-query paged attention over uint8 (E4M3) caches; returns (out16, out64 or None,
+    status)."""
+    q = _u16(query)
+    kc = _c(key_cache, np.uint8)
+    vc = _c(value_cache, np.uint8)
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    qs = _c(query_start, np.int32)
+    TQ, H, D = q.shape
+    NB, H2, B, D2 = kc.shape
+    assert H2 == H and D2 == D and qs.shape[0] == cl.shape[0] + 1 and qs[-1] == TQ
+    out16 = np.zeros((TQ, H, D), dtype=np.uint16)
+    out64 = np.zeros((TQ, H, D), dtype=np.float64) if want64 else None
+    rc = lib().oracle_prefill_fp8(out16.ctypes.data, out64.ctypes.data if want64 else None,
+                                  q.ctypes.data, kc.ctypes.data, vc.ctypes.data, bt.ctypes.data,
+                                  bt.shape[1], cl.ctypes.data, qs.ctypes.data, cl.shape[0], H, D,
+                                  B, NB, float(scale), float(k_scale), float(v_scale))
     return out16, out64, rc
 
 

@@ -453,6 +453,69 @@ int oracle_decode_fp8(uint16_t* out16, double* out64, const uint16_t* query,
   return bad ? -1 : 0;
 }
 
+/* Multi-query paged attention over FP8 caches: the causal attention of
+ * oracle_prefill on the dequantised values K_i = E4M3(code) * k_scale,
+ * V_i = E4M3(code) * v_scale (exact in binary64).  Returns -1 on the same
+ * bad inputs as oracle_prefill. */
+int oracle_prefill_fp8(uint16_t* out16, double* out64, const uint16_t* query,
+                       const uint8_t* key_cache, const uint8_t* value_cache,
+                       const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                       const int32_t* query_start, int num_seqs, int num_heads, int head_dim,
+                       int block_size, int num_blocks, double scale, double k_scale,
+                       double v_scale) {
+  int bad = 0;
+  const long pairs = (long)num_seqs * num_heads;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (long sh = 0; sh < pairs; ++sh) {
+    const int s = (int)(sh / num_heads);
+    const int h = (int)(sh % num_heads);
+    const int c = context_lens[s];
+    const int q0 = query_start[s];
+    const int q_len = query_start[s + 1] - q0;
+    int ok = (c >= 0) && (c <= max_blocks * block_size) && (q_len >= 0) && (q_len <= c);
+    double* x = (double*)malloc(sizeof(double) * (size_t)(c > 0 ? c : 1));
+    double* qd = (double*)malloc(sizeof(double) * (size_t)head_dim);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)head_dim);
+    for (int j = 0; ok && j < q_len; ++j) {
+      const int p = c - q_len + j; /* position of new token j: it sees keys 0..p */
+      const size_t row = ((size_t)(q0 + j) * num_heads + h) * head_dim;
+      for (int d = 0; d < head_dim; ++d) qd[d] = oracle_half_to_double(query[row + d]);
+      for (int i = 0; ok && i <= p; ++i) {
+        const int phys = block_tables[(size_t)s * max_blocks + i / block_size];
+        if (phys < 0 || phys >= num_blocks) { ok = 0; break; }
+        const uint8_t* k =
+            key_cache + (((size_t)phys * num_heads + h) * block_size + i % block_size) * head_dim;
+        double dot = 0.0;
+        for (int d = 0; d < head_dim; ++d) dot += qd[d] * (oracle_e4m3_to_double(k[d]) * k_scale);
+        x[i] = dot * scale;
+      }
+      if (!ok) break;
+      double m = x[0];
+      for (int i = 1; i <= p; ++i) if (x[i] > m) m = x[i];
+      double denom = 0.0;
+      for (int d = 0; d < head_dim; ++d) acc[d] = 0.0;
+      for (int i = 0; i <= p; ++i) {
+        const double w = exp(x[i] - m);
+        const int phys = block_tables[(size_t)s * max_blocks + i / block_size];
+        const uint8_t* v =
+            value_cache + (((size_t)phys * num_heads + h) * block_size + i % block_size) * head_dim;
+        denom += w;
+        for (int d = 0; d < head_dim; ++d) acc[d] += w * (oracle_e4m3_to_double(v[d]) * v_scale);
+      }
+      for (int d = 0; d < head_dim; ++d) {
+        const double o = acc[d] / denom;
+        if (out64) out64[row + d] = o;
+        if (out16) out16[row + d] = oracle_double_to_half(o);
+      }
+    }
+    if (!ok) bad |= 1;
+    free(x);
+    free(qd);
+    free(acc);
+  }
+  return bad ? -1 : 0;
+}
+
 /* Threads the decode loop uses (OpenMP's maximum, 1 without OpenMP). */
 int oracle_num_threads(void) {
 #ifdef _OPENMP
