@@ -542,14 +542,26 @@ def run_prefill_bench(args):
     dev = torch.device("cuda", 0)
     w = configs.prefill_7b()
     dv = gpu.materialize_prefill(w, dev)
+    fp8 = args.kv_dtype == "fp8"
+    ks, vs = configs.fp8_scales(w)
+    if fp8:  # the same pool as E4M3 codes (the library's conversion)
+        for name, sc in (("key_cache", ks), ("value_cache", vs)):
+            codes = torch.empty(dv[name].shape, dtype=torch.uint8, device=dev)
+            pa.pa_convert_cache_fp8(dv[name], codes, sc)
+            dv[name] = codes
     tq = int(np.sum(w.extra["q_lens"]))
     out = torch.empty((tq, w.num_heads, w.head_dim), dtype=torch.float16, device=dev)
     max_q = int(max(w.extra["q_lens"]))
     stream = torch.cuda.current_stream(dev)
 
     def call():
-        pa.pa_prefill(out, dv["query"], dv["key_cache"], dv["value_cache"], dv["block_tables"],
-                      dv["context_lens"], dv["query_start"], w.scale, max_q)
+        if fp8:
+            pa.pa_prefill_fp8(out, dv["query"], dv["key_cache"], dv["value_cache"],
+                              dv["block_tables"], dv["context_lens"], dv["query_start"], w.scale,
+                              ks, vs, max_q)
+        else:
+            pa.pa_prefill(out, dv["query"], dv["key_cache"], dv["value_cache"], dv["block_tables"],
+                          dv["context_lens"], dv["query_start"], w.scale, max_q)
 
     K, W = max(3, min(args.steps, 200)), max(3, args.warmup)
     for _ in range(W):
@@ -575,13 +587,15 @@ def run_prefill_bench(args):
             peak, kind = float(json.load(f)["bf16_tflops"]), "measured (bf16 burst; fp16 runs at the bf16 rate)"
     except (OSError, KeyError, ValueError):
         peak, kind = 1900.0, "fallback"
-    kv_bytes = int(np.sum(w.context_lens)) * w.num_heads * w.head_dim * 2 * 2
+    kv_bytes = int(np.sum(w.context_lens)) * w.num_heads * w.head_dim * 2 * (1 if fp8 else 2)
     tflops = flops / sec / 1e12
     return {
         "metric": "multi-query paged attention TFLOP/s (causal algorithmic FLOPs over call time)",
         "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": W,
-        "ms_per_call": round(sec * 1e3, 4), "higher_is_better": True, "dtype": "f16 in, f32 accumulate",
-        "data": "synthetic", "config": {"workload": w.name, "num_seqs": w.num_seqs,
+        "ms_per_call": round(sec * 1e3, 4), "higher_is_better": True,
+        "dtype": ("e4m3 KV cache widened to f16" if fp8 else "f16") + " operands, f32 accumulate",
+        "data": "synthetic", "config": {"workload": w.name, "kv_dtype": args.kv_dtype,
+                                        "num_seqs": w.num_seqs,
                                         "num_heads": w.num_heads, "head_dim": w.head_dim,
                                         "block_size": w.block_size, "query_tokens": tq,
                                         "context_tokens": int(np.sum(w.context_lens))},
@@ -590,17 +604,21 @@ def run_prefill_bench(args):
                      "kv_bytes_per_call": kv_bytes,
                      "kv_gbs": round(kv_bytes / sec / 1e9, 1)},
         "clocks": clk, "gpu_launches": K + W,
-        "cpu_baseline": None if args.no_cpu_baseline else prefill_cpu_baseline(w, budget_s=10.0),
+        "cpu_baseline": None if args.no_cpu_baseline else prefill_cpu_baseline(w, budget_s=10.0,
+                                                                               fp8=fp8),
     }
 
 
-def prefill_cpu_baseline(w, budget_s: float):
+def prefill_cpu_baseline(w, budget_s: float, fp8: bool = False):
     """The oracle's multi-query attention on a bounded sample of the same workload: the last
     32 new tokens of sequence 0 over its whole context, every head (the causally truncated
     problem that gives exactly those rows)."""
     import oracle
     from workloads import gpu
     kc, vc = gpu.host_pool(w, 0)
+    ks, vs = configs.fp8_scales(w)
+    if fp8:
+        kc, vc = oracle.quantize_e4m3(kc, ks), oracle.quantize_e4m3(vc, vs)
     q = gpu.host_queries(w)
     qs = configs.query_start(w)
     ql, c, n = int(w.extra["q_lens"][0]), int(w.context_lens[0]), 32
@@ -610,8 +628,12 @@ def prefill_cpu_baseline(w, budget_s: float):
     reps, t_total = 0, 0.0
     while t_total < budget_s or reps < 1:
         t0 = time.perf_counter()
-        _, _, rc = oracle.prefill(rows, kc, vc, bt, np.array([c], np.int32), np.array([0, n], np.int32),
-                                  w.scale, want64=False)
+        if fp8:
+            _, _, rc = oracle.prefill_fp8(rows, kc, vc, bt, np.array([c], np.int32),
+                                          np.array([0, n], np.int32), w.scale, ks, vs, want64=False)
+        else:
+            _, _, rc = oracle.prefill(rows, kc, vc, bt, np.array([c], np.int32),
+                                      np.array([0, n], np.int32), w.scale, want64=False)
         t_total += time.perf_counter() - t0
         reps += 1
         assert rc == 0

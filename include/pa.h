@@ -229,6 +229,24 @@ pa_status pa_prefill(void* out, const void* query, const void* key_cache, const 
                      int num_blocks, float scale, int max_query_len, pa_stream_t stream);
 
 /*
+ * pa_prefill over FP8 (E4M3) caches [P2 §3.3: FP8 KV caches; format and
+ * scaling as for pa_decode_fp8]: the same causal attention with
+ * K_paged[s,h,i,:] = E4M3(key code) * k_scale and V likewise with v_scale.
+ * key_cache / value_cache are uint8 [num_blocks][num_heads][block_size]
+ * [head_dim] codes; query and out stay fp16.  The kernel widens each K / V
+ * tile to fp16 in shared memory (exact) and runs the same tensor-core
+ * products; the key scale is folded into the logit scale and the value scale
+ * applied with the final division.  k_scale and v_scale must be finite and
+ * positive (else PA_ERR_INVALID_ARG).  Everything else as pa_prefill.
+ */
+pa_status pa_prefill_fp8(void* out, const void* query, const void* key_cache,
+                         const void* value_cache, const int32_t* block_tables,
+                         int max_blocks_per_seq, const int32_t* context_lens,
+                         const int32_t* query_start, int num_seqs, int num_query_tokens,
+                         int num_heads, int head_dim, int block_size, int num_blocks, float scale,
+                         float k_scale, float v_scale, int max_query_len, pa_stream_t stream);
+
+/*
  * Block swap between the device cache and a host copy [P4 §三: when GPU
  * memory runs short the scheduler moves some blocks to CPU memory and brings
  * them back when needed (blocks_to_swap_out / blocks_to_swap_in); P2 §4.3:

@@ -55,6 +55,9 @@ _lib.pa_convert_cache_fp8.restype = _i32
 _lib.pa_prefill.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                             _i32, _f32, _i32, _vp]
 _lib.pa_prefill.restype = _i32
+_lib.pa_prefill_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
+                                _i32, _i32, _f32, _f32, _f32, _i32, _vp]
+_lib.pa_prefill_fp8.restype = _i32
 _lib.pa_swap_blocks.argtypes = [_vp, _vp, _i32, _vp, _i32, _sz, ctypes.c_int64, ctypes.c_int64, _vp]
 _lib.pa_swap_blocks.restype = _i32
 _lib.pa_copy_blocks_fp8.argtypes = [_vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _vp]
@@ -248,6 +251,21 @@ def pa_prefill(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
                query_start: torch.Tensor, scale: float, max_query_len: int, stream=None) -> None:
     """Multi-query paged attention (chunked prefill / mixed batches): out[TQ,H,D] for the new
     tokens query[TQ,H,D]; query_start int32 [S+1] (see pa_prefill in include/pa.h)."""
+    _prefill(out, query, key_cache, value_cache, block_tables, context_lens, query_start, scale,
+             max_query_len, stream, None)
+
+
+def pa_prefill_fp8(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                   value_cache: torch.Tensor, block_tables: torch.Tensor,
+                   context_lens: torch.Tensor, query_start: torch.Tensor, scale: float,
+                   k_scale: float, v_scale: float, max_query_len: int, stream=None) -> None:
+    """pa_prefill over E4M3 caches (uint8 or float8_e4m3fn tensors) with per-tensor scales."""
+    _prefill(out, query, key_cache, value_cache, block_tables, context_lens, query_start, scale,
+             max_query_len, stream, (float(k_scale), float(v_scale)))
+
+
+def _prefill(out, query, key_cache, value_cache, block_tables, context_lens, query_start, scale,
+             max_query_len, stream, fp8) -> None:
     TQ, H, D = query.shape
     NB, H2, B, D2 = key_cache.shape
     S = context_lens.shape[0]
@@ -257,14 +275,17 @@ def pa_prefill(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
         raise ValueError("out / block_tables shape")
     if query_start.shape != (S + 1,):
         raise ValueError("query_start must be [num_seqs + 1]")
-    st = _lib.pa_prefill(_ptr(out, "out", torch.float16), _ptr(query, "query", torch.float16),
-                         _ptr(key_cache, "key_cache", torch.float16),
-                         _ptr(value_cache, "value_cache", torch.float16),
-                         _ptr(block_tables, "block_tables", torch.int32), block_tables.shape[1],
-                         _ptr(context_lens, "context_lens", torch.int32),
-                         _ptr(query_start, "query_start", torch.int32), S, TQ, H, D, B, NB,
-                         float(scale), int(max_query_len), _stream(stream))
-    _check(st, "pa_prefill")
+    common = (_ptr(out, "out", torch.float16), _ptr(query, "query", torch.float16),
+              _cache_ptr(key_cache, "key_cache", fp8 is not None),
+              _cache_ptr(value_cache, "value_cache", fp8 is not None),
+              _ptr(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+              _ptr(context_lens, "context_lens", torch.int32),
+              _ptr(query_start, "query_start", torch.int32), S, TQ, H, D, B, NB, float(scale))
+    if fp8 is None:
+        st = _lib.pa_prefill(*common, int(max_query_len), _stream(stream))
+    else:
+        st = _lib.pa_prefill_fp8(*common, fp8[0], fp8[1], int(max_query_len), _stream(stream))
+    _check(st, "pa_prefill_fp8" if fp8 is not None else "pa_prefill")
 
 
 def _swap_ptr(t: torch.Tensor, name: str) -> int:
@@ -331,7 +352,7 @@ def raise_on_device_errors(stream=None) -> None:
 __all__ = [
     "pa_decode", "pa_reshape_and_cache", "pa_copy_blocks", "pa_slot_mapping", "pa_check_errors",
     "pa_decode_fp8", "pa_reshape_and_cache_fp8", "pa_copy_blocks_fp8", "pa_convert_cache_fp8",
-    "pa_swap_blocks", "pa_prefill",
+    "pa_swap_blocks", "pa_prefill", "pa_prefill_fp8",
     "pa_status_string", "pa_decode_workspace_size", "pa_decode_partition_tokens",
     "pa_decode_set_partition_tokens", "decode_workspace", "raise_on_device_errors", "PAError",
 ]

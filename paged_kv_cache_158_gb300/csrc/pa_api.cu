@@ -430,16 +430,21 @@ pa_status pa_swap_blocks(void* const* dst_caches, const void* const* src_caches,
              : PA_ERR_CUDA;
 }
 
-pa_status pa_prefill(void* out, const void* query, const void* key_cache, const void* value_cache,
-                     const int32_t* block_tables, int max_blocks_per_seq,
-                     const int32_t* context_lens, const int32_t* query_start, int num_seqs,
-                     int num_query_tokens, int num_heads, int head_dim, int block_size,
-                     int num_blocks, float scale, int max_query_len, pa_stream_t stream) {
+// Shared by pa_prefill and pa_prefill_fp8 (the latter with E4M3 caches and
+// their scales).
+static pa_status prefill_impl(bool fp8, void* out, const void* query, const void* key_cache,
+                              const void* value_cache, const int32_t* block_tables,
+                              int max_blocks_per_seq, const int32_t* context_lens,
+                              const int32_t* query_start, int num_seqs, int num_query_tokens,
+                              int num_heads, int head_dim, int block_size, int num_blocks,
+                              float scale, float k_scale, float v_scale, int max_query_len,
+                              pa_stream_t stream) {
   if (!head_dim_ok(head_dim) || !(block_size == 8 || block_size == 16 || block_size == 32))
     return PA_ERR_UNSUPPORTED;
   if (num_seqs < 0 || num_query_tokens < 0 || num_heads <= 0 || num_blocks <= 0 ||
       max_blocks_per_seq <= 0 || max_query_len < 0)
     return PA_ERR_INVALID_ARG;
+  if (fp8 && (!scale_ok(k_scale) || !scale_ok(v_scale))) return PA_ERR_INVALID_ARG;
   if (num_seqs == 0 || num_query_tokens == 0 || max_query_len == 0) return PA_OK;
   if (!pa::prefill_rows_fit(num_blocks, num_heads, block_size)) return PA_ERR_UNSUPPORTED;
   if ((long long)num_seqs * ((max_query_len + 127) / 128) * num_heads >= (1LL << 31))
@@ -470,10 +475,34 @@ pa_status pa_prefill(void* out, const void* query, const void* key_cache, const 
   g.num_blocks = num_blocks;
   g.max_blocks = max_blocks_per_seq;
   g.max_query_len = max_query_len;
-  g.scale_log2 = (float)((double)scale * 1.4426950408889634073599246810019);
+  g.fp8 = fp8;
+  g.v_scale = fp8 ? v_scale : 1.f;
+  g.scale_log2 = (float)((double)scale * (fp8 ? (double)k_scale : 1.0) *
+                         1.4426950408889634073599246810019);
   return pa::launch_prefill(g, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
+}
+
+pa_status pa_prefill(void* out, const void* query, const void* key_cache, const void* value_cache,
+                     const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* context_lens, const int32_t* query_start, int num_seqs,
+                     int num_query_tokens, int num_heads, int head_dim, int block_size,
+                     int num_blocks, float scale, int max_query_len, pa_stream_t stream) {
+  return prefill_impl(false, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                      context_lens, query_start, num_seqs, num_query_tokens, num_heads, head_dim,
+                      block_size, num_blocks, scale, 1.f, 1.f, max_query_len, stream);
+}
+
+pa_status pa_prefill_fp8(void* out, const void* query, const void* key_cache,
+                         const void* value_cache, const int32_t* block_tables,
+                         int max_blocks_per_seq, const int32_t* context_lens,
+                         const int32_t* query_start, int num_seqs, int num_query_tokens,
+                         int num_heads, int head_dim, int block_size, int num_blocks, float scale,
+                         float k_scale, float v_scale, int max_query_len, pa_stream_t stream) {
+  return prefill_impl(true, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                      context_lens, query_start, num_seqs, num_query_tokens, num_heads, head_dim,
+                      block_size, num_blocks, scale, k_scale, v_scale, max_query_len, stream);
 }
 
 pa_status pa_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,

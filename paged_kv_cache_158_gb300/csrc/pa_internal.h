@@ -100,7 +100,9 @@ struct PrefillArgs {
   unsigned int* err;
   int num_seqs, num_query_tokens, num_heads, head_dim, block_size, num_blocks, max_blocks;
   int max_query_len;
-  float scale_log2;
+  float scale_log2;   // scale * log2(e) (times the key scale for FP8 caches)
+  bool fp8;           // E4M3 caches (uint8 codes)
+  float v_scale;      // FP8 caches: value scale
 };
 cudaError_t launch_prefill(const PrefillArgs& args, cudaStream_t stream);
 // The cache's rows (num_blocks * num_heads * block_size) fit the kernel's int coordinates.

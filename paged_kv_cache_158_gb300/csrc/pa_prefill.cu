@@ -51,23 +51,27 @@ namespace {
 constexpr int kQT = 128;   // query rows per CTA (MMA M)
 constexpr int kKT = 128;   // KV tokens per tile (MMA N of S, K of P.V)
 
-template <int D>
+template <int D, bool F8>
 struct PrefillTraits {
   static constexpr int NA = D / 64;                 // 128-byte swizzle atoms per row
   static constexpr int ATOM = 128 * 128;            // bytes of one [128 rows][64 fp16] atom array
   static constexpr int QB = kQT * D * 2;
   static constexpr int KB = kKT * D * 2;
+  static constexpr int STB = kKT * D;               // FP8 caches: one tile of codes
   static constexpr int OFF_Q = 0;                   // Q tile x at OFF_Q + x*QB
   static constexpr int OFF_K0 = 2 * QB;             // stage s: K at OFF_K0 + s*2*KB, V after it
-  static constexpr int OFF_BAR = OFF_K0 + 4 * KB;
+  static constexpr int OFF_ST = OFF_K0 + 4 * KB;    // FP8 caches: K codes, then V codes
+  static constexpr int OFF_BAR = OFF_ST + (F8 ? 2 * STB : 0);
   // Barriers, TMEM slot and alignment slack; at least 120 KB so that one CTA
   // holds an SM (each CTA allocates all 512 TMEM columns).
   static constexpr int SMEM_USED = OFF_BAR + 256 + 1024;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+  static_assert(SMEM <= 232448, "beyond the opt-in shared memory of one CTA");
   // Two softmax warpgroups and one producer warpgroup (its first warp issues
-  // the TMA copies and the MMAs).  Registers: the kernel is compiled for 384
-  // threads at kRegsLaunch each; the producer warpgroup gives registers back
-  // and the softmax warpgroups take them (the split never exceeds the launch
+  // the MMAs, its second the TMA copies; with FP8 caches the other two widen
+  // the codes to fp16).  Registers: the kernel is compiled for 384 threads at
+  // kRegsLaunch each; the producer warpgroup gives registers back and the
+  // softmax warpgroups take them (the split never exceeds the launch
   // allocation: kRegsSplit <= 384 * registers per thread at launch).
   static constexpr int THREADS = 384;
   static constexpr uint32_t TMEM_COLS = 512;        // S_x: 128 columns each, O_x: D columns each
@@ -97,7 +101,8 @@ struct PrefillParams {
   int qpairs;                    // pairs of query tiles per sequence covered by the grid
   int max_query_len;             // host bound of the chunk lengths
   int oob_row;                   // a row coordinate past the cache (zero-filled loads)
-  float scale_log2;
+  float scale_log2;              // scale * log2(e), times the key scale for FP8 caches
+  float v_scale;                 // value scale (1 for fp16 caches)
 };
 
 // Per-CTA geometry of one query tile (x = 0, 1 of the pair).
@@ -106,6 +111,28 @@ struct QTile {
   int pos_min;   // position of row 0
   int n_kv;      // KV tiles it needs
 };
+
+// FP8 caches: widens one tile of codes (kKT rows x D codes, row-major) into
+// the fp16 operand layout the TMA copies of an fp16 cache produce with
+// 128-byte swizzle (atoms of 128 rows x 64 halves; the 16-byte chunk c of
+// row r at r * 128 + ((c ^ (r & 7)) * 16)).  64 threads; E4M3 -> fp16 is
+// exact.
+template <int D>
+__device__ __forceinline__ void widen_tile(const unsigned char* src, unsigned char* dst, int ctid) {
+  constexpr int CPR = D / 16;  // 16-code chunks per row
+  constexpr int ATOM = 128 * 128;
+#pragma unroll 4
+  for (int i = ctid; i < kKT * CPR; i += 64) {
+    const int r = i / CPR, j = i % CPR;
+    const uint4 c = lds128(src + r * D + 16 * j);
+    const uint4 h0 = e4m3x8_to_f16x8(make_uint2(c.x, c.y));
+    const uint4 h1 = e4m3x8_to_f16x8(make_uint2(c.z, c.w));
+    const int c0 = 2 * (j % 4);
+    unsigned char* row = dst + (j / 4) * ATOM + r * 128;
+    *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7)) << 4)) = h0;
+    *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) = h1;
+  }
+}
 
 // A waiting thread's view of an mbarrier: the next phase it expects.  Used
 // only where at most one phase can complete between two waits (a parity
@@ -120,18 +147,20 @@ struct Waiter {
   }
 };
 
-template <int D>
-__global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
+template <int D, bool F8>
+__global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const PrefillParams a) {
-  using T = PrefillTraits<D>;
+  using T = PrefillTraits<D, F8>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(sm);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + T::OFF_BAR);
   // barriers: 0 q_full; 1,2 k_full[st]; 3,4 s_full[x]; 5,6 p_full[x]; 7,8 o_full[x]; 9 done;
-  // 10,11 k_empty[st]; 12,13 v_full[st]; 14,15 v_empty[st]
+  // 10,11 k_empty[st]; 12,13 v_full[st]; 14,15 v_empty[st]; FP8 caches: 16 kc_full, 17 kc_empty,
+  // 18 vc_full, 19 vc_empty (the staged codes of the next K / V tile).  With FP8 caches the
+  // fp16 stages are filled by the two widening warps (k_full / v_full: one arrival each).
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + T::OFF_BAR + 192);
   int* fail = reinterpret_cast<int*>(sm + T::OFF_BAR + 196);
@@ -149,8 +178,8 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
 
   if (tid == 0) {
     mbar_init(bar(0), 1);
-    mbar_init(bar(1), 1);
-    mbar_init(bar(2), 1);
+    mbar_init(bar(1), F8 ? 2 : 1);
+    mbar_init(bar(2), F8 ? 2 : 1);
     mbar_init(bar(3), 1);
     mbar_init(bar(4), 1);
     mbar_init(bar(5), 128);
@@ -158,7 +187,16 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
     mbar_init(bar(7), 1);
     mbar_init(bar(8), 1);
     mbar_init(bar(9), T::THREADS);
-    for (int i = 10; i < 16; ++i) mbar_init(bar(i), 1);
+    mbar_init(bar(10), 1);
+    mbar_init(bar(11), 1);
+    mbar_init(bar(12), F8 ? 2 : 1);
+    mbar_init(bar(13), F8 ? 2 : 1);
+    mbar_init(bar(14), 1);
+    mbar_init(bar(15), 1);
+    mbar_init(bar(16), 1);
+    mbar_init(bar(17), 2);
+    mbar_init(bar(18), 1);
+    mbar_init(bar(19), 2);
     *fail = 0;
     fence_mbar_init();
     prefetch_tensormap(&tq);
@@ -234,29 +272,46 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       // Program order per tile: K(t) then V(t); K(t + 1) needs the QK of
       // tile t - 1, which the MMA warp issues after the P.V of tile t - 2 that
       // frees V(t)'s stage, so this order never waits on a later release.
+      // FP8 caches: the codes of tile t go to the staging buffer (one tile of K
+      // codes and one of V codes, row-major, one box of B rows per block) once
+      // the widening warps have read tile t - 1's; the fp16 stages are theirs.
       auto issue = [&](int t, int row, bool is_v) {
-        const int st = t & 1;
-        const uint32_t dst = s_base + T::OFF_K0 + st * 2 * T::KB + (is_v ? T::KB : 0);
-        const uint32_t fb = bar((is_v ? 12 : 1) + st);
-        if (lane == 0) mbar_arrive_expect_tx(fb, T::KB);
-        __syncwarp();
-        if (lane < bpt) {  // lane b issues block b's boxes
-          const uint32_t roff = (uint32_t)(lane * a.block_size * 128);
+        if constexpr (F8) {
+          const uint32_t dst = s_base + T::OFF_ST + (is_v ? T::STB : 0);
+          const uint32_t fb = bar(is_v ? 18 : 16);
+          if (lane == 0) mbar_arrive_expect_tx(fb, T::STB);
+          __syncwarp();
+          if (lane < bpt)
+            tma_load_2d(dst + (uint32_t)(lane * a.block_size * D), is_v ? &tv : &tk, 0, row, fb);
+        } else {
+          const int st = t & 1;
+          const uint32_t dst = s_base + T::OFF_K0 + st * 2 * T::KB + (is_v ? T::KB : 0);
+          const uint32_t fb = bar((is_v ? 12 : 1) + st);
+          if (lane == 0) mbar_arrive_expect_tx(fb, T::KB);
+          __syncwarp();
+          if (lane < bpt) {  // lane b issues block b's boxes
+            const uint32_t roff = (uint32_t)(lane * a.block_size * 128);
 #pragma unroll
-          for (int at = 0; at < T::NA; ++at)
-            tma_load_2d(dst + at * T::ATOM + roff, is_v ? &tv : &tk, at * 64, row, fb);
+            for (int at = 0; at < T::NA; ++at)
+              tma_load_2d(dst + at * T::ATOM + roff, is_v ? &tv : &tk, at * 64, row, fb);
+          }
         }
       };
+      // The barrier a copy of tile t waits on before it may start, and its parity.
+      auto free_bar = [&](int t, bool is_v) {
+        return F8 ? bar(is_v ? 19 : 17) : bar((is_v ? 14 : 10) + (t & 1));
+      };
+      auto free_par = [&](int t) { return F8 ? (uint32_t)((t - 1) & 1) : (uint32_t)(((t >> 1) - 1) & 1); };
+      const int first_wait = F8 ? 1 : 2;
       int row = tile_row(0);
       int k_issued = 0, v_issued = 0;
       bool ok = true;
       for (int t = 0; t < n_kv && ok; ++t) {
-        const int st = t & 1;
-        if (t >= 2) ok = __all_sync(kFullMask, mbar_wait_bounded(bar(10 + st), ((t >> 1) - 1) & 1));
+        if (t >= first_wait) ok = __all_sync(kFullMask, mbar_wait_bounded(free_bar(t, false), free_par(t)));
         if (!ok) break;
         issue(t, row, false);
         ++k_issued;
-        if (t >= 2) ok = __all_sync(kFullMask, mbar_wait_bounded(bar(14 + st), ((t >> 1) - 1) & 1));
+        if (t >= first_wait) ok = __all_sync(kFullMask, mbar_wait_bounded(free_bar(t, true), free_par(t)));
         if (!ok) break;
         issue(t, row, true);
         ++v_issued;
@@ -266,9 +321,44 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
         *fail = 1;
         // Let the copies this warp started land (bounded) before the shared
         // memory is released.
-        for (int u = max(0, k_issued - 2); u < k_issued; ++u) wait_k(u);
-        for (int u = max(0, v_issued - 2); u < v_issued; ++u) wait_v(u);
+        if constexpr (F8) {
+          if (k_issued > 0) mbar_wait_bounded(bar(16), (k_issued - 1) & 1);
+          if (v_issued > 0) mbar_wait_bounded(bar(18), (v_issued - 1) & 1);
+        } else {
+          for (int u = max(0, k_issued - 2); u < k_issued; ++u) wait_k(u);
+          for (int u = max(0, v_issued - 2); u < v_issued; ++u) wait_v(u);
+        }
       }
+    } else if (F8 && (warp == 10 || warp == 11) && n_kv > 0) {
+      // ---------------- FP8 caches: the two widening warps.  Per tile t, in
+      // the order K then V: wait for the staged codes and for the fp16 stage
+      // t & 1 to be free (the QK / P.V products of tile t - 2 are done), widen,
+      // make the writes visible to the tensor cores, then release the staging
+      // buffer and fill the stage (one arrival per warp on each barrier).
+      const int ctid = tid - 320;
+      bool ok = true;
+      for (int t = 0; t < n_kv && ok; ++t) {
+        const int st = t & 1;
+#pragma unroll
+        for (int kv = 0; kv < 2 && ok; ++kv) {
+          ok = __all_sync(kFullMask, mbar_wait_bounded(bar(kv ? 18 : 16), t & 1));
+          if (ok && t >= 2)
+            ok = __all_sync(kFullMask, mbar_wait_bounded(bar((kv ? 14 : 10) + st), ((t >> 1) - 1) & 1));
+          if (!ok || *fail) {
+            ok = false;
+            break;
+          }
+          widen_tile<D>(sm + T::OFF_ST + kv * T::STB, sm + T::OFF_K0 + st * 2 * T::KB + kv * T::KB,
+                        ctid);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(bar(kv ? 19 : 17));
+            mbar_arrive(bar((kv ? 12 : 1) + st));
+          }
+        }
+      }
+      if (!ok && lane == 0) *fail = 1;
     } else if (warp == 8 && n_kv > 0) {
     // ---------------- MMA issuer (lane 0; the warp zeroes V rows past the context)
     int qk[2] = {0, 0}, pv[2] = {0, 0}, krel = 0, vrel = 0;
@@ -467,7 +557,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
       const bool done = mbar_wait_bounded(bar(7 + x), (qt.n_kv - 1) & 1);
       if (done && !*fail) {
         tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float inv = l > 0.f ? a.v_scale / l : 0.f;  // v_scale: FP8 values (1 for fp16)
         __half* orow = static_cast<__half*>(a.out) +
                        ((size_t)(q0 + (2 * pq + x) * kQT + row) * H + h) * D;
 #pragma unroll
@@ -515,28 +605,32 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// fp16 tensors with 128-byte swizzle (operand layout), or bytes unswizzled
+// (FP8 codes, widened in shared memory).
 bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
-            const cuuint64_t* strides, const cuuint32_t* box) {
+            const cuuint64_t* strides, const cuuint32_t* box, bool bytes = false) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims,
-            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+            (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t launch_prefill_t(const PrefillArgs& g, cudaStream_t stream) {
-  using T = PrefillTraits<D>;
+  using T = PrefillTraits<D, F8>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
     cudaFuncAttributes fa{};
-    attr_err = cudaFuncGetAttributes(&fa, prefill_kernel<D>);
+    attr_err = cudaFuncGetAttributes(&fa, prefill_kernel<D, F8>);
     if (attr_err == cudaSuccess && fa.numRegs * T::THREADS < kRegsSplit)
       attr_err = cudaErrorInvalidConfiguration;  // never launch a split that could not be granted
     if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(prefill_kernel<D>,
+      attr_err = cudaFuncSetAttribute(prefill_kernel<D, F8>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -546,10 +640,12 @@ cudaError_t launch_prefill_t(const PrefillArgs& g, cudaStream_t stream) {
   const cuuint32_t qbox[3] = {64, 1, (cuuint32_t)kQT};
   const long long rows = (long long)g.num_blocks * g.num_heads * g.block_size;
   const cuuint64_t kdims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-  const cuuint64_t kstr[1] = {(cuuint64_t)D * 2};
-  const cuuint32_t kbox[2] = {64, (cuuint32_t)g.block_size};
-  if (!encode(&tq, g.query, 3, qdims, qstr, qbox) || !encode(&tk, g.key_cache, 2, kdims, kstr, kbox) ||
-      !encode(&tv, g.value_cache, 2, kdims, kstr, kbox))
+  const cuuint64_t kstr[1] = {(cuuint64_t)D * (F8 ? 1 : 2)};
+  // fp16: boxes of one 64-element swizzle atom; FP8: one box covers a row.
+  const cuuint32_t kbox[2] = {(cuuint32_t)(F8 ? D : 64), (cuuint32_t)g.block_size};
+  if (!encode(&tq, g.query, 3, qdims, qstr, qbox) ||
+      !encode(&tk, g.key_cache, 2, kdims, kstr, kbox, F8) ||
+      !encode(&tv, g.value_cache, 2, kdims, kstr, kbox, F8))
     return cudaErrorInvalidValue;
   PrefillParams p{};
   p.out = g.out;
@@ -566,8 +662,9 @@ cudaError_t launch_prefill_t(const PrefillArgs& g, cudaStream_t stream) {
   p.max_query_len = g.max_query_len;
   p.oob_row = (int)rows;
   p.scale_log2 = g.scale_log2;
+  p.v_scale = F8 ? g.v_scale : 1.f;
   const long long grid = (long long)g.num_seqs * p.qpairs * g.num_heads;
-  return launch_pdl(prefill_kernel<D>, dim3((unsigned)grid), dim3(T::THREADS), (size_t)T::SMEM,
+  return launch_pdl(prefill_kernel<D, F8>, dim3((unsigned)grid), dim3(T::THREADS), (size_t)T::SMEM,
                     stream, tq, tk, tv, p);
 }
 
@@ -579,7 +676,11 @@ bool prefill_rows_fit(int num_blocks, int num_heads, int block_size) {
 
 cudaError_t launch_prefill(const PrefillArgs& g, cudaStream_t stream) {
   if (g.num_seqs == 0 || g.max_query_len == 0) return cudaSuccess;
-  return g.head_dim == 64 ? launch_prefill_t<64>(g, stream) : launch_prefill_t<128>(g, stream);
+  if (g.fp8)
+    return g.head_dim == 64 ? launch_prefill_t<64, true>(g, stream)
+                            : launch_prefill_t<128, true>(g, stream);
+  return g.head_dim == 64 ? launch_prefill_t<64, false>(g, stream)
+                          : launch_prefill_t<128, false>(g, stream);
 }
 
 }  // namespace pa

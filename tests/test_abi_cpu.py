@@ -152,3 +152,12 @@ def test_prefill_rejects_bad_arguments_before_any_launch():
     assert f(g, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, -1, None) == 1
     assert f(None, None, None, None, None, 4, None, None, 0, 0, 2, 128, 16, 8, 0.1, 8, None) == 0
     assert f(g, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 1 << 27, 0.1, 8, None) == 2   # rows >= 2^31
+    f8 = lib.pa_prefill_fp8
+    fl = ctypes.c_float
+    f8.argtypes = [vp, vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, fl, fl, fl, i, vp]
+    assert f8(g, g, g, g, g, 4, g, g, 2, 10, 2, 96, 16, 8, 0.1, 1.0, 1.0, 8, None) == 2   # head_dim
+    for ks, vs in ((0.0, 1.0), (1.0, -1.0), (float("inf"), 1.0), (1.0, float("nan"))):
+        assert f8(g, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, ks, vs, 8, None) == 1
+    assert f8(g + 4, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, 1.0, 1.0, 8, None) == 1
+    assert f8(None, None, None, None, None, 4, None, None, 0, 0, 2, 128, 16, 8, 0.1, 1.0, 1.0, 8,
+              None) == 0
