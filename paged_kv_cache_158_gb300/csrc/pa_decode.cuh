@@ -79,7 +79,10 @@ namespace pa {
 template <int D, int B, bool F8 = false>
 struct DecodeTraits {
   static constexpr int NW = 4;                // warps per CTA
-  static constexpr int NST = 3;               // stages per warp
+  // Stages per warp.  FP8 chunks are half the bytes and the FP8 kernel is
+  // bound by latency, not HBM: two stages and a register budget for five
+  // CTAs per SM (20 warps) beat three stages at four CTAs.
+  static constexpr int NST = F8 ? 2 : 3;
   static constexpr int THREADS = NW * 32;
   // Tokens per chunk: fp16 chunks lie inside one block; FP8 chunks are 16
   // tokens and span BPC = 16 / B blocks when B < 16 (partitions are
@@ -97,7 +100,7 @@ struct DecodeTraits {
   static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;  // K rows then V rows
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(TPL >= 1 && TPL <= LR && (TPL & (TPL - 1)) == 0, "lane layout");
-  static_assert(NST == 3, "next-item block ids are kept in three registers");
+  static_assert(NST == 2 || NST == 3, "stage ring");
 
   // Fixed part of the dynamic shared memory (bytes), in layout order.
   static constexpr size_t kStages = size_t(NW) * NST * STAGE_BYTES;
@@ -357,7 +360,7 @@ __device__ __forceinline__ void process_chunk(const unsigned char* Ks, const uns
 }
 
 template <int D, int B, bool F8>
-__global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS)
+__global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
     decode_partition_kernel(const DecodeParams a) {
   using T = DecodeTraits<D, B, F8>;
   extern __shared__ __align__(128) unsigned char smem[];
