@@ -79,10 +79,11 @@ namespace pa {
 template <int D, int B, bool F8 = false>
 struct DecodeTraits {
   static constexpr int NW = 4;                // warps per CTA
-  // Stages per warp.  FP8 chunks are half the bytes and the FP8 kernel is
-  // bound by latency, not HBM: two stages and a register budget for five
-  // CTAs per SM (20 warps) beat three stages at four CTAs.
-  static constexpr int NST = F8 ? 2 : 3;
+  // Stages per warp.  Two stages instead of three leave room for more
+  // resident CTAs (fp16: 3 per SM instead of 2, by shared memory; FP8: 5
+  // instead of 4, with the register budget below) at the same bytes in
+  // flight per SM, and more warps hide more latency.
+  static constexpr int NST = 2;
   static constexpr int THREADS = NW * 32;
   // Tokens per chunk: fp16 chunks lie inside one block; FP8 chunks are 16
   // tokens and span BPC = 16 / B blocks when B < 16 (partitions are
@@ -543,8 +544,13 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
           const int j = k - n_my;
           int ph[T::BPC];
 #pragma unroll
-          for (int b = 0; b < T::BPC; ++b)
-            ph[b] = j == 0 ? nxp[0][b] : (j == 1 ? nxp[1][b] : nxp[2][b]);
+          for (int b = 0; b < T::BPC; ++b) {  // j < NST: a register select, no local memory
+            int v = nxp[0][b];
+#pragma unroll
+            for (int jj = 1; jj < T::NST; ++jj)
+              if (j == jj) v = nxp[jj][b];
+            ph[b] = v;
+          }
           issue_chunk<D, B, F8>(a, nx, ph, warp + j * T::NW, stage, bar, policy, leader);
         } else {
           break;
