@@ -81,7 +81,7 @@ def decode_bytes(w, bt, ctx, kv_elem_bytes: int = 2) -> int:
 # Sources that define the decode kernels (the ncu traffic is tied to these).
 DECODE_SOURCES = ("pa_decode.cuh", "pa_decode_inst.inc", "pa_decode_d64.cu", "pa_decode_d128.cu",
                   "pa_decode_f8_d64.cu", "pa_decode_f8_d128.cu", "pa_device.cuh", "pa_launch.cuh",
-                  "pa_internal.h")
+                  "pa_internal.h", "pa_api.cu")   # pa_api.cu: launch configuration (partition size)
 
 
 def source_hash() -> str:

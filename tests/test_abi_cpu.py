@@ -161,3 +161,18 @@ def test_prefill_rejects_bad_arguments_before_any_launch():
     assert f8(g + 4, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, 1.0, 1.0, 8, None) == 1
     assert f8(None, None, None, None, None, 4, None, None, 0, 0, 2, 128, 16, 8, 0.1, 1.0, 1.0, 8,
               None) == 0
+
+
+def test_partition_size_follows_batch_size():
+    """Small batches (fewer than 4096 items of 512 tokens) take 256-token partitions, larger
+    ones 512; the override wins and is rounded up to a multiple of 32 (host-only logic)."""
+    import paged_kv_cache_158_gb300 as pa
+    try:
+        assert pa.pa_decode_partition_tokens(32, 40, 1024) == 256       # 2560 items
+        assert pa.pa_decode_partition_tokens(256, 32, 4096) == 512      # 65536 items
+        assert pa.pa_decode_partition_tokens(64, 32, 2056) == 512       # 10240 items
+        assert pa.pa_decode_partition_tokens(1, 1, 0) == 256            # empty contexts
+        pa.pa_decode_set_partition_tokens(100)
+        assert pa.pa_decode_partition_tokens(256, 32, 4096) == 128
+    finally:
+        pa.pa_decode_set_partition_tokens(0)

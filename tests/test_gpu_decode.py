@@ -218,8 +218,8 @@ def test_decode_more_sequences_than_one_launch(part):
 
 @pytest.mark.parametrize("part", [0, 32])
 def test_decode_long_contexts_many_partitions(part):
-    """Contexts up to 20 000 tokens: 40 partitions of 512, or 625 of 32 (the merge walks its
-    partials in rounds of 32), every output."""
+    """Contexts up to 20 000 tokens: 79 partitions of 256 (the default for so small a batch),
+    or 625 of 32 (the merge walks its partials in rounds of 32), every output."""
     pa.pa_decode_set_partition_tokens(part)
     w = configs.small_random(5200 + part, 3, 2, 128, 32, 20000, min_context=15000)
     dw = gpu.materialize(w, device=DEV)
@@ -228,3 +228,4 @@ def test_decode_long_contexts_many_partitions(part):
     assert rc == 0
     decode_gate(out, ref64, f"long contexts part{part}")
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
