@@ -383,9 +383,12 @@ pa_status pa_check_errors(pa_stream_t stream, uint32_t* error_bits);
 const char* pa_status_string(pa_status status);
 
 /*
- * Tokens per context partition pa_decode will use for this shape on the
- * current device (a multiple of 32).  Exposed so callers can reason about
- * workspace use; 0 on invalid arguments.
+ * Tokens per context partition pa_decode will use for this shape (a
+ * multiple of 32): 256 when num_seqs * num_heads * ceil(max_context_len /
+ * 512) < 4096 (small batches, which would otherwise end on a tail of their
+ * last items), else 512; the override below wins.  A pure function of the
+ * arguments.  Exposed so callers can reason about workspace use; 0 on
+ * invalid arguments.
  */
 int pa_decode_partition_tokens(int num_seqs, int num_heads, int max_context_len);
 
