@@ -51,9 +51,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--eager", action="store_true", help="time eager launches only (no CUDA graph)")
-    ap.add_argument("--op", choices=["step", "swap", "prefill"], default="step",
+    ap.add_argument("--op", choices=["step", "swap", "prefill", "cache"], default="step",
                     help="swap: time block swap-out/in of whole sequences to pinned host memory; "
-                         "prefill: time multi-query paged attention on the 7B-shaped chunked prefill")
+                         "prefill: time multi-query paged attention on the 7B-shaped chunked prefill; "
+                         "cache: time the cache write and the copy-on-write block copy of a step")
     ap.add_argument("--kv-dtype", choices=["fp16", "fp8"], default="fp16",
                     help="KV-cache element type (fp8: E4M3 codes with per-tensor scales)")
     return ap.parse_args()
@@ -533,6 +534,81 @@ def prefill_flops(w) -> int:
     return 4 * w.head_dim * w.num_heads * tot
 
 
+def run_cache(args):
+    """The step's cache write (layer 0: every new token of the step into its slot) and, for the
+    shared-prefix workload, its copy-on-write block copies (every layer), each timed alone with
+    CUDA events; GB/s = (bytes read + bytes written) / time.  KB-scale writes are launch-bound;
+    the shared-prefix step writes 49 k tokens (0.8 GB each way)."""
+    import torch
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = make_workload(args.workload, args.layers)
+    fp8 = args.kv_dtype == "fp8"
+    st = Step(w, dev, fp8=fp8)
+    pa, dw = st.pa, st.dw
+    T = dw.token_seq.numel()
+    H, D, B = w.num_heads, w.head_dim, w.block_size
+    elem = 1 if fp8 else 2
+    slots = torch.empty(T, dtype=torch.int64, device=dev)
+    pa.pa_slot_mapping(slots, dw.block_tables, dw.token_seq, dw.token_pos, B, w.num_blocks)
+    K, W = max(3, min(args.steps, 200)), max(3, args.warmup)
+
+    def timed(fn):
+        """Mean device time of one call: K calls captured in a CUDA graph and replayed, so
+        the host's per-call cost (argument marshalling, launch) is not timed."""
+        for _ in range(W):
+            fn()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(K):
+                fn()
+        g.replay()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stream = torch.cuda.current_stream(dev)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / K * 1e-3
+
+    def write():
+        if fp8:
+            pa.pa_reshape_and_cache_fp8(dw.keys_new[0], dw.values_new[0], dw.key_caches[0],
+                                        dw.value_caches[0], slots, *st.fp8_scales)
+        else:
+            pa.pa_reshape_and_cache(dw.keys_new[0], dw.values_new[0], dw.key_caches[0],
+                                    dw.value_caches[0], slots)
+
+    t_w = timed(write)
+    wbytes = T * H * D * (2 * 2 + elem * 2)          # fp16 K/V read, cache elements written
+    out = {"metric": "cache write and copy-on-write block copy GB/s ((bytes read + bytes written) "
+                     "over CUDA-event time)",
+           "value": round(wbytes / t_w / 1e9, 2), "unit": "GB/s", "n_gpus": 1, "steps": K,
+           "warmup": W, "higher_is_better": True, "dtype": args.kv_dtype, "data": "synthetic",
+           "config": {"workload": w.name, "kv_dtype": args.kv_dtype, "new_tokens": T},
+           "cache_write": {"tokens": T, "bytes": wbytes, "us": round(t_w * 1e6, 3),
+                           "gbs": round(wbytes / t_w / 1e9, 2)},
+           "timing": "K calls captured in one CUDA graph, one replay timed with CUDA events",
+           "gpu_launches": 2 * K + W}
+    if st.copy_pairs is not None and st.copy_pairs.numel():
+        P = st.copy_pairs.shape[0]
+        copy = (lambda: pa.pa_copy_blocks_fp8(dw.key_caches, dw.value_caches, st.copy_pairs)) if fp8 \
+            else (lambda: pa.pa_copy_blocks(dw.key_caches, dw.value_caches, st.copy_pairs))
+        t_c = timed(copy)
+        cbytes = P * len(dw.layers) * 2 * H * B * D * elem * 2
+        out["block_copy"] = {"pairs": P, "layers": len(dw.layers), "bytes": cbytes,
+                             "us": round(t_c * 1e6, 3), "gbs": round(cbytes / t_c / 1e9, 2),
+                             "note": "source and destination blocks fit in L2"}
+        out["gpu_launches"] += 2 * K + W
+    status, bits = pa.pa_check_errors()
+    if status != pa.PA_OK:
+        raise RuntimeError(f"device error word: {pa.pa_status_string(status)} 0x{bits:x}")
+    return out
+
+
 def run_prefill_bench(args):
     import torch
 
@@ -724,6 +800,9 @@ def main():
         import torch
         torch.cuda.set_device(0)
         print(json.dumps(run_swap(args)), flush=True)
+        return
+    if args.op == "cache":
+        print(json.dumps(run_cache(args)), flush=True)
         return
     rank, world, local = dist_setup(args.gpus)
     line = run_ours(args, rank, world, local)
