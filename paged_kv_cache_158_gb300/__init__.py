@@ -29,6 +29,9 @@ _lib.pa_decode_workspace_size.restype = _sz
 _lib.pa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                            ctypes.c_float, _i32, _vp, _sz, _vp]
 _lib.pa_decode.restype = _i32
+_lib.pa_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                                   ctypes.c_float, _i32, _vp]
+_lib.pa_decode_noalloc.restype = _i32
 _lib.pa_reshape_and_cache.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp]
 _lib.pa_reshape_and_cache.restype = _i32
 _lib.pa_copy_blocks.argtypes = [_vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _vp]
@@ -158,6 +161,22 @@ def pa_decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
                         float(scale), int(max_context_len), _ptr(workspace, "workspace", torch.uint8),
                         workspace.numel(), _stream(stream))
     _check(st, "pa_decode")
+
+
+def pa_decode_noalloc(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                      value_cache: torch.Tensor, block_tables: torch.Tensor,
+                      context_lens: torch.Tensor, scale: float, max_context_len: int,
+                      stream=None) -> None:
+    """pa_decode with the library's fixed scratch instead of a workspace (see
+    pa_decode_noalloc in include/pa.h: calls on one device must be serialised)."""
+    S, H, D, B, NB = _decode_shapes(out, query, key_cache, value_cache, block_tables, context_lens)
+    st = _lib.pa_decode_noalloc(_ptr(out, "out", torch.float16), _ptr(query, "query", torch.float16),
+                                _ptr(key_cache, "key_cache", torch.float16),
+                                _ptr(value_cache, "value_cache", torch.float16),
+                                _ptr(block_tables, "block_tables", torch.int32),
+                                block_tables.shape[1], _ptr(context_lens, "context_lens", torch.int32),
+                                S, H, D, B, NB, float(scale), int(max_context_len), _stream(stream))
+    _check(st, "pa_decode_noalloc")
 
 
 def pa_decode_fp8(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
@@ -352,7 +371,7 @@ def raise_on_device_errors(stream=None) -> None:
 __all__ = [
     "pa_decode", "pa_reshape_and_cache", "pa_copy_blocks", "pa_slot_mapping", "pa_check_errors",
     "pa_decode_fp8", "pa_reshape_and_cache_fp8", "pa_copy_blocks_fp8", "pa_convert_cache_fp8",
-    "pa_swap_blocks", "pa_prefill", "pa_prefill_fp8",
+    "pa_swap_blocks", "pa_prefill", "pa_prefill_fp8", "pa_decode_noalloc",
     "pa_status_string", "pa_decode_workspace_size", "pa_decode_partition_tokens",
     "pa_decode_set_partition_tokens", "decode_workspace", "raise_on_device_errors", "PAError",
 ]

@@ -57,6 +57,11 @@ def test_noalloc_decode_matches_workspace_decode_twice():
             assert np.all(np.isfinite(g))
             assert np.all(np.abs(g - r) <= ATOL + RTOL * np.abs(r))
             assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+            via = torch.full_like(ref, float("nan"))     # the Python binding of the same call
+            pa.pa_decode_noalloc(via, dw.queries[i], dw.key_caches[i], dw.value_caches[i],
+                                 dw.block_tables, dw.context_lens, w.scale, w.max_context_len)
+            torch.cuda.synchronize()
+            assert torch.equal(via.view(torch.int16), ref.view(torch.int16))
         assert pa.pa_check_errors() == (pa.PA_OK, 0)
     finally:
         pa.pa_decode_set_partition_tokens(0)
