@@ -269,6 +269,25 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
   return r;
 }
 
+// (a0 * b0 + c0, a1 * b1 + c1) as one packed fp32 fused multiply-add
+// (sm_100 family): each lane is an IEEE fma rounded to nearest, so the
+// result is bit-identical to two fmaf calls in half the instructions.
+__device__ __forceinline__ float2 ffma2(float a0, float a1, uint64_t b, uint64_t c) {
+  uint64_t a, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  float2 out;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(out.x), "=f"(out.y) : "l"(r));
+  return out;
+}
+
+// The same value in both halves of a packed fp32 pair.
+__device__ __forceinline__ uint64_t f32x2_splat(float v) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(v));
+  return r;
+}
+
 // Eight E4M3 codes (element order in memory) -> 4 packed fp16 pairs.
 __device__ __forceinline__ uint4 e4m3x8_to_f16x8(const uint2& c) {
   uint4 r;

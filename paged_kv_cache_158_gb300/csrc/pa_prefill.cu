@@ -513,10 +513,11 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
       // the fp16 P.V product); the row sum adds those exact fp16 values in fp32.
       float sq[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[kKT / 2];
+      const uint64_t sc2 = f32x2_splat(a.scale_log2), neg2 = f32x2_splat(neg);
 #pragma unroll
       for (int j = 0; j < kKT / 2; ++j) {
-        pk[j] = exp2_f16x2(fmaf(xv[2 * j], a.scale_log2, neg),
-                           fmaf(xv[2 * j + 1], a.scale_log2, neg));
+        const float2 y = ffma2(xv[2 * j], xv[2 * j + 1], sc2, neg2);  // packed: two fmas at once
+        pk[j] = exp2_f16x2(y.x, y.y);
         sq[j & 3] = add_f16x2_f32(pk[j], sq[j & 3]);
       }
       l = l * alpha + ((sq[0] + sq[1]) + (sq[2] + sq[3]));
