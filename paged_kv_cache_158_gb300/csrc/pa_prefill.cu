@@ -23,14 +23,16 @@
 //  * Each thread owns one query row (TMEM lane = row): it reads its S row
 //    with tcgen05.ld, applies the causal and context masks, keeps the online
 //    softmax (m in raw logit units, l in fp32, exponentials in base 2 with
-//    the scale folded into one fused multiply-add; the exponentials of a
-//    pair of arguments run as one packed fp16 ex2, whose fp16 results are
-//    the P operand of the second MMA and are summed in fp32 for l), and
-//    rescales its O row in TMEM when its reference maximum moves, which it
-//    does only when the row's maximum exceeds it by more than 2^8 (weights
-//    stay <= 256, exact in fp16 range and summed in fp32).  Masks are applied only on tiles that reach the
-//    diagonal or the context end.  V rows past the context are zeroed in shared
-//    memory (0 * NaN in stale slots would poison the sum).
+//    the scale folded into a packed fused multiply-add; the exponentials of
+//    a pair of arguments run as one packed fp16 ex2, whose fp16 results are
+//    the P operand of the second MMA and are summed in fp32 for l).  m is a
+//    reference, not necessarily the maximum: it is set to the row's maximum
+//    on its first tile and moves only when a weight would overflow fp16
+//    (a logit more than 16 above m in base-2 units); only then is the tile's
+//    maximum computed, the tile's weights redone and the O row in TMEM
+//    rescaled.  Masks are applied only on tiles that reach the diagonal or
+//    the context end.  V rows past the context are zeroed in shared memory
+//    (0 * NaN in stale slots would poison the sum).
 //  * Work per KV tile: the TMA of the next tile overlaps the softmax and
 //    both MMAs of the current one; the softmax and the MMAs of one CTA run
 //    back to back (one CTA per SM by shared memory).
@@ -472,55 +474,82 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
     const uint32_t t_s = tmem + 128 * x + lane_off;
     const uint32_t t_o = tmem + T::COL_O + D * x + lane_off;
     const int qpos = qt.pos_min + row;
-    const float lazy_raw = 8.f / a.scale_log2;  // 8 in base-2 units, as a raw logit difference
     float m = -INFINITY, l = 0.f;
     Waiter s_w{bar(3 + x)};
     bool ok = true;
     for (int t = 0; t < qt.n_kv; ++t) {
-      ok = s_w.wait();
-      if (!ok || *fail) { ok = false; break; }
+      // Warp-uniform outcome: the tensor-memory accesses below are warp-collective.
+      ok = __all_sync(kFullMask, s_w.wait() && !*fail);
+      if (!ok) break;
       tc_fence_after();
-      uint32_t sr[kKT];
-#pragma unroll
-      for (int cb = 0; cb < kKT / 32; ++cb)
-        tmem_ld32(t_s + cb * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cb * 32]));
-      tmem_wait_ld();  // one wait for all four loads
-      float xv[kKT];
-#pragma unroll
-      for (int j = 0; j < kKT; ++j) xv[j] = __uint_as_float(sr[j]);
+      // The row's logits of this tile, masked past the diagonal and the
+      // context end (only on tiles that reach them).
       const int kv0 = t * kKT;
-      if (kv0 + kKT - 1 > qt.pos_min) {  // tile reaches the diagonal (or the context end)
-        const int lim = min(qpos, c - 1) - kv0;
+      auto load_logits = [&](float (&xv)[kKT]) {
+        uint32_t sr[kKT];
 #pragma unroll
-        for (int j = 0; j < kKT; ++j)
-          if (j > lim) xv[j] = -INFINITY;
-      }
-      // Independent partial maxima and sums keep the dependency chains short
-      // (one warp per scheduler runs this code).
-      float mq[4] = {m, -INFINITY, -INFINITY, -INFINITY};
+        for (int cb = 0; cb < kKT / 32; ++cb)
+          tmem_ld32(t_s + cb * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cb * 32]));
+        tmem_wait_ld();  // one wait for all four loads
 #pragma unroll
-      for (int j = 0; j < kKT; j += 8)
+        for (int j = 0; j < kKT; ++j) xv[j] = __uint_as_float(sr[j]);
+        if (kv0 + kKT - 1 > qt.pos_min) {
+          const int lim = min(qpos, c - 1) - kv0;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) mq[u] = fmax3(mq[u], xv[j + 2 * u], xv[j + 2 * u + 1]);
-      const float tile_max = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-      // Lazy reference: m moves only when the row's maximum exceeds it by more
-      // than 8 in base-2 units, so weights stay <= 2^8 and O is rarely rescaled
-      // (the final division by l uses the same reference).
-      const float mx = tile_max > m + lazy_raw ? tile_max : m;
-      const float alpha = (mx == -INFINITY || mx == m) ? 1.f : exp2_approx((m - mx) * a.scale_log2);
-      const float neg = (mx == -INFINITY) ? 0.f : -mx * a.scale_log2;
-      // Weights as fp16 pairs straight from the packed exponential (they feed
-      // the fp16 P.V product); the row sum adds those exact fp16 values in fp32.
-      float sq[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int j = 0; j < kKT; ++j)
+            if (j > lim) xv[j] = -INFINITY;
+        }
+      };
+      // Weights against the row's reference m (raw logit units) as fp16 pairs
+      // straight from the packed exponential (they feed the fp16 P.V product);
+      // the row sum adds those exact fp16 values in fp32.  m is only a
+      // reference, so weights may exceed 1: the tile's maximum is computed only
+      // on the row's first tile and when a weight overflows fp16 (the tile
+      // holds a logit more than 16 above m in base-2 units; the sum is then not
+      // finite).  Then m moves to the maximum and the weights are recomputed
+      // from the logits reloaded from tensor memory (S is intact until P is
+      // written over it).
+      float sq[4];
       uint32_t pk[kKT / 2];
-      const uint64_t sc2 = f32x2_splat(a.scale_log2), neg2 = f32x2_splat(neg);
+      const uint64_t sc2 = f32x2_splat(a.scale_log2);
+      auto weights = [&](const float (&xv)[kKT], float ref) {
+        const uint64_t neg2 = f32x2_splat(ref == -INFINITY ? 0.f : -ref * a.scale_log2);
 #pragma unroll
-      for (int j = 0; j < kKT / 2; ++j) {
-        const float2 y = ffma2(xv[2 * j], xv[2 * j + 1], sc2, neg2);  // packed: two fmas at once
-        pk[j] = exp2_f16x2(y.x, y.y);
-        sq[j & 3] = add_f16x2_f32(pk[j], sq[j & 3]);
+        for (int u = 0; u < 4; ++u) sq[u] = 0.f;
+#pragma unroll
+        for (int j = 0; j < kKT / 2; ++j) {
+          const float2 y = ffma2(xv[2 * j], xv[2 * j + 1], sc2, neg2);  // packed: two fmas at once
+          pk[j] = exp2_f16x2(y.x, y.y);
+          sq[j & 3] = add_f16x2_f32(pk[j], sq[j & 3]);
+        }
+        return (sq[0] + sq[1]) + (sq[2] + sq[3]);
+      };
+      // The tensor-memory loads are warp-collective, so the choice of path is
+      // made for the whole warp: if any row needs the maximum, every row of the
+      // warp recomputes against its own (still exact for the others).
+      float mx = m, ls = 0.f;
+      bool slow = __any_sync(kFullMask, m == -INFINITY);
+      if (!slow) {
+        float xv[kKT];
+        load_logits(xv);
+        ls = weights(xv, m);
+        // a weight overflowed (or a NaN logit) in some row of the warp
+        slow = __any_sync(kFullMask, !(ls <= 3.4028234663852886e38f));
       }
-      l = l * alpha + ((sq[0] + sq[1]) + (sq[2] + sq[3]));
+      if (slow) {
+        float xv[kKT];
+        load_logits(xv);
+        // Independent partial maxima keep the dependency chains short.
+        float mq[4] = {m, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int j = 0; j < kKT; j += 8)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) mq[u] = fmax3(mq[u], xv[j + 2 * u], xv[j + 2 * u + 1]);
+        mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+        ls = weights(xv, mx);
+      }
+      const float alpha = (mx == -INFINITY || mx == m) ? 1.f : exp2_approx((m - mx) * a.scale_log2);
+      l = l * alpha + ls;
       m = mx;
       // O(x, t - 1) is complete here: S(x, t) was computed after it.
       if (t > 0 && __any_sync(kFullMask, alpha != 1.f)) {
@@ -555,8 +584,8 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
     if (ok && qt.n_kv > 0) {
       // The last P.V of this tile (phase n_kv - 1; the earlier ones completed
       // before S of the last tile was computed, so the parity is unambiguous).
-      const bool done = mbar_wait_bounded(bar(7 + x), (qt.n_kv - 1) & 1);
-      if (done && !*fail) {
+      const bool done = __all_sync(kFullMask, mbar_wait_bounded(bar(7 + x), (qt.n_kv - 1) & 1) && !*fail);
+      if (done) {
         tc_fence_after();
         const float inv = l > 0.f ? a.v_scale / l : 0.f;  // v_scale: FP8 values (1 for fp16)
         __half* orow = static_cast<__half*>(a.out) +

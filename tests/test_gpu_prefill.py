@@ -142,3 +142,16 @@ def test_prefill_long_chunk_and_many_decode_rows():
     out = run_prefill(w, dv)
     decode_gate(out, oracle_prefill(w), "long chunk + 150 decode rows")
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+@pytest.mark.parametrize("scale", [0.4, 1.5, 4.0])
+def test_prefill_large_logits_rescale_path(scale):
+    """Logit scales far above 1/sqrt(D) make later tiles hold logits many base-2 units above
+    the row's running reference, so weights overflow fp16 and the tile is redone against its
+    maximum with O and l rescaled; every output still matches the oracle."""
+    w = configs.prefill_workload(f"scale{scale}", 4700, *MIXED, 3, 128, 16)
+    w.logit_scale = scale
+    dv = gpu.materialize_prefill(w, DEV)
+    out = run_prefill(w, dv)
+    decode_gate(out, oracle_prefill(w), f"prefill scale {scale}")
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)

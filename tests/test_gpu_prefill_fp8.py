@@ -123,3 +123,13 @@ def test_prefill_fp8_scales_checked_and_bad_block_flagged():
     w.block_tables[1, 0] = 0
     kc8, vc8 = oracle_pool(w)
     decode_gate(out[:40], oracle_out(w, kc8, vc8)[:40], "fp8 unaffected sequence")
+
+
+@pytest.mark.parametrize("scale", [0.4, 4.0])
+def test_prefill_fp8_large_logits_rescale_path(scale):
+    w = configs.prefill_workload(f"f8scale{scale}", 6400, *MIXED, 3, 128, 16)
+    w.logit_scale = scale
+    dv = materialize_fp8(w)
+    out = run(w, dv)
+    decode_gate(out, oracle_out(w, *oracle_pool(w)), f"fp8 prefill scale {scale}")
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)

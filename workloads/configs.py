@@ -48,10 +48,11 @@ class Workload:
     free_order: np.ndarray | None = None
     description: str = ""
     extra: dict = field(default_factory=dict)
+    logit_scale: float | None = None      # the attention scale if not 1/sqrt(head_dim)
 
     @property
     def scale(self) -> float:
-        return 1.0 / math.sqrt(self.head_dim)
+        return self.logit_scale if self.logit_scale is not None else 1.0 / math.sqrt(self.head_dim)
 
     @property
     def max_context_len(self) -> int:
