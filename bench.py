@@ -11,6 +11,7 @@ peak, attention tokens/s per layer and us per layer.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c3|c5|c2|c4|c1]
                     [--kv-dtype fp16|fp8]
     python bench.py --impl reference ...   # the CPU oracle as the reference arm
+    python bench.py --op scan [--kv-dtype fp8]  # time per call vs context length
 
 --kv-dtype fp8 runs the same step on FP8 (E4M3) caches: the bytes count one
 byte per cached K/V element, so compare it with fp16 on tokens/s as well.
@@ -51,10 +52,11 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--eager", action="store_true", help="time eager launches only (no CUDA graph)")
-    ap.add_argument("--op", choices=["step", "swap", "prefill", "cache"], default="step",
+    ap.add_argument("--op", choices=["step", "swap", "prefill", "cache", "scan"], default="step",
                     help="swap: time block swap-out/in of whole sequences to pinned host memory; "
                          "prefill: time multi-query paged attention on the 7B-shaped chunked prefill; "
-                         "cache: time the cache write and the copy-on-write block copy of a step")
+                         "cache: time the cache write and the copy-on-write block copy of a step; "
+                         "scan: decode time per call against context length (fixed + marginal)")
     ap.add_argument("--kv-dtype", choices=["fp16", "fp8"], default="fp16",
                     help="KV-cache element type (fp8: E4M3 codes with per-tensor scales)")
     return ap.parse_args()
@@ -609,6 +611,115 @@ def run_cache(args):
     return out
 
 
+def run_scan(args):
+    """Decode time per call against context length: the workload's batch shape (S, H, D, B)
+    with every sequence at one context length c in {256 .. 4096}, each point timed as a CUDA
+    graph of calls over distinct layers (more than 2 GB of cache per replay, so nothing is
+    served from L2).  A least-squares line time = fixed + bytes / marginal splits each call's
+    time into a per-call fixed part (launch chain, ramp-up and drain, the tail of the last
+    items, the merge) and the streaming rate of the partition pass."""
+    import torch
+
+    import paged_kv_cache_158_gb300 as pa
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = make_workload(args.workload, 1)
+    S, H, D, B = w.num_seqs, w.num_heads, w.head_dim, w.block_size
+    fp8 = args.kv_dtype == "fp8"
+    elem = 1 if fp8 else 2
+    if args.partition_tokens:
+        pa.pa_decode_set_partition_tokens(args.partition_tokens)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(158100)
+    K = max(3, min(args.steps, 20))
+    points, launches = [], 0
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    for c in (256, 512, 1024, 2048, 4096):
+        nbl = (c + B - 1) // B
+        NB = S * nbl
+        layer_bytes = 2 * NB * H * B * D * elem
+        L = max(2, int(2.5e9 // layer_bytes))
+        caches = []
+        for _ in range(L):
+            pair = []
+            for _kv in range(2):
+                if fp8:  # random codes with bit 3 clear: never an E4M3 NaN
+                    x = torch.randint(0, 256, (NB, H, B, D), dtype=torch.uint8, device=dev,
+                                      generator=gen) & 0xF7
+                else:
+                    x = torch.randn((NB, H, B, D), dtype=torch.float16, device=dev, generator=gen)
+                pair.append(x)
+            perm = torch.randperm(NB, device=dev, generator=gen).to(torch.int32)
+            caches.append((pair[0], pair[1], perm.view(S, nbl).contiguous()))
+        q = torch.randn((S, H, D), dtype=torch.float16, device=dev, generator=gen)
+        out = torch.empty_like(q)
+        ctx = torch.full((S,), c, dtype=torch.int32, device=dev)
+        ws = pa.decode_workspace(S, H, D, c, device=dev)
+        scale = 1.0 / D ** 0.5
+
+        def calls():
+            for kc, vc, bt in caches:
+                if fp8:
+                    pa.pa_decode_fp8(out, q, kc, vc, bt, ctx, scale, 0.02, 0.02, c, ws)
+                else:
+                    pa.pa_decode(out, q, kc, vc, bt, ctx, scale, c, ws)
+
+        for _ in range(max(3, args.warmup)):
+            calls()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                calls()
+        torch.cuda.synchronize(dev)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        stream = torch.cuda.current_stream(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(K):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        us = a.elapsed_time(b) * 1e3 / (K * L)
+        nbytes = decode_bytes(w, None, np.full(S, c), elem)
+        points.append({"context_len": c, "layers": L, "us_per_call": round(us, 3),
+                       "bytes_per_call": nbytes, "gbs": round(nbytes / us / 1e3, 1),
+                       "partition_tokens": pa.pa_decode_partition_tokens(S, H, c)})
+        launches += K * L * 3 + max(3, args.warmup) * L * 3
+        del caches, g
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+    pa.pa_decode_set_partition_tokens(0)
+    status, bits = pa.pa_check_errors()
+    if status != pa.PA_OK:
+        raise RuntimeError(f"device error word: {pa.pa_status_string(status)} 0x{bits:x}")
+    xb = np.array([p["bytes_per_call"] for p in points], dtype=np.float64)
+    yt = np.array([p["us_per_call"] for p in points], dtype=np.float64)
+    slope, fixed = np.polyfit(xb, yt, 1)
+    marginal = 1.0 / slope / 1e3  # bytes per us -> GB/s
+    peak, kind = measured_peak()
+    return {"metric": "paged-decode time per call vs context length: fixed us per call and "
+                      "marginal GB/s (least-squares line over the points)",
+            "value": round(marginal, 1), "unit": "GB/s", "n_gpus": 1, "steps": K,
+            "warmup": max(3, args.warmup), "higher_is_better": True, "dtype": args.kv_dtype,
+            "data": "synthetic (seeded torch generator; FP8 codes with bit 3 clear)",
+            "config": {"workload": f"{w.name} batch shape, uniform context lengths",
+                       "num_seqs": S, "num_heads": H, "head_dim": D, "block_size": B,
+                       "kv_dtype": args.kv_dtype, "l2": "more than 2 GB of cache per replay"},
+            "fixed_us_per_call": round(float(fixed), 2), "marginal_gbs": round(marginal, 1),
+            "marginal_frac_of_peak": round(marginal / peak, 4), "peak_gbs": peak, "peak_kind": kind,
+            "points": points, "clocks": clk, "gpu_launches": launches}
+
+
 def run_prefill_bench(args):
     import torch
 
@@ -803,6 +914,9 @@ def main():
         return
     if args.op == "cache":
         print(json.dumps(run_cache(args)), flush=True)
+        return
+    if args.op == "scan":
+        print(json.dumps(run_scan(args)), flush=True)
         return
     rank, world, local = dist_setup(args.gpus)
     line = run_ours(args, rank, world, local)
