@@ -379,6 +379,21 @@ pa_status pa_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,
  */
 pa_status pa_check_errors(pa_stream_t stream, uint32_t* error_bits);
 
+/*
+ * Self-test of the library's stall handling.  Every wait of a library kernel
+ * on its own asynchronous copies is bounded: after about one second it gives
+ * up, the kernel finishes the work it can, sets PA_ERRBIT_TIMEOUT in the
+ * device error word and returns, so a stalled pipeline ends as a reported
+ * status instead of a hung GPU.  This call launches one thread that waits,
+ * through that same bounded wait, on a shared-memory barrier that never
+ * completes (it expects two arrivals and receives one); about one second
+ * later the wait gives up and the timeout bit is set.  The next
+ * pa_check_errors returns PA_ERR_TIMEOUT with error_bits ==
+ * PA_ERRBIT_TIMEOUT (and clears the word); the context stays usable.
+ * Asynchronous on `stream`; returns PA_ERR_CUDA if the launch fails.
+ */
+pa_status pa_selftest_wait_timeout(pa_stream_t stream);
+
 /* A static, human-readable name of a status. */
 const char* pa_status_string(pa_status status);
 

@@ -38,6 +38,8 @@ _lib.pa_copy_blocks.argtypes = [_vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i3
 _lib.pa_copy_blocks.restype = _i32
 _lib.pa_slot_mapping.argtypes = [_vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _vp]
 _lib.pa_slot_mapping.restype = _i32
+_lib.pa_selftest_wait_timeout.argtypes = [_vp]
+_lib.pa_selftest_wait_timeout.restype = _i32
 _lib.pa_check_errors.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
 _lib.pa_check_errors.restype = _i32
 _lib.pa_status_string.argtypes = [_i32]
@@ -355,6 +357,12 @@ def pa_slot_mapping(slot_mapping: torch.Tensor, block_tables: torch.Tensor, toke
     _check(st, "pa_slot_mapping")
 
 
+def pa_selftest_wait_timeout(stream=None) -> None:
+    """Launches a kernel whose bounded wait never completes (see pa_selftest_wait_timeout in
+    include/pa.h): about a second later the device error word holds PA_ERRBIT_TIMEOUT."""
+    _check(_lib.pa_selftest_wait_timeout(_stream(stream)), "pa_selftest_wait_timeout")
+
+
 def pa_check_errors(stream=None) -> tuple[int, int]:
     """Synchronise the stream and read + clear the device error word: (status, bits)."""
     bits = ctypes.c_uint32(0)
@@ -370,6 +378,7 @@ def raise_on_device_errors(stream=None) -> None:
 
 __all__ = [
     "pa_decode", "pa_reshape_and_cache", "pa_copy_blocks", "pa_slot_mapping", "pa_check_errors",
+    "pa_selftest_wait_timeout",
     "pa_decode_fp8", "pa_reshape_and_cache_fp8", "pa_copy_blocks_fp8", "pa_convert_cache_fp8",
     "pa_swap_blocks", "pa_prefill", "pa_prefill_fp8", "pa_decode_noalloc",
     "pa_status_string", "pa_decode_workspace_size", "pa_decode_partition_tokens",

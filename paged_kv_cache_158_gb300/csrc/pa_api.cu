@@ -532,6 +532,15 @@ pa_status pa_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,
              : PA_ERR_CUDA;
 }
 
+pa_status pa_selftest_wait_timeout(pa_stream_t stream) {
+  DeviceState ds;
+  pa_status st = device_state(&ds, false);
+  if (st != PA_OK) return st;
+  return pa::launch_selftest_wait(ds.err, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
 pa_status pa_check_errors(pa_stream_t stream, uint32_t* error_bits) {
   if (error_bits) *error_bits = 0;
   DeviceState ds;

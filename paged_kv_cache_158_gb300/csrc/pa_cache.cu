@@ -250,6 +250,23 @@ int log2_exact(int x) {
   return l;
 }
 
+// A wait that nothing completes.  The barrier expects two arrivals and gets
+// one, so its first phase never ends; the thread waits through the same
+// bounded wait as the library's copy pipelines, which gives up after
+// kWaitLimitNs and reports the timeout in the device error word.  No copy
+// or other asynchronous operation is in flight when the kernel returns.
+__global__ void selftest_wait_kernel(unsigned int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 2);
+  fence_mbar_init();
+  mbar_arrive(b);
+  if (!mbar_wait_bounded(b, 0)) atomicOr(err, PA_ERRBIT_TIMEOUT);
+}
+
 int sm_count() {
   int dev = 0, n = 148;
   cudaGetDevice(&dev);
@@ -262,6 +279,10 @@ int sm_count() {
 cudaError_t launch_zero_words(unsigned int* words, int n, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
   return launch_pdl(zero_words_kernel, dim3(1), dim3(128), 0, stream, words, n);
+}
+
+cudaError_t launch_selftest_wait(unsigned int* err, cudaStream_t stream) {
+  return launch_pdl(selftest_wait_kernel, dim3(1), dim3(32), 0, stream, err);
 }
 
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* key_cache,

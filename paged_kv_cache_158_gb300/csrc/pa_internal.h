@@ -59,6 +59,9 @@ cudaError_t decode_prepare_device(int device);
 
 // Zeroes n 32-bit words on the stream (one small kernel).
 cudaError_t launch_zero_words(unsigned int* words, int n, cudaStream_t stream);
+// One thread waits, through the kernels' bounded wait, on a barrier that
+// never completes; the wait gives up and sets PA_ERRBIT_TIMEOUT in `err`.
+cudaError_t launch_selftest_wait(unsigned int* err, cudaStream_t stream);
 
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* key_cache,
                                      void* value_cache, const int64_t* slot_mapping,

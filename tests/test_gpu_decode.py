@@ -3,6 +3,8 @@ small and mid-size inputs (several tiles, ragged tails, many partitions)
 and on sampled outputs at the full workload sizes in the benchmark's launch
 configuration; plus the invariants the pages fix (permutation of physical
 blocks, run-to-run determinism) and edge cases."""
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -229,3 +231,24 @@ def test_decode_long_contexts_many_partitions(part):
     decode_gate(out, ref64, f"long contexts part{part}")
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
 
+
+def test_bounded_wait_gives_up_and_reports_timeout():
+    """A kernel whose bounded wait never completes (a barrier that gets one of its two
+    arrivals) ends after about a second with the timeout bit in the device error word; the
+    word clears on reading and the context stays usable: a decode afterwards matches the
+    oracle."""
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    pa.pa_selftest_wait_timeout()
+    st, bits = pa.pa_check_errors()
+    dt = time.perf_counter() - t0
+    assert (st, bits) == (pa.PA_ERR_TIMEOUT, pa.PA_ERRBIT_TIMEOUT)
+    assert 0.9 < dt < 10.0
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+    w = configs.small_random(4242, 5, 3, 128, 16, 200, min_context=1)
+    dw = gpu.materialize(w, device=DEV)
+    out = run_decode(dw)
+    _, ref64, rc = full_oracle(w, write_new=False)
+    assert rc == 0
+    decode_gate(out, ref64, "decode after a timed-out wait")
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
