@@ -101,6 +101,7 @@ struct PrefillParams {
   int num_blocks;
   int block_size;
   int qpairs;                    // pairs of query tiles per sequence covered by the grid
+  int wave_groups;               // (sequence, head) groups whose pairs all start in the first wave
   int max_query_len;             // host bound of the chunk lengths
   int oob_row;                   // a row coordinate past the cache (zero-filled loads)
   float scale_log2;              // scale * log2(e), times the key scale for FP8 caches
@@ -171,12 +172,27 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int H = a.num_heads;
-  // Pairs of one (sequence, head) are adjacent in the grid, heaviest first:
-  // they run together and read the same K/V tiles, the second from L2.
-  const int pq = a.qpairs - 1 - (int)(blockIdx.x % a.qpairs);
-  const int rest = blockIdx.x / a.qpairs;
-  const int h = rest % H;
-  const int s = rest / H;
+  // Grid order (one CTA per SM, CTAs start in index order).  The first
+  // wave_groups (sequence, head) groups come whole, their pairs adjacent and
+  // heaviest first: they run together and read the same K/V tiles, the
+  // later ones from L2.  The other groups follow rank by rank, every
+  // group's heaviest pair before any group's next one, so the heavy pairs
+  // start on the SMs that free first and the lighter ones trail their
+  // partners by a few tiles (K/V still in L2).
+  const int P = a.qpairs;
+  const int b = (int)blockIdx.x;
+  const int first = a.wave_groups * P;
+  int grp, pq;
+  if (b < first) {
+    grp = b / P;
+    pq = P - 1 - b % P;
+  } else {
+    const int rem = a.num_seqs * H - a.wave_groups;
+    grp = a.wave_groups + (b - first) % rem;
+    pq = P - 1 - (b - first) / rem;
+  }
+  const int h = grp % H;
+  const int s = grp / H;
 
   if (tid == 0) {
     mbar_init(bar(0), 1);
@@ -689,6 +705,15 @@ cudaError_t launch_prefill_t(const PrefillArgs& g, cudaStream_t stream) {
   p.num_blocks = g.num_blocks;
   p.block_size = g.block_size;
   p.qpairs = (g.max_query_len + 2 * kQT - 1) / (2 * kQT);
+  {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return cudaErrorInvalidValue;
+    const long long groups = (long long)g.num_seqs * g.num_heads;
+    const long long whole = sms / p.qpairs;  // one CTA per SM
+    p.wave_groups = (int)(whole < groups ? whole : groups);
+  }
   p.max_query_len = g.max_query_len;
   p.oob_row = (int)rows;
   p.scale_log2 = g.scale_log2;
