@@ -122,18 +122,25 @@ struct QTile {
 // exact.
 template <int D>
 __device__ __forceinline__ void widen_tile(const unsigned char* src, unsigned char* dst, int ctid) {
-  constexpr int CPR = D / 16;  // 16-code chunks per row
+  constexpr int CPR = D / 16;     // 16-code chunks per row
   constexpr int ATOM = 128 * 128;
+  constexpr int STEP = 64 / CPR;  // rows between one thread's chunks
+  static_assert(STEP % 8 == 0, "a thread's chunks share one swizzle phase");
+  // Thread ctid widens chunk j of rows r0, r0 + STEP, ...: the chunk column
+  // and the row's swizzle phase (r & 7) are the same for all of them, so the
+  // addresses are two bases and compile-time offsets.
+  const int j = ctid % CPR, r0 = ctid / CPR;
+  const int c0 = 2 * (j % 4);
+  const unsigned char* sp = src + r0 * D + 16 * j;
+  unsigned char* dp = dst + (j / 4) * ATOM + r0 * 128;
+  const int o0 = (c0 ^ (r0 & 7)) << 4, o1 = ((c0 + 1) ^ (r0 & 7)) << 4;
 #pragma unroll 4
-  for (int i = ctid; i < kKT * CPR; i += 64) {
-    const int r = i / CPR, j = i % CPR;
-    const uint4 c = lds128(src + r * D + 16 * j);
+  for (int k = 0; k < kKT / STEP; ++k) {
+    const uint4 c = lds128(sp + k * STEP * D);
     const uint4 h0 = e4m3x8_to_f16x8(make_uint2(c.x, c.y));
     const uint4 h1 = e4m3x8_to_f16x8(make_uint2(c.z, c.w));
-    const int c0 = 2 * (j % 4);
-    unsigned char* row = dst + (j / 4) * ATOM + r * 128;
-    *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7)) << 4)) = h0;
-    *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) = h1;
+    *reinterpret_cast<uint4*>(dp + k * STEP * 128 + o0) = h0;
+    *reinterpret_cast<uint4*>(dp + k * STEP * 128 + o1) = h1;
   }
 }
 
