@@ -369,10 +369,10 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
           ok = __all_sync(kFullMask, mbar_wait_bounded(bar(kv ? 18 : 16), t & 1));
           if (ok && t >= 2)
             ok = __all_sync(kFullMask, mbar_wait_bounded(bar((kv ? 14 : 10) + st), ((t >> 1) - 1) & 1));
-          if (!ok || *fail) {
-            ok = false;
-            break;
-          }
+          // Warp-uniform: the failure flag may be set by another warp between
+          // two lanes' reads, and the widening ends in a __syncwarp.
+          ok = __all_sync(kFullMask, ok && !*fail);
+          if (!ok) break;
           widen_tile<D>(sm + T::OFF_ST + kv * T::STB, sm + T::OFF_K0 + st * 2 * T::KB + kv * T::KB,
                         ctid);
           fence_proxy_async_smem();
