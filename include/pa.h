@@ -110,23 +110,27 @@ pa_status pa_decode(void* out, const void* query, const void* key_cache, const v
 
 /*
  * pa_decode without a workspace argument, for callers that cannot allocate
- * device memory at the moment they decode: code running inside a CUDA graph
- * capture in global mode (cudaMalloc is an error there), processes that give
- * all of HBM to the KV pool up front and keep no allocator headroom, and hot
- * paths that must not call cudaMalloc/cudaFree because those may synchronise
- * the device.  The pages have no counterpart; it is a deployment convenience.
+ * device memory at the moment they decode: processes that give all of HBM
+ * to the KV pool up front and keep no allocator headroom, hot paths that must
+ * not call cudaMalloc/cudaFree because those may synchronise the device, and
+ * plain C callers that own no device allocator.  The pages have no
+ * counterpart; it is a deployment convenience.
  *
  * Same arguments, result and arithmetic as pa_decode.  The scratch is a fixed
  * array of PA_DECODE_NOALLOC_SCRATCH_BYTES in the library's own device memory
- * (a __device__ variable: each device that loads the library holds it until
- * the process exits).  This call allocates nothing and calls no allocating
- * routine.
+ * (a __device__ variable).  This call allocates nothing and calls no
+ * allocating routine.
  *   - If pa_decode_workspace_size(num_seqs, num_heads, head_dim,
  *     max_context_len) exceeds PA_DECODE_NOALLOC_SCRATCH_BYTES the call
  *     returns PA_ERR_UNSUPPORTED and launches nothing.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before capturing a stream on that device.
+ *   - The first call on each device is a warm-up.  Under CUDA's lazy module
+ *     loading (the default) it loads the module that holds the array, which
+ *     commits the array's bytes on that device until the process exits, and
+ *     it looks up the array's device address (cudaGetSymbolAddress, with that
+ *     device current) and caches it.  Make that first call before the rest of
+ *     device memory is reserved (for the KV pool, say) and before any stream
+ *     capture on that device.  If it fails (PA_ERR_CUDA, typically out of
+ *     memory) the CUDA last error is cleared and a later call may retry.
  *   - All calls on a device share the one array, which keeps the previous
  *     call's contents; the work counters are zeroed by every call.  Calls
  *     that overlap on the GPU (e.g. on two streams) race on the array and

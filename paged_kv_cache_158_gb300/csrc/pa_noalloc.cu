@@ -3,20 +3,25 @@
 //
 // pa_decode needs a scratch workspace for its per-partition partial results
 // and its work counter, and leaves it to the caller to provide one.  Some
-// callers have no way to get one at that point: code that runs while a stream
-// is being captured into a CUDA graph in global capture mode (where a
-// cudaMalloc is an error), serving processes that reserve all of HBM for the
-// KV pool at start-up and keep no allocator headroom, and runtimes that must
-// not call cudaMalloc / cudaFree on their hot path because those calls can
-// synchronise the device.  This entry point gives them the same decode with
-// the scratch taken from a fixed array in the library's own device memory.
+// callers have no way to get one at that point: serving processes that
+// reserve all of HBM for the KV pool at start-up and keep no allocator
+// headroom, runtimes that must not call cudaMalloc / cudaFree on their hot
+// path because those calls can synchronise the device, and host code that
+// owns no allocator at all (a plain C caller handed device pointers by
+// someone else).  This entry point gives them the same decode with the
+// scratch taken from a fixed array in the library's own device memory.
 //
-// The array is a file-scope __device__ variable: it is created when the
-// module is loaded into a device's context and every device that loads the
-// library holds its PA_DECODE_NOALLOC_SCRATCH_BYTES until the process exits.
-// Host code cannot use the array's name as a device address, so the first
-// call on each device looks the address up with cudaGetSymbolAddress (with
-// that device current) and caches it; later calls reuse the cached address.
+// The array is a file-scope __device__ variable.  This file's device code is
+// a module of its own, and under CUDA's lazy module loading (the default) a
+// module is loaded into a device's context the first time it is used, not
+// when the library is loaded: the array's PA_DECODE_NOALLOC_SCRATCH_BYTES are
+// committed on a device by the first pa_decode_noalloc call there, and stay
+// until the process exits.  Host code cannot use the array's name as a
+// device address, so that first call also looks the address up with
+// cudaGetSymbolAddress (with the device current) and caches it; later calls
+// reuse the cached address.  The first call on each device is therefore a
+// warm-up: make it before the rest of device memory is handed to the KV pool
+// and before any stream capture.
 #include <mutex>
 
 #include "pa_internal.h"
@@ -37,8 +42,12 @@ pa_status scratch_address(void** out) {
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_pa_decode_scratch) != cudaSuccess || p == nullptr)
+    if (cudaGetSymbolAddress(&p, g_pa_decode_scratch) != cudaSuccess || p == nullptr) {
+      // Typically out of memory while loading the module: clear the sticky
+      // last error so it is not reported again by a later, unrelated check.
+      cudaGetLastError();
       return PA_ERR_CUDA;
+    }
     g_scratch_ptr[dev] = p;
   }
   *out = g_scratch_ptr[dev];

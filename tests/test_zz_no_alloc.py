@@ -1,11 +1,14 @@
 """pa_decode_noalloc, the decode entry point for callers that cannot allocate
-device memory when they decode (inside a global-mode graph capture, with all
-of HBM given to the KV pool, or on a path where cudaMalloc/cudaFree may not
-synchronise the device).  It must give the same result as pa_decode with a
+device memory when they decode (all of HBM given to the KV pool, a hot path
+where cudaMalloc/cudaFree may synchronise the device, or a plain C caller with
+no device allocator).  It must give the same result as pa_decode with a
 caller-allocated workspace, on two calls in a row (the fixed scratch keeps the
 previous call's contents), and refuse shapes whose scratch would not fit.
 
-Called through the C ABI with ctypes.  Collected last on purpose."""
+Called through the C ABI with ctypes.  Collected last on purpose, so that a
+run stopping at its first failure has run every other test first; it passes
+alone in a fresh process too (its first call is then the per-device warm-up
+that loads the scratch array)."""
 import ctypes
 
 import numpy as np
