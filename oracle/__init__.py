@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
     L.oracle_prefill_fp8.restype = i32
     L.oracle_num_threads.argtypes = []
     L.oracle_num_threads.restype = i32
+    L.oracle_set_num_threads.argtypes = [i32]
+    L.oracle_set_num_threads.restype = None
     _LIB = L
     return L
 
@@ -286,3 +288,8 @@ def prefill_fp8(query, key_cache, value_cache, block_tables, context_lens, query
 
 def num_threads() -> int:
     return int(lib().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops from now on (timing only)."""
+    lib().oracle_set_num_threads(int(n))

@@ -368,9 +368,11 @@ static uint8_t quantize_e4m3(uint16_t h, float scale) {
   return oracle_double_to_e4m3((double)y);
 }
 
-/* Elementwise quantisation of n fp16 values (a whole cache, layout kept). */
+/* Elementwise quantisation of n fp16 values (a whole cache, layout kept).
+   Elements are independent; the loop is split over threads. */
 void oracle_quantize_e4m3_array(uint8_t* out, const uint16_t* in, size_t n, float scale) {
-  for (size_t i = 0; i < n; ++i) out[i] = quantize_e4m3(in[i], scale);
+#pragma omp parallel for schedule(static)
+  for (long long i = 0; i < (long long)n; ++i) out[i] = quantize_e4m3(in[i], scale);
 }
 
 /* Cache write into FP8 caches (same slots as oracle_reshape_and_cache). */
@@ -516,12 +518,22 @@ int oracle_prefill_fp8(uint16_t* out16, double* out64, const uint16_t* query,
   return bad ? -1 : 0;
 }
 
-/* Threads the decode loop uses (OpenMP's maximum, 1 without OpenMP). */
+/* Threads the parallel loops use (OpenMP's maximum, 1 without OpenMP). */
 int oracle_num_threads(void) {
 #ifdef _OPENMP
   extern int omp_get_max_threads(void);
   return omp_get_max_threads();
 #else
   return 1;
+#endif
+}
+
+/* Sets the threads later parallel loops use (n >= 1; no effect without OpenMP). */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  extern void omp_set_num_threads(int);
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
 #endif
 }
