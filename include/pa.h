@@ -179,14 +179,24 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* key_cac
  *   key_caches,
  *   value_caches   HOST arrays of num_layers device pointers, each to an fp16
  *                  [num_blocks][num_heads][block_size][head_dim] cache
- *   block_mapping  device int64 [num_pairs][2]
+ *   block_mapping  int64 [num_pairs][2], device memory or pinned host memory
+ *                  (the kernel reads pinned memory over the CPU-GPU link);
+ *                  pageable host memory returns PA_ERR_INVALID_ARG
  * Preconditions: destination ids are distinct and no destination is also a
- * source in the same call.  For num_pairs <= 1024 the kernel checks them:
- * a pair whose destination is another pair's destination or source is
- * skipped (not copied) and sets PA_ERRBIT_COPY, so nothing races; larger
- * mappings are not checked and violating them races.  An id outside
- * [0, num_blocks) skips that pair and sets PA_ERRBIT_COPY.  num_pairs == 0
- * is a no-op.  Bit-exact.
+ * source in the same call (a pair copying a block onto itself is allowed).
+ * They are checked for any num_pairs:
+ *   - a pinned host mapping is checked on the host when the call is made
+ *     (O(P log P)); a violation returns PA_ERR_INVALID_ARG and launches
+ *     nothing.  The mapping must not change until the stream reaches the
+ *     copy (a CUDA graph that captured the call does not re-check it);
+ *   - a device mapping is checked on the device: every pair's CTA scans the
+ *     whole mapping, and a pair whose destination is another pair's
+ *     destination or source is skipped (not copied) and sets
+ *     PA_ERRBIT_COPY, so nothing races.  The scans cost num_pairs^2 x 16
+ *     bytes of L2 reads in all (above 1024 pairs one CTA copies a pair's
+ *     block in every layer, so each pair is scanned once).
+ * An id outside [0, num_blocks) skips that pair and sets PA_ERRBIT_COPY.
+ * num_pairs == 0 is a no-op.  Bit-exact.
  */
 pa_status pa_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
                          const int64_t* block_mapping, int num_pairs, int num_heads, int head_dim,
@@ -277,10 +287,13 @@ pa_status pa_prefill_fp8(void* out, const void* query, const void* key_cache,
  *   block_bytes    a multiple of 16
  *   src_num_blocks, dst_num_blocks  pool sizes; an id outside [0, n) skips
  *                  the pair and sets PA_ERRBIT_COPY
- * Destination blocks must be distinct: for num_pairs <= 1024 a pair whose
- * destination repeats another's is skipped and sets PA_ERRBIT_COPY (larger
- * mappings are not checked).  Source and destination pools must not
- * overlap.  Bit-exact.  The
+ * Destination blocks must be distinct, for any num_pairs: a pinned host
+ * mapping is checked on the host when the call is made (a repeated
+ * destination returns PA_ERR_INVALID_ARG and launches nothing; the mapping
+ * must not change until the stream reaches the copy), and a device mapping
+ * on the device, where every pair's CTA scans the whole mapping, so a pair
+ * whose destination repeats another's is skipped and sets PA_ERRBIT_COPY.  Source and
+ * destination pools must not overlap.  Bit-exact.  The
  * host side must stay allocated and unchanged until the stream reaches the
  * copy.
  */

@@ -240,7 +240,8 @@ def pa_convert_cache_fp8(src: torch.Tensor, dst: torch.Tensor, scale: float, str
 
 
 def pa_copy_blocks(key_caches, value_caches, block_mapping: torch.Tensor, stream=None) -> None:
-    """Copy-on-write block copy across all layers; block_mapping is int64 [P, 2] (src, dst)."""
+    """Copy-on-write block copy across all layers; block_mapping is int64 [P, 2] (src, dst),
+    a CUDA tensor or pinned host memory (a pinned mapping is also checked on the host)."""
     _copy_blocks(key_caches, value_caches, block_mapping, stream, False)
 
 
@@ -259,10 +260,10 @@ def _copy_blocks(key_caches, value_caches, block_mapping, stream, fp8: bool) -> 
             raise ValueError("all caches must share one shape")
     kp = (ctypes.c_void_p * L)(*[_cache_ptr(t, "key_caches[i]", fp8) for t in key_caches])
     vp = (ctypes.c_void_p * L)(*[_cache_ptr(t, "value_caches[i]", fp8) for t in value_caches])
-    if block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
-        raise ValueError("block_mapping must be [P, 2]")
+    if block_mapping.dtype != torch.int64 or block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
+        raise ValueError("block_mapping must be int64 [P, 2]")
     fn = _lib.pa_copy_blocks_fp8 if fp8 else _lib.pa_copy_blocks
-    st = fn(kp, vp, L, _ptr(block_mapping, "block_mapping", torch.int64), block_mapping.shape[0],
+    st = fn(kp, vp, L, _swap_ptr(block_mapping, "block_mapping"), block_mapping.shape[0],
             H, D, B, NB, _stream(stream))
     _check(st, "pa_copy_blocks_fp8" if fp8 else "pa_copy_blocks")
 

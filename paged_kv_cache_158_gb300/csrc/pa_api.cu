@@ -1,6 +1,7 @@
 // C ABI of libpa.so: argument checks, launch planning and the device error
 // word.  Every computation runs in the kernels of the other translation
 // units; this file only validates, sizes and launches.
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <vector>
@@ -127,6 +128,35 @@ const void* device_address(const void* p, int dev) {
     case cudaMemoryTypeHost: return at.devicePointer;
     default: return nullptr;
   }
+}
+
+// True when the host can read p directly: pinned (page-locked) host memory.
+bool host_readable(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost;
+}
+
+// Conflicts of a block mapping the host can read (int64 [num_pairs][2] of
+// (src, dst)): a destination that appears twice, or, with dst_also_src, a
+// destination that is also another pair's source.  O(P log P).
+bool host_mapping_conflicts(const int64_t* m, int num_pairs, bool dst_also_src) {
+  std::vector<int64_t> d((size_t)num_pairs);
+  for (int i = 0; i < num_pairs; ++i) d[(size_t)i] = m[2 * (size_t)i + 1];
+  std::sort(d.begin(), d.end());
+  if (std::adjacent_find(d.begin(), d.end()) != d.end()) return true;
+  if (dst_also_src) {
+    // Destinations are distinct here, so a source found among them is another
+    // pair's destination unless it is the pair's own (a copy onto itself).
+    for (int i = 0; i < num_pairs; ++i) {
+      const int64_t src = m[2 * (size_t)i], dst = m[2 * (size_t)i + 1];
+      if (src != dst && std::binary_search(d.begin(), d.end(), src)) return true;
+    }
+  }
+  return false;
 }
 
 bool scale_ok(float s) { return s > 0.f && s <= 3.4028234663852886e38f; }  // finite, positive
@@ -268,11 +298,19 @@ pa_status copy_blocks_impl(int elem_bytes, void* const* key_caches, void* const*
         !aligned16(value_caches[l]))
       return PA_ERR_INVALID_ARG;
   }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  const void* map_dev = device_address(block_mapping, dev);
+  if (!map_dev) return PA_ERR_INVALID_ARG;
+  const bool on_host = host_readable(block_mapping);
+  if (on_host && host_mapping_conflicts(block_mapping, num_pairs, true)) return PA_ERR_INVALID_ARG;
   DeviceState ds;
   pa_status st = device_state(&ds, false);
   if (st != PA_OK) return st;
-  return pa::launch_copy_blocks(key_caches, value_caches, num_layers, block_mapping, num_pairs,
-                                num_heads, head_dim, block_size, elem_bytes, num_blocks, ds.err,
+  return pa::launch_copy_blocks(key_caches, value_caches, num_layers,
+                                static_cast<const int64_t*>(map_dev), num_pairs,
+                                num_heads, head_dim, block_size, elem_bytes, num_blocks, !on_host,
+                                ds.err,
                                 reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
@@ -415,6 +453,8 @@ pa_status pa_swap_blocks(void* const* dst_caches, const void* const* src_caches,
   if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
   const void* map_dev = device_address(block_mapping, dev);
   if (!map_dev) return PA_ERR_INVALID_ARG;
+  const bool on_host = host_readable(block_mapping);
+  if (on_host && host_mapping_conflicts(block_mapping, num_pairs, false)) return PA_ERR_INVALID_ARG;
   std::vector<void*> dst(num_caches);
   std::vector<const void*> src(num_caches);
   for (int c = 0; c < num_caches; ++c) {
@@ -430,7 +470,7 @@ pa_status pa_swap_blocks(void* const* dst_caches, const void* const* src_caches,
   return pa::launch_swap_blocks(dst.data(), src.data(), num_caches,
                                 static_cast<const int64_t*>(map_dev), num_pairs,
                                 (long long)block_bytes, (long long)src_num_blocks,
-                                (long long)dst_num_blocks, ds.err,
+                                (long long)dst_num_blocks, !on_host, ds.err,
                                 reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;

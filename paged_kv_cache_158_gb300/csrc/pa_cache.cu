@@ -119,52 +119,62 @@ struct LayerPtrs {
   uint4* v[kCopyMaxLayers];
 };
 
-// Block copies and swaps check their mapping for conflicting pairs on the
-// device when it has at most this many pairs.
-constexpr int kMappingCheckMaxPairs = 1024;
+// Block copies and swaps check their whole mapping for conflicting pairs on
+// the device: every CTA scans all pairs for the one it copies (the mapping's
+// 16 bytes per pair stay in L2).  Up to this many pairs
+// one CTA copies one (pair, cache, chunk) and the grid covers every cache;
+// above it one CTA copies its pair's whole block in every cache, so each
+// pair's scan runs once instead of once per cache and chunk (the scans then
+// cost pairs^2 x 16 bytes of L2 reads in all).
+constexpr int kMappingScanPerCachePairs = 1024;
 
 // True when another pair of the mapping writes `dst` or reads it (with
-// `dst_also_src`), i.e. copying this pair would race.  Checked by the whole
-// CTA for mappings of at most kMappingCheckMaxPairs pairs.
+// `dst_also_src`), i.e. copying this pair would race.  Every thread of the
+// CTA must call it (it ends with a CTA-wide vote).  With scan false (the
+// host already checked the whole mapping) it returns false at once.
 __device__ __forceinline__ bool mapping_conflict(const int64_t* __restrict__ block_mapping,
                                                  int num_pairs, int pair, long long dst,
-                                                 bool dst_also_src) {
-  __shared__ int conflict;
-  if (threadIdx.x == 0) conflict = 0;
-  __syncthreads();
-  if (num_pairs <= kMappingCheckMaxPairs) {
-    for (int q = threadIdx.x; q < num_pairs; q += blockDim.x) {
-      if (q == pair) continue;
-      if (block_mapping[2 * q + 1] == dst || (dst_also_src && block_mapping[2 * q] == dst))
-        conflict = 1;
-    }
+                                                 bool dst_also_src, bool scan) {
+  if (!scan) return false;
+  int hit = 0;
+  for (int q = threadIdx.x; q < num_pairs; q += blockDim.x) {
+    const long long qd = block_mapping[2 * q + 1];
+    const long long qs = dst_also_src ? block_mapping[2 * q] : -1;
+    if (q != pair && (qd == dst || qs == dst)) hit = 1;
   }
-  __syncthreads();
-  return conflict != 0;
+  return __syncthreads_or(hit) != 0;
 }
 
+__device__ __forceinline__ void copy_vecs(const uint4* __restrict__ s, uint4* __restrict__ d,
+                                          long long n, long long first, long long stride) {
+  for (long long i = first; i < n; i += stride) d[i] = s[i];
+}
+
+// blockIdx.y = pair; blockIdx.z = layer * 2 + (0 key | 1 value) when
+// per_cache, else the CTA loops over all 2 * num_layers caches of the launch.
 __global__ void __launch_bounds__(256)
     copy_blocks_kernel(LayerPtrs ptrs, const int64_t* __restrict__ block_mapping, int pair_base,
-                       int num_pairs, long long block_vecs, long long num_blocks,
-                       unsigned int* err) {
+                       int num_pairs, long long block_vecs, long long num_blocks, int num_caches,
+                       bool per_cache, bool scan, unsigned int* err) {
   pdl_wait();
   pdl_launch_dependents();
   const int pair = pair_base + blockIdx.y;
-  const int layer = blockIdx.z >> 1;
   const long long src = block_mapping[2 * pair];
   const long long dst = block_mapping[2 * pair + 1];
-  // every thread of the CTA reaches the check's barriers
-  const bool conflict = mapping_conflict(block_mapping, num_pairs, pair, dst, true);
+  // every thread of the CTA reaches the check's vote
+  const bool conflict = mapping_conflict(block_mapping, num_pairs, pair, dst, true, scan);
   if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks || conflict) {
     if (blockIdx.x == 0 && blockIdx.z == 0 && threadIdx.x == 0) atomicOr(err, PA_ERRBIT_COPY);
     return;
   }
-  uint4* base = (blockIdx.z & 1) ? ptrs.v[layer] : ptrs.k[layer];
-  const uint4* s = base + src * block_vecs;
-  uint4* d = base + dst * block_vecs;
   const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < block_vecs; i += stride)
-    d[i] = s[i];
+  const long long first = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int z0 = per_cache ? (int)blockIdx.z : 0;
+  const int z1 = per_cache ? z0 + 1 : num_caches;
+  for (int z = z0; z < z1; ++z) {
+    uint4* base = (z & 1) ? ptrs.v[z >> 1] : ptrs.k[z >> 1];
+    copy_vecs(base + src * block_vecs, base + dst * block_vecs, block_vecs, first, stride);
+  }
 }
 
 // ---- block swap between device and host pools
@@ -182,33 +192,40 @@ struct SwapPtrs {
 
 constexpr int kSwapUnroll = 4;
 
+// blockIdx.y = pair; blockIdx.z = cache when per_cache, else the CTA loops
+// over all caches of the launch.
 __global__ void __launch_bounds__(256)
     swap_blocks_kernel(SwapPtrs ptrs, const int64_t* __restrict__ block_mapping, int pair_base,
                        int num_pairs, long long block_vecs, long long src_num_blocks,
-                       long long dst_num_blocks, unsigned int* err) {
+                       long long dst_num_blocks, int num_caches, bool per_cache, bool scan,
+                       unsigned int* err) {
   pdl_wait();
   pdl_launch_dependents();
   const int pair = pair_base + blockIdx.y;
   const long long src = block_mapping[2 * pair];
   const long long dst = block_mapping[2 * pair + 1];
-  // every thread of the CTA reaches the check's barriers
-  const bool conflict = mapping_conflict(block_mapping, num_pairs, pair, dst, false);
+  // every thread of the CTA reaches the check's vote
+  const bool conflict = mapping_conflict(block_mapping, num_pairs, pair, dst, false, scan);
   if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks || conflict) {
     if (blockIdx.x == 0 && blockIdx.z == 0 && threadIdx.x == 0) atomicOr(err, PA_ERRBIT_COPY);
     return;
   }
-  const uint4* s = ptrs.src[blockIdx.z] + src * block_vecs;
-  uint4* d = ptrs.dst[blockIdx.z] + dst * block_vecs;
   const long long stride = (long long)gridDim.x * blockDim.x;
-  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  for (; i + (kSwapUnroll - 1) * stride < block_vecs; i += kSwapUnroll * stride) {
-    uint4 t[kSwapUnroll];
+  const int z0 = per_cache ? (int)blockIdx.z : 0;
+  const int z1 = per_cache ? z0 + 1 : num_caches;
+  for (int z = z0; z < z1; ++z) {
+    const uint4* s = ptrs.src[z] + src * block_vecs;
+    uint4* d = ptrs.dst[z] + dst * block_vecs;
+    long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + (kSwapUnroll - 1) * stride < block_vecs; i += kSwapUnroll * stride) {
+      uint4 t[kSwapUnroll];
 #pragma unroll
-    for (int u = 0; u < kSwapUnroll; ++u) t[u] = s[i + u * stride];
+      for (int u = 0; u < kSwapUnroll; ++u) t[u] = s[i + u * stride];
 #pragma unroll
-    for (int u = 0; u < kSwapUnroll; ++u) d[i + u * stride] = t[u];
+      for (int u = 0; u < kSwapUnroll; ++u) d[i + u * stride] = t[u];
+    }
+    for (; i < block_vecs; i += stride) d[i] = s[i];
   }
-  for (; i < block_vecs; i += stride) d[i] = s[i];
 }
 
 // ---- slot map ("vLLM推理加速深度解读：PagedAttention如何提升10x吞吐量" §2.3)
@@ -349,7 +366,7 @@ cudaError_t launch_convert_cache_fp8(const void* src, void* dst, long long num_e
 cudaError_t launch_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
                                const int64_t* block_mapping, int num_pairs, int num_heads,
                                int head_dim, int block_size, int elem_bytes, int num_blocks,
-                               unsigned int* err, cudaStream_t stream) {
+                               bool scan, unsigned int* err, cudaStream_t stream) {
   if (num_pairs == 0 || num_layers == 0) return cudaSuccess;
   const long long block_vecs = (long long)num_heads * block_size * head_dim * elem_bytes / 16;
   const int threads = 256;
@@ -362,12 +379,13 @@ cudaError_t launch_copy_blocks(void* const* key_caches, void* const* value_cache
       ptrs.k[i] = static_cast<uint4*>(key_caches[l0 + i]);
       ptrs.v[i] = static_cast<uint4*>(value_caches[l0 + i]);
     }
+    const bool per_cache = num_pairs <= kMappingScanPerCachePairs;
     for (int p0 = 0; p0 < num_pairs; p0 += 65535) {
       const int np = num_pairs - p0 < 65535 ? num_pairs - p0 : 65535;
-      dim3 grid((unsigned)xblocks, (unsigned)np, (unsigned)(2 * nl));
+      dim3 grid(per_cache ? (unsigned)xblocks : 1u, (unsigned)np, per_cache ? (unsigned)(2 * nl) : 1u);
       const cudaError_t e = launch_pdl(copy_blocks_kernel, grid, dim3(threads), 0, stream, ptrs,
                                        block_mapping, p0, num_pairs, block_vecs,
-                                       (long long)num_blocks, err);
+                                       (long long)num_blocks, 2 * nl, per_cache, scan, err);
       if (e != cudaSuccess) return e;
     }
   }
@@ -377,7 +395,8 @@ cudaError_t launch_copy_blocks(void* const* key_caches, void* const* value_cache
 cudaError_t launch_swap_blocks(void* const* dst_caches, const void* const* src_caches,
                                int num_caches, const int64_t* block_mapping, int num_pairs,
                                long long block_bytes, long long src_num_blocks,
-                               long long dst_num_blocks, unsigned int* err, cudaStream_t stream) {
+                               long long dst_num_blocks, bool scan, unsigned int* err,
+                               cudaStream_t stream) {
   if (num_pairs == 0 || num_caches == 0) return cudaSuccess;
   const long long block_vecs = block_bytes / 16;
   const int threads = 256;
@@ -390,12 +409,13 @@ cudaError_t launch_swap_blocks(void* const* dst_caches, const void* const* src_c
       ptrs.src[i] = static_cast<const uint4*>(src_caches[c0 + i]);
       ptrs.dst[i] = static_cast<uint4*>(dst_caches[c0 + i]);
     }
+    const bool per_cache = num_pairs <= kMappingScanPerCachePairs;
     for (int p0 = 0; p0 < num_pairs; p0 += 65535) {
       const int np = num_pairs - p0 < 65535 ? num_pairs - p0 : 65535;
-      dim3 grid((unsigned)xblocks, (unsigned)np, (unsigned)nc);
+      dim3 grid(per_cache ? (unsigned)xblocks : 1u, (unsigned)np, per_cache ? (unsigned)nc : 1u);
       const cudaError_t e = launch_pdl(swap_blocks_kernel, grid, dim3(threads), 0, stream, ptrs,
                                        block_mapping, p0, num_pairs, block_vecs, src_num_blocks,
-                                       dst_num_blocks, err);
+                                       dst_num_blocks, nc, per_cache, scan, err);
       if (e != cudaSuccess) return e;
     }
   }

@@ -82,14 +82,16 @@ cudaError_t launch_convert_cache_fp8(const void* src, void* dst, long long num_e
 cudaError_t launch_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
                                const int64_t* block_mapping, int num_pairs, int num_heads,
                                int head_dim, int block_size, int elem_bytes, int num_blocks,
-                               unsigned int* err, cudaStream_t stream);
+                               bool scan, unsigned int* err, cudaStream_t stream);
 
 // block_bytes: a multiple of 16; pointers are device addresses (device
-// memory or mapped pinned host memory).
+// memory or mapped pinned host memory).  scan: the kernel checks the mapping
+// for conflicting pairs (false when the host already checked it).
 cudaError_t launch_swap_blocks(void* const* dst_caches, const void* const* src_caches,
                                int num_caches, const int64_t* block_mapping, int num_pairs,
                                long long block_bytes, long long src_num_blocks,
-                               long long dst_num_blocks, unsigned int* err, cudaStream_t stream);
+                               long long dst_num_blocks, bool scan, unsigned int* err,
+                               cudaStream_t stream);
 
 // Multi-query paged attention (tensor cores): arguments as in pa_prefill.
 struct PrefillArgs {

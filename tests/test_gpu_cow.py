@@ -118,3 +118,68 @@ def test_copy_blocks_conflicting_pairs_are_skipped_and_flagged():
     for src, dst in ([3, 7], [8, 9]):          # the pairs without a conflict
         ek[dst], ev[dst] = before_k[src], before_v[src]
     assert np.array_equal(u16(kc), ek) and np.array_equal(u16(vc), ev)
+
+
+def _random_caches(rng, layers, NB, H, B, D):
+    out = []
+    for _ in range(2 * layers):
+        raw = rng.integers(0, 1 << 16, (NB, H, B, D), dtype=np.uint16)
+        out.append(torch.from_numpy(raw.view(np.int16)).cuda().view(torch.float16))
+    return out[:layers], out[layers:]
+
+
+def test_copy_blocks_large_mapping_conflicts_are_skipped_and_flagged():
+    """1500 pairs over 3 layers (above the 1024 pairs where each CTA copies one
+    cache): a repeated destination skips both of its pairs, a destination that
+    is another pair's source skips the writing pair, every other pair copies
+    exactly once."""
+    rng = np.random.default_rng(13)
+    P, NB, H, B, D, L = 1500, 3200, 1, 4, 64, 3
+    kcs, vcs = _random_caches(rng, L, NB, H, B, D)
+    before = [u16(t).copy() for t in kcs + vcs]
+    src = rng.permutation(1500).astype(np.int64)
+    dst = (1500 + rng.permutation(1500)).astype(np.int64)
+    mapping = np.stack([src, dst], 1)
+    mapping[700, 1] = mapping[900, 1]          # pairs 700 and 900 share a destination
+    mapping[1200, 1] = mapping[5, 0]           # pair 1200 writes the block pair 5 reads
+    skipped = {700, 900, 1200}
+    pa.pa_copy_blocks(kcs, vcs, torch.from_numpy(mapping).to(DEV))
+    st, bits = pa.pa_check_errors()
+    assert st == pa.PA_ERR_OUT_OF_RANGE and bits == pa.PA_ERRBIT_COPY
+    for t, b in zip(kcs + vcs, before):
+        expect = b.copy()
+        for p in range(P):
+            if p not in skipped:
+                expect[mapping[p, 1]] = b[mapping[p, 0]]
+        assert np.array_equal(u16(t), expect)
+
+
+def test_copy_blocks_pinned_mapping_checked_on_host():
+    """A mapping in pinned host memory is checked before anything launches:
+    a repeated destination (here among 2000 pairs) or a destination that is
+    another pair's source is refused with PA_ERR_INVALID_ARG and the caches are
+    unchanged; a clean pinned mapping copies like a device one."""
+    rng = np.random.default_rng(14)
+    P, NB, H, B, D = 2000, 4100, 1, 4, 64
+    kcs, vcs = _random_caches(rng, 1, NB, H, B, D)
+    before = [u16(t).copy() for t in kcs + vcs]
+    src = rng.permutation(2000).astype(np.int64)
+    dst = (2000 + rng.permutation(2000)).astype(np.int64)
+    clean = np.stack([src, dst], 1)
+    for bad_row, bad_col, value in ((1999, 1, clean[3, 1]), (17, 1, clean[40, 0])):
+        bad = clean.copy()
+        bad[bad_row, bad_col] = value
+        with pytest.raises(pa.PAError) as e:
+            pa.pa_copy_blocks(kcs, vcs, torch.from_numpy(bad).pin_memory())
+        assert e.value.status == pa.PA_ERR_INVALID_ARG
+        torch.cuda.synchronize()
+        for t, b in zip(kcs + vcs, before):
+            assert np.array_equal(u16(t), b)
+    pa.pa_copy_blocks(kcs, vcs, torch.from_numpy(clean).pin_memory())
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+    for t, b in zip(kcs + vcs, before):
+        expect = b.copy()
+        expect[clean[:, 1]] = b[clean[:, 0]]
+        assert np.array_equal(u16(t), expect)
+    with pytest.raises(ValueError):            # pageable host memory: the device cannot reach it
+        pa.pa_copy_blocks(kcs, vcs, torch.from_numpy(clean))

@@ -193,3 +193,32 @@ def test_swap_more_caches_and_pairs_than_one_launch():
     expect[big[:, 1]] = host_view(d_pool)[big[:, 0]]
     assert np.array_equal(ref[0], expect)
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+def test_swap_large_mapping_duplicate_destination():
+    """1300 pairs (above the 1024 where each CTA copies one cache): with the
+    mapping on the device, the two pairs sharing a destination are skipped and
+    flagged and the rest move; the same mapping in pinned host memory is
+    refused on the host before anything launches."""
+    rng = np.random.default_rng(11)
+    P = 1300
+    dev, host = pools(rng, 2, 1400, 1350, (1, 4, 64), torch.float16)
+    ref_host = [host_view(t) for t in host]
+    ref_dev = [host_view(t) for t in dev]
+    mapping = np.stack([rng.permutation(1400)[:P], rng.permutation(1350)[:P]], 1).astype(np.int64)
+    mapping[1000, 1] = mapping[77, 1]
+    with pytest.raises(pa.PAError) as e:
+        pa.pa_swap_blocks(host, dev, torch.from_numpy(mapping).pin_memory())
+    assert e.value.status == pa.PA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    for t, r in zip(host, ref_host):
+        assert np.array_equal(host_view(t), r)
+    pa.pa_swap_blocks(host, dev, torch.from_numpy(mapping).to(DEV))
+    st, bits = pa.pa_check_errors()
+    assert st == pa.PA_ERR_OUT_OF_RANGE and bits == pa.PA_ERRBIT_COPY
+    for t, r, d in zip(host, ref_host, ref_dev):
+        expect = r.copy()
+        for p in range(P):
+            if p not in (77, 1000):
+                expect[mapping[p, 1]] = d[mapping[p, 0]]
+        assert np.array_equal(host_view(t), expect)
