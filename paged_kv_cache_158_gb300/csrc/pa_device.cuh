@@ -171,14 +171,16 @@ __device__ __forceinline__ float exp2_approx(float x) {
   return y;
 }
 
-// (2^a, 2^b) as a packed fp16 pair (low half = 2^a): the arguments are
-// rounded to fp16 and one ex2.approx.f16x2 computes both.
-__device__ __forceinline__ uint32_t exp2_f16x2(float a, float b) {
+// (2^a, 2^b) as a packed fp16 pair (low half = 2^a): both exponentials in
+// fp32 (ex2.approx.ftz.f32), then rounded once to fp16 (a weight's relative
+// error is then that rounding, at most 2^-11).
+__device__ __forceinline__ uint32_t exp2_f32_to_f16x2(float a, float b) {
   uint32_t r;
   asm("{\n"
-      "  .reg .b32 x;\n"
-      "  cvt.rn.f16x2.f32 x, %2, %1;\n"
-      "  ex2.approx.f16x2 %0, x;\n"
+      "  .reg .f32 ea, eb;\n"
+      "  ex2.approx.ftz.f32 ea, %1;\n"
+      "  ex2.approx.ftz.f32 eb, %2;\n"
+      "  cvt.rn.f16x2.f32 %0, eb, ea;\n"
       "}\n"
       : "=r"(r)
       : "f"(a), "f"(b));

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import paged_kv_cache_158_gb300 as pa
-from pa_testlib import decode_gate, live_slot_mask, poison_dead_slots_device, poison_dead_slots_host
+from pa_testlib import prefill_gate, live_slot_mask, poison_dead_slots_device, poison_dead_slots_host
 from workloads import configs, gpu
 
 pytestmark = pytest.mark.gpu
@@ -56,7 +56,7 @@ def test_prefill_mixed_batch_all_outputs(D, B):
     poison_dead_slots_device(dv["key_cache"], dv["value_cache"], mask)
     out = run_prefill(w, dv)
     ref64 = oracle_prefill(w, mask)
-    decode_gate(out, ref64, f"prefill D{D} B{B}")
+    prefill_gate(out, ref64, f"prefill D{D} B{B}")
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
 
 
@@ -65,7 +65,7 @@ def test_prefill_tile_edges(q_len, ctx):
     w = configs.prefill_workload(f"edge_{q_len}_{ctx}", 4100 + q_len, [q_len, 5], [ctx, 9], 2, 128, 16)
     dv = gpu.materialize_prefill(w, DEV)
     out = run_prefill(w, dv)
-    decode_gate(out, oracle_prefill(w), f"prefill q{q_len} c{ctx}")
+    prefill_gate(out, oracle_prefill(w), f"prefill q{q_len} c{ctx}")
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
 
 
@@ -76,7 +76,7 @@ def test_prefill_deterministic_and_decode_rows_match_decode():
     b = run_prefill(w, dv)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     ref64 = oracle_prefill(w)
-    decode_gate(a, ref64, "prefill det")
+    prefill_gate(a, ref64, "prefill det")
     # the one-token chunks against the decode kernel on the same cache
     qs = configs.query_start(w)
     rows = torch.from_numpy(qs[1:4].astype(np.int64)).to(DEV)
@@ -86,7 +86,7 @@ def test_prefill_deterministic_and_decode_rows_match_decode():
     outd = torch.empty_like(q)
     ws = pa.decode_workspace(3, w.num_heads, w.head_dim, 1000)
     pa.pa_decode(outd, q, dv["key_cache"], dv["value_cache"], bt, cl, w.scale, 1000, ws)
-    decode_gate(outd, ref64[qs[1:4]], "decode rows")
+    prefill_gate(outd, ref64[qs[1:4]], "decode rows")
 
 
 def test_prefill_7b_full_size_sampled_rows():
@@ -111,7 +111,7 @@ def test_prefill_7b_full_size_sampled_rows():
                                           np.array([p_last + 1], np.int32),
                                           np.array([0, 16], np.int32), w.scale)
             assert rc == 0
-            decode_gate(out[qs[s] + j0:qs[s] + j0 + 16], ref64, f"{w.name} s{s} rows {j0}..")
+            prefill_gate(out[qs[s] + j0:qs[s] + j0 + 16], ref64, f"{w.name} s{s} rows {j0}..")
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
 
 
@@ -129,7 +129,7 @@ def test_prefill_bad_inputs_flagged():
     # the other sequence is unaffected
     w.block_tables[1, 0] = 0
     ref64 = oracle_prefill(w)
-    decode_gate(out[:40], ref64[:40], "unaffected sequence")
+    prefill_gate(out[:40], ref64[:40], "unaffected sequence")
 
 
 def test_prefill_long_chunk_and_many_decode_rows():
@@ -140,7 +140,7 @@ def test_prefill_long_chunk_and_many_decode_rows():
     w = configs.prefill_workload("long_many", 4600, q_lens, ctx, 2, 128, 16)
     dv = gpu.materialize_prefill(w, DEV)
     out = run_prefill(w, dv)
-    decode_gate(out, oracle_prefill(w), "long chunk + 150 decode rows")
+    prefill_gate(out, oracle_prefill(w), "long chunk + 150 decode rows")
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
 
 
@@ -153,5 +153,5 @@ def test_prefill_large_logits_rescale_path(scale):
     w.logit_scale = scale
     dv = gpu.materialize_prefill(w, DEV)
     out = run_prefill(w, dv)
-    decode_gate(out, oracle_prefill(w), f"prefill scale {scale}")
+    prefill_gate(out, oracle_prefill(w), f"prefill scale {scale}")
     assert pa.pa_check_errors() == (pa.PA_OK, 0)

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 import paged_kv_cache_158_gb300 as pa
-from pa_testlib import decode_gate, live_slot_mask, poison_dead_slots_device_fp8, poison_dead_slots_host_fp8
+from pa_testlib import prefill_gate, live_slot_mask, poison_dead_slots_device_fp8, poison_dead_slots_host_fp8
 from workloads import configs, gpu
 
 pytestmark = pytest.mark.gpu
@@ -73,7 +73,7 @@ def test_prefill_fp8_mixed_batch_all_outputs(D, B):
     out = run(w, dv)
     kc8, vc8 = oracle_pool(w)
     poison_dead_slots_host_fp8(kc8, vc8, mask)
-    decode_gate(out, oracle_out(w, kc8, vc8), f"fp8 prefill D{D} B{B}")
+    prefill_gate(out, oracle_out(w, kc8, vc8), f"fp8 prefill D{D} B{B}")
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
 
 
@@ -82,7 +82,7 @@ def test_prefill_fp8_tile_edges(q_len, ctx):
     w = configs.prefill_workload(f"f8edge_{q_len}_{ctx}", 6100 + q_len, [q_len, 5], [ctx, 9], 2, 128, 16)
     dv = materialize_fp8(w)
     out = run(w, dv)
-    decode_gate(out, oracle_out(w, *oracle_pool(w)), f"fp8 prefill q{q_len} c{ctx}")
+    prefill_gate(out, oracle_out(w, *oracle_pool(w)), f"fp8 prefill q{q_len} c{ctx}")
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
 
 
@@ -104,7 +104,7 @@ def test_prefill_fp8_7b_full_size_sampled_rows():
             p_last = c - ql + j0 + 15
             ref64 = oracle_out(w, kc8, vc8, q[qs[s] + j0:qs[s] + j0 + 16], w.block_tables[s:s + 1],
                                np.array([p_last + 1], np.int32), np.array([0, 16], np.int32))
-            decode_gate(out[qs[s] + j0:qs[s] + j0 + 16], ref64, f"fp8 {w.name} s{s} rows {j0}..")
+            prefill_gate(out[qs[s] + j0:qs[s] + j0 + 16], ref64, f"fp8 {w.name} s{s} rows {j0}..")
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
 
 
@@ -122,7 +122,7 @@ def test_prefill_fp8_scales_checked_and_bad_block_flagged():
     assert st == pa.PA_ERR_OUT_OF_RANGE and bits & pa.PA_ERRBIT_BLOCK_ID
     w.block_tables[1, 0] = 0
     kc8, vc8 = oracle_pool(w)
-    decode_gate(out[:40], oracle_out(w, kc8, vc8)[:40], "fp8 unaffected sequence")
+    prefill_gate(out[:40], oracle_out(w, kc8, vc8)[:40], "fp8 unaffected sequence")
 
 
 @pytest.mark.parametrize("scale", [0.4, 4.0])
@@ -131,5 +131,5 @@ def test_prefill_fp8_large_logits_rescale_path(scale):
     w.logit_scale = scale
     dv = materialize_fp8(w)
     out = run(w, dv)
-    decode_gate(out, oracle_out(w, *oracle_pool(w)), f"fp8 prefill scale {scale}")
+    prefill_gate(out, oracle_out(w, *oracle_pool(w)), f"fp8 prefill scale {scale}")
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
