@@ -59,6 +59,9 @@ def parse_args():
                          "scan: decode time per call against context length (fixed + marginal)")
     ap.add_argument("--kv-dtype", choices=["fp16", "fp8"], default="fp16",
                     help="KV-cache element type (fp8: E4M3 codes with per-tensor scales)")
+    ap.add_argument("--also", default="c5",
+                    help="comma-separated workloads measured after the main one in the same run "
+                         "(single GPU only; 'none' to skip); each gets its own record under 'also'")
     return ap.parse_args()
 
 
@@ -75,8 +78,9 @@ def decode_bytes(w, bt, ctx, kv_elem_bytes: int = 2) -> int:
     """Algorithmic bytes of one decode call: per (s, h): q (2D) + K and V of the c_s live
     tokens (2 * c_s * D * kv_elem_bytes) + out (2D); per s: ceil(c_s/B) table entries and
     one context length."""
-    S, H, D, B = w.num_seqs, w.num_heads, w.head_dim, w.block_size
+    H, D, B = w.num_heads, w.head_dim, w.block_size
     ctx = np.asarray(ctx, dtype=np.int64)
+    S = len(ctx)
     per_pair = 2 * D + 2 * kv_elem_bytes * ctx * D + 2 * D
     return int(H * per_pair.sum() + 4 * (-(-ctx // B)).sum() + 4 * S)
 
@@ -301,16 +305,15 @@ def timed_flushed(fn, K, device, world, stream, flush):
     return max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), world)
 
 
-def run_ours(args, rank, world, local):
+def measure_step(args, w, fp8: bool, device, world):
+    """Everything the bench reports for one workload's decode step: the graph step (the
+    value), the eager step with CUDA events around every decode call (the roofline's
+    achieved), the clocks sampled during both, and the end-to-end step from pinned host
+    buffers.  Returns (record, launches in the timed regions)."""
     import torch
 
     import paged_kv_cache_158_gb300 as pa
 
-    device = torch.device("cuda", local if world > 1 else 0)
-    if args.partition_tokens:
-        pa.pa_decode_set_partition_tokens(args.partition_tokens)
-    w = make_workload(args.workload, args.layers)
-    fp8 = args.kv_dtype == "fp8"
     st = Step(w, device, fp8)
     L = len(st.dw.layers)
     stream = torch.cuda.current_stream(device)
@@ -373,23 +376,13 @@ def run_ours(args, rank, world, local):
         if flush_buf is not None:
             e2e["l2"] = ("not flushed: consecutive steps run back to back, and this step's cache "
                          "fits in the L2, so it may be served from L2")
-
-    line = {
-        "metric": "paged-decode KV GB/s (algorithmic q + gathered K/V + out bytes over step time)",
+    rec = {
         "value": round(value, 2),
-        "unit": "GB/s",
-        "n_gpus": world,
-        "steps": K,
-        "warmup": args.warmup,
         "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
         "dtype": "e4m3 KV cache, f16 q/out, f32 accumulate" if fp8 else "f16 in, f32 accumulate",
-        "data": "synthetic (seeded SplitMix64 / Box-Muller values, seeded block tables)",
         "config": {
             "workload": w.name,
-            "kv_dtype": args.kv_dtype,
+            "kv_dtype": "fp8" if fp8 else "fp16",
             "layers": L, "num_seqs": w.num_seqs, "num_heads": w.num_heads, "head_dim": w.head_dim,
             "block_size": w.block_size, "num_blocks_per_layer": w.num_blocks,
             "context_tokens": ctx_tokens, "max_context_len": st.max_ctx,
@@ -421,14 +414,62 @@ def run_ours(args, rank, world, local):
             "frac": round(achieved / peak, 4),
             "launch_us": round(dec_avg_ms * 1e3, 3),
             "launch_us_p10_p50_p90": [round(float(np.percentile(dec_ms, q)) * 1e3, 3) for q in (10, 50, 90)],
+            "bytes_per_launch": st.bytes_per_decode,
             "traffic": committed_traffic(w.name + ("_fp8" if fp8 else "")),
         },
         "clocks": clk,
-        "gpu_launches": st.launches_per_step() * K * (2 if ms_graph is not None else 1),
         "e2e": e2e,
     }
+    launches = st.launches_per_step() * K * (2 if ms_graph is not None else 1)
+    del st
+    torch.cuda.synchronize(device)
+    torch.cuda.empty_cache()
+    return rec, launches
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import paged_kv_cache_158_gb300 as pa
+
+    device = torch.device("cuda", local if world > 1 else 0)
+    if args.partition_tokens:
+        pa.pa_decode_set_partition_tokens(args.partition_tokens)
+    w = make_workload(args.workload, args.layers)
+    fp8 = args.kv_dtype == "fp8"
+    rec, launches = measure_step(args, w, fp8, device, world)
+    line = {
+        "metric": "paged-decode KV GB/s (algorithmic q + gathered K/V + out bytes over step time)",
+        "value": rec["value"],
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": rec["ms_per_step"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": rec["dtype"],
+        "data": "synthetic (seeded SplitMix64 / Box-Muller values, seeded block tables)",
+    }
+    line.update({k: v for k, v in rec.items() if k not in line})
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=12.0, fp8=fp8)
+    # The other workload with a bandwidth target, measured the same way in the same process
+    # (single GPU only): one record per workload under "also".
+    extra = [x for x in args.also.split(",") if x and x != "none" and x != args.workload]
+    if world == 1 and extra:
+        line["also"] = []
+        for name in extra:
+            wx = make_workload(name, 0)
+            rx, lx = measure_step(args, wx, fp8, device, world)
+            rx["metric"] = line["metric"]
+            rx["unit"] = "GB/s"
+            if rank == 0 and not args.no_cpu_baseline:
+                rx["cpu_baseline"] = cpu_baseline(wx, budget_s=6.0, fp8=fp8, single_thread_s=0.0)
+            line["also"].append(rx)
+            launches += lx
+    line["gpu_launches"] = launches
     return line
 
 
@@ -882,27 +923,45 @@ def prefill_cpu_baseline(w, budget_s: float, fp8: bool = False):
 
 # ------------------------------------------------------------ CPU oracle
 
-def oracle_sample(w, fp8: bool = False):
-    """Host inputs of the bounded sample: layer 0 of the workload, every sequence and head,
-    and a call running the oracle's decode on them (FP8: the oracle quantises the pool)."""
+def oracle_sample(w, fp8: bool = False, seqs: int | None = None):
+    """Host inputs of the bounded sample: layer 0 of the workload, every head of the first
+    `seqs` sequences (default: all), and a call running the oracle's decode on them (FP8: the
+    oracle quantises the pool)."""
     import oracle
     from workloads import gpu
     if w.block_tables is None:
         raise ValueError("the CPU baseline sample needs static block tables")
     kc, vc = gpu.host_pool(w, 0)
     q, _, _ = gpu.host_small(w, 0)
+    n = w.num_seqs if seqs is None else seqs
+    q, bt, ctx = q[:n], w.block_tables[:n], w.context_lens[:n]
     if fp8:
         ks, vs = configs.fp8_scales(w)
         kc, vc = oracle.quantize_e4m3(kc, ks), oracle.quantize_e4m3(vc, vs)
-        return oracle, lambda: oracle.decode_fp8(q, kc, vc, w.block_tables, w.context_lens, w.scale,
-                                                 ks, vs, want64=False)
-    return oracle, lambda: oracle.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale,
-                                         want64=False)
+        return oracle, lambda: oracle.decode_fp8(q, kc, vc, bt, ctx, w.scale, ks, vs, want64=False)
+    return oracle, lambda: oracle.decode(q, kc, vc, bt, ctx, w.scale, want64=False)
 
 
-def cpu_baseline(w, budget_s: float, fp8: bool = False):
-    oracle, run = oracle_sample(w, fp8)
-    nbytes = decode_bytes(w, w.block_tables, w.context_lens, 1 if fp8 else 2)
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def _time_oracle(run, budget_s: float):
     reps, t_total = 0, 0.0
     while t_total < budget_s or reps < 1:
         t0 = time.perf_counter()
@@ -910,11 +969,34 @@ def cpu_baseline(w, budget_s: float, fp8: bool = False):
         t_total += time.perf_counter() - t0
         reps += 1
         assert rc == 0
-    return {"value": round(nbytes * reps / t_total / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
-            "kind": "oracle",
-            "sample": f"{w.name} layer 0 decode (all {w.num_seqs} seqs x {w.num_heads} heads), "
-                      f"{reps} repetitions, {t_total:.1f} s",
-            "host_cpus": os.cpu_count()}
+    return reps, t_total
+
+
+def cpu_baseline(w, budget_s: float, fp8: bool = False, single_thread_s: float = 4.0):
+    """The oracle's decode of layer 0 on all host cores for about budget_s seconds, and (if
+    single_thread_s > 0) on one core for about that long over the first 4 sequences."""
+    oracle, run = oracle_sample(w, fp8)
+    nbytes = decode_bytes(w, w.block_tables, w.context_lens, 1 if fp8 else 2)
+    reps, t_total = _time_oracle(run, budget_s)
+    out = {"value": round(nbytes * reps / t_total / 1e9, 4), "unit": "GB/s",
+           "cores": oracle.num_threads(), "kind": "oracle",
+           "sample": f"{w.name} layer 0 decode (all {w.num_seqs} seqs x {w.num_heads} heads), "
+                     f"{reps} repetitions, {t_total:.1f} s",
+           "host_cpus": os.cpu_count(), "cpu_model": cpu_model()}
+    if single_thread_s > 0:
+        n = min(4, w.num_seqs)
+        _, run1 = oracle_sample(w, fp8, seqs=n)
+        nb1 = decode_bytes(w, w.block_tables[:n], w.context_lens[:n], 1 if fp8 else 2)
+        threads = oracle.num_threads()
+        oracle.set_num_threads(1)
+        try:
+            r1, t1 = _time_oracle(run1, single_thread_s)
+        finally:
+            oracle.set_num_threads(threads)
+        out["single_thread"] = {"value": round(nb1 * r1 / t1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                                "sample": f"{w.name} layer 0 decode of sequences 0..{n - 1} (all "
+                                          f"{w.num_heads} heads), {r1} repetitions, {t1:.1f} s"}
+    return out
 
 
 def run_reference(args, rank, world):
