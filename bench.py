@@ -59,6 +59,9 @@ def parse_args():
                          "scan: decode time per call against context length (fixed + marginal)")
     ap.add_argument("--kv-dtype", choices=["fp16", "fp8"], default="fp16",
                     help="KV-cache element type (fp8: E4M3 codes with per-tensor scales)")
+    ap.add_argument("--prefill-workload", choices=["chunked", "mixed"], default="chunked",
+                    help="--op prefill: 4 x 512-token chunks (chunked) or 2 chunks plus 64 decode "
+                         "rows in one call (mixed; also timed as separate prefill and decode calls)")
     ap.add_argument("--also", default="c5",
                     help="comma-separated workloads measured after the main one in the same run "
                          "(single GPU only; 'none' to skip); each gets its own record under 'also'")
@@ -806,7 +809,7 @@ def run_prefill_bench(args):
     from workloads import gpu
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
-    w = configs.prefill_7b()
+    w = configs.prefill_7b_mixed() if args.prefill_workload == "mixed" else configs.prefill_7b()
     fp8 = args.kv_dtype == "fp8"
     ks, vs = configs.fp8_scales(w)
     tq = int(np.sum(w.extra["q_lens"]))
@@ -847,14 +850,23 @@ def run_prefill_bench(args):
     clocks = ClockSampler(None)
     clocks.start()
     time.sleep(0.3)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for i in range(K):
-        call(i)
-    b.record(stream)
-    torch.cuda.synchronize(dev)
+
+    def time_calls(fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(K):
+            fn(i)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / K * 1e-3
+
+    sec = time_calls(call)
+    split = None
+    if args.prefill_workload == "mixed":
+        split = mixed_split_timing(w, copies, fp8, ks, vs, time_calls, W)
+        split["mixed_ms"] = round(sec * 1e3, 4)
+        split["mixed_over_separate"] = round(sec * 1e3 / split["separate_ms"], 4)
     clk = clocks.stop()
-    sec = a.elapsed_time(b) / K * 1e-3
     flops = prefill_flops(w)
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -880,10 +892,61 @@ def run_prefill_bench(args):
                      "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "flops_per_call": flops,
                      "kv_bytes_per_call": kv_bytes,
                      "kv_gbs": round(kv_bytes / sec / 1e9, 1)},
-        "clocks": clk, "gpu_launches": K + W,
+        "clocks": clk, "gpu_launches": (K + W) * (1 if split is None else 4),
+        "separate_calls": split,
         "cpu_baseline": None if args.no_cpu_baseline else prefill_cpu_baseline(w, budget_s=10.0,
                                                                                fp8=fp8),
     }
+
+
+def mixed_split_timing(w, copies, fp8, ks, vs, time_calls, warmup):
+    """The mixed batch's two parts as separate calls on the same inputs: pa_prefill over the
+    chunk sequences only and pa_decode over the decode sequences only (their query rows are
+    contiguous after the chunks'), each timed over the same input rotation."""
+    import torch
+
+    import paged_kv_cache_158_gb300 as pa
+    ql = np.asarray(w.extra["q_lens"])
+    nch = int(np.sum(ql > 1))
+    assert np.all(ql[:nch] > 1) and np.all(ql[nch:] == 1), "chunks first, then decode rows"
+    qs = configs.query_start(w)
+    r0 = int(qs[nch])
+    max_q = int(ql[:nch].max())
+    dec_ctx = int(w.context_lens[nch:].max())
+    ws = [pa.decode_workspace(len(ql) - nch, w.num_heads, w.head_dim, dec_ctx) for _ in copies]
+    n = len(copies)
+
+    def chunks(i):
+        dv = copies[i % n]
+        args = (dv["out"][:r0], dv["query"][:r0], dv["key_cache"], dv["value_cache"],
+                dv["block_tables"][:nch], dv["context_lens"][:nch], dv["query_start"][:nch + 1],
+                w.scale)
+        if fp8:
+            pa.pa_prefill_fp8(*args, ks, vs, max_q)
+        else:
+            pa.pa_prefill(*args, max_q)
+
+    def decode(i):
+        dv = copies[i % n]
+        args = (dv["out"][r0:], dv["query"][r0:], dv["key_cache"], dv["value_cache"],
+                dv["block_tables"][nch:], dv["context_lens"][nch:], w.scale)
+        if fp8:
+            pa.pa_decode_fp8(*args, ks, vs, dec_ctx, ws[i % n])
+        else:
+            pa.pa_decode(*args, dec_ctx, ws[i % n])
+
+    for i in range(warmup):
+        chunks(i)
+        decode(i)
+    torch.cuda.synchronize()
+    t_c = time_calls(chunks)
+    t_d = time_calls(decode)
+    t_both = time_calls(lambda i: (chunks(i), decode(i)))
+    return {"chunk_sequences": nch, "decode_sequences": len(ql) - nch,
+            "prefill_chunks_ms": round(t_c * 1e3, 4), "decode_rows_ms": round(t_d * 1e3, 4),
+            "separate_ms": round(t_both * 1e3, 4),
+            "what": "pa_prefill over the chunk sequences then pa_decode over the decode "
+                    "sequences, back to back on one stream"}
 
 
 def prefill_cpu_baseline(w, budget_s: float, fp8: bool = False):

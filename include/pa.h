@@ -231,10 +231,14 @@ pa_status pa_copy_blocks(void* const* key_caches, void* const* value_caches, int
  * [0, num_blocks) reads zeros and is flagged PA_ERRBIT_BLOCK_ID.
  *
  * Supported: head_dim in {64, 128}, block_size in {8, 16, 32}, num_blocks *
- * num_heads * block_size < 2^31.  Runs on the tensor cores (tcgen05.mma,
- * fp16 operands, fp32 accumulation in tensor memory); the softmax weights
- * are rounded once to fp16 for the second product (the denominator sums them
- * in fp32 before rounding); the result is rounded once to fp16.
+ * num_heads * block_size < 2^31.  Chunks (q_len >= 2) run on the tensor
+ * cores (tcgen05.mma, fp16 operands, fp32 accumulation in tensor memory);
+ * one-token rows run in the same launch on CUDA cores, with the decode
+ * kernel's fp32 online softmax over the whole context.  The softmax weights
+ * are computed in fp32 and rounded once to fp16 for the second product (the
+ * denominator sums them in fp32); the result is rounded once to fp16.  The
+ * call allocates nothing; batches of more than 4096 sequences take one
+ * launch per 4096.
  */
 pa_status pa_prefill(void* out, const void* query, const void* key_cache, const void* value_cache,
                      const int32_t* block_tables, int max_blocks_per_seq,

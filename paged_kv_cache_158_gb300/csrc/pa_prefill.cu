@@ -49,6 +49,7 @@
 #include "pa_device.cuh"
 #include "pa_internal.h"
 #include "pa_launch.cuh"
+#include "pa_prefill_rows.cuh"
 #include "pa_umma.cuh"
 
 namespace pa {
@@ -68,9 +69,15 @@ struct PrefillTraits {
   static constexpr int OFF_K0 = 2 * QB;             // stage s: K at OFF_K0 + s*2*KB, V after it
   static constexpr int OFF_ST = OFF_K0 + 4 * KB;    // FP8 caches: K codes, then V codes
   static constexpr int OFF_BAR = OFF_ST + (F8 ? 2 * STB : 0);
-  // Barriers, TMEM slot and alignment slack; at least 120 KB so that one CTA
-  // holds an SM (each CTA allocates all 512 TMEM columns).
-  static constexpr int SMEM_USED = OFF_BAR + 256 + 1024;
+  // Decode rows: their rings use the Q and K/V stage area, their mbarriers
+  // (up to 12 warps x 4 stages) and softmax weights follow the barriers.
+  static constexpr int ROW_AREA = 2 * QB + 4 * KB;
+  static constexpr int OFF_RBAR = OFF_BAR + 256;
+  static constexpr int OFF_RPW = OFF_RBAR + prows::kRowWarps * 4 * 8;
+  // Barriers, TMEM slot, decode-row metadata and alignment slack; at least
+  // 120 KB so that one CTA holds an SM (each CTA allocates all 512 TMEM
+  // columns).
+  static constexpr int SMEM_USED = OFF_RPW + prows::kRowWarps * 16 * 4 + 1024;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   static_assert(SMEM <= 232448, "beyond the opt-in shared memory of one CTA");
   // Two softmax warpgroups and one producer warpgroup (its first warp issues
@@ -93,19 +100,26 @@ constexpr int kRegsProducer = 96;
 constexpr int kRegsSplit = 2 * 128 * kRegsSoftmax + 128 * kRegsProducer;
 static_assert(kRegsSplit <= 65536, "register split exceeds the register file");
 
+// Sequences per launch: the unit table of one launch lives in the Q area.
+constexpr int kSeqsPerLaunch = 4096;
+
 struct PrefillParams {
   void* out;                     // fp16 [TQ][H][D]
+  const void* query;             // fp16 [TQ][H][D] (decode rows read it directly)
+  const void* key_cache;         // caches (decode rows copy from them directly)
+  const void* value_cache;
   const int32_t* block_tables;   // [S][max_blocks]
   const int32_t* context_lens;   // [S]
   const int32_t* query_start;    // [S + 1]
   unsigned int* err;
-  int num_seqs;
+  int seq_begin;                 // first sequence of this launch
+  int num_seqs;                  // sequences of this launch
   int num_heads;
   int max_blocks;
   int num_blocks;
   int block_size;
-  int qpairs;                    // pairs of query tiles per sequence covered by the grid
-  int wave_groups;               // (sequence, head) groups whose pairs all start in the first wave
+  int qpairs;                    // most pairs of query tiles a sequence may need
+  int sms;                       // SM count (one CTA per SM)
   int max_query_len;             // host bound of the chunk lengths
   int oob_row;                   // a row coordinate past the cache (zero-filled loads)
   float scale_log2;              // scale * log2(e), times the key scale for FP8 caches
@@ -183,29 +197,11 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int H = a.num_heads;
-  // Grid order (one CTA per SM, CTAs start in index order).  The first
-  // wave_groups (sequence, head) groups come whole, their pairs adjacent and
-  // heaviest first: they run together and read the same K/V tiles, the
-  // later ones from L2.  The other groups follow rank by rank, every
-  // group's heaviest pair before any group's next one, so the heavy pairs
-  // start on the SMs that free first and the lighter ones trail their
-  // partners by a few tiles (K/V still in L2).
-  const int P = a.qpairs;
-  const int b = (int)blockIdx.x;
-  const int first = a.wave_groups * P;
-  int grp, pq;
-  if (b < first) {
-    grp = b / P;
-    pq = P - 1 - b % P;
-  } else {
-    const int rem = a.num_seqs * H - a.wave_groups;
-    grp = a.wave_groups + (b - first) % rem;
-    pq = P - 1 - (b - first) / rem;
-  }
-  const int h = grp % H;
-  const int s = grp / H;
-
-  if (tid == 0) {
+  // Set-up that does not depend on the unit runs beside the planning: warp 2
+  // initialises the tensor-core path's barriers and prefetches the tensor
+  // maps, warp 0 allocates the tensor memory (all CTAs; a decode row gives it
+  // back unused).
+  if (tid == 64) {
     mbar_init(bar(0), 1);
     mbar_init(bar(1), F8 ? 2 : 1);
     mbar_init(bar(2), F8 ? 2 : 1);
@@ -236,20 +232,88 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
     tmem_alloc(smem_u32(tmem_slot), T::TMEM_COLS);
     tmem_relinquish();
   }
+  // This CTA's unit (see pa_prefill_rows.cuh for the order), with its
+  // sequence's query rows and context length.  query_start and context_lens
+  // are inputs of the call, complete before its first kernel, so they are
+  // read before pdl_wait; the table and scratch live in the Q area until then.
+  // Up to 32 sequences: warp 1 alone; more: the whole block.
+  int* scratch = reinterpret_cast<int*>(sm) + kSeqsPerLaunch;
+  prows::Unit* unit_s = reinterpret_cast<prows::Unit*>(scratch + 20);
+  if (a.num_seqs <= 32) {
+    if (warp == 1)
+      prows::plan_small(a.query_start + a.seq_begin, a.context_lens + a.seq_begin, a.num_seqs, H,
+                        a.qpairs, a.sms, (int)blockIdx.x, unit_s, scratch + 19);
+  } else {
+    int tot = 0;
+    const prows::Unit u = prows::plan_unit_block(a.query_start + a.seq_begin,
+                                                 a.context_lens + a.seq_begin, a.num_seqs, H,
+                                                 a.qpairs, a.sms, (int)blockIdx.x,
+                                                 reinterpret_cast<int*>(sm), scratch, &tot);
+    if (tid == 0) {
+      *unit_s = u;
+      scratch[19] = tot;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const prows::Unit unit = *unit_s;
+  if (blockIdx.x == 0 && tid == 0 && scratch[19] > (int)gridDim.x)
+    atomicOr(a.err, PA_ERRBIT_CONTEXT);  // inconsistent query_start: units beyond the grid
+  if (unit.kind != 1) {
+    // No tensor-core work: a decode row runs on CUDA cores (after the wait,
+    // since it reads the caches); then the tensor memory goes back.
+    if (unit.kind == 2) {
+      pdl_wait();
+      pdl_launch_dependents();
+      const int s = a.seq_begin + unit.s, q_len = unit.q_len, c = unit.c;
+      const bool bad = q_len != 1 || c < 1 || c > a.max_blocks * a.block_size ||
+                       q_len > a.max_query_len;
+      if (bad && unit.h == 0 && tid == 0) atomicOr(a.err, PA_ERRBIT_CONTEXT);
+      if (!bad) {
+        const int32_t* bt = a.block_tables + (size_t)s * a.max_blocks;
+        uint64_t* dbars = reinterpret_cast<uint64_t*>(sm + T::OFF_RBAR);
+        float* pw = reinterpret_cast<float*>(sm + T::OFF_RPW);
+        if (tid == 0) {
+          for (int i = 0; i < prows::kRowWarps * 4; ++i) mbar_init(smem_u32(&dbars[i]), 1);
+          fence_mbar_init();
+        }
+        __syncthreads();
+        if (a.block_size == 8) {
+          constexpr int NST = prows::row_stages<D, 8, F8>(T::ROW_AREA);
+          prows::decode_row<D, 8, F8, NST>(a.query, a.key_cache, a.value_cache, bt, H,
+                                            a.block_size, a.num_blocks, a.scale_log2, a.v_scale,
+                                            a.err, a.out, unit.h, unit.q0, c, sm, dbars, pw, fail);
+        } else {
+          constexpr int NST = prows::row_stages<D, 16, F8>(T::ROW_AREA);
+          prows::decode_row<D, 16, F8, NST>(a.query, a.key_cache, a.value_cache, bt, H,
+                                             a.block_size, a.num_blocks, a.scale_log2, a.v_scale,
+                                             a.err, a.out, unit.h, unit.q0, c, sm, dbars, pw,
+                                             fail);
+        }
+      }
+    }
+    if (warp == 0) tmem_dealloc(tmem, T::TMEM_COLS);
+    return;
+  }
+  // The unit's values came through shared memory; a shuffle from lane 0 lets
+  // the compiler keep them in uniform registers (as values derived from
+  // blockIdx would be), which leaves the softmax warps their registers: read
+  // as plain per-thread values they cost the kernel 5 % in throughput.
+  const int s = __shfl_sync(kFullMask, a.seq_begin + unit.s, 0);
+  const int h = __shfl_sync(kFullMask, unit.h, 0);
+  const int pq = __shfl_sync(kFullMask, unit.pq, 0);
 
   pdl_wait();
   pdl_launch_dependents();
 
-  const int q0 = a.query_start[s];
-  const int q_len = a.query_start[s + 1] - q0;
-  const int c = a.context_lens[s];
+  const int q0 = __shfl_sync(kFullMask, unit.q0, 0);
+  const int q_len = __shfl_sync(kFullMask, unit.q_len, 0);
+  const int c = __shfl_sync(kFullMask, unit.c, 0);
   const bool bad = q_len < 0 || q_len > c || c > a.max_blocks * a.block_size ||
                    q_len > a.max_query_len;
-  if (bad && pq == a.qpairs - 1 && h == 0 && tid == 0) atomicOr(a.err, PA_ERRBIT_CONTEXT);
+  if (bad && pq == 0 && h == 0 && tid == 0) atomicOr(a.err, PA_ERRBIT_CONTEXT);
   QTile qx[2];
 #pragma unroll
   for (int x = 0; x < 2; ++x) {
@@ -706,11 +770,13 @@ cudaError_t launch_prefill_t(const PrefillArgs& g, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   PrefillParams p{};
   p.out = g.out;
+  p.query = g.query;
+  p.key_cache = g.key_cache;
+  p.value_cache = g.value_cache;
   p.block_tables = g.block_tables;
   p.context_lens = g.context_lens;
   p.query_start = g.query_start;
   p.err = g.err;
-  p.num_seqs = g.num_seqs;
   p.num_heads = g.num_heads;
   p.max_blocks = g.max_blocks;
   p.num_blocks = g.num_blocks;
@@ -721,17 +787,29 @@ cudaError_t launch_prefill_t(const PrefillArgs& g, cudaStream_t stream) {
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return cudaErrorInvalidValue;
-    const long long groups = (long long)g.num_seqs * g.num_heads;
-    const long long whole = sms / p.qpairs;  // one CTA per SM
-    p.wave_groups = (int)(whole < groups ? whole : groups);
+    p.sms = sms;
   }
   p.max_query_len = g.max_query_len;
   p.oob_row = (int)rows;
   p.scale_log2 = g.scale_log2;
   p.v_scale = F8 ? g.v_scale : 1.f;
-  const long long grid = (long long)g.num_seqs * p.qpairs * g.num_heads;
-  return launch_pdl(prefill_kernel<D, F8>, dim3((unsigned)grid), dim3(T::THREADS), (size_t)T::SMEM,
-                    stream, tq, tk, tv, p);
+  // One launch per window of sequences.  The grid bounds the window's units:
+  // a sequence of q tokens needs ceil(q / 256) units per head, at most qpairs,
+  // and over the window sum(ceil(q / 256)) <= (TQ + 255 * n) / 256.
+  for (int sb = 0; sb < g.num_seqs; sb += kSeqsPerLaunch) {
+    const int n = g.num_seqs - sb < kSeqsPerLaunch ? g.num_seqs - sb : kSeqsPerLaunch;
+    p.seq_begin = sb;
+    p.num_seqs = n;
+    long long per_head = (long long)n * p.qpairs;
+    const long long by_tokens = ((long long)g.num_query_tokens + 255LL * n) / 256;
+    if (by_tokens < per_head) per_head = by_tokens;
+    const long long grid = per_head * g.num_heads;
+    if (grid <= 0) continue;
+    const cudaError_t e = launch_pdl(prefill_kernel<D, F8>, dim3((unsigned)grid),
+                                     dim3(T::THREADS), (size_t)T::SMEM, stream, tq, tk, tv, p);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace

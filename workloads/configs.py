@@ -252,6 +252,17 @@ def prefill_7b() -> Workload:
                             [512] * 4, [2048] * 4, 32, 128, 16, spare_blocks=0, cid=6)
 
 
+def prefill_7b_mixed() -> Workload:
+    """LLaMA-7B-shaped mixed batch: 2 sequences with a 512-token chunk after a 1536-token
+    cached prefix (context 2048) and 64 decode sequences (one new token each, contexts
+    U{512..2048}), H32 D128 B16."""
+    d = synth.Draws(SEED_BASE + 7)
+    dec_ctx = [d.integer(512, 2048) for _ in range(64)]
+    return prefill_workload("p2_mixed_S66_H32_D128_B16_q2x512_64x1", SEED_BASE + 7,
+                            [512] * 2 + [1] * 64, [2048] * 2 + dec_ctx, 32, 128, 16,
+                            spare_blocks=0, cid=7)
+
+
 def fp8_scales(w: Workload) -> tuple[float, float]:
     """Per-tensor scales (k_scale, v_scale) of a workload's FP8 caches: about
     1/70 and 1/84 of the values' standard deviation, so that values up to
