@@ -264,10 +264,11 @@ class Step:
         self.max_parts = -(-self.max_ctx // self.partition_tokens)
 
     def launches_per_step(self) -> int:
-        """Library kernels per step: slot map; per layer the cache write, the
-        work-counter init, the partition pass and (with several partitions) the merge."""
+        """Library kernels per step: slot map; per layer the cache write, the partition pass
+        and (with several partitions) the merge (the step's workspace stays zeroed, so no
+        work-counter init)."""
         L = len(self.dw.layers)
-        per_layer = 3 + (1 if self.max_parts > 1 else 0)
+        per_layer = 2 + (1 if self.max_parts > 1 else 0)
         return 1 + L * per_layer + (1 if self.copy_pairs is not None else 0)
 
 
@@ -408,7 +409,7 @@ def measure_step(args, w, fp8: bool, device, world):
         "roofline": {
             "bound": "hbm",
             "kernel": ("pa_decode_fp8" if fp8 else "pa_decode") +
-                      " (work-counter init + partition + merge kernels; CUDA events "
+                      " (partition + merge kernels, workspace kept zeroed; CUDA events "
                       "bracket each call in the eager pass)",
             "achieved": round(achieved, 2),
             "peak": peak,

@@ -89,9 +89,10 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int m
  *   max_context_len  host-side upper bound of context_lens (sizes the launch;
  *                  a larger c_s is clipped and flagged PA_ERRBIT_CONTEXT)
  *   workspace      device scratch of at least pa_decode_workspace_size(...)
- *                  bytes, 16-byte aligned; contents on entry are ignored and
- *                  undefined on exit.  Calls that share one workspace must
- *                  not overlap on the GPU.
+ *                  bytes, 16-byte aligned; contents on entry are ignored (its
+ *                  work counters are zeroed first) and on exit the counters
+ *                  are zero and the rest undefined (see pa_decode_ex).  Calls
+ *                  that share one workspace must not overlap on the GPU.
  *
  * Arithmetic: fp16 inputs, fp32 dot products, online softmax and
  * accumulation; the result is rounded once to fp16 (nearest even).  The
@@ -104,6 +105,28 @@ pa_status pa_decode(void* out, const void* query, const void* key_cache, const v
                     const int32_t* context_lens, int num_seqs, int num_heads, int head_dim,
                     int block_size, int num_blocks, float scale, int max_context_len,
                     void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_decode with flags.  With flags == 0 it is pa_decode.
+ *
+ * PA_DECODE_ZEROED_WORKSPACE: the workspace's work counters are zero when
+ * the call starts, so the call launches no kernel to zero them (one kernel
+ * fewer on each layer's dependency chain: 1.9 % on the 13B-shaped decode
+ * step).  Every call leaves the counters zero, whatever its flags, so the
+ * flag holds for a workspace that was zero-filled once before its first call
+ * (e.g. cudaMemsetAsync) and since then only passed to pa_decode* calls.  A
+ * call that timed out (PA_ERR_TIMEOUT) leaves them zero as well; a workspace
+ * whose bytes anything else wrote must be zero-filled again.  Counters that
+ * are not zero make the call skip or repeat work without any report.
+ * Not part of the pages; a launch-latency option.
+ */
+#define PA_DECODE_ZEROED_WORKSPACE 1u
+pa_status pa_decode_ex(void* out, const void* query, const void* key_cache, const void* value_cache,
+                       const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* context_lens, int num_seqs, int num_heads, int head_dim,
+                       int block_size, int num_blocks, float scale, int max_context_len,
+                       void* workspace, size_t workspace_bytes, unsigned int flags,
+                       pa_stream_t stream);
 
 /* Size of the fixed scratch area pa_decode_noalloc uses (32 MiB per device). */
 #define PA_DECODE_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
@@ -354,6 +377,15 @@ pa_status pa_decode_fp8(void* out, const void* query, const void* key_cache,
                         int num_heads, int head_dim, int block_size, int num_blocks, float scale,
                         float k_scale, float v_scale, int max_context_len, void* workspace,
                         size_t workspace_bytes, pa_stream_t stream);
+
+/* pa_decode_fp8 with flags (see pa_decode_ex). */
+pa_status pa_decode_fp8_ex(void* out, const void* query, const void* key_cache,
+                           const void* value_cache, const int32_t* block_tables,
+                           int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                           int num_heads, int head_dim, int block_size, int num_blocks,
+                           float scale, float k_scale, float v_scale, int max_context_len,
+                           void* workspace, size_t workspace_bytes, unsigned int flags,
+                           pa_stream_t stream);
 
 /*
  * Converts a whole fp16 buffer to E4M3 codes element by element with the

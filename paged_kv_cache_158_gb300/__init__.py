@@ -29,6 +29,9 @@ _lib.pa_decode_workspace_size.restype = _sz
 _lib.pa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                            ctypes.c_float, _i32, _vp, _sz, _vp]
 _lib.pa_decode.restype = _i32
+_lib.pa_decode_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                              ctypes.c_float, _i32, _vp, _sz, ctypes.c_uint, _vp]
+_lib.pa_decode_ex.restype = _i32
 _lib.pa_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                    ctypes.c_float, _i32, _vp]
 _lib.pa_decode_noalloc.restype = _i32
@@ -52,6 +55,9 @@ _f32 = ctypes.c_float
 _lib.pa_decode_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                _f32, _f32, _f32, _i32, _vp, _sz, _vp]
 _lib.pa_decode_fp8.restype = _i32
+_lib.pa_decode_fp8_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                                  _f32, _f32, _f32, _i32, _vp, _sz, ctypes.c_uint, _vp]
+_lib.pa_decode_fp8_ex.restype = _i32
 _lib.pa_reshape_and_cache_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                           _f32, _f32, _vp]
 _lib.pa_reshape_and_cache_fp8.restype = _i32
@@ -71,6 +77,7 @@ _lib.pa_copy_blocks_fp8.restype = _i32
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_OUT_OF_RANGE, PA_ERR_TIMEOUT = range(6)
 PA_ERRBIT_BLOCK_ID, PA_ERRBIT_CONTEXT, PA_ERRBIT_SLOT = 0x1, 0x2, 0x4
 PA_ERRBIT_COPY, PA_ERRBIT_TOKEN, PA_ERRBIT_TIMEOUT = 0x8, 0x10, 0x20
+PA_DECODE_ZEROED_WORKSPACE = 0x1
 
 
 class PAError(RuntimeError):
@@ -133,9 +140,10 @@ def pa_decode_set_partition_tokens(tokens: int) -> None:
 
 def decode_workspace(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,
                      device=None) -> torch.Tensor:
-    """A device byte buffer of pa_decode_workspace_size(...) bytes (allocated by torch)."""
+    """A zero-filled device byte buffer of pa_decode_workspace_size(...) bytes (allocated by
+    torch), so it may be passed with PA_DECODE_ZEROED_WORKSPACE (see pa_decode_ex)."""
     n = pa_decode_workspace_size(num_seqs, num_heads, head_dim, max_context_len)
-    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
 
 
 def _decode_shapes(out, query, key_cache, value_cache, block_tables, context_lens):
@@ -163,6 +171,23 @@ def pa_decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
                         float(scale), int(max_context_len), _ptr(workspace, "workspace", torch.uint8),
                         workspace.numel(), _stream(stream))
     _check(st, "pa_decode")
+
+
+def pa_decode_ex(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                 value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                 scale: float, max_context_len: int, workspace: torch.Tensor, flags: int = 0,
+                 stream=None) -> None:
+    """pa_decode with flags (PA_DECODE_ZEROED_WORKSPACE; see pa_decode_ex in include/pa.h)."""
+    S, H, D, B, NB = _decode_shapes(out, query, key_cache, value_cache, block_tables, context_lens)
+    st = _lib.pa_decode_ex(_ptr(out, "out", torch.float16), _ptr(query, "query", torch.float16),
+                           _ptr(key_cache, "key_cache", torch.float16),
+                           _ptr(value_cache, "value_cache", torch.float16),
+                           _ptr(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+                           _ptr(context_lens, "context_lens", torch.int32), S, H, D, B, NB,
+                           float(scale), int(max_context_len),
+                           _ptr(workspace, "workspace", torch.uint8), workspace.numel(), int(flags),
+                           _stream(stream))
+    _check(st, "pa_decode_ex")
 
 
 def pa_decode_noalloc(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
@@ -196,6 +221,25 @@ def pa_decode_fp8(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tenso
                             _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
                             _stream(stream))
     _check(st, "pa_decode_fp8")
+
+
+def pa_decode_fp8_ex(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                     value_cache: torch.Tensor, block_tables: torch.Tensor,
+                     context_lens: torch.Tensor, scale: float, k_scale: float, v_scale: float,
+                     max_context_len: int, workspace: torch.Tensor, flags: int = 0,
+                     stream=None) -> None:
+    """pa_decode_fp8 with flags (see pa_decode_ex)."""
+    S, H, D, B, NB = _decode_shapes(out, query, key_cache, value_cache, block_tables, context_lens)
+    st = _lib.pa_decode_fp8_ex(_ptr(out, "out", torch.float16), _ptr(query, "query", torch.float16),
+                               _cache_ptr(key_cache, "key_cache", True),
+                               _cache_ptr(value_cache, "value_cache", True),
+                               _ptr(block_tables, "block_tables", torch.int32),
+                               block_tables.shape[1],
+                               _ptr(context_lens, "context_lens", torch.int32), S, H, D, B, NB,
+                               float(scale), float(k_scale), float(v_scale), int(max_context_len),
+                               _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
+                               int(flags), _stream(stream))
+    _check(st, "pa_decode_fp8_ex")
 
 
 def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
@@ -381,7 +425,8 @@ __all__ = [
     "pa_decode", "pa_reshape_and_cache", "pa_copy_blocks", "pa_slot_mapping", "pa_check_errors",
     "pa_selftest_wait_timeout",
     "pa_decode_fp8", "pa_reshape_and_cache_fp8", "pa_copy_blocks_fp8", "pa_convert_cache_fp8",
-    "pa_swap_blocks", "pa_prefill", "pa_prefill_fp8", "pa_decode_noalloc",
+    "pa_swap_blocks", "pa_prefill", "pa_prefill_fp8", "pa_decode_noalloc", "pa_decode_ex",
+    "pa_decode_fp8_ex",
     "pa_status_string", "pa_decode_workspace_size", "pa_decode_partition_tokens",
     "pa_decode_set_partition_tokens", "decode_workspace", "raise_on_device_errors", "PAError",
 ]

@@ -219,8 +219,9 @@ pa_status decode_impl(bool fp8, void* out, const void* query, const void* key_ca
                       int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
                       int num_heads, int head_dim, int block_size, int num_blocks, float scale,
                       float k_scale, float v_scale, int max_context_len, void* workspace,
-                      size_t workspace_bytes, pa_stream_t stream) {
+                      size_t workspace_bytes, unsigned int flags, pa_stream_t stream) {
   if (!head_dim_ok(head_dim) || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+  if (flags & ~PA_DECODE_ZEROED_WORKSPACE) return PA_ERR_INVALID_ARG;
   if (num_seqs < 0 || num_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 ||
       max_context_len < 0)
     return PA_ERR_INVALID_ARG;
@@ -259,8 +260,12 @@ pa_status decode_impl(bool fp8, void* out, const void* query, const void* key_ca
   p.scale_log2 = (float)((double)scale * (double)k_scale * 1.4426950408889634073599246810019);
   p.v_scale = v_scale;
 
+  // The kernels leave the counters zero; a caller that keeps them so skips the
+  // zeroing kernel.
   unsigned int* counters = reinterpret_cast<unsigned int*>(ws + w.counters_off);
-  if (pa::launch_zero_words(counters, (int)(w.zero_bytes / 4), cs) != cudaSuccess) return PA_ERR_CUDA;
+  if (!(flags & PA_DECODE_ZEROED_WORKSPACE) &&
+      pa::launch_zero_words(counters, (int)(w.zero_bytes / 4), cs) != cudaSuccess)
+    return PA_ERR_CUDA;
   for (int b = 0; b < w.launches; ++b) {
     p.seq_begin = b * pa::kMaxSeqsPerLaunch;
     p.num_seqs = num_seqs - p.seq_begin < pa::kMaxSeqsPerLaunch ? num_seqs - p.seq_begin
@@ -353,7 +358,18 @@ pa_status pa_decode(void* out, const void* query, const void* key_cache, const v
                     void* workspace, size_t workspace_bytes, pa_stream_t stream) {
   return decode_impl(false, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
                      context_lens, num_seqs, num_heads, head_dim, block_size, num_blocks, scale,
-                     1.f, 1.f, max_context_len, workspace, workspace_bytes, stream);
+                     1.f, 1.f, max_context_len, workspace, workspace_bytes, 0u, stream);
+}
+
+pa_status pa_decode_ex(void* out, const void* query, const void* key_cache,
+                       const void* value_cache, const int32_t* block_tables,
+                       int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                       int num_heads, int head_dim, int block_size, int num_blocks, float scale,
+                       int max_context_len, void* workspace, size_t workspace_bytes,
+                       unsigned int flags, pa_stream_t stream) {
+  return decode_impl(false, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_heads, head_dim, block_size, num_blocks, scale,
+                     1.f, 1.f, max_context_len, workspace, workspace_bytes, flags, stream);
 }
 
 pa_status pa_decode_fp8(void* out, const void* query, const void* key_cache,
@@ -365,7 +381,20 @@ pa_status pa_decode_fp8(void* out, const void* query, const void* key_cache,
   if (!scale_ok(k_scale) || !scale_ok(v_scale)) return PA_ERR_INVALID_ARG;
   return decode_impl(true, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
                      context_lens, num_seqs, num_heads, head_dim, block_size, num_blocks, scale,
-                     k_scale, v_scale, max_context_len, workspace, workspace_bytes, stream);
+                     k_scale, v_scale, max_context_len, workspace, workspace_bytes, 0u, stream);
+}
+
+pa_status pa_decode_fp8_ex(void* out, const void* query, const void* key_cache,
+                           const void* value_cache, const int32_t* block_tables,
+                           int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                           int num_heads, int head_dim, int block_size, int num_blocks,
+                           float scale, float k_scale, float v_scale, int max_context_len,
+                           void* workspace, size_t workspace_bytes, unsigned int flags,
+                           pa_stream_t stream) {
+  if (!scale_ok(k_scale) || !scale_ok(v_scale)) return PA_ERR_INVALID_ARG;
+  return decode_impl(true, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_heads, head_dim, block_size, num_blocks, scale,
+                     k_scale, v_scale, max_context_len, workspace, workspace_bytes, flags, stream);
 }
 
 pa_status pa_reshape_and_cache(const void* key, const void* value, void* key_cache,

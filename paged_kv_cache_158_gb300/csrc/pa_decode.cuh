@@ -488,7 +488,17 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
   uint32_t ph_c = 0;
   pdl_wait();
   pdl_launch_dependents();
-  if (tid == 0) misc[1] = (int)(gridDim.x + atomicAdd(a.counter, 1u));
+  // Fetches from the work counter.  Every CTA with a first item fetches once
+  // before its loop and once per item it runs, so a launch makes exactly
+  // min(grid, total) + total fetches; the one that gets the last value puts
+  // the counter back to zero for the next call.
+  const unsigned last_fetch = (unsigned)(min((int)gridDim.x, total) + total - 1);
+  auto fetch = [&]() {
+    const unsigned v = atomicAdd(a.counter, 1u);
+    if (v == last_fetch) atomicExch(a.counter, 0u);
+    return (int)(gridDim.x + v);
+  };
+  if (tid == 0) misc[1] = fetch();
   __syncthreads();
   int nxt = misc[1];
 
@@ -503,7 +513,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
       for (int i = tid; i < nx.nblk; i += T::THREADS) cp_async_4(dst + i, row + nx.blk0 + i);
     }
     cp_async_commit();
-    if (tid == 0) misc[2 + (iter & 1)] = (int)(gridDim.x + atomicAdd(a.counter, 1u));
+    if (tid == 0) misc[2 + (iter & 1)] = fetch();
 
     const int* bt = bt_s + buf * bt_cap;
     const size_t sh = (size_t)(a.seq_begin + it.s) * H + it.h;
@@ -658,6 +668,16 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
       }
     }
     if (misc[8] != 0 || !has_next) {
+      // A CTA that gave up still makes the fetches it would have made (the
+      // items it skips are lost and the call reports the timeout), so the
+      // counter comes back to zero.
+      if (misc[8] != 0 && tid == 0) {
+        int n1 = nxt, n2 = misc[2 + (iter & 1)];
+        while (n1 < total) {
+          n1 = n2;
+          n2 = fetch();
+        }
+      }
       // No copy of this warp may still be in flight when the CTA exits.
       for (uint32_t g = u; g < iss; ++g)
         mbar_wait_bounded(smem_u32(&my_bars[g % T::NST]), (g / T::NST) & 1);

@@ -39,8 +39,9 @@ from __future__ import annotations
 
 import torch
 
-from . import (decode_workspace, pa_copy_blocks, pa_copy_blocks_fp8, pa_decode, pa_decode_fp8,
-               pa_reshape_and_cache, pa_reshape_and_cache_fp8, pa_slot_mapping)
+from . import (PA_DECODE_ZEROED_WORKSPACE, decode_workspace, pa_copy_blocks, pa_copy_blocks_fp8,
+               pa_decode_ex, pa_decode_fp8_ex, pa_reshape_and_cache, pa_reshape_and_cache_fp8,
+               pa_slot_mapping)
 
 
 def _pow2_groups(n: int) -> list[tuple[int, int]]:
@@ -186,16 +187,19 @@ class DecodeStep:
                                  self.value_caches[i], self.slots, s)
 
     def _decode(self, i: int, s) -> None:
-        """Layer i's paged decode."""
+        """Layer i's paged decode.  The step's workspace is zero-filled at construction and
+        only ever passed to the decode calls, which leave its counters zero, so no call needs
+        to zero them first (PA_DECODE_ZEROED_WORKSPACE)."""
         f8 = self.fp8_scales
+        fl = PA_DECODE_ZEROED_WORKSPACE
         if f8:
-            pa_decode_fp8(self.outs[i], self.queries[i], self.key_caches[i], self.value_caches[i],
-                          self.block_tables, self.context_lens, self.scale, f8[0], f8[1],
-                          self.max_context_len, self.workspace, s)
+            pa_decode_fp8_ex(self.outs[i], self.queries[i], self.key_caches[i],
+                             self.value_caches[i], self.block_tables, self.context_lens, self.scale,
+                             f8[0], f8[1], self.max_context_len, self.workspace, fl, s)
         else:
-            pa_decode(self.outs[i], self.queries[i], self.key_caches[i], self.value_caches[i],
-                      self.block_tables, self.context_lens, self.scale, self.max_context_len,
-                      self.workspace, s)
+            pa_decode_ex(self.outs[i], self.queries[i], self.key_caches[i], self.value_caches[i],
+                         self.block_tables, self.context_lens, self.scale, self.max_context_len,
+                         self.workspace, fl, s)
 
     def capture(self, warmup: int = 2, host: bool = False) -> None:
         """Warm up (eager runs), then capture one step into a CUDA graph; with host=True the

@@ -249,3 +249,48 @@ def test_bounded_wait_gives_up_and_reports_timeout():
     assert rc == 0
     decode_gate(out, ref64, "decode after a timed-out wait")
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("part", [0, 32])
+def test_zeroed_workspace_flag_matches_default_and_keeps_counters_zero(part, fp8):
+    """PA_DECODE_ZEROED_WORKSPACE: five calls in a row on one zero-filled
+    workspace (1100 sequences: two launches, two work counters) give the same
+    bits as the default call, and every call leaves the counters zero."""
+    from pa_testlib import materialize_fp8
+    pa.pa_decode_set_partition_tokens(part)
+    w = configs.small_random(5400 + part + fp8, 1100, 2, 128, 16, 200, min_context=0)
+    dw = materialize_fp8(w) if fp8 else gpu.materialize(w, device=DEV)
+    ks, vs = configs.fp8_scales(w)
+    ws = pa.decode_workspace(w.num_seqs, w.num_heads, w.head_dim, w.max_context_len)
+    ws_ref = pa.decode_workspace(w.num_seqs, w.num_heads, w.head_dim, w.max_context_len)
+    args = (dw.queries[0], dw.key_caches[0], dw.value_caches[0], dw.block_tables, dw.context_lens,
+            w.scale)
+    ref = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=DEV)
+    if fp8:
+        pa.pa_decode_fp8(ref, *args, ks, vs, w.max_context_len, ws_ref)
+    else:
+        pa.pa_decode(ref, *args, w.max_context_len, ws_ref)
+    for _ in range(5):
+        out = torch.full_like(ref, float("nan"))
+        if fp8:
+            pa.pa_decode_fp8_ex(out, *args, ks, vs, w.max_context_len, ws,
+                                pa.PA_DECODE_ZEROED_WORKSPACE)
+        else:
+            pa.pa_decode_ex(out, *args, w.max_context_len, ws, pa.PA_DECODE_ZEROED_WORKSPACE)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+        assert int(ws[:8].view(torch.int32).abs().sum()) == 0    # both launches' counters
+    assert int(ws_ref[:8].view(torch.int32).abs().sum()) == 0
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+def test_decode_ex_refuses_unknown_flags():
+    w = configs.small_random(5500, 3, 2, 64, 16, 40)
+    dw = gpu.materialize(w, device=DEV)
+    ws = pa.decode_workspace(w.num_seqs, w.num_heads, w.head_dim, w.max_context_len)
+    out = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=DEV)
+    with pytest.raises(pa.PAError) as e:
+        pa.pa_decode_ex(out, dw.queries[0], dw.key_caches[0], dw.value_caches[0], dw.block_tables,
+                        dw.context_lens, w.scale, w.max_context_len, ws, 0x2)
+    assert e.value.status == pa.PA_ERR_INVALID_ARG
