@@ -1,8 +1,11 @@
 """Benchmark of the paged decode hot path on GB300.
 
-One step = one decode step of the workload through the library: the slot
-map of the new tokens, then for every layer the cache write of the new
-tokens and the paged decode (partition pass + merge).  The headline metric
+One step = one decode step of the workload through the library: for every
+layer the cache write of the new tokens and the paged decode (partition pass
++ merge).  When every sequence brings one new token at position c - 1 (all
+decode workloads but the shared-prefix one) the write is fused into the
+decode (pa_decode_append); otherwise, and with --no-append, the step runs the
+slot map and a cache-write kernel before each decode.  The headline metric
 is paged-decode KV GB/s: algorithmic bytes of all decode calls of the step
 (q + the gathered K/V of the c_s live tokens + out + block-table entries and
 context lengths) over the step time; also reported as % of the measured HBM
@@ -62,6 +65,9 @@ def parse_args():
     ap.add_argument("--prefill-workload", choices=["chunked", "mixed"], default="chunked",
                     help="--op prefill: 4 x 512-token chunks (chunked) or 2 chunks plus 64 decode "
                          "rows in one call (mixed; also timed as separate prefill and decode calls)")
+    ap.add_argument("--no-append", action="store_true",
+                    help="run the cache write as its own kernel (slot map + pa_reshape_and_cache) "
+                         "instead of fused into the decode")
     ap.add_argument("--also", default="c5",
                     help="comma-separated workloads measured after the main one in the same run "
                          "(single GPU only; 'none' to skip); each gets its own record under 'also'")
@@ -221,7 +227,7 @@ def weak_scaling_value(bytes_per_rank_step: int, world: int, ms_per_step_max: fl
 class Step:
     """Device state of the workload and its decode step (the library's DecodeStep)."""
 
-    def __init__(self, w, device, fp8: bool = False):
+    def __init__(self, w, device, fp8: bool = False, append: bool = True):
         import torch
 
         import paged_kv_cache_158_gb300 as pa
@@ -253,10 +259,13 @@ class Step:
         self.max_ctx = int(self.ctx_host.max())
         outs = [torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=device)
                 for _ in dw.layers]
+        # One new token per sequence at position c - 1 (every decode workload but the shared
+        # prefix one, which writes whole suffixes): the cache write rides in the decode.
+        self.append = append and copy_pairs is None and bool(np.all(w.context_lens > 0))
         self.step = DecodeStep(dw.key_caches, dw.value_caches, dw.queries, dw.keys_new, dw.values_new,
                                outs, dw.block_tables, dw.context_lens, dw.token_seq, dw.token_pos,
                                w.block_size, w.num_blocks, w.scale, self.max_ctx, copy_pairs,
-                               self.fp8_scales)
+                               self.fp8_scales, append=self.append)
         self.outs = outs
         self.copy_pairs = copy_pairs
         self.bytes_per_decode = decode_bytes(w, self.bt_host, self.ctx_host, 1 if fp8 else 2)
@@ -266,8 +275,11 @@ class Step:
     def launches_per_step(self) -> int:
         """Library kernels per step: slot map; per layer the cache write, the partition pass
         and (with several partitions) the merge (the step's workspace stays zeroed, so no
-        work-counter init)."""
+        work-counter init).  With the cache write fused into the decode: per layer the
+        partition pass and the merge only."""
         L = len(self.dw.layers)
+        if self.append:
+            return L * (1 + (1 if self.max_parts > 1 else 0))
         per_layer = 2 + (1 if self.max_parts > 1 else 0)
         return 1 + L * per_layer + (1 if self.copy_pairs is not None else 0)
 
@@ -318,7 +330,7 @@ def measure_step(args, w, fp8: bool, device, world):
 
     import paged_kv_cache_158_gb300 as pa
 
-    st = Step(w, device, fp8)
+    st = Step(w, device, fp8, append=not args.no_append)
     L = len(st.dw.layers)
     stream = torch.cuda.current_stream(device)
     for _ in range(args.warmup):
@@ -397,6 +409,8 @@ def measure_step(args, w, fp8: bool, device, world):
                    "timed); steps timed one by one with CUDA events"),
             "kv_pool_gb": round(w.pool_bytes_all_layers() / (2 if fp8 else 1) / 1e9, 3),
             "cuda_graph": ms_graph is not None,
+            "cache_write": ("fused into the decode (pa_decode_append)" if st.append else
+                            "slot map + pa_reshape_and_cache before each decode"),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
@@ -408,9 +422,12 @@ def measure_step(args, w, fp8: bool, device, world):
                   "ms_per_step": round(ms_eager / K, 4)},
         "roofline": {
             "bound": "hbm",
-            "kernel": ("pa_decode_fp8" if fp8 else "pa_decode") +
-                      " (partition + merge kernels, workspace kept zeroed; CUDA events "
-                      "bracket each call in the eager pass)",
+            "kernel": ("pa_decode_append" if st.append else "pa_decode") + ("_fp8" if fp8 else "") +
+                      (" (partition kernel with the new token's cache write fused in, + merge;"
+                       if st.append else " (partition + merge kernels;") +
+                      " workspace kept zeroed; CUDA events bracket each call in the eager pass;"
+                      " bytes are the decode's alone: the 4*S*H*D*elem of the fused write are"
+                      " not counted)",
             "achieved": round(achieved, 2),
             "peak": peak,
             "peak_kind": peak_kind,

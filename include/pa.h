@@ -118,15 +118,64 @@ pa_status pa_decode(void* out, const void* query, const void* key_cache, const v
  * call that timed out (PA_ERR_TIMEOUT) leaves them zero as well; a workspace
  * whose bytes anything else wrote must be zero-filled again.  Counters that
  * are not zero make the call skip or repeat work without any report.
- * Not part of the pages; a launch-latency option.
+ * The call's first kernel is then the decode itself, which may start while
+ * the kernel enqueued just before the call still runs (programmatic launch):
+ * it waits for that kernel before it reads any input, unless
+ * PA_DECODE_INPUTS_READY is passed as well.
+ *
+ * PA_DECODE_INPUTS_READY (with PA_DECODE_ZEROED_WORKSPACE; alone it changes
+ * nothing): the kernel enqueued on the stream just before this call writes
+ * none of the call's inputs (query, caches, block tables, context lengths,
+ * and for pa_decode_append the new keys and values).  The decode then reads
+ * its context lengths, the first block-table slices and the first cache
+ * chunks while that kernel finishes, instead of after it; the results are
+ * written only after it has ended.  A preceding kernel that does write an
+ * input (a cache write, a block copy or swap-in, a kernel producing the
+ * queries) makes the call read stale values without any report.  The
+ * library's decode step passes it for every layer but the first when the
+ * cache write is fused in (the kernel before layer i's decode is then layer
+ * i - 1's decode): 1 % on the 13B-shaped step.
+ * Not part of the pages; launch-latency options.
  */
 #define PA_DECODE_ZEROED_WORKSPACE 1u
+#define PA_DECODE_INPUTS_READY 2u
 pa_status pa_decode_ex(void* out, const void* query, const void* key_cache, const void* value_cache,
                        const int32_t* block_tables, int max_blocks_per_seq,
                        const int32_t* context_lens, int num_seqs, int num_heads, int head_dim,
                        int block_size, int num_blocks, float scale, int max_context_len,
                        void* workspace, size_t workspace_bytes, unsigned int flags,
                        pa_stream_t stream);
+
+/*
+ * The decode step of one layer in one call: the cache write of each
+ * sequence's new token [P1 §3.2: the new token's K/V go to slot
+ * block*B + offset of its block; P3 §2.3] fused into pa_decode_ex.  For every
+ * sequence s with c_s = context_lens[s] >= 1 the new token is the one at
+ * position c_s - 1:
+ *
+ *   key_cache[block_tables[s][(c_s-1) / B]][h][(c_s-1) % B][:] = key_new[s][h][:]   (same for V)
+ *
+ * and the decode over [0, c_s) then uses it.  Result and cache contents are
+ * bit-identical to pa_slot_mapping + pa_reshape_and_cache of those rows (the
+ * token of sequence s at position c_s - 1) followed by pa_decode_ex, with one
+ * kernel fewer on the layer's dependency chain.
+ *
+ *   key_new,
+ *   value_new      fp16 [num_seqs][num_heads][head_dim], 16-byte aligned
+ *   key_cache,
+ *   value_cache    written (one row per (sequence, head)); otherwise as for
+ *                  pa_decode_ex, as are the other arguments and flags
+ * A sequence with c_s == 0 writes nothing.  A sequence whose c_s is clipped
+ * (past its table or max_context_len; PA_ERRBIT_CONTEXT) or whose block for
+ * position c_s - 1 is out of range (PA_ERRBIT_BLOCK_ID) writes nothing.
+ */
+pa_status pa_decode_append(void* out, const void* query, const void* key_new,
+                           const void* value_new, void* key_cache, void* value_cache,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, int num_seqs, int num_heads, int head_dim,
+                           int block_size, int num_blocks, float scale, int max_context_len,
+                           void* workspace, size_t workspace_bytes, unsigned int flags,
+                           pa_stream_t stream);
 
 /* Size of the fixed scratch area pa_decode_noalloc uses (32 MiB per device). */
 #define PA_DECODE_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
@@ -377,6 +426,20 @@ pa_status pa_decode_fp8(void* out, const void* query, const void* key_cache,
                         int num_heads, int head_dim, int block_size, int num_blocks, float scale,
                         float k_scale, float v_scale, int max_context_len, void* workspace,
                         size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_decode_append over FP8 caches: the new rows are quantised as
+ * pa_reshape_and_cache_fp8 quantises them (k_scale for keys, v_scale for
+ * values; bit-identical codes) and the decode is pa_decode_fp8_ex's.
+ */
+pa_status pa_decode_append_fp8(void* out, const void* query, const void* key_new,
+                               const void* value_new, void* key_cache, void* value_cache,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int num_seqs, int num_heads,
+                               int head_dim, int block_size, int num_blocks, float scale,
+                               float k_scale, float v_scale, int max_context_len,
+                               void* workspace, size_t workspace_bytes, unsigned int flags,
+                               pa_stream_t stream);
 
 /* pa_decode_fp8 with flags (see pa_decode_ex). */
 pa_status pa_decode_fp8_ex(void* out, const void* query, const void* key_cache,

@@ -32,6 +32,9 @@ _lib.pa_decode.restype = _i32
 _lib.pa_decode_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                               ctypes.c_float, _i32, _vp, _sz, ctypes.c_uint, _vp]
 _lib.pa_decode_ex.restype = _i32
+_lib.pa_decode_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                                  _i32, ctypes.c_float, _i32, _vp, _sz, ctypes.c_uint, _vp]
+_lib.pa_decode_append.restype = _i32
 _lib.pa_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                    ctypes.c_float, _i32, _vp]
 _lib.pa_decode_noalloc.restype = _i32
@@ -58,6 +61,9 @@ _lib.pa_decode_fp8.restype = _i32
 _lib.pa_decode_fp8_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                   _f32, _f32, _f32, _i32, _vp, _sz, ctypes.c_uint, _vp]
 _lib.pa_decode_fp8_ex.restype = _i32
+_lib.pa_decode_append_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32,
+                                      _i32, _i32, _f32, _f32, _f32, _i32, _vp, _sz, ctypes.c_uint, _vp]
+_lib.pa_decode_append_fp8.restype = _i32
 _lib.pa_reshape_and_cache_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                           _f32, _f32, _vp]
 _lib.pa_reshape_and_cache_fp8.restype = _i32
@@ -78,6 +84,7 @@ PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_OUT_OF_RANGE,
 PA_ERRBIT_BLOCK_ID, PA_ERRBIT_CONTEXT, PA_ERRBIT_SLOT = 0x1, 0x2, 0x4
 PA_ERRBIT_COPY, PA_ERRBIT_TOKEN, PA_ERRBIT_TIMEOUT = 0x8, 0x10, 0x20
 PA_DECODE_ZEROED_WORKSPACE = 0x1
+PA_DECODE_INPUTS_READY = 0x2
 
 
 class PAError(RuntimeError):
@@ -177,7 +184,8 @@ def pa_decode_ex(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor
                  value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
                  scale: float, max_context_len: int, workspace: torch.Tensor, flags: int = 0,
                  stream=None) -> None:
-    """pa_decode with flags (PA_DECODE_ZEROED_WORKSPACE; see pa_decode_ex in include/pa.h)."""
+    """pa_decode with flags (PA_DECODE_ZEROED_WORKSPACE, PA_DECODE_INPUTS_READY; see pa_decode_ex
+    in include/pa.h)."""
     S, H, D, B, NB = _decode_shapes(out, query, key_cache, value_cache, block_tables, context_lens)
     st = _lib.pa_decode_ex(_ptr(out, "out", torch.float16), _ptr(query, "query", torch.float16),
                            _ptr(key_cache, "key_cache", torch.float16),
@@ -188,6 +196,30 @@ def pa_decode_ex(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor
                            _ptr(workspace, "workspace", torch.uint8), workspace.numel(), int(flags),
                            _stream(stream))
     _check(st, "pa_decode_ex")
+
+
+def pa_decode_append(out: torch.Tensor, query: torch.Tensor, key_new: torch.Tensor,
+                     value_new: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                     block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                     max_context_len: int, workspace: torch.Tensor, flags: int = 0,
+                     stream=None) -> None:
+    """The cache write of each sequence's new token (key_new / value_new [S,H,D], written at
+    position context_lens[s] - 1) fused into pa_decode_ex (see pa_decode_append in include/pa.h)."""
+    S, H, D, B, NB = _decode_shapes(out, query, key_cache, value_cache, block_tables, context_lens)
+    if tuple(key_new.shape) != (S, H, D) or tuple(value_new.shape) != (S, H, D):
+        raise ValueError("key_new / value_new must be [S, H, D]")
+    st = _lib.pa_decode_append(_ptr(out, "out", torch.float16), _ptr(query, "query", torch.float16),
+                               _ptr(key_new, "key_new", torch.float16),
+                               _ptr(value_new, "value_new", torch.float16),
+                               _ptr(key_cache, "key_cache", torch.float16),
+                               _ptr(value_cache, "value_cache", torch.float16),
+                               _ptr(block_tables, "block_tables", torch.int32),
+                               block_tables.shape[1],
+                               _ptr(context_lens, "context_lens", torch.int32), S, H, D, B, NB,
+                               float(scale), int(max_context_len),
+                               _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
+                               int(flags), _stream(stream))
+    _check(st, "pa_decode_append")
 
 
 def pa_decode_noalloc(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
@@ -240,6 +272,31 @@ def pa_decode_fp8_ex(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Te
                                _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
                                int(flags), _stream(stream))
     _check(st, "pa_decode_fp8_ex")
+
+
+def pa_decode_append_fp8(out: torch.Tensor, query: torch.Tensor, key_new: torch.Tensor,
+                         value_new: torch.Tensor, key_cache: torch.Tensor,
+                         value_cache: torch.Tensor, block_tables: torch.Tensor,
+                         context_lens: torch.Tensor, scale: float, k_scale: float, v_scale: float,
+                         max_context_len: int, workspace: torch.Tensor, flags: int = 0,
+                         stream=None) -> None:
+    """pa_decode_append over FP8 (E4M3, uint8) caches (the new rows are quantised)."""
+    S, H, D, B, NB = _decode_shapes(out, query, key_cache, value_cache, block_tables, context_lens)
+    if tuple(key_new.shape) != (S, H, D) or tuple(value_new.shape) != (S, H, D):
+        raise ValueError("key_new / value_new must be [S, H, D]")
+    st = _lib.pa_decode_append_fp8(_ptr(out, "out", torch.float16),
+                                   _ptr(query, "query", torch.float16),
+                                   _ptr(key_new, "key_new", torch.float16),
+                                   _ptr(value_new, "value_new", torch.float16),
+                                   _cache_ptr(key_cache, "key_cache", True),
+                                   _cache_ptr(value_cache, "value_cache", True),
+                                   _ptr(block_tables, "block_tables", torch.int32),
+                                   block_tables.shape[1],
+                                   _ptr(context_lens, "context_lens", torch.int32), S, H, D, B, NB,
+                                   float(scale), float(k_scale), float(v_scale),
+                                   int(max_context_len), _ptr(workspace, "workspace", torch.uint8),
+                                   workspace.numel(), int(flags), _stream(stream))
+    _check(st, "pa_decode_append_fp8")
 
 
 def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
@@ -426,7 +483,7 @@ __all__ = [
     "pa_selftest_wait_timeout",
     "pa_decode_fp8", "pa_reshape_and_cache_fp8", "pa_copy_blocks_fp8", "pa_convert_cache_fp8",
     "pa_swap_blocks", "pa_prefill", "pa_prefill_fp8", "pa_decode_noalloc", "pa_decode_ex",
-    "pa_decode_fp8_ex",
+    "pa_decode_fp8_ex", "pa_decode_append", "pa_decode_append_fp8",
     "pa_status_string", "pa_decode_workspace_size", "pa_decode_partition_tokens",
     "pa_decode_set_partition_tokens", "decode_workspace", "raise_on_device_errors", "PAError",
 ]

@@ -12,7 +12,7 @@ namespace pa {
 #define PA_DECLARE_DECODE(sfx)                                                           \
   cudaError_t launch_decode_partition_##sfx(const DecodeParams&, int, int, size_t,      \
                                             cudaStream_t);                              \
-  int decode_ctas_per_sm_##sfx(int, size_t);                                            \
+  int decode_ctas_per_sm_##sfx(int, size_t, bool);                                      \
   size_t decode_fixed_smem_##sfx(int);                                                  \
   cudaError_t decode_prepare_##sfx();
 PA_DECLARE_DECODE(d64)
@@ -45,16 +45,16 @@ size_t decode_smem_bytes(bool fp8, int head_dim, int block_size, int part_tokens
                             : decode_fixed_smem_f8_d128(block_size))
           : (head_dim == 64 ? decode_fixed_smem_d64(block_size) : decode_fixed_smem_d128(block_size));
   const size_t bt = 2 * (size_t)(part_tokens / block_size + 1) * 4;
-  const size_t seq = (2 * (size_t)seqs_in_launch + 1) * 4;
+  const size_t seq = (2 * (size_t)seqs_in_launch + 1) * 4 + (size_t)seqs_in_launch;  // + clip flags
   return (fixed + bt + seq + 15) & ~size_t(15);
 }
 
-int decode_ctas_per_sm(bool fp8, int head_dim, int block_size, size_t smem) {
+int decode_ctas_per_sm(bool fp8, int head_dim, int block_size, size_t smem, bool append) {
   if (fp8)
-    return head_dim == 64 ? decode_ctas_per_sm_f8_d64(block_size, smem)
-                          : decode_ctas_per_sm_f8_d128(block_size, smem);
-  return head_dim == 64 ? decode_ctas_per_sm_d64(block_size, smem)
-                        : decode_ctas_per_sm_d128(block_size, smem);
+    return head_dim == 64 ? decode_ctas_per_sm_f8_d64(block_size, smem, append)
+                          : decode_ctas_per_sm_f8_d128(block_size, smem, append);
+  return head_dim == 64 ? decode_ctas_per_sm_d64(block_size, smem, append)
+                        : decode_ctas_per_sm_d128(block_size, smem, append);
 }
 
 cudaError_t decode_prepare_device(int) {
@@ -219,9 +219,12 @@ pa_status decode_impl(bool fp8, void* out, const void* query, const void* key_ca
                       int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
                       int num_heads, int head_dim, int block_size, int num_blocks, float scale,
                       float k_scale, float v_scale, int max_context_len, void* workspace,
-                      size_t workspace_bytes, unsigned int flags, pa_stream_t stream) {
+                      size_t workspace_bytes, unsigned int flags, pa_stream_t stream,
+                      const void* key_new = nullptr, const void* value_new = nullptr) {
   if (!head_dim_ok(head_dim) || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
-  if (flags & ~PA_DECODE_ZEROED_WORKSPACE) return PA_ERR_INVALID_ARG;
+  if (flags & ~(PA_DECODE_ZEROED_WORKSPACE | PA_DECODE_INPUTS_READY)) return PA_ERR_INVALID_ARG;
+  if ((key_new == nullptr) != (value_new == nullptr)) return PA_ERR_INVALID_ARG;
+  if (key_new && (!aligned16(key_new) || !aligned16(value_new))) return PA_ERR_INVALID_ARG;
   if (num_seqs < 0 || num_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 ||
       max_context_len < 0)
     return PA_ERR_INVALID_ARG;
@@ -259,6 +262,9 @@ pa_status decode_impl(bool fp8, void* out, const void* query, const void* key_ca
   p.max_parts = w.max_parts;
   p.scale_log2 = (float)((double)scale * (double)k_scale * 1.4426950408889634073599246810019);
   p.v_scale = v_scale;
+  p.key_new = key_new;
+  p.value_new = value_new;
+  p.k_scale = k_scale;
 
   // The kernels leave the counters zero; a caller that keeps them so skips the
   // zeroing kernel.
@@ -271,8 +277,12 @@ pa_status decode_impl(bool fp8, void* out, const void* query, const void* key_ca
     p.num_seqs = num_seqs - p.seq_begin < pa::kMaxSeqsPerLaunch ? num_seqs - p.seq_begin
                                                                  : pa::kMaxSeqsPerLaunch;
     p.counter = counters + b;
+    // The zeroing kernel, or the previous launch, waited before it triggered
+    // this one; otherwise only the caller's word says the inputs are complete.
+    p.inputs_ready = b > 0 || !(flags & PA_DECODE_ZEROED_WORKSPACE) ||
+                     (flags & PA_DECODE_INPUTS_READY) != 0;
     const size_t smem = pa::decode_smem_bytes(fp8, head_dim, block_size, w.part_tokens, p.num_seqs);
-    const int per_sm = pa::decode_ctas_per_sm(fp8, head_dim, block_size, smem);
+    const int per_sm = pa::decode_ctas_per_sm(fp8, head_dim, block_size, smem, key_new != nullptr);
     long long grid = (long long)per_sm * ds.sms;
     const long long items_ub = (long long)p.num_seqs * num_heads * w.max_parts;
     if (grid > items_ub) grid = items_ub;
@@ -395,6 +405,36 @@ pa_status pa_decode_fp8_ex(void* out, const void* query, const void* key_cache,
   return decode_impl(true, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
                      context_lens, num_seqs, num_heads, head_dim, block_size, num_blocks, scale,
                      k_scale, v_scale, max_context_len, workspace, workspace_bytes, flags, stream);
+}
+
+pa_status pa_decode_append(void* out, const void* query, const void* key_new,
+                           const void* value_new, void* key_cache, void* value_cache,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, int num_seqs, int num_heads, int head_dim,
+                           int block_size, int num_blocks, float scale, int max_context_len,
+                           void* workspace, size_t workspace_bytes, unsigned int flags,
+                           pa_stream_t stream) {
+  if (!key_new || !value_new) return PA_ERR_INVALID_ARG;
+  return decode_impl(false, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_heads, head_dim, block_size, num_blocks, scale,
+                     1.f, 1.f, max_context_len, workspace, workspace_bytes, flags, stream,
+                     key_new, value_new);
+}
+
+pa_status pa_decode_append_fp8(void* out, const void* query, const void* key_new,
+                               const void* value_new, void* key_cache, void* value_cache,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int num_seqs, int num_heads,
+                               int head_dim, int block_size, int num_blocks, float scale,
+                               float k_scale, float v_scale, int max_context_len,
+                               void* workspace, size_t workspace_bytes, unsigned int flags,
+                               pa_stream_t stream) {
+  if (!key_new || !value_new) return PA_ERR_INVALID_ARG;
+  if (!scale_ok(k_scale) || !scale_ok(v_scale)) return PA_ERR_INVALID_ARG;
+  return decode_impl(true, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_heads, head_dim, block_size, num_blocks, scale,
+                     k_scale, v_scale, max_context_len, workspace, workspace_bytes, flags, stream,
+                     key_new, value_new);
 }
 
 pa_status pa_reshape_and_cache(const void* key, const void* value, void* key_cache,

@@ -54,17 +54,8 @@ __global__ void __launch_bounds__(256)
 // 16-byte output vector i (16 codes) of the [T][H][D] inputs: it reads the
 // 16 fp16 values (32 bytes), divides each by the tensor's scale in IEEE
 // binary32 (round to nearest) and rounds the quotient to the nearest E4M3
-// code, saturating to +-448.
-__device__ __forceinline__ uint4 quantize16(const uint4& lo, const uint4& hi, float scale) {
-  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-  uint32_t c[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float2 f = half2_bits_to_float2(w[j]);
-    c[j] = f32x2_to_e4m3x2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
-  }
-  return make_uint4(c[0] | c[1] << 16, c[2] | c[3] << 16, c[4] | c[5] << 16, c[6] | c[7] << 16);
-}
+// code, saturating to +-448 (quantize16, shared with the decode that writes
+// its new token itself).
 
 template <int D>
 __global__ void __launch_bounds__(256)

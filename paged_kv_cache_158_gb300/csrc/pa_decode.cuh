@@ -51,6 +51,13 @@
 //    (the pending merges form a serial latency chain in the kernel's tail).
 //  * The summation order depends only on logical token positions, so the
 //    result is bit-identical under any relabelling of physical blocks.
+//  * Cache write fused in (key_new set): the new token of each sequence sits
+//    at position c - 1, in the last chunk of its last partition.  The warp
+//    that owns that chunk, once the chunk has landed, writes the new key and
+//    value rows (quantised for FP8 caches, as the cache-write kernel does)
+//    to the cache and over the stale rows of its stage, then proceeds: the
+//    same result and cache contents as the cache write followed by decode,
+//    in one kernel.
 //  * FP8 caches (F8: one E4M3 byte per element, one scale per cache tensor)
 //    read a token's row in half the bytes, so per byte of HBM the kernel
 //    does twice the arithmetic; the fp16 layout above is then bound by
@@ -230,6 +237,41 @@ __device__ __forceinline__ void issue_chunk(const DecodeParams& a, const ItemInf
   }
 }
 
+// The fused cache write of one sequence's new token (warp-wide; call only
+// for the chunk that holds position pos = c - 1): the new key/value rows of
+// (sequence, head h), prefetched as lane < D/8's 16 bytes each in k, v, go to
+// the cache slot of pos and over the chunk's staged rows at `row` (the
+// stage's K rows at Ks, V rows at Vs); for FP8 caches they are quantised as
+// the cache-write kernel quantises them.
+template <int D, int B, bool F8>
+__device__ __forceinline__ void append_new_token(const DecodeParams& a, int h, int phys, int pos,
+                                                 int row, unsigned char* Ks, unsigned char* Vs,
+                                                 int lane, const uint4& k, const uint4& v) {
+  using T = DecodeTraits<D, B, F8>;
+  const size_t dst = (((size_t)phys * a.num_heads + h) * B + pos % B) * D * T::ELEM;  // bytes
+  unsigned char* kc = static_cast<unsigned char*>(const_cast<void*>(a.key_cache)) + dst;
+  unsigned char* vc = static_cast<unsigned char*>(const_cast<void*>(a.value_cache)) + dst;
+  unsigned char* ks = Ks + (size_t)row * D * T::ELEM;
+  unsigned char* vs = Vs + (size_t)row * D * T::ELEM;
+  if (lane < D / 8) {
+    if constexpr (F8) {
+      const uint2 kq = quantize8(k, a.k_scale), vq = quantize8(v, a.v_scale);
+      reinterpret_cast<uint2*>(kc)[lane] = kq;
+      reinterpret_cast<uint2*>(vc)[lane] = vq;
+      reinterpret_cast<uint2*>(ks)[lane] = kq;
+      reinterpret_cast<uint2*>(vs)[lane] = vq;
+    } else {
+      reinterpret_cast<uint4*>(kc)[lane] = k;
+      reinterpret_cast<uint4*>(vc)[lane] = v;
+      reinterpret_cast<uint4*>(ks)[lane] = k;
+      reinterpret_cast<uint4*>(vs)[lane] = v;
+    }
+  }
+  // The next bulk copy into this stage must not overtake these writes.
+  fence_proxy_async_smem();
+  __syncwarp();
+}
+
 // A lane's query slice: DPL fp16 values (16 or 32 bytes).
 template <int DPL>
 struct QSlice {
@@ -360,7 +402,9 @@ __device__ __forceinline__ void process_chunk(const unsigned char* Ks, const uns
   }
 }
 
-template <int D, int B, bool F8>
+// APPEND: the variant with the new token's cache write fused in (a separate
+// instantiation, so the plain decode keeps its registers and schedule).
+template <int D, int B, bool F8, bool APPEND>
 __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
     decode_partition_kernel(const DecodeParams a) {
   using T = DecodeTraits<D, B, F8>;
@@ -382,6 +426,8 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
   cur_ptr += 2 * bt_cap * 4;
   int* cum = reinterpret_cast<int*>(cur_ptr);   // nseq + 1
   int* ctx_s = cum + (a.num_seqs + 1);          // nseq
+  // nseq flags: the sequence's context length was clipped (APPEND: no write)
+  unsigned char* clip_s = reinterpret_cast<unsigned char*>(ctx_s + a.num_seqs);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -395,12 +441,17 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
   }
   if (tid == 0) misc[8] = 0;
   fence_mbar_init();
-  // The call's inputs (context lengths, block tables, queries, caches) were
-  // written before the call's first kernel, which lets this kernel launch
-  // only after its own wait: they are complete here, so the scan, the first
-  // item's block-table slice and its first copies start before pdl_wait.
-  // Only the work counter (zeroed by the kernel just before this one) and
-  // the workspace partials are touched after it.
+  // A launch may start while the kernel before it on the stream still runs
+  // (programmatic launch).  The call's inputs (context lengths, block tables,
+  // queries, caches) may come from that kernel (a cache write, say), so the
+  // first kernel of a call waits before it reads them.  When an earlier
+  // kernel of the same call has waited already (the counter-zeroing kernel,
+  // or the previous launch of a split batch), it triggered this launch only
+  // after its wait: the inputs are complete here, and the scan, the first
+  // item's block-table slice and its first copies run before pdl_wait, over
+  // the previous kernel's tail.  The work counter and the workspace partials
+  // are touched only after the wait.
+  if (!a.inputs_ready) pdl_wait();
 
   // ---- per-sequence item counts and their exclusive prefix sums ---------
   {
@@ -413,8 +464,10 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
       const int i = base + j;
       int v = 0;
       if (i < nseq) {
-        const int c = effective_len(a.context_lens[a.seq_begin + i], a, B, blockIdx.x == 0);
+        const int raw = a.context_lens[a.seq_begin + i];
+        const int c = effective_len(raw, a, B, blockIdx.x == 0);
         ctx_s[i] = c;
+        if constexpr (APPEND) clip_s[i] = raw != c;
         v = H * num_parts(c, P);
       }
       vals[j] = v;
@@ -580,6 +633,22 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
     float o[T::DPL];
 #pragma unroll
     for (int i = 0; i < T::DPL; ++i) o[i] = 0.f;
+    // APPEND: the last item of a (sequence, head) holds its new token in
+    // chunk a_chunk; the warp that owns that chunk loads the new rows now, so
+    // the loads are long done when the chunk lands.
+    int a_chunk = -1;
+    uint4 a_k = make_uint4(0, 0, 0, 0), a_v = a_k;
+    if constexpr (APPEND) {
+      if (it.t_end == it.c && it.c > 0 && !clip_s[it.s] &&
+          ((it.c - 1 - it.t_begin) / T::TC) % T::NW == warp) {
+        a_chunk = (it.c - 1 - it.t_begin) / T::TC;
+        if (lane < D / 8) {
+          const size_t src = sh * D;  // fp16 elements of (sequence, head) in key_new / value_new
+          a_k = reinterpret_cast<const uint4*>(static_cast<const __half*>(a.key_new) + src)[lane];
+          a_v = reinterpret_cast<const uint4*>(static_cast<const __half*>(a.value_new) + src)[lane];
+        }
+      }
+    }
 
     for (int i = 0; i < n_my; ++i) {
       const int st = st_c;
@@ -603,7 +672,18 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
       int ph[T::BPC];
       chunk_ids<D, B, F8>(ph, bt, it, chunk);
       if (rows > 0 && chunk_ids_ok<D, B, F8>(a, ph, rows)) {
-        const unsigned char* Ks = my_stages + st * T::STAGE_BYTES;
+        unsigned char* Ks = my_stages + st * T::STAGE_BYTES;
+        // Fused cache write: this chunk holds the sequence's new token (a
+        // clipped context length was reported and writes nothing).
+        if (APPEND && chunk == a_chunk) {
+          const int row = it.c - 1 - t0;
+          int phys = ph[0];  // the block of that row (a register select, no local memory)
+#pragma unroll
+          for (int b = 1; b < T::BPC; ++b)
+            if (row / B == b) phys = ph[b];
+          append_new_token<D, B, F8>(a, it.h, phys, it.c - 1, row, Ks, Ks + T::CHUNK_BYTES, lane,
+                                     a_k, a_v);
+        }
         if (rows == T::TC)
           process_chunk<D, B, F8, true>(Ks, Ks + T::CHUNK_BYTES, rows, q, a.scale_log2, my_p, lane,
                                         m, l, o);
@@ -692,8 +772,9 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
 }
 
 // Merge the partitions of each (sequence, head): one warp per pair.  The
-// context length (an input, complete before the call) is read before
-// pdl_wait; after it, the partitions' (m, l) and their first kPre partial
+// context length is read before pdl_wait (the partition launch before this
+// one triggered it only after its own wait, so the call's inputs are
+// complete); after the wait, the partitions' (m, l) and their first kPre partial
 // outputs are loaded together, then the warp reduces max and sum by shuffles
 // and accumulates the weighted partials in partition order, D/32 dimensions
 // per lane.
@@ -773,23 +854,32 @@ cudaError_t launch_reduce_t(const DecodeParams& p, int total_seqs, cudaStream_t 
 
 template <int D, int B, bool F8>
 cudaError_t launch_partition_t(const DecodeParams& p, int grid, size_t smem, cudaStream_t st) {
-  return launch_pdl(decode_partition_kernel<D, B, F8>, dim3(grid),
+  if (p.key_new != nullptr)
+    return launch_pdl(decode_partition_kernel<D, B, F8, true>, dim3(grid),
+                      dim3(DecodeTraits<D, B, F8>::THREADS), smem, st, p);
+  return launch_pdl(decode_partition_kernel<D, B, F8, false>, dim3(grid),
                     dim3(DecodeTraits<D, B, F8>::THREADS), smem, st, p);
 }
 
 template <int D, int B, bool F8>
-int ctas_per_sm_t(size_t smem) {
+int ctas_per_sm_t(size_t smem, bool append) {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_partition_kernel<D, B, F8>,
-                                                    DecodeTraits<D, B, F8>::THREADS, smem) !=
-      cudaSuccess)
-    return 1;
+  const cudaError_t e =
+      append ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                   &n, decode_partition_kernel<D, B, F8, true>, DecodeTraits<D, B, F8>::THREADS, smem)
+             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                   &n, decode_partition_kernel<D, B, F8, false>, DecodeTraits<D, B, F8>::THREADS,
+                   smem);
+  if (e != cudaSuccess) return 1;
   return n > 0 ? n : 1;
 }
 
 template <int D, int B, bool F8>
 cudaError_t prepare_t() {
-  return cudaFuncSetAttribute(decode_partition_kernel<D, B, F8>,
+  const cudaError_t e = cudaFuncSetAttribute(decode_partition_kernel<D, B, F8, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(decode_partition_kernel<D, B, F8, true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
 }
 

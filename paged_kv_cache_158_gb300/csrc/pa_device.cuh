@@ -308,4 +308,37 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float first, float second) {
   return r;
 }
 
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (tensor core, TMA, bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 16 E4M3 codes of 16 fp16 values (the 32 bytes lo, hi): each value is
+// divided by the tensor's scale in IEEE binary32 (round to nearest) and the
+// quotient rounded to the nearest E4M3 code, saturating to +-448.  The one
+// quantisation every FP8 cache write uses.
+__device__ __forceinline__ uint4 quantize16(const uint4& lo, const uint4& hi, float scale) {
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  uint32_t c[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float2 f = half2_bits_to_float2(w[j]);
+    c[j] = f32x2_to_e4m3x2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
+  }
+  return make_uint4(c[0] | c[1] << 16, c[2] | c[3] << 16, c[4] | c[5] << 16, c[6] | c[7] << 16);
+}
+
+// 8 E4M3 codes of 8 fp16 values (16 bytes), elementwise as quantize16.
+__device__ __forceinline__ uint2 quantize8(const uint4& v, float scale) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t c[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 f = half2_bits_to_float2(w[j]);
+    c[j] = f32x2_to_e4m3x2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
+  }
+  return make_uint2(c[0] | c[1] << 16, c[2] | c[3] << 16);
+}
+
 }  // namespace pa

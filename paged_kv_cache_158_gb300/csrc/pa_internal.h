@@ -40,6 +40,15 @@ struct DecodeParams {
   int max_parts;              // ceil(max_context_len / part_tokens)
   float scale_log2;           // scale * log2(e) (* k_scale for E4M3 caches): base-2 logits
   float v_scale;              // E4M3 caches: multiplies the output (unused for fp16)
+  // Decode with the cache write fused in (null otherwise): fp16 [S][H][D]
+  // rows written to position context_len - 1 of each sequence before use.
+  const void* key_new;
+  const void* value_new;
+  float k_scale;              // E4M3 caches: quantisation scale of key_new (v_scale for values)
+  // 1: a kernel before this one in the same call already waited for the
+  // stream's earlier work, so the inputs are complete when this launch starts
+  // and its prologue reads them before its own wait; 0: it waits first.
+  int inputs_ready;
 };
 
 // Partition-kernel launch: picks the instantiation for (cache element type,
@@ -52,8 +61,9 @@ cudaError_t launch_decode_reduce(const DecodeParams& p, int head_dim, int block_
 // Dynamic shared memory of the partition kernel.
 size_t decode_smem_bytes(bool fp8, int head_dim, int block_size, int part_tokens,
                          int seqs_in_launch);
-// Resident CTAs per SM of the partition kernel for that shared-memory size.
-int decode_ctas_per_sm(bool fp8, int head_dim, int block_size, size_t smem_bytes);
+// Resident CTAs per SM of the partition kernel (append: the variant with the
+// cache write fused in) for that shared-memory size.
+int decode_ctas_per_sm(bool fp8, int head_dim, int block_size, size_t smem_bytes, bool append);
 // One-time per-device kernel attributes (dynamic shared memory opt-in).
 cudaError_t decode_prepare_device(int device);
 

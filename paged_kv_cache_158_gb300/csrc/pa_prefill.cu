@@ -232,11 +232,15 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
     tmem_alloc(smem_u32(tmem_slot), T::TMEM_COLS);
     tmem_relinquish();
   }
+  // The launch may start while the kernel before it on the stream still runs
+  // (programmatic launch), and that kernel may write this call's inputs: the
+  // set-up above overlaps its tail, everything below reads inputs and runs
+  // after the wait.
+  pdl_wait();
   // This CTA's unit (see pa_prefill_rows.cuh for the order), with its
-  // sequence's query rows and context length.  query_start and context_lens
-  // are inputs of the call, complete before its first kernel, so they are
-  // read before pdl_wait; the table and scratch live in the Q area until then.
-  // Up to 32 sequences: warp 1 alone; more: the whole block.
+  // sequence's query rows and context length; the table and scratch live in
+  // the Q area until the first loads.  Up to 32 sequences: warp 1 alone;
+  // more: the whole block.
   int* scratch = reinterpret_cast<int*>(sm) + kSeqsPerLaunch;
   prows::Unit* unit_s = reinterpret_cast<prows::Unit*>(scratch + 20);
   if (a.num_seqs <= 32) {
@@ -262,10 +266,9 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
   if (blockIdx.x == 0 && tid == 0 && scratch[19] > (int)gridDim.x)
     atomicOr(a.err, PA_ERRBIT_CONTEXT);  // inconsistent query_start: units beyond the grid
   if (unit.kind != 1) {
-    // No tensor-core work: a decode row runs on CUDA cores (after the wait,
-    // since it reads the caches); then the tensor memory goes back.
+    // No tensor-core work: a decode row runs on CUDA cores; then the tensor
+    // memory goes back.
     if (unit.kind == 2) {
-      pdl_wait();
       pdl_launch_dependents();
       const int s = a.seq_begin + unit.s, q_len = unit.q_len, c = unit.c;
       const bool bad = q_len != 1 || c < 1 || c > a.max_blocks * a.block_size ||
@@ -305,7 +308,6 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
   const int h = __shfl_sync(kFullMask, unit.h, 0);
   const int pq = __shfl_sync(kFullMask, unit.pq, 0);
 
-  pdl_wait();
   pdl_launch_dependents();
 
   const int q0 = __shfl_sync(kFullMask, unit.q0, 0);

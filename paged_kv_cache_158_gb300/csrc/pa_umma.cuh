@@ -32,12 +32,6 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy (tensor core, TMA) accesses.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ---- tensor memory ---------------------------------------------------------
 
 // One full warp: allocates ncols TMEM columns (a power of two >= 32) and

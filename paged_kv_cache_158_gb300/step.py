@@ -2,7 +2,10 @@
 
 A decode step is: (optional) the copy-on-write block copies the block
 manager planned, the slot map of the new tokens, then for every layer the
-cache write of the new tokens and the paged decode.  Launching it takes
+cache write of the new tokens and the paged decode.  When every sequence
+brings one new token at position context_len - 1 (append=True), each layer's
+cache write is fused into its decode (pa_decode_append) and the slot map is
+not needed: one kernel fewer per layer.  Launching it takes
 ~2-3 library calls per layer; capturing it once in a CUDA graph and
 replaying it removes the per-launch CPU cost and most launch gaps, as the
 pages' model runner does for decode ("【硬核】啃透vLLM源码：从PagedAttention到
@@ -39,9 +42,15 @@ from __future__ import annotations
 
 import torch
 
-from . import (PA_DECODE_ZEROED_WORKSPACE, decode_workspace, pa_copy_blocks, pa_copy_blocks_fp8,
-               pa_decode_ex, pa_decode_fp8_ex, pa_reshape_and_cache, pa_reshape_and_cache_fp8,
-               pa_slot_mapping)
+from . import (PA_DECODE_INPUTS_READY, PA_DECODE_ZEROED_WORKSPACE, decode_workspace, pa_copy_blocks, pa_copy_blocks_fp8,
+               pa_decode_append, pa_decode_append_fp8, pa_decode_ex, pa_decode_fp8_ex,
+               pa_reshape_and_cache, pa_reshape_and_cache_fp8, pa_slot_mapping)
+
+
+def _overlap(a: torch.Tensor, b: torch.Tensor) -> bool:
+    """The two tensors' byte ranges intersect."""
+    a0, b0 = a.data_ptr(), b.data_ptr()
+    return a0 < b0 + b.numel() * b.element_size() and b0 < a0 + a.numel() * a.element_size()
 
 
 def _pow2_groups(n: int) -> list[tuple[int, int]]:
@@ -59,7 +68,7 @@ class DecodeStep:
                  block_tables: torch.Tensor, context_lens: torch.Tensor, token_seq: torch.Tensor,
                  token_pos: torch.Tensor, block_size: int, num_blocks: int, scale: float,
                  max_context_len: int, copy_pairs: torch.Tensor | None = None,
-                 fp8_scales: tuple[float, float] | None = None):
+                 fp8_scales: tuple[float, float] | None = None, append: bool = False):
         n = len(key_caches)
         if not (len(value_caches) == len(queries) == len(keys_new) == len(values_new) == len(outs) == n):
             raise ValueError("one cache, query, new key/value and output per layer")
@@ -72,6 +81,20 @@ class DecodeStep:
         self.scale, self.max_context_len = float(scale), int(max_context_len)
         self.copy_pairs = copy_pairs
         self.fp8_scales = None if fp8_scales is None else (float(fp8_scales[0]), float(fp8_scales[1]))
+        # append: the decode step's usual shape, one new token per sequence at position
+        # context_lens[s] - 1 with its rows keys_new[i][s] / values_new[i][s]; each layer's cache
+        # write is then fused into its decode (pa_decode_append), and the slot map is not needed.
+        self.append = bool(append)
+        if self.append and any(k.shape != queries[0].shape for k in list(keys_new) + list(values_new)):
+            raise ValueError("append: new keys/values must be [S, H, D], one row per sequence")
+        # In append mode the kernel just before layer i's decode (i >= 1) is layer i - 1's
+        # decode, which writes only its output: layer i's decode may then read its inputs
+        # while that one finishes (PA_DECODE_INPUTS_READY), unless the output is one of them.
+        self._ready = [False] * n
+        for i in range(1, n if self.append else 0):
+            ins = (queries[i], keys_new[i], values_new[i], key_caches[i], value_caches[i],
+                   block_tables, context_lens)
+            self._ready[i] = not any(_overlap(outs[i - 1], t) for t in ins)
         dev = queries[0].device
         S, H, D = queries[0].shape
         self.slots = torch.empty(token_seq.numel(), dtype=torch.int64, device=dev)
@@ -93,8 +116,9 @@ class DecodeStep:
         if self.copy_pairs is not None and self.copy_pairs.numel():
             (pa_copy_blocks_fp8 if f8 else pa_copy_blocks)(self.key_caches, self.value_caches,
                                                            self.copy_pairs, s)
-        pa_slot_mapping(self.slots, self.block_tables, self.token_seq, self.token_pos, self.block_size,
-                        self.num_blocks, s)
+        if not self.append:
+            pa_slot_mapping(self.slots, self.block_tables, self.token_seq, self.token_pos,
+                            self.block_size, self.num_blocks, s)
         for i in range(self.num_layers):
             self._write(i, s)
             if decode_events is not None:
@@ -155,8 +179,9 @@ class DecodeStep:
         if self.copy_pairs is not None and self.copy_pairs.numel():
             (pa_copy_blocks_fp8 if f8 else pa_copy_blocks)(self.key_caches, self.value_caches,
                                                            self.copy_pairs, s)
-        pa_slot_mapping(self.slots, self.block_tables, self.token_seq, self.token_pos, self.block_size,
-                        self.num_blocks, s)
+        if not self.append:
+            pa_slot_mapping(self.slots, self.block_tables, self.token_seq, self.token_pos,
+                            self.block_size, self.num_blocks, s)
         starts = {g0 for g0, _ in groups}
         # Downloads in the mirror-image groups: ..., 4, 2, 1, 1 layers at the end.
         L = self.num_layers
@@ -177,7 +202,9 @@ class DecodeStep:
         s.wait_stream(up)
 
     def _write(self, i: int, s) -> None:
-        """Layer i's cache write of the new tokens."""
+        """Layer i's cache write of the new tokens (in append mode it is part of the decode)."""
+        if self.append:
+            return
         f8 = self.fp8_scales
         if f8:
             pa_reshape_and_cache_fp8(self.keys_new[i], self.values_new[i], self.key_caches[i],
@@ -191,7 +218,19 @@ class DecodeStep:
         only ever passed to the decode calls, which leave its counters zero, so no call needs
         to zero them first (PA_DECODE_ZEROED_WORKSPACE)."""
         f8 = self.fp8_scales
-        fl = PA_DECODE_ZEROED_WORKSPACE
+        fl = PA_DECODE_ZEROED_WORKSPACE | (PA_DECODE_INPUTS_READY if self._ready[i] else 0)
+        if self.append:
+            if f8:
+                pa_decode_append_fp8(self.outs[i], self.queries[i], self.keys_new[i],
+                                     self.values_new[i], self.key_caches[i], self.value_caches[i],
+                                     self.block_tables, self.context_lens, self.scale, f8[0], f8[1],
+                                     self.max_context_len, self.workspace, fl, s)
+            else:
+                pa_decode_append(self.outs[i], self.queries[i], self.keys_new[i], self.values_new[i],
+                                 self.key_caches[i], self.value_caches[i], self.block_tables,
+                                 self.context_lens, self.scale, self.max_context_len,
+                                 self.workspace, fl, s)
+            return
         if f8:
             pa_decode_fp8_ex(self.outs[i], self.queries[i], self.key_caches[i],
                              self.value_caches[i], self.block_tables, self.context_lens, self.scale,

@@ -31,6 +31,20 @@ def test_library_exports_every_declared_symbol():
     assert not missing, missing
 
 
+def test_binding_constants_match_the_header():
+    """Every status code, error bit and flag the header defines has the same
+    value in the Python binding."""
+    import paged_kv_cache_158_gb300 as pa
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    consts = {n: int(v, 0) for n, v in re.findall(r"#define\s+(PA_[A-Z_]+)\s+(0x[0-9a-fA-F]+|\d+)u?\b",
+                                                  text)}
+    consts.update({n: int(v) for n, v in re.findall(r"\b(PA_[A-Z_]+)\s*=\s*(\d+)", text)})
+    assert {"PA_OK", "PA_ERR_TIMEOUT", "PA_ERRBIT_TIMEOUT", "PA_DECODE_ZEROED_WORKSPACE",
+            "PA_DECODE_INPUTS_READY"} <= set(consts)
+    for n, v in consts.items():
+        assert getattr(pa, n) == v, n
+
+
 def test_status_strings_and_sizes_on_host():
     lib = ctypes.CDLL(LIB)
     lib.pa_status_string.restype = ctypes.c_char_p

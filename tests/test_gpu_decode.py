@@ -292,5 +292,106 @@ def test_decode_ex_refuses_unknown_flags():
     out = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=DEV)
     with pytest.raises(pa.PAError) as e:
         pa.pa_decode_ex(out, dw.queries[0], dw.key_caches[0], dw.value_caches[0], dw.block_tables,
-                        dw.context_lens, w.scale, w.max_context_len, ws, 0x2)
+                        dw.context_lens, w.scale, w.max_context_len, ws, 0x4)
     assert e.value.status == pa.PA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("append", [False, True])
+def test_zeroed_workspace_decode_sees_the_swap_in_just_before_it(append):
+    """With PA_DECODE_ZEROED_WORKSPACE the decode kernel is the call's first
+    and is launched programmatically behind the previous kernel on the
+    stream, which may still be running when it starts.  Here that kernel is a
+    swap-in of every sequence's only block from pinned host memory (the first
+    sequences' blocks last in the mapping, so they are still on their way
+    when the decode could start).  Ten rounds, each putting the old blocks
+    back first, give the bits of the same call made after a synchronize: the
+    outputs, and with append (the decode writes position 15 itself) the
+    caches too, whose new rows must not be overwritten by the swap-in."""
+    S, H, D, B = 512, 8, 128, 16
+    gen = torch.Generator().manual_seed(5600 + append)
+    rnd = lambda *shape: torch.randn(*shape, generator=gen).to(torch.float16)  # noqa: E731
+    k_old, v_old = rnd(S, H, B, D).to(DEV), rnd(S, H, B, D).to(DEV)
+    hk, hv = rnd(S, H, B, D).pin_memory(), rnd(S, H, B, D).pin_memory()
+    q, k_app, v_app = (rnd(S, H, D).to(DEV) for _ in range(3))
+    rows = torch.arange(S - 1, -1, -1, dtype=torch.int64)
+    mapping = torch.stack([rows, rows], dim=1).contiguous().to(DEV)
+    kc, vc = torch.empty_like(k_old), torch.empty_like(v_old)
+    bt = torch.arange(S, dtype=torch.int32, device=DEV).view(S, 1)
+    ctx = torch.full((S,), B, dtype=torch.int32, device=DEV)
+    ws = pa.decode_workspace(S, H, D, B)
+    scale = D ** -0.5
+
+    def step(out, flags, sync):
+        kc.copy_(k_old)
+        vc.copy_(v_old)
+        pa.pa_swap_blocks([kc, vc], [hk, hv], mapping)
+        if sync:
+            torch.cuda.synchronize()
+        if append:
+            pa.pa_decode_append(out, q, k_app, v_app, kc, vc, bt, ctx, scale, B, ws, flags)
+        else:
+            pa.pa_decode_ex(out, q, kc, vc, bt, ctx, scale, B, ws, flags)
+        torch.cuda.synchronize()
+
+    ref = torch.empty((S, H, D), dtype=torch.float16, device=DEV)
+    step(ref, 0, True)
+    ref_k, ref_v = kc.clone(), vc.clone()
+    stale = torch.empty_like(ref)
+    kc.copy_(k_old)
+    vc.copy_(v_old)
+    pa.pa_decode_ex(stale, q, kc, vc, bt, ctx, scale, B, ws)
+    torch.cuda.synchronize()
+    assert not torch.equal(stale.view(torch.int16), ref.view(torch.int16))   # the blocks matter
+    for _ in range(10):
+        out = torch.full_like(ref, float("nan"))
+        step(out, pa.PA_DECODE_ZEROED_WORKSPACE, False)
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+        assert torch.equal(kc.view(torch.int16), ref_k.view(torch.int16))
+        assert torch.equal(vc.view(torch.int16), ref_v.view(torch.int16))
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+@pytest.mark.parametrize("append", [False, True])
+def test_inputs_ready_behind_another_layers_decode(append):
+    """PA_DECODE_INPUTS_READY as the decode step uses it: four layers' calls in
+    a row on one workspace, each but the first behind the previous layer's
+    decode (which writes none of its inputs), give the bits of calls made one
+    at a time after a synchronize."""
+    import dataclasses
+    w = dataclasses.replace(configs.small_random(5700 + append, 300, 4, 128, 16, 900, min_context=1),
+                            num_layers=4)
+    dw = gpu.materialize(w, device=DEV)
+    ws = pa.decode_workspace(w.num_seqs, w.num_heads, w.head_dim, w.max_context_len)
+    shape = (w.num_seqs, w.num_heads, w.head_dim)
+    kn = [torch.randn(shape, generator=torch.Generator().manual_seed(5710 + i)).to(torch.float16)
+          .to(DEV) for i in range(4)]
+    vn = [torch.randn(shape, generator=torch.Generator().manual_seed(5720 + i)).to(torch.float16)
+          .to(DEV) for i in range(4)]
+    kc0 = [t.clone() for t in dw.key_caches]
+    vc0 = [t.clone() for t in dw.value_caches]
+
+    def layer(i, out, flags):
+        args = (dw.key_caches[i], dw.value_caches[i], dw.block_tables, dw.context_lens, w.scale)
+        if append:
+            pa.pa_decode_append(out, dw.queries[i], kn[i], vn[i], *args, w.max_context_len, ws, flags)
+        else:
+            pa.pa_decode_ex(out, dw.queries[i], *args, w.max_context_len, ws, flags)
+
+    refs = []
+    for i in range(4):
+        refs.append(torch.empty(shape, dtype=torch.float16, device=DEV))
+        layer(i, refs[-1], 0)
+        torch.cuda.synchronize()
+    ref_caches = [t.clone() for t in dw.key_caches + dw.value_caches]
+    for _ in range(3):
+        for t, t0 in zip(dw.key_caches + dw.value_caches, kc0 + vc0):
+            t.copy_(t0)
+        outs = [torch.full(shape, float("nan"), dtype=torch.float16, device=DEV) for _ in range(4)]
+        for i in range(4):
+            layer(i, outs[i], pa.PA_DECODE_ZEROED_WORKSPACE | (pa.PA_DECODE_INPUTS_READY if i else 0))
+        torch.cuda.synchronize()
+        for o, r in zip(outs, refs):
+            assert torch.equal(o.view(torch.int16), r.view(torch.int16))
+        for t, r in zip(dw.key_caches + dw.value_caches, ref_caches):
+            assert torch.equal(t.view(torch.int16), r.view(torch.int16))
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)

@@ -27,13 +27,13 @@ DEV = "cuda"
 SIGN16 = np.uint16(0x8000)
 
 
-def make_step(w, dw, max_ctx=None, copy_pairs=None, fp8_scales=None):
+def make_step(w, dw, max_ctx=None, copy_pairs=None, fp8_scales=None, append=False):
     outs = [torch.full((w.num_seqs, w.num_heads, w.head_dim), float("nan"), dtype=torch.float16,
                        device=DEV) for _ in dw.layers]
     return DecodeStep(dw.key_caches, dw.value_caches, dw.queries, dw.keys_new, dw.values_new, outs,
                       dw.block_tables, dw.context_lens, dw.token_seq, dw.token_pos, w.block_size,
                       w.num_blocks, w.scale, int(w.context_lens.max()) if max_ctx is None else max_ctx,
-                      copy_pairs, fp8_scales)
+                      copy_pairs, fp8_scales, append=append)
 
 
 class OracleLayer:
@@ -98,8 +98,8 @@ def _second_step_inputs(w, dw, host=None):
     return q, kn, vn, ctx, seqs, pos
 
 
-def _run_graph_against_oracle(w, dw, fp8_scales=None, host=False):
-    st = make_step(w, dw, fp8_scales=fp8_scales)
+def _run_graph_against_oracle(w, dw, fp8_scales=None, host=False, append=False):
+    st = make_step(w, dw, fp8_scales=fp8_scales, append=append)
     hb = None
     if host:
         pin = lambda t: t.cpu().pin_memory()  # noqa: E731
@@ -139,23 +139,27 @@ def _run_graph_against_oracle(w, dw, fp8_scales=None, host=False):
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
 
 
-def test_graph_step_13b_four_layers_against_oracle():
+@pytest.mark.parametrize("append", [False, True])
+def test_graph_step_13b_four_layers_against_oracle(append):
+    """append: each layer's cache write fused into its decode (pa_decode_append)."""
     w = configs.config3(num_layers=4)
-    _run_graph_against_oracle(w, gpu.materialize(w, device=DEV))
+    _run_graph_against_oracle(w, gpu.materialize(w, device=DEV), append=append)
 
 
-def test_host_graph_step_13b_four_layers_against_oracle():
+@pytest.mark.parametrize("append", [False, True])
+def test_host_graph_step_13b_four_layers_against_oracle(append):
     """The end-to-end form: inputs from pinned host buffers, outputs to pinned
     host buffers, one captured graph; the device input buffers are poisoned
     before each replay."""
     w = configs.config3(num_layers=4)
-    _run_graph_against_oracle(w, gpu.materialize(w, device=DEV), host=True)
+    _run_graph_against_oracle(w, gpu.materialize(w, device=DEV), host=True, append=append)
 
 
-def test_graph_step_long_context_fp8_against_oracle():
+@pytest.mark.parametrize("append", [False, True])
+def test_graph_step_long_context_fp8_against_oracle(append):
     w = configs.config5(num_layers=2)
     sc = configs.fp8_scales(w)
-    _run_graph_against_oracle(w, materialize_fp8(w, layers=[0, 1]), fp8_scales=sc)
+    _run_graph_against_oracle(w, materialize_fp8(w, layers=[0, 1]), fp8_scales=sc, append=append)
 
 
 def test_graph_step_shared_prefix_copy_on_write_against_oracle():
