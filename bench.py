@@ -3,9 +3,9 @@
 One step = one decode step of the workload through the library: for every
 layer the cache write of the new tokens and the paged decode (partition pass
 + merge).  When every sequence brings one new token at position c - 1 (all
-decode workloads but the shared-prefix one) the write is fused into the
-decode (pa_decode_append); otherwise, and with --no-append, the step runs the
-slot map and a cache-write kernel before each decode.  The headline metric
+decode workloads but the shared-prefix one) and the caches are fp16, the write
+is fused into the decode (pa_decode_append); otherwise (and with --append off)
+the step runs the slot map and a cache-write kernel before each decode.  The headline metric
 is paged-decode KV GB/s: algorithmic bytes of all decode calls of the step
 (q + the gathered K/V of the c_s live tokens + out + block-table entries and
 context lengths) over the step time; also reported as % of the measured HBM
@@ -65,9 +65,12 @@ def parse_args():
     ap.add_argument("--prefill-workload", choices=["chunked", "mixed"], default="chunked",
                     help="--op prefill: 4 x 512-token chunks (chunked) or 2 chunks plus 64 decode "
                          "rows in one call (mixed; also timed as separate prefill and decode calls)")
-    ap.add_argument("--no-append", action="store_true",
-                    help="run the cache write as its own kernel (slot map + pa_reshape_and_cache) "
-                         "instead of fused into the decode")
+    ap.add_argument("--append", choices=["auto", "on", "off"], default="auto",
+                    help="cache write fused into the decode (pa_decode_append: on), or its own "
+                         "kernel after a slot map (off); auto: fused for fp16 caches, separate "
+                         "for FP8 caches (the faster of the two on each)")
+    ap.add_argument("--no-append", dest="append", action="store_const", const="off",
+                    help="same as --append off")
     ap.add_argument("--also", default="c5",
                     help="comma-separated workloads measured after the main one in the same run "
                          "(single GPU only; 'none' to skip); each gets its own record under 'also'")
@@ -227,7 +230,7 @@ def weak_scaling_value(bytes_per_rank_step: int, world: int, ms_per_step_max: fl
 class Step:
     """Device state of the workload and its decode step (the library's DecodeStep)."""
 
-    def __init__(self, w, device, fp8: bool = False, append: bool = True):
+    def __init__(self, w, device, fp8: bool = False, append: str = "auto"):
         import torch
 
         import paged_kv_cache_158_gb300 as pa
@@ -260,8 +263,12 @@ class Step:
         outs = [torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=device)
                 for _ in dw.layers]
         # One new token per sequence at position c - 1 (every decode workload but the shared
-        # prefix one, which writes whole suffixes): the cache write rides in the decode.
-        self.append = append and copy_pairs is None and bool(np.all(w.context_lens > 0))
+        # prefix one, which writes whole suffixes): with fp16 caches the cache write rides in
+        # the decode.  With FP8 caches the fused kernel measured slower than the separate write
+        # (long-context step 6221 vs 6521 GB/s), so the FP8 step keeps the write kernel unless
+        # --append forces the fused one.
+        self.append = (append == "on" or (append == "auto" and not fp8)) and copy_pairs is None \
+            and bool(np.all(w.context_lens > 0))
         self.step = DecodeStep(dw.key_caches, dw.value_caches, dw.queries, dw.keys_new, dw.values_new,
                                outs, dw.block_tables, dw.context_lens, dw.token_seq, dw.token_pos,
                                w.block_size, w.num_blocks, w.scale, self.max_ctx, copy_pairs,
@@ -330,7 +337,7 @@ def measure_step(args, w, fp8: bool, device, world):
 
     import paged_kv_cache_158_gb300 as pa
 
-    st = Step(w, device, fp8, append=not args.no_append)
+    st = Step(w, device, fp8, append=args.append)
     L = len(st.dw.layers)
     stream = torch.cuda.current_stream(device)
     for _ in range(args.warmup):

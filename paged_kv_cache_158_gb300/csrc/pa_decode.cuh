@@ -238,38 +238,42 @@ __device__ __forceinline__ void issue_chunk(const DecodeParams& a, const ItemInf
 }
 
 // The fused cache write of one sequence's new token (warp-wide; call only
-// for the chunk that holds position pos = c - 1): the new key/value rows of
-// (sequence, head h), prefetched as lane < D/8's 16 bytes each in k, v, go to
-// the cache slot of pos and over the chunk's staged rows at `row` (the
-// stage's K rows at Ks, V rows at Vs); for FP8 caches they are quantised as
-// the cache-write kernel quantises them.
+// for the chunk that holds position pos = c - 1).  Lanes 0..15 carry the new
+// key row and lanes 16..31 the value row of (sequence, head h), 16 bytes of
+// fp16 each (lanes whose index within the half is >= D/8 carry nothing): w
+// is that piece, or for FP8 caches its 8 E4M3 codes in w.x, w.y (quantised
+// as the cache-write kernel quantises them).  The piece goes to the cache
+// slot of pos and over the chunk's staged row `row` (K rows at Ks, V rows at
+// Vs).
 template <int D, int B, bool F8>
 __device__ __forceinline__ void append_new_token(const DecodeParams& a, int h, int phys, int pos,
                                                  int row, unsigned char* Ks, unsigned char* Vs,
-                                                 int lane, const uint4& k, const uint4& v) {
+                                                 int lane, const uint4& w) {
   using T = DecodeTraits<D, B, F8>;
-  const size_t dst = (((size_t)phys * a.num_heads + h) * B + pos % B) * D * T::ELEM;  // bytes
-  unsigned char* kc = static_cast<unsigned char*>(const_cast<void*>(a.key_cache)) + dst;
-  unsigned char* vc = static_cast<unsigned char*>(const_cast<void*>(a.value_cache)) + dst;
-  unsigned char* ks = Ks + (size_t)row * D * T::ELEM;
-  unsigned char* vs = Vs + (size_t)row * D * T::ELEM;
-  if (lane < D / 8) {
-    if constexpr (F8) {
-      const uint2 kq = quantize8(k, a.k_scale), vq = quantize8(v, a.v_scale);
-      reinterpret_cast<uint2*>(kc)[lane] = kq;
-      reinterpret_cast<uint2*>(vc)[lane] = vq;
-      reinterpret_cast<uint2*>(ks)[lane] = kq;
-      reinterpret_cast<uint2*>(vs)[lane] = vq;
-    } else {
-      reinterpret_cast<uint4*>(kc)[lane] = k;
-      reinterpret_cast<uint4*>(vc)[lane] = v;
-      reinterpret_cast<uint4*>(ks)[lane] = k;
-      reinterpret_cast<uint4*>(vs)[lane] = v;
-    }
+  constexpr int PIECE = 8 * T::ELEM;  // bytes of one lane's piece in the cache
+  const bool is_v = lane >= 16;
+  const int idx = lane & 15;
+  const size_t dst = (((size_t)phys * a.num_heads + h) * B + pos % B) * D * T::ELEM +
+                     (size_t)idx * PIECE;  // bytes
+  unsigned char* c = static_cast<unsigned char*>(const_cast<void*>(is_v ? a.value_cache : a.key_cache));
+  unsigned char* st = (is_v ? Vs : Ks) + (size_t)row * D * T::ELEM + idx * PIECE;
+  // The staged row first, then the fence that keeps the next bulk copy into
+  // this stage from overtaking it; the cache store goes last, so the fence
+  // does not wait for it.
+  if (idx < D / 8) {
+    if constexpr (F8)
+      *reinterpret_cast<uint2*>(st) = make_uint2(w.x, w.y);
+    else
+      *reinterpret_cast<uint4*>(st) = w;
   }
-  // The next bulk copy into this stage must not overtake these writes.
   fence_proxy_async_smem();
   __syncwarp();
+  if (idx < D / 8) {
+    if constexpr (F8)
+      *reinterpret_cast<uint2*>(c + dst) = make_uint2(w.x, w.y);
+    else
+      *reinterpret_cast<uint4*>(c + dst) = w;
+  }
 }
 
 // A lane's query slice: DPL fp16 values (16 or 32 bytes).
@@ -634,25 +638,33 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
 #pragma unroll
     for (int i = 0; i < T::DPL; ++i) o[i] = 0.f;
     // APPEND: the last item of a (sequence, head) holds its new token in
-    // chunk a_chunk; the warp that owns that chunk loads the new rows now, so
-    // the loads are long done when the chunk lands.
+    // chunk a_chunk; the warp that owns that chunk loads the new rows now
+    // (lanes 0..15 the key row, 16..31 the value row), so the loads are long
+    // done when the chunk lands.
     int a_chunk = -1;
-    uint4 a_k = make_uint4(0, 0, 0, 0), a_v = a_k;
+    uint4 a_w = make_uint4(0, 0, 0, 0);
     if constexpr (APPEND) {
       if (it.t_end == it.c && it.c > 0 && !clip_s[it.s] &&
           ((it.c - 1 - it.t_begin) / T::TC) % T::NW == warp) {
         a_chunk = (it.c - 1 - it.t_begin) / T::TC;
-        if (lane < D / 8) {
-          const size_t src = sh * D;  // fp16 elements of (sequence, head) in key_new / value_new
-          a_k = reinterpret_cast<const uint4*>(static_cast<const __half*>(a.key_new) + src)[lane];
-          a_v = reinterpret_cast<const uint4*>(static_cast<const __half*>(a.value_new) + src)[lane];
-        }
+        const __half* row = static_cast<const __half*>(lane >= 16 ? a.value_new : a.key_new) + sh * D;
+        if ((lane & 15) < D / 8) a_w = reinterpret_cast<const uint4*>(row)[lane & 15];
       }
     }
 
     for (int i = 0; i < n_my; ++i) {
       const int st = st_c;
       const uint32_t bar = my_bars_s + 8 * st;
+      const int chunk = warp + i * T::NW;
+      // FP8: the new rows' codes are made while this chunk's copy is still in
+      // flight (eight IEEE divisions per lane).
+      if constexpr (APPEND && F8) {
+        if (chunk == a_chunk) {
+          const uint2 q = quantize8(a_w, lane >= 16 ? a.v_scale : a.k_scale);
+          a_w.x = q.x;
+          a_w.y = q.y;
+        }
+      }
       bool ok = mbar_wait_bounded(bar, ph_c);
       ok = __all_sync(kFullMask, ok);
       if (!ok) {
@@ -666,7 +678,6 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
         }
         break;
       }
-      const int chunk = warp + i * T::NW;
       const int t0 = it.t_begin + chunk * T::TC;
       const int rows = min(T::TC, it.t_end - t0);
       int ph[T::BPC];
@@ -682,7 +693,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
           for (int b = 1; b < T::BPC; ++b)
             if (row / B == b) phys = ph[b];
           append_new_token<D, B, F8>(a, it.h, phys, it.c - 1, row, Ks, Ks + T::CHUNK_BYTES, lane,
-                                     a_k, a_v);
+                                     a_w);
         }
         if (rows == T::TC)
           process_chunk<D, B, F8, true>(Ks, Ks + T::CHUNK_BYTES, rows, q, a.scale_log2, my_p, lane,
