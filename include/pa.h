@@ -337,6 +337,39 @@ pa_status pa_prefill_fp8(void* out, const void* query, const void* key_cache,
                          float k_scale, float v_scale, int max_query_len, pa_stream_t stream);
 
 /*
+ * pa_prefill and pa_prefill_fp8 with flags.  With flags == 0 they are
+ * pa_prefill and pa_prefill_fp8.  The kernel may start while the kernel
+ * enqueued just before the call still runs (programmatic launch); by default
+ * it waits for that kernel before it reads any input.
+ *
+ * PA_PREFILL_INPUTS_READY: the kernel enqueued on the stream just before this
+ * call writes none of the call's inputs (query, caches, block tables,
+ * context lengths, query_start).  The kernel then plans its work, loads its
+ * query and K/V tiles and computes while that kernel finishes, and waits for
+ * it only before it stores the output.  Calls on independent data (other
+ * layers' or other batches' prefill calls, say) then overlap: a call's first
+ * CTAs fill the SMs the previous call's last wave leaves idle.  A preceding
+ * kernel that writes an input (a cache write, a projection producing the
+ * queries) makes the call read stale values without any report.  Not part
+ * of the pages; a launch-latency option.  Unknown flag bits return
+ * PA_ERR_INVALID_ARG.
+ */
+#define PA_PREFILL_INPUTS_READY 2u
+pa_status pa_prefill_ex(void* out, const void* query, const void* key_cache,
+                        const void* value_cache, const int32_t* block_tables,
+                        int max_blocks_per_seq, const int32_t* context_lens,
+                        const int32_t* query_start, int num_seqs, int num_query_tokens,
+                        int num_heads, int head_dim, int block_size, int num_blocks, float scale,
+                        int max_query_len, unsigned int flags, pa_stream_t stream);
+pa_status pa_prefill_fp8_ex(void* out, const void* query, const void* key_cache,
+                            const void* value_cache, const int32_t* block_tables,
+                            int max_blocks_per_seq, const int32_t* context_lens,
+                            const int32_t* query_start, int num_seqs, int num_query_tokens,
+                            int num_heads, int head_dim, int block_size, int num_blocks,
+                            float scale, float k_scale, float v_scale, int max_query_len,
+                            unsigned int flags, pa_stream_t stream);
+
+/*
  * Block swap between the device cache and a host copy [P4 §三: when GPU
  * memory runs short the scheduler moves some blocks to CPU memory and brings
  * them back when needed (blocks_to_swap_out / blocks_to_swap_in); P2 §4.3:

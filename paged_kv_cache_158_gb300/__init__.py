@@ -75,6 +75,12 @@ _lib.pa_prefill.restype = _i32
 _lib.pa_prefill_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
                                 _i32, _i32, _f32, _f32, _f32, _i32, _vp]
 _lib.pa_prefill_fp8.restype = _i32
+_lib.pa_prefill_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                               _i32, _f32, _i32, ctypes.c_uint32, _vp]
+_lib.pa_prefill_ex.restype = _i32
+_lib.pa_prefill_fp8_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
+                                   _i32, _i32, _f32, _f32, _f32, _i32, ctypes.c_uint32, _vp]
+_lib.pa_prefill_fp8_ex.restype = _i32
 _lib.pa_swap_blocks.argtypes = [_vp, _vp, _i32, _vp, _i32, _sz, ctypes.c_int64, ctypes.c_int64, _vp]
 _lib.pa_swap_blocks.restype = _i32
 _lib.pa_copy_blocks_fp8.argtypes = [_vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _vp]
@@ -85,6 +91,7 @@ PA_ERRBIT_BLOCK_ID, PA_ERRBIT_CONTEXT, PA_ERRBIT_SLOT = 0x1, 0x2, 0x4
 PA_ERRBIT_COPY, PA_ERRBIT_TOKEN, PA_ERRBIT_TIMEOUT = 0x8, 0x10, 0x20
 PA_DECODE_ZEROED_WORKSPACE = 0x1
 PA_DECODE_INPUTS_READY = 0x2
+PA_PREFILL_INPUTS_READY = 0x2
 
 
 class PAError(RuntimeError):
@@ -378,6 +385,25 @@ def pa_prefill(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
              max_query_len, stream, None)
 
 
+def pa_prefill_ex(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                  value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                  query_start: torch.Tensor, scale: float, max_query_len: int, flags: int = 0,
+                  stream=None) -> None:
+    """pa_prefill with flags (PA_PREFILL_INPUTS_READY; see pa_prefill_ex in include/pa.h)."""
+    _prefill(out, query, key_cache, value_cache, block_tables, context_lens, query_start, scale,
+             max_query_len, stream, None, flags)
+
+
+def pa_prefill_fp8_ex(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                      value_cache: torch.Tensor, block_tables: torch.Tensor,
+                      context_lens: torch.Tensor, query_start: torch.Tensor, scale: float,
+                      k_scale: float, v_scale: float, max_query_len: int, flags: int = 0,
+                      stream=None) -> None:
+    """pa_prefill_fp8 with flags (see pa_prefill_ex in include/pa.h)."""
+    _prefill(out, query, key_cache, value_cache, block_tables, context_lens, query_start, scale,
+             max_query_len, stream, (float(k_scale), float(v_scale)), flags)
+
+
 def pa_prefill_fp8(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
                    value_cache: torch.Tensor, block_tables: torch.Tensor,
                    context_lens: torch.Tensor, query_start: torch.Tensor, scale: float,
@@ -388,7 +414,7 @@ def pa_prefill_fp8(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tens
 
 
 def _prefill(out, query, key_cache, value_cache, block_tables, context_lens, query_start, scale,
-             max_query_len, stream, fp8) -> None:
+             max_query_len, stream, fp8, flags=None) -> None:
     TQ, H, D = query.shape
     NB, H2, B, D2 = key_cache.shape
     S = context_lens.shape[0]
@@ -404,11 +430,12 @@ def _prefill(out, query, key_cache, value_cache, block_tables, context_lens, que
               _ptr(block_tables, "block_tables", torch.int32), block_tables.shape[1],
               _ptr(context_lens, "context_lens", torch.int32),
               _ptr(query_start, "query_start", torch.int32), S, TQ, H, D, B, NB, float(scale))
-    if fp8 is None:
-        st = _lib.pa_prefill(*common, int(max_query_len), _stream(stream))
-    else:
-        st = _lib.pa_prefill_fp8(*common, fp8[0], fp8[1], int(max_query_len), _stream(stream))
-    _check(st, "pa_prefill_fp8" if fp8 is not None else "pa_prefill")
+    name = "pa_prefill" + ("_fp8" if fp8 is not None else "") + ("_ex" if flags is not None else "")
+    args = common + ((fp8[0], fp8[1]) if fp8 is not None else ()) + (int(max_query_len),)
+    if flags is not None:
+        args += (int(flags),)
+    st = getattr(_lib, name)(*args, _stream(stream))
+    _check(st, name)
 
 
 def _swap_ptr(t: torch.Tensor, name: str) -> int:
@@ -483,7 +510,8 @@ __all__ = [
     "pa_selftest_wait_timeout",
     "pa_decode_fp8", "pa_reshape_and_cache_fp8", "pa_copy_blocks_fp8", "pa_convert_cache_fp8",
     "pa_swap_blocks", "pa_prefill", "pa_prefill_fp8", "pa_decode_noalloc", "pa_decode_ex",
-    "pa_decode_fp8_ex", "pa_decode_append", "pa_decode_append_fp8",
+    "pa_decode_fp8_ex", "pa_decode_append", "pa_decode_append_fp8", "pa_prefill_ex",
+    "pa_prefill_fp8_ex",
     "pa_status_string", "pa_decode_workspace_size", "pa_decode_partition_tokens",
     "pa_decode_set_partition_tokens", "decode_workspace", "raise_on_device_errors", "PAError",
 ]

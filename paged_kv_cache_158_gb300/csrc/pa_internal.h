@@ -118,6 +118,7 @@ struct PrefillArgs {
   float scale_log2;   // scale * log2(e) (times the key scale for FP8 caches)
   bool fp8;           // E4M3 caches (uint8 codes)
   float v_scale;      // FP8 caches: value scale
+  bool inputs_ready;  // the kernel before the call writes none of its inputs (read before the wait)
 };
 cudaError_t launch_prefill(const PrefillArgs& args, cudaStream_t stream);
 // The cache's rows (num_blocks * num_heads * block_size) fit the kernel's int coordinates.

@@ -65,9 +65,15 @@ struct PrefillTraits {
   static constexpr int QB = kQT * D * 2;
   static constexpr int KB = kKT * D * 2;
   static constexpr int STB = kKT * D;               // FP8 caches: one tile of codes
+  // V stages.  A third one for fp16 caches (a V tile's copy could start a
+  // whole KV-tile period earlier) fits the shared memory but measured 2 %
+  // slower on the 7B-shaped chunked prefill (1086 vs 1108 TFLOP/s); FP8
+  // caches have no room for it.
+  static constexpr int NVS = 2;
   static constexpr int OFF_Q = 0;                   // Q tile x at OFF_Q + x*QB
-  static constexpr int OFF_K0 = 2 * QB;             // stage s: K at OFF_K0 + s*2*KB, V after it
-  static constexpr int OFF_ST = OFF_K0 + 4 * KB;    // FP8 caches: K codes, then V codes
+  static constexpr int OFF_K0 = 2 * QB;             // K stage s at OFF_K0 + s*KB (s < 2)
+  static constexpr int OFF_V0 = OFF_K0 + 2 * KB;    // V stage s at OFF_V0 + s*KB (s < NVS)
+  static constexpr int OFF_ST = OFF_V0 + NVS * KB;  // FP8 caches: K codes, then V codes
   static constexpr int OFF_BAR = OFF_ST + (F8 ? 2 * STB : 0);
   // Decode rows: their rings use the Q and K/V stage area, their mbarriers
   // (up to 12 warps x 4 stages) and softmax weights follow the barriers.
@@ -124,6 +130,7 @@ struct PrefillParams {
   int oob_row;                   // a row coordinate past the cache (zero-filled loads)
   float scale_log2;              // scale * log2(e), times the key scale for FP8 caches
   float v_scale;                 // value scale (1 for fp16 caches)
+  int inputs_ready;              // 1: inputs are read before the wait, outputs stored after it
 };
 
 // Per-CTA geometry of one query tile (x = 0, 1 of the pair).
@@ -186,10 +193,13 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
   const uint32_t s_base = smem_u32(sm);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + T::OFF_BAR);
   // barriers: 0 q_full; 1,2 k_full[st]; 3,4 s_full[x]; 5,6 p_full[x]; 7,8 o_full[x]; 9 done;
-  // 10,11 k_empty[st]; 12,13 v_full[st]; 14,15 v_empty[st]; FP8 caches: 16 kc_full, 17 kc_empty,
-  // 18 vc_full, 19 vc_empty (the staged codes of the next K / V tile).  With FP8 caches the
-  // fp16 stages are filled by the two widening warps (k_full / v_full: one arrival each).
+  // 10,11 k_empty[st]; 12,13,20 v_full[st]; 14,15,21 v_empty[st]; FP8 caches: 16 kc_full,
+  // 17 kc_empty, 18 vc_full, 19 vc_empty (the staged codes of the next K / V tile).  With FP8
+  // caches the fp16 stages are filled by the two widening warps (k_full / v_full: one arrival
+  // each).
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  auto v_full = [&](int st) { return bar(st < 2 ? 12 + st : 20); };
+  auto v_empty = [&](int st) { return bar(st < 2 ? 14 + st : 21); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + T::OFF_BAR + 192);
   int* fail = reinterpret_cast<int*>(sm + T::OFF_BAR + 196);
 
@@ -222,6 +232,8 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
     mbar_init(bar(17), 2);
     mbar_init(bar(18), 1);
     mbar_init(bar(19), 2);
+    mbar_init(bar(20), F8 ? 2 : 1);
+    mbar_init(bar(21), 1);
     *fail = 0;
     fence_mbar_init();
     prefetch_tensormap(&tq);
@@ -233,10 +245,12 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
     tmem_relinquish();
   }
   // The launch may start while the kernel before it on the stream still runs
-  // (programmatic launch), and that kernel may write this call's inputs: the
-  // set-up above overlaps its tail, everything below reads inputs and runs
-  // after the wait.
-  pdl_wait();
+  // (programmatic launch).  That kernel may write this call's inputs, so by
+  // default everything below runs after the wait; the set-up above overlaps
+  // its tail.  With inputs_ready (the caller's word that it writes none of
+  // them) the planning, the loads and the products run at once, and only the
+  // output stores wait (decode rows wait first).
+  if (!a.inputs_ready) pdl_wait();
   // This CTA's unit (see pa_prefill_rows.cuh for the order), with its
   // sequence's query rows and context length; the table and scratch live in
   // the Q area until the first loads.  Up to 32 sequences: warp 1 alone;
@@ -269,6 +283,7 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
     // No tensor-core work: a decode row runs on CUDA cores; then the tensor
     // memory goes back.
     if (unit.kind == 2) {
+      pdl_wait();
       pdl_launch_dependents();
       const int s = a.seq_begin + unit.s, q_len = unit.q_len, c = unit.c;
       const bool bad = q_len != 1 || c < 1 || c > a.max_blocks * a.block_size ||
@@ -330,12 +345,13 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
   // after which warp 0 frees the tensor memory.
   if (warp >= 8) {
     setmaxnreg_dec<kRegsProducer>();
-    // K and V of tile t sit in stage t & 1 of two separate rings: k_full / v_full
-    // (barriers 1 + st / 12 + st) complete once per tile, parity (t >> 1) & 1;
-    // k_empty / v_empty (10 + st / 14 + st) once per tile that used the stage.
+    // K of tile t sits in stage t & 1 of a two-stage ring, V in stage t % NVS of
+    // its own ring: k_full / v_full complete once per tile, parity (t >> 1) & 1
+    // and (t / NVS) & 1; k_empty / v_empty once per tile that used the stage.
     // K is released after the tile's QK products, V after its P.V products.
+    constexpr int NVS = T::NVS;
     auto wait_k = [&](int t) { return mbar_wait_bounded(bar(1 + (t & 1)), (t >> 1) & 1); };
-    auto wait_v = [&](int t) { return mbar_wait_bounded(bar(12 + (t & 1)), (t >> 1) & 1); };
+    auto wait_v = [&](int t) { return mbar_wait_bounded(v_full(t % NVS), (t / NVS) & 1); };
     if (warp == 9 && n_kv > 0) {
       // ---------------- TMA warp: Q tiles, then K/V tiles into a two-stage ring
       const int32_t* bt = a.block_tables + (size_t)s * a.max_blocks;
@@ -379,9 +395,9 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
           if (lane < bpt)
             tma_load_2d(dst + (uint32_t)(lane * a.block_size * D), is_v ? &tv : &tk, 0, row, fb);
         } else {
-          const int st = t & 1;
-          const uint32_t dst = s_base + T::OFF_K0 + st * 2 * T::KB + (is_v ? T::KB : 0);
-          const uint32_t fb = bar((is_v ? 12 : 1) + st);
+          const uint32_t dst = is_v ? s_base + T::OFF_V0 + (t % NVS) * T::KB
+                                    : s_base + T::OFF_K0 + (t & 1) * T::KB;
+          const uint32_t fb = is_v ? v_full(t % NVS) : bar(1 + (t & 1));
           if (lane == 0) mbar_arrive_expect_tx(fb, T::KB);
           __syncwarp();
           if (lane < bpt) {  // lane b issues block b's boxes
@@ -394,19 +410,24 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
       };
       // The barrier a copy of tile t waits on before it may start, and its parity.
       auto free_bar = [&](int t, bool is_v) {
-        return F8 ? bar(is_v ? 19 : 17) : bar((is_v ? 14 : 10) + (t & 1));
+        return F8 ? bar(is_v ? 19 : 17) : is_v ? v_empty(t % NVS) : bar(10 + (t & 1));
       };
-      auto free_par = [&](int t) { return F8 ? (uint32_t)((t - 1) & 1) : (uint32_t)(((t >> 1) - 1) & 1); };
-      const int first_wait = F8 ? 1 : 2;
+      auto free_par = [&](int t, bool is_v) {
+        return F8 ? (uint32_t)((t - 1) & 1)
+                  : is_v ? (uint32_t)((t / NVS - 1) & 1) : (uint32_t)(((t >> 1) - 1) & 1);
+      };
+      auto first_wait = [&](bool is_v) { return F8 ? 1 : is_v ? NVS : 2; };
       int row = tile_row(0);
       int k_issued = 0, v_issued = 0;
       bool ok = true;
       for (int t = 0; t < n_kv && ok; ++t) {
-        if (t >= first_wait) ok = __all_sync(kFullMask, mbar_wait_bounded(free_bar(t, false), free_par(t)));
+        if (t >= first_wait(false))
+          ok = __all_sync(kFullMask, mbar_wait_bounded(free_bar(t, false), free_par(t, false)));
         if (!ok) break;
         issue(t, row, false);
         ++k_issued;
-        if (t >= first_wait) ok = __all_sync(kFullMask, mbar_wait_bounded(free_bar(t, true), free_par(t)));
+        if (t >= first_wait(true))
+          ok = __all_sync(kFullMask, mbar_wait_bounded(free_bar(t, true), free_par(t, true)));
         if (!ok) break;
         issue(t, row, true);
         ++v_issued;
@@ -421,7 +442,7 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
           if (v_issued > 0) mbar_wait_bounded(bar(18), (v_issued - 1) & 1);
         } else {
           for (int u = max(0, k_issued - 2); u < k_issued; ++u) wait_k(u);
-          for (int u = max(0, v_issued - 2); u < v_issued; ++u) wait_v(u);
+          for (int u = max(0, v_issued - NVS); u < v_issued; ++u) wait_v(u);
         }
       }
     } else if (F8 && (warp == 10 || warp == 11) && n_kv > 0) {
@@ -437,14 +458,15 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
 #pragma unroll
         for (int kv = 0; kv < 2 && ok; ++kv) {
           ok = __all_sync(kFullMask, mbar_wait_bounded(bar(kv ? 18 : 16), t & 1));
+          static_assert(!F8 || NVS == 2, "the widening warps fill two-stage rings");
           if (ok && t >= 2)
             ok = __all_sync(kFullMask, mbar_wait_bounded(bar((kv ? 14 : 10) + st), ((t >> 1) - 1) & 1));
           // Warp-uniform: the failure flag may be set by another warp between
           // two lanes' reads, and the widening ends in a __syncwarp.
           ok = __all_sync(kFullMask, ok && !*fail);
           if (!ok) break;
-          widen_tile<D>(sm + T::OFF_ST + kv * T::STB, sm + T::OFF_K0 + st * 2 * T::KB + kv * T::KB,
-                        ctid);
+          widen_tile<D>(sm + T::OFF_ST + kv * T::STB,
+                        sm + (kv ? T::OFF_V0 : T::OFF_K0) + st * T::KB, ctid);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -467,8 +489,8 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
     // adds a compile-time offset.
     const uint64_t q_desc0 = umma_desc_sw128(s_base + T::OFF_Q, 16, 1024);
     const uint64_t k_desc0 = umma_desc_sw128(s_base + T::OFF_K0, 16, 1024);
-    const uint64_t v_desc0 = umma_desc_sw128(s_base + T::OFF_K0 + T::KB, T::ATOM, 1024);
-    constexpr uint64_t kStageStep = (uint64_t)(2 * T::KB) >> 4;
+    const uint64_t v_desc0 = umma_desc_sw128(s_base + T::OFF_V0, T::ATOM, 1024);
+    constexpr uint64_t kStageStep = (uint64_t)T::KB >> 4;
     auto qk_mma = [&](int x, int t, bool release) {
       const uint64_t qd = q_desc0 + (uint64_t)((x * T::QB) >> 4);
       const uint64_t kd = k_desc0 + (t & 1) * kStageStep;
@@ -486,7 +508,7 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
       }
     };
     auto pv_mma = [&](int x, int t, bool release) {
-      const uint64_t vd = v_desc0 + (t & 1) * kStageStep;
+      const uint64_t vd = v_desc0 + (t % NVS) * kStageStep;
       tc_fence_after();
 #pragma unroll
       for (int k = 0; k < kKT / 16; ++k)
@@ -495,7 +517,7 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
       umma_commit_if(leader, bar(7 + x));
       ++pv[x];
       if (release) {  // the last reader of V stage t & 1
-        umma_commit_if(leader, bar(14 + (t & 1)));
+        umma_commit_if(leader, v_empty(t % NVS));
         ++vrel;
       }
     };
@@ -504,7 +526,7 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
     auto zero_v_tail = [&](int t) {
       const int first = c - t * kKT;
       if (first >= kKT) return;
-      unsigned char* v = sm + T::OFF_K0 + (t & 1) * 2 * T::KB + T::KB;
+      unsigned char* v = sm + T::OFF_V0 + (t % NVS) * T::KB;
       const int nchunks = (kKT - max(first, 0)) * 8;
       for (int i = lane; i < nchunks * T::NA; i += 32) {
         const int at = i / nchunks, r = max(first, 0) + (i % nchunks) / 8, ch = i % 8;
@@ -549,7 +571,7 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
           if (pv[i] > 0) mbar_wait_bounded(bar(7 + i), (pv[i] - 1) & 1);
         }
         if (krel > 0) mbar_wait_bounded(bar(10 + ((krel - 1) & 1)), ((krel - 1) >> 1) & 1);
-        if (vrel > 0) mbar_wait_bounded(bar(14 + ((vrel - 1) & 1)), ((vrel - 1) >> 1) & 1);
+        if (vrel > 0) mbar_wait_bounded(v_empty((vrel - 1) % NVS), ((vrel - 1) / NVS) & 1);
       }
     }
     }
@@ -678,6 +700,7 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
       // The last P.V of this tile (phase n_kv - 1; the earlier ones completed
       // before S of the last tile was computed, so the parity is unambiguous).
       const bool done = __all_sync(kFullMask, mbar_wait_bounded(bar(7 + x), (qt.n_kv - 1) & 1) && !*fail);
+      pdl_wait();  // the output may be read or written by the kernel before this one
       if (done) {
         tc_fence_after();
         const float inv = l > 0.f ? a.v_scale / l : 0.f;  // v_scale: FP8 values (1 for fp16)
@@ -795,6 +818,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& g, cudaStream_t stream) {
   p.oob_row = (int)rows;
   p.scale_log2 = g.scale_log2;
   p.v_scale = F8 ? g.v_scale : 1.f;
+  p.inputs_ready = g.inputs_ready ? 1 : 0;
   // One launch per window of sequences.  The grid bounds the window's units:
   // a sequence of q tokens needs ceil(q / 256) units per head, at most qpairs,
   // and over the window sum(ceil(q / 256)) <= (TQ + 255 * n) / 256.

@@ -155,3 +155,56 @@ def test_prefill_large_logits_rescale_path(scale):
     out = run_prefill(w, dv)
     prefill_gate(out, oracle_prefill(w), f"prefill scale {scale}")
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+def _fp8_copy(w, dv):
+    ks, vs = configs.fp8_scales(w)
+    for name, sc in (("key_cache", ks), ("value_cache", vs)):
+        codes = torch.empty(dv[name].shape, dtype=torch.uint8, device=DEV)
+        pa.pa_convert_cache_fp8(dv[name], codes, sc)
+        dv[name] = codes
+    return ks, vs
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("shape", ["mixed", "7b"])
+def test_inputs_ready_back_to_back_calls_match_serial_calls(shape, fp8):
+    """PA_PREFILL_INPUTS_READY as the bench uses it: calls over three independent copies of the
+    inputs, three rounds back to back, each call behind the previous one (which writes only its
+    own output), give the bits of the same calls made one at a time after a synchronize.  The
+    7B-shaped batch has two waves of CTAs, so a call's first CTAs run beside the previous call's
+    last ones; the mixed batch has decode rows.  The mixed batch's output is also held to the
+    oracle."""
+    if shape == "mixed":
+        w = configs.prefill_workload("ready", 4300 + fp8, *MIXED, 4, 128, 16)
+    else:
+        w = configs.prefill_7b()
+    copies = [gpu.materialize_prefill(w, DEV) for _ in range(3)]
+    scales = [_fp8_copy(w, dv) for dv in copies] if fp8 else [None] * 3
+    tq = int(np.sum(w.extra["q_lens"]))
+    max_q = int(max(w.extra["q_lens"]))
+
+    def call(dv, sc, out, flags):
+        args = (out, dv["query"], dv["key_cache"], dv["value_cache"], dv["block_tables"],
+                dv["context_lens"], dv["query_start"], w.scale)
+        if fp8:
+            pa.pa_prefill_fp8_ex(*args, sc[0], sc[1], max_q, flags)
+        else:
+            pa.pa_prefill_ex(*args, max_q, flags)
+
+    refs = []
+    for dv, sc in zip(copies, scales):
+        refs.append(torch.full((tq, w.num_heads, w.head_dim), float("nan"), dtype=torch.float16,
+                               device=DEV))
+        call(dv, sc, refs[-1], 0)
+        torch.cuda.synchronize()
+    outs = [torch.full_like(r, float("nan")) for r in refs]
+    for _ in range(3):
+        for dv, sc, o in zip(copies, scales, outs):
+            call(dv, sc, o, pa.PA_PREFILL_INPUTS_READY)
+    torch.cuda.synchronize()
+    for o, r in zip(outs, refs):
+        assert torch.equal(o.view(torch.int16), r.view(torch.int16))
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+    if shape == "mixed" and not fp8:
+        prefill_gate(outs[0], oracle_prefill(w), "prefill inputs_ready")
