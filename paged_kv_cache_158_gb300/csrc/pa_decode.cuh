@@ -200,13 +200,17 @@ __device__ __forceinline__ bool chunk_ids_ok(const DecodeParams& a, const int (&
 
 // Issues the bulk copies of one chunk into a stage: for each block of the
 // chunk with live rows, its K rows and its V rows (contiguous in the
-// [NB][H][B][D] layout); only live rows are copied.  Warp-uniform: every
-// lane executes it with the same operands and only `leader` issues.
+// [NB][H][B][D] layout); only live rows are copied.  kn, vn (fp16 caches with
+// the cache write fused in, for the chunk holding a sequence's new token;
+// null otherwise): the chunk's last row comes from these new rows instead of
+// the cache, which does not hold them yet.  Warp-uniform: every lane executes
+// it with the same operands and only `leader` issues.
 template <int D, int B, bool F8>
 __device__ __forceinline__ void issue_chunk(const DecodeParams& a, const ItemInfo& it,
                                             const int (&phys)[DecodeTraits<D, B, F8>::BPC],
                                             int chunk, uint32_t stage, uint32_t bar,
-                                            uint64_t policy, bool leader) {
+                                            uint64_t policy, bool leader,
+                                            const void* kn = nullptr, const void* vn = nullptr) {
   using T = DecodeTraits<D, B, F8>;
   const int t0 = it.t_begin + chunk * T::TC;
   const int rows = min(T::TC, it.t_end - t0);
@@ -220,12 +224,18 @@ __device__ __forceinline__ void issue_chunk(const DecodeParams& a, const ItemInf
     return;
   }
   mbar_arrive_expect_tx_if(leader, bar, 2u * (uint32_t)rows * D * T::ELEM);
+  const int crows = kn != nullptr ? rows - 1 : rows;  // rows that come from the cache
+  if (kn != nullptr) {
+    const uint32_t soff = (uint32_t)(rows - 1) * D * T::ELEM;
+    bulk_g2s_hint_if(leader, stage + soff, kn, D * T::ELEM, bar, policy);
+    bulk_g2s_hint_if(leader, stage + T::CHUNK_BYTES + soff, vn, D * T::ELEM, bar, policy);
+  }
   // Byte offset of (block 0, head h, row t0 % B) and the stride between blocks.
   const size_t head_off = ((size_t)it.h * B + (t0 % B)) * D * T::ELEM;
   const size_t blk_stride = (size_t)a.num_heads * B * D * T::ELEM;
 #pragma unroll
   for (int b = 0; b < T::BPC; ++b) {
-    const int r = min(B, rows - b * B);
+    const int r = min(B, crows - b * B);
     if (r <= 0) break;
     const size_t off = (size_t)phys[b] * blk_stride + head_off;
     const uint32_t bytes = (uint32_t)r * D * T::ELEM;
@@ -243,8 +253,9 @@ __device__ __forceinline__ void issue_chunk(const DecodeParams& a, const ItemInf
 // fp16 each (lanes whose index within the half is >= D/8 carry nothing): w
 // is that piece, or for FP8 caches its 8 E4M3 codes in w.x, w.y (quantised
 // as the cache-write kernel quantises them).  The piece goes to the cache
-// slot of pos and over the chunk's staged row `row` (K rows at Ks, V rows at
-// Vs).
+// slot of pos; for FP8 caches also over the chunk's staged row `row` (K rows
+// at Ks, V rows at Vs), which the bulk copy filled with the slot's old codes
+// (for fp16 caches the copy already took that row from the new rows).
 template <int D, int B, bool F8>
 __device__ __forceinline__ void append_new_token(const DecodeParams& a, int h, int phys, int pos,
                                                  int row, unsigned char* Ks, unsigned char* Vs,
@@ -260,14 +271,11 @@ __device__ __forceinline__ void append_new_token(const DecodeParams& a, int h, i
   // The staged row first, then the fence that keeps the next bulk copy into
   // this stage from overtaking it; the cache store goes last, so the fence
   // does not wait for it.
-  if (idx < D / 8) {
-    if constexpr (F8)
-      *reinterpret_cast<uint2*>(st) = make_uint2(w.x, w.y);
-    else
-      *reinterpret_cast<uint4*>(st) = w;
+  if constexpr (F8) {
+    if (idx < D / 8) *reinterpret_cast<uint2*>(st) = make_uint2(w.x, w.y);
+    fence_proxy_async_smem();
+    __syncwarp();
   }
-  fence_proxy_async_smem();
-  __syncwarp();
   if (idx < D / 8) {
     if constexpr (F8)
       *reinterpret_cast<uint2*>(c + dst) = make_uint2(w.x, w.y);
@@ -528,6 +536,19 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
   const bool leader = lane == 0;
   const uint32_t my_stages_s = smem_u32(my_stages);
   const uint32_t my_bars_s = smem_u32(my_bars);
+  // fp16 caches with the cache write fused in: the new K and V rows that
+  // replace the last row of the chunk holding c - 1 in an item's last
+  // partition (null for every other chunk, and for clipped contexts).
+  auto new_rows = [&](const ItemInfo& x, int chunk, const void*& kn, const void*& vn) {
+    kn = vn = nullptr;
+    if constexpr (APPEND && !F8) {
+      if (x.t_end == x.c && x.c > 0 && !clip_s[x.s] && chunk == (x.c - 1 - x.t_begin) / T::TC) {
+        const size_t off = ((size_t)(a.seq_begin + x.s) * H + x.h) * D;
+        kn = static_cast<const __half*>(a.key_new) + off;
+        vn = static_cast<const __half*>(a.value_new) + off;
+      }
+    }
+  };
   // The first item's first copies, still before the wait (warp-uniform; the
   // leader issues).
   {
@@ -536,8 +557,10 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
       const int chunk = warp + (int)iss * T::NW;
       int ph[T::BPC];
       chunk_ids<D, B, F8>(ph, bt_s, it, chunk);
+      const void *kn, *vn;
+      new_rows(it, chunk, kn, vn);
       issue_chunk<D, B, F8>(a, it, ph, chunk, my_stages_s + iss * T::STAGE_BYTES,
-                            my_bars_s + 8 * iss, policy, leader);
+                            my_bars_s + 8 * iss, policy, leader, kn, vn);
     }
   }
   // Stage of the next issue and of the next consumption (with its phase).
@@ -606,7 +629,9 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
           const int chunk = warp + k * T::NW;
           int ph[T::BPC];
           chunk_ids<D, B, F8>(ph, bt, it, chunk);
-          issue_chunk<D, B, F8>(a, it, ph, chunk, stage, bar, policy, leader);
+          const void *kn, *vn;
+          new_rows(it, chunk, kn, vn);
+          issue_chunk<D, B, F8>(a, it, ph, chunk, stage, bar, policy, leader, kn, vn);
         } else if (k - n_my < n_nx) {
           const int j = k - n_my;
           int ph[T::BPC];
@@ -618,7 +643,9 @@ __global__ void __launch_bounds__(DecodeTraits<D, B, F8>::THREADS, F8 ? 5 : 1)
               if (j == jj) v = nxp[jj][b];
             ph[b] = v;
           }
-          issue_chunk<D, B, F8>(a, nx, ph, warp + j * T::NW, stage, bar, policy, leader);
+          const void *kn, *vn;
+          new_rows(nx, warp + j * T::NW, kn, vn);
+          issue_chunk<D, B, F8>(a, nx, ph, warp + j * T::NW, stage, bar, policy, leader, kn, vn);
         } else {
           break;
         }
