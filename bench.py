@@ -260,8 +260,10 @@ class Step:
         self.bt_host = dw.block_tables.cpu().numpy()
         self.ctx_host = w.context_lens.copy()
         self.max_ctx = int(self.ctx_host.max())
-        outs = [torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=device)
-                for _ in dw.layers]
+        # One [L, S, H, D] allocation: consecutive layers' outputs back to back (fewer, larger
+        # read-back copies in the end-to-end step).
+        outs = list(torch.empty((len(dw.layers), w.num_seqs, w.num_heads, w.head_dim),
+                                dtype=torch.float16, device=device).unbind(0))
         # One new token per sequence at position c - 1 (every decode workload but the shared
         # prefix one, which writes whole suffixes): with fp16 caches the cache write rides in
         # the decode.  With FP8 caches the fused kernel measured slower than the separate write
@@ -510,11 +512,14 @@ def measure_e2e(st, args, world, device):
     import torch
     dw = st.dw
     pin = lambda t: t.detach().cpu().pin_memory()  # noqa: E731
-    h_q = [pin(t) for t in dw.queries]
-    h_k = [pin(t) for t in dw.keys_new]
-    h_v = [pin(t) for t in dw.values_new]
+    # Each kind's per-layer host buffers are views of one pinned [L, ...] tensor, like the
+    # device ones, so the step merges consecutive layers' copies.
+    h_q = list(pin(torch.stack(dw.queries)).unbind(0))
+    h_k = list(pin(torch.stack(dw.keys_new)).unbind(0))
+    h_v = list(pin(torch.stack(dw.values_new)).unbind(0))
     h_small = [pin(t) for t in (dw.block_tables, dw.context_lens, dw.token_seq, dw.token_pos)]
-    h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in st.outs]
+    h_out = list(torch.empty((len(st.outs),) + tuple(st.outs[0].shape), dtype=st.outs[0].dtype,
+                             pin_memory=True).unbind(0))
     h2d = sum(t.numel() * t.element_size() for t in h_q + h_k + h_v + h_small)
     d2h = sum(t.numel() * t.element_size() for t in h_out)
     st.step.bind_host(h_q, h_k, h_v, h_out, *h_small)
@@ -541,7 +546,11 @@ def measure_e2e(st, args, world, device):
     return {"value": round(st.bytes_per_decode * L * world / dt / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(dt * 1e3, 4), "steps": K, "cuda_graph": use_graph,
             "copies": "uploads on a copy stream ahead of the compute (waits at layers 0, 1, 2, 4, "
-                      "...); outputs read back on a second copy stream right behind the decodes",
+                      "...); outputs read back on a second copy stream right behind the decodes; "
+                      "one copy per layer group and tensor kind (per-layer buffers are views of "
+                      "one [L, ...] tensor on each side)",
+            "copies_per_step": sum(len(r) for r in st.step.host["up_runs"].values()) +
+                               sum(len(r) for r in st.step.host["down_runs"].values()) + 4,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 

@@ -53,6 +53,36 @@ def _overlap(a: torch.Tensor, b: torch.Tensor) -> bool:
     return a0 < b0 + b.numel() * b.element_size() and b0 < a0 + a.numel() * a.element_size()
 
 
+def _follows(a: torch.Tensor, b: torch.Tensor) -> bool:
+    """b starts where a ends, in the same storage (both contiguous, same dtype)."""
+    return (a.dtype == b.dtype and a.is_contiguous() and b.is_contiguous()
+            and a.untyped_storage().data_ptr() == b.untyped_storage().data_ptr()
+            and b.storage_offset() == a.storage_offset() + a.numel())
+
+
+def _span(ts: list[torch.Tensor]) -> torch.Tensor:
+    """One flat view over tensors that follow each other in one storage."""
+    if len(ts) == 1:
+        return ts[0]
+    t0 = ts[0]
+    return t0.new_empty(0).set_(t0.untyped_storage(), t0.storage_offset(),
+                                (sum(t.numel() for t in ts),))
+
+
+def _copy_runs(pairs: list[tuple[torch.Tensor, torch.Tensor]]) -> list[tuple[torch.Tensor, torch.Tensor]]:
+    """(source, destination) pairs merged into one pair per maximal run whose sources follow
+    each other in one storage and whose destinations do too: one copy instead of several."""
+    runs, i = [], 0
+    while i < len(pairs):
+        j = i + 1
+        while j < len(pairs) and _follows(pairs[j - 1][0], pairs[j][0]) and \
+                _follows(pairs[j - 1][1], pairs[j][1]):
+            j += 1
+        runs.append((_span([p[0] for p in pairs[i:j]]), _span([p[1] for p in pairs[i:j]])))
+        i = j
+    return runs
+
+
 def _pow2_groups(n: int) -> list[tuple[int, int]]:
     """Layer ranges [0, 1), [1, 2), [2, 4), [4, 8), ... covering n layers."""
     out, a = [], 0
@@ -144,7 +174,19 @@ class DecodeStep:
             if h.shape != d.shape or h.dtype != d.dtype or not h.is_contiguous():
                 raise ValueError("a host buffer does not match its device buffer")
         dev = self.queries[0].device
+        # The copies of each layer group (uploads) and of each mirror-image group (downloads),
+        # merged where consecutive layers' buffers lie back to back on both sides (for example
+        # views of one [L, ...] tensor): fewer, larger copies on the copy engines.
+        groups = _pow2_groups(n)
+        up_runs = {g0: _copy_runs([(h[i], d[i]) for h, d in ((queries, self.queries),
+                                                              (keys_new, self.keys_new),
+                                                              (values_new, self.values_new))
+                                   for i in range(g0, g1)])
+                   for g0, g1 in groups}
+        down_runs = {n - g0: _copy_runs([(self.outs[j], outs[j]) for j in range(n - g1, n - g0)])
+                     for g0, g1 in groups}
         self.host = {
+            "up_runs": up_runs, "down_runs": down_runs,
             "q": list(queries), "k": list(keys_new), "v": list(values_new), "out": list(outs),
             "small": [(block_tables, self.block_tables), (context_lens, self.context_lens),
                       (token_seq, self.token_seq), (token_pos, self.token_pos)],
@@ -167,10 +209,8 @@ class DecodeStep:
         groups = _pow2_groups(self.num_layers)
         with torch.cuda.stream(up):
             for g0, g1 in groups:
-                for i in range(g0, g1):
-                    self.queries[i].copy_(hb["q"][i], non_blocking=True)
-                    self.keys_new[i].copy_(hb["k"][i], non_blocking=True)
-                    self.values_new[i].copy_(hb["v"][i], non_blocking=True)
+                for h, d in hb["up_runs"][g0]:
+                    d.copy_(h, non_blocking=True)
                 hb["ev_in"][g0].record(up)
         with torch.cuda.stream(s):
             for h, d in hb["small"]:
@@ -195,8 +235,8 @@ class DecodeStep:
                 hb["ev_out"][i].record(s)
                 down.wait_event(hb["ev_out"][i])
                 with torch.cuda.stream(down):
-                    for j in range(ends[i + 1], i + 1):
-                        hb["out"][j].copy_(self.outs[j], non_blocking=True)
+                    for d, h in hb["down_runs"][i + 1]:
+                        h.copy_(d, non_blocking=True)
         # The step ends when its last output is on the host.
         s.wait_stream(down)
         s.wait_stream(up)

@@ -15,9 +15,13 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def make_step(w, dw, copy_pairs=None, fp8_scales=None):
-    outs = [torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16, device=DEV)
-            for _ in dw.layers]
+def make_step(w, dw, copy_pairs=None, fp8_scales=None, stacked_outs=False):
+    if stacked_outs:
+        outs = list(torch.empty((len(dw.layers), w.num_seqs, w.num_heads, w.head_dim),
+                                dtype=torch.float16, device=DEV).unbind(0))
+    else:
+        outs = [torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float16,
+                            device=DEV) for _ in dw.layers]
     return DecodeStep(dw.key_caches, dw.value_caches, dw.queries, dw.keys_new, dw.values_new, outs,
                       dw.block_tables, dw.context_lens, dw.token_seq, dw.token_pos, w.block_size,
                       w.num_blocks, w.scale, int(w.context_lens.max()), copy_pairs, fp8_scales)
@@ -98,22 +102,38 @@ def test_graph_step_with_copy_on_write():
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
 
 
-@pytest.mark.parametrize("cfg,layers,use_graph", [(2, [0], False), (5, [0, 1], True), (1, [0, 1, 2], True)])
-def test_host_staged_step_matches_device_step(cfg, layers, use_graph):
+@pytest.mark.parametrize("cfg,layers,use_graph,stacked", [
+    (2, [0], False, False), (5, [0, 1], True, False), (1, [0, 1, 2], True, False),
+    (3, list(range(11)), True, True), (3, list(range(11)), False, True)])
+def test_host_staged_step_matches_device_step(cfg, layers, use_graph, stacked):
     """Inputs uploaded from pinned host buffers and outputs read back, overlapped layer by
     layer (eager or as one graph): the host outputs and the caches are bit-identical to the
     device-resident step's, also after the host inputs change in place; the device input
-    buffers are poisoned before each run, so every input must come through the copies."""
+    buffers are poisoned before each run, so every input must come through the copies.
+    stacked: each kind's per-layer buffers are views of one [L, ...] tensor on both sides, so
+    the step merges the copies of each layer group (11 layers: groups of 1, 1, 2, 4, 3)."""
     w = configs.ALL[cfg]() if cfg != 5 else configs.config5(num_layers=2)
+    if cfg == 3:
+        w = configs.config3(num_layers=len(layers))
     dw_ref = gpu.materialize(w, layers=layers, device=DEV)
     ref = make_step(w, dw_ref)
     dw = gpu.materialize(w, layers=layers, device=DEV)
-    st = make_step(w, dw)
+    st = make_step(w, dw, stacked_outs=stacked)
     pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-    h_q, h_k, h_v = ([pin(t) for t in ts] for ts in (dw.queries, dw.keys_new, dw.values_new))
+    if stacked:
+        h_q, h_k, h_v = (list(pin(torch.stack(ts)).unbind(0))
+                         for ts in (dw.queries, dw.keys_new, dw.values_new))
+        h_out = list(torch.full((len(st.outs),) + tuple(st.outs[0].shape), float("nan"),
+                                dtype=torch.float16).pin_memory().unbind(0))
+    else:
+        h_q, h_k, h_v = ([pin(t) for t in ts] for ts in (dw.queries, dw.keys_new, dw.values_new))
+        h_out = [torch.full(o.shape, float("nan"), dtype=o.dtype).pin_memory() for o in st.outs]
     h_small = [pin(t) for t in (dw.block_tables, dw.context_lens, dw.token_seq, dw.token_pos)]
-    h_out = [torch.full(o.shape, float("nan"), dtype=o.dtype).pin_memory() for o in st.outs]
     st.bind_host(h_q, h_k, h_v, h_out, *h_small)
+    n_copies = sum(len(r) for r in st.host["up_runs"].values()) + \
+        sum(len(r) for r in st.host["down_runs"].values())
+    n_groups = len(st.host["up_runs"])
+    assert n_copies == (4 * n_groups if stacked else 4 * len(layers))
 
     def poison():
         for t in dw.queries + dw.keys_new + dw.values_new:

@@ -94,10 +94,23 @@ def materialize(w: Workload, layers=None, device="cuda", fill_caches: bool = Tru
         vn.append(upload_u16(synth.host_tensor(w.seed, w.value_new_stream(l), (T, w.num_heads, w.head_dim),
                                                w.kv_bank()), device))
     del scratch
+    # Each kind's per-layer tensors are views of one [L, ...] allocation, so consecutive
+    # layers' rows lie back to back (the decode step can then upload several layers in one copy).
+    qs, kn, vn = _stacked(qs), _stacked(kn), _stacked(vn)
     bt = None if w.block_tables is None else torch.from_numpy(w.block_tables).to(device)
     return DeviceWorkload(w, kcs, vcs, qs, kn, vn, bt, torch.from_numpy(w.context_lens).to(device),
                           torch.from_numpy(tok_seq).to(device), torch.from_numpy(tok_pos).to(device),
                           layers)
+
+
+def _stacked(ts: list) -> list:
+    """The tensors copied into one [len(ts), ...] allocation, returned as its per-row views."""
+    if not ts:
+        return ts
+    big = torch.empty((len(ts),) + tuple(ts[0].shape), dtype=ts[0].dtype, device=ts[0].device)
+    for i, t in enumerate(ts):
+        big[i].copy_(t)
+    return list(big.unbind(0))
 
 
 def host_pool(w: Workload, layer: int) -> tuple[np.ndarray, np.ndarray]:
