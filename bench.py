@@ -451,6 +451,8 @@ def measure_step(args, w, fp8: bool, device, world):
         "e2e": e2e,
     }
     launches = st.launches_per_step() * K * (2 if ms_graph is not None else 1)
+    if e2e is not None:  # the end-to-end pass is timed too
+        launches += st.launches_per_step() * e2e["steps"]
     del st
     torch.cuda.synchronize(device)
     torch.cuda.empty_cache()
