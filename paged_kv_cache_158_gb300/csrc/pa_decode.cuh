@@ -862,10 +862,10 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams a
     for (int j = 0; j < cnt; ++j) {
       const float w = __shfl_sync(kFullMask, wl, j);
       const int p = p0 + j;
-      Vec v;
+      Vec v = pre[0];  // a register select over pre[] (no local memory)
       if (p < kPre) {
 #pragma unroll
-        for (int k = 0; k < kPre; ++k)
+        for (int k = 1; k < kPre; ++k)
           if (k == p) v = pre[k];
       } else {
         v = *reinterpret_cast<const Vec*>(ob + (size_t)p * D);
