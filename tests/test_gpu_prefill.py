@@ -1,8 +1,9 @@
 """GPU parity of multi-query paged attention (chunked prefill and mixed
 prefill + decode batches, tensor cores) against the oracle: every output of
 small ragged batches (chunks crossing tile boundaries, one-token chunks,
-empty chunks, whole-context chunks, NaN in every dead slot), sampled rows of
-the 7B-shaped chunked prefill at full size, and the error reporting."""
+empty chunks, whole-context chunks, NaN in every dead slot), every output of
+the 7B-shaped chunked prefill at full size (and sampled rows of it), and the
+error reporting."""
 import numpy as np
 import pytest
 import torch
@@ -112,6 +113,18 @@ def test_prefill_7b_full_size_sampled_rows():
                                           np.array([0, 16], np.int32), w.scale)
             assert rc == 0
             prefill_gate(out[qs[s] + j0:qs[s] + j0 + 16], ref64, f"{w.name} s{s} rows {j0}..")
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+def test_prefill_7b_whole_call_against_oracle():
+    """The 7B-shaped chunked prefill at full size (4 x 512 new tokens over 2048-token
+    contexts, 32 heads): every output against the oracle (about 60 GFLOP in binary64 on the
+    host cores)."""
+    w = configs.prefill_7b()
+    dv = gpu.materialize_prefill(w, DEV)
+    out = run_prefill(w, dv)
+    torch.cuda.synchronize()
+    prefill_gate(out, oracle_prefill(w), f"{w.name} whole call")
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
 
 

@@ -1,7 +1,7 @@
 """GPU parity of multi-query paged attention over FP8 (E4M3) caches against the
 oracle: every output of small ragged batches (chunks crossing tile
 boundaries, one-token and empty chunks, NaN codes in every dead slot),
-sampled rows of the 7B-shaped chunked prefill at full size, and the
+the 7B-shaped chunked prefill at full size (whole call, and sampled rows), and the
 argument and error reporting.  The device codes come from the library's
 conversion kernel (tested bit-exact on its own); the oracle quantises its
 own host copy of the pool."""
@@ -105,6 +105,18 @@ def test_prefill_fp8_7b_full_size_sampled_rows():
             ref64 = oracle_out(w, kc8, vc8, q[qs[s] + j0:qs[s] + j0 + 16], w.block_tables[s:s + 1],
                                np.array([p_last + 1], np.int32), np.array([0, 16], np.int32))
             prefill_gate(out[qs[s] + j0:qs[s] + j0 + 16], ref64, f"fp8 {w.name} s{s} rows {j0}..")
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+def test_prefill_fp8_7b_whole_call_against_oracle():
+    """The 7B-shaped chunked prefill at full size over FP8 caches: every output against the
+    oracle's dequantising prefill on its own quantised copy of the pool."""
+    w = configs.prefill_7b()
+    dv = materialize_fp8(w)
+    out = run(w, dv)
+    torch.cuda.synchronize()
+    kc8, vc8 = oracle_pool(w)
+    prefill_gate(out, oracle_out(w, kc8, vc8), f"fp8 {w.name} whole call")
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
 
 
