@@ -198,6 +198,54 @@ __device__ __forceinline__ Unit plan_unit_warp(int k, int H, int qpairs, int sms
   return u;
 }
 
+// plan_unit_warp's order in closed form for a launch whose nseq sequences all
+// have the same k > 0 pairs (fixed-size chunks): the first wave's whole
+// groups, then rank by rank, with integer arithmetic instead of warp-wide
+// selections (every lane computes the same unit).
+__device__ __forceinline__ Unit plan_unit_uniform(int nseq, int k, int H, int sms, int b,
+                                                  int* total_units) {
+  Unit u{0, 0, 0, 0, 0, 0, 0};
+  const int G = H * k;  // units of one sequence
+  const int cu = nseq * G;
+  *total_units = cu;
+  if (b >= cu) return u;
+  int u1, s_w, g_w;  // units of the first wave; its last sequence and whole groups in it
+  const int s = sms / G;
+  if (s >= nseq) {
+    u1 = cu;
+    s_w = nseq;
+    g_w = 0;
+  } else {
+    g_w = (sms - s * G) / k;
+    s_w = s;
+    u1 = s * G + g_w * k;
+  }
+  u.kind = 1;
+  if (b < u1) {
+    u.s = b / G;
+    const int r = b - u.s * G;
+    u.h = r / k;
+    u.pq = k - 1 - r % k;
+    return u;
+  }
+  // Rank r: the remaining groups' pair k - 1 - r (H - g_w groups of sequence s_w, then H
+  // of each later sequence).
+  const int per_rank = (H - g_w) + (nseq - s_w - 1) * H;
+  int t = b - u1;
+  const int rank = t / per_rank;
+  t -= rank * per_rank;
+  u.pq = k - 1 - rank;
+  if (t < H - g_w) {
+    u.s = s_w;
+    u.h = g_w + t;
+  } else {
+    t -= H - g_w;
+    u.s = s_w + 1 + t / H;
+    u.h = t % H;
+  }
+  return u;
+}
+
 // This CTA's unit over many sequences: the table in shared memory and
 // block-wide selections.  Every thread calls it (block barriers inside).
 __device__ __forceinline__ Unit plan_unit_table(const int32_t* qs, int nseq, int H, int qpairs,
@@ -292,7 +340,10 @@ __device__ __noinline__ void plan_small(const int32_t* qs, const int32_t* ctx, i
   }
   const int k = lane < nseq ? table_entry(q1 - q0, qpairs) : 0;
   int tot = 0;
-  Unit u = plan_unit_warp(k, H, qpairs, sms, b, &tot);
+  const int kmin = __reduce_min_sync(kFullMask, lane < nseq ? k : 0x7fffffff);
+  const int kmax = __reduce_max_sync(kFullMask, lane < nseq ? k : -0x7fffffff);
+  Unit u = kmin == kmax && kmin > 0 ? plan_unit_uniform(nseq, kmin, H, sms, b, &tot)
+                                    : plan_unit_warp(k, H, qpairs, sms, b, &tot);
   const int src = u.kind != 0 ? u.s : 0;
   u.q0 = __shfl_sync(kFullMask, q0, src);
   u.q_len = __shfl_sync(kFullMask, q1, src) - u.q0;

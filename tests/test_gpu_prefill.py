@@ -221,3 +221,18 @@ def test_inputs_ready_back_to_back_calls_match_serial_calls(shape, fp8):
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
     if shape == "mixed" and not fp8:
         prefill_gate(outs[0], oracle_prefill(w), "prefill inputs_ready")
+
+
+@pytest.mark.parametrize("nseq,q_len,H", [(3, 700, 8), (7, 128, 32), (32, 300, 4), (5, 512, 32)])
+def test_prefill_uniform_chunks_every_output(nseq, q_len, H):
+    """Batches whose sequences all bring the same number of query-tile pairs take the
+    planner's closed form (the first wave's whole groups, then rank by rank); every output
+    row against the oracle (a unit mapped twice would leave another unfilled)."""
+    rng = np.random.default_rng(4400 + nseq)
+    ctx = [q_len + int(rng.integers(0, 400)) for _ in range(nseq)]
+    w = configs.prefill_workload("uniform", 4400 + nseq, [q_len] * nseq, ctx, H, 128, 16)
+    dv = gpu.materialize_prefill(w, DEV)
+    out = run_prefill(w, dv)
+    torch.cuda.synchronize()
+    prefill_gate(out, oracle_prefill(w), f"uniform S{nseq} q{q_len} H{H}")
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
