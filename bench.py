@@ -548,7 +548,9 @@ def measure_e2e(st, args, world, device):
     return {"value": round(st.bytes_per_decode * L * world / dt / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(dt * 1e3, 4), "steps": K, "cuda_graph": use_graph,
             "copies": "uploads on a copy stream ahead of the compute (waits at layers 0, 1, 2, 4, "
-                      "...); outputs read back on a second copy stream right behind the decodes; "
+                      "...; the group starting at layer g is copied once the compute reaches "
+                      "layer g // 2); outputs read back on a second copy stream right behind the "
+                      "decodes; "
                       "one copy per layer group and tensor kind (per-layer buffers are views of "
                       "one [L, ...] tensor on each side)",
             "copies_per_step": sum(len(r) for r in st.step.host["up_runs"].values()) +

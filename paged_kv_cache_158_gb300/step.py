@@ -192,6 +192,7 @@ class DecodeStep:
                       (token_seq, self.token_seq), (token_pos, self.token_pos)],
             "up": torch.cuda.Stream(dev), "down": torch.cuda.Stream(dev),
             "ev_in": [torch.cuda.Event() for _ in range(n)],
+            "ev_gate": [torch.cuda.Event() for _ in range(n)],
             "ev_out": [torch.cuda.Event() for _ in range(n)],
         }
 
@@ -207,11 +208,21 @@ class DecodeStep:
         up.wait_stream(s)
         down.wait_stream(s)
         groups = _pow2_groups(self.num_layers)
-        with torch.cuda.stream(up):
-            for g0, g1 in groups:
+        L = self.num_layers
+
+        def upload(g0):
+            with torch.cuda.stream(up):
                 for h, d in hb["up_runs"][g0]:
                     d.copy_(h, non_blocking=True)
                 hb["ev_in"][g0].record(up)
+
+        # Uploads are paced: group [g0, g1) starts copying when the compute reaches layer
+        # g0 // 2, half the group's length ahead of its first use.  Issuing every upload at the
+        # step's start makes a burst of host-to-device writes that slows the first layers'
+        # decode more than its bytes suggest (13B-shaped step: 4.16 vs 4.05 ms).
+        gate = {}
+        for g0, _ in groups:
+            gate.setdefault(g0 // 2, []).append(g0)
         with torch.cuda.stream(s):
             for h, d in hb["small"]:
                 d.copy_(h, non_blocking=True)
@@ -224,9 +235,13 @@ class DecodeStep:
                             self.block_size, self.num_blocks, s)
         starts = {g0 for g0, _ in groups}
         # Downloads in the mirror-image groups: ..., 4, 2, 1, 1 layers at the end.
-        L = self.num_layers
         ends = {L - g0: L - g1 for g0, g1 in groups}   # group end (exclusive) -> group start
         for i in range(L):
+            for g0 in gate.get(i, []):
+                if i > 0:
+                    hb["ev_gate"][g0].record(s)
+                    up.wait_event(hb["ev_gate"][g0])
+                upload(g0)
             if i in starts:
                 s.wait_event(hb["ev_in"][i])
             self._write(i, s)
