@@ -519,7 +519,13 @@ def measure_e2e(st, args, world, device):
     h_q = list(pin(torch.stack(dw.queries)).unbind(0))
     h_k = list(pin(torch.stack(dw.keys_new)).unbind(0))
     h_v = list(pin(torch.stack(dw.values_new)).unbind(0))
-    h_small = [pin(t) for t in (dw.block_tables, dw.context_lens, dw.token_seq, dw.token_pos)]
+    # The small int32 inputs back to back in one pinned buffer (one upload, like the device side).
+    smalls = (dw.block_tables, dw.context_lens, dw.token_seq, dw.token_pos)
+    flat = pin(torch.cat([t.reshape(-1) for t in smalls]))
+    h_small, off = [], 0
+    for t in smalls:
+        h_small.append(flat[off:off + t.numel()].view(t.shape))
+        off += t.numel()
     h_out = list(torch.empty((len(st.outs),) + tuple(st.outs[0].shape), dtype=st.outs[0].dtype,
                              pin_memory=True).unbind(0))
     h2d = sum(t.numel() * t.element_size() for t in h_q + h_k + h_v + h_small)
@@ -554,7 +560,8 @@ def measure_e2e(st, args, world, device):
                       "one copy per layer group and tensor kind (per-layer buffers are views of "
                       "one [L, ...] tensor on each side)",
             "copies_per_step": sum(len(r) for r in st.step.host["up_runs"].values()) +
-                               sum(len(r) for r in st.step.host["down_runs"].values()) + 4,
+                               sum(len(r) for r in st.step.host["down_runs"].values()) +
+                               len(st.step.host["small_runs"]),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 

@@ -185,8 +185,10 @@ class DecodeStep:
                    for g0, g1 in groups}
         down_runs = {n - g0: _copy_runs([(self.outs[j], outs[j]) for j in range(n - g1, n - g0)])
                      for g0, g1 in groups}
+        small = [(block_tables, self.block_tables), (context_lens, self.context_lens),
+                 (token_seq, self.token_seq), (token_pos, self.token_pos)]
         self.host = {
-            "up_runs": up_runs, "down_runs": down_runs,
+            "up_runs": up_runs, "down_runs": down_runs, "small_runs": _copy_runs(small),
             "q": list(queries), "k": list(keys_new), "v": list(values_new), "out": list(outs),
             "small": [(block_tables, self.block_tables), (context_lens, self.context_lens),
                       (token_seq, self.token_seq), (token_pos, self.token_pos)],
@@ -224,7 +226,7 @@ class DecodeStep:
         for g0, _ in groups:
             gate.setdefault(g0 // 2, []).append(g0)
         with torch.cuda.stream(s):
-            for h, d in hb["small"]:
+            for h, d in hb["small_runs"]:
                 d.copy_(h, non_blocking=True)
         f8 = self.fp8_scales
         if self.copy_pairs is not None and self.copy_pairs.numel():

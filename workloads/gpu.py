@@ -97,10 +97,18 @@ def materialize(w: Workload, layers=None, device="cuda", fill_caches: bool = Tru
     # Each kind's per-layer tensors are views of one [L, ...] allocation, so consecutive
     # layers' rows lie back to back (the decode step can then upload several layers in one copy).
     qs, kn, vn = _stacked(qs), _stacked(kn), _stacked(vn)
-    bt = None if w.block_tables is None else torch.from_numpy(w.block_tables).to(device)
-    return DeviceWorkload(w, kcs, vcs, qs, kn, vn, bt, torch.from_numpy(w.context_lens).to(device),
-                          torch.from_numpy(tok_seq).to(device), torch.from_numpy(tok_pos).to(device),
-                          layers)
+    # The step's small int32 inputs (block tables, context lengths, new tokens' sequences and
+    # positions) as views of one allocation, back to back (one upload in the decode step).
+    small = [np.ascontiguousarray(a, dtype=np.int32) for a in
+             (w.block_tables if w.block_tables is not None else np.zeros((0,), np.int32),
+              w.context_lens, tok_seq, tok_pos)]
+    flat = torch.from_numpy(np.concatenate([a.reshape(-1) for a in small])).to(device)
+    views, off = [], 0
+    for a in small:
+        views.append(flat[off:off + a.size].view(a.shape))
+        off += a.size
+    bt = None if w.block_tables is None else views[0]
+    return DeviceWorkload(w, kcs, vcs, qs, kn, vn, bt, views[1], views[2], views[3], layers)
 
 
 def _stacked(ts: list) -> list:
