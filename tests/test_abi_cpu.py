@@ -202,3 +202,21 @@ def test_partition_size_follows_batch_size():
         assert pa.pa_decode_partition_tokens(256, 32, 4096) == 128
     finally:
         pa.pa_decode_set_partition_tokens(0)
+
+
+def test_plain_c_caller_links_and_gets_host_side_answers(tmp_path):
+    """A C program (tests/c_abi/host_paths.c) compiled against include/pa.h and linked with
+    libpa.so, no Python in between: status strings, workspace and partition sizes, and bad
+    arguments refused before any CUDA call."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    exe = tmp_path / "host_paths"
+    lib_dir = os.path.dirname(LIB)
+    subprocess.run([gcc, "-std=c11", "-O1", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "c_abi", "host_paths.c"), "-L", lib_dir, "-lpa",
+                    "-Wl,-rpath," + lib_dir, "-o", str(exe)], check=True)
+    res = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert res.returncode == 0 and res.stdout.strip() == "ok", res.stdout + res.stderr
