@@ -879,14 +879,18 @@ def run_prefill_bench(args):
     # own output, so the calls pass PA_PREFILL_INPUTS_READY and a call's first CTAs start on the
     # SMs the previous call's last wave leaves idle.  The same calls without the flag (each
     # waits for the previous one before it reads anything) are timed too: serial_ms_per_call.
+    # The caller knows its batch: it passes the count of one-token sequences, which sizes the
+    # launch exactly and lets one CTA run four heads of a decode row.
+    n_rows = int(np.sum(np.asarray(w.extra["q_lens"]) == 1))
+
     def call(i=0, flags=pa.PA_PREFILL_INPUTS_READY):
         dv = copies[i % NCOPY]
         args = (dv["out"], dv["query"], dv["key_cache"], dv["value_cache"], dv["block_tables"],
                 dv["context_lens"], dv["query_start"], w.scale)
         if fp8:
-            pa.pa_prefill_fp8_ex(*args, ks, vs, max_q, flags)
+            pa.pa_prefill_fp8_ex(*args, ks, vs, max_q, n_rows, flags)
         else:
-            pa.pa_prefill_ex(*args, max_q, flags)
+            pa.pa_prefill_ex(*args, max_q, n_rows, flags)
 
     K, W = max(3, min(args.steps, 200)), max(3, args.warmup)
     for i in range(W):
@@ -937,6 +941,7 @@ def run_prefill_bench(args):
                                         "num_heads": w.num_heads, "head_dim": w.head_dim,
                                         "block_size": w.block_size, "query_tokens": tq,
                                         "context_tokens": int(np.sum(w.context_lens)),
+                                        "num_decode_rows_passed": n_rows,
                                         "l2": f"inputs larger than L2: consecutive calls rotate "
                                               f"over {NCOPY} copies of the inputs "
                                               f"({NCOPY * input_bytes / 1e6:.0f} MB in all)"},

@@ -298,15 +298,19 @@ pa_status pa_copy_blocks(void* const* key_caches, void* const* value_caches, int
  *   query_start    int32 [num_seqs + 1], non-decreasing, query_start[0] = 0,
  *                  query_start[num_seqs] = num_query_tokens
  *   max_query_len  host-side upper bound of q_len (sizes the launch)
- * A sequence with q_len < 0, q_len > c_s, c_s past its table or q_len >
- * max_query_len is skipped and flagged PA_ERRBIT_CONTEXT; a block id outside
+ * A sequence with q_len < 0, q_len > c_s, c_s past its table, q_len >
+ * max_query_len or query rows outside [0, num_query_tokens) is skipped and
+ * flagged PA_ERRBIT_CONTEXT; a block id outside
  * [0, num_blocks) reads zeros and is flagged PA_ERRBIT_BLOCK_ID.
  *
  * Supported: head_dim in {64, 128}, block_size in {8, 16, 32}, num_blocks *
  * num_heads * block_size < 2^31.  Chunks (q_len >= 2) run on the tensor
  * cores (tcgen05.mma, fp16 operands, fp32 accumulation in tensor memory);
  * one-token rows run in the same launch on CUDA cores, with the decode
- * kernel's fp32 online softmax over the whole context.  The softmax weights
+ * kernel's fp32 online softmax over the whole context: one CTA per row and
+ * head, or per row and four heads when the launch knows how many one-token
+ * rows the batch holds (max_query_len == 1, or num_decode_rows given to
+ * pa_prefill_ex / pa_prefill_fp8_ex).  The softmax weights
  * are computed in fp32 and rounded once to fp16 for the second product (the
  * denominator sums them in fp32); the result is rounded once to fp16.  The
  * call allocates nothing; batches of more than 4096 sequences take one
@@ -337,10 +341,24 @@ pa_status pa_prefill_fp8(void* out, const void* query, const void* key_cache,
                          float k_scale, float v_scale, int max_query_len, pa_stream_t stream);
 
 /*
- * pa_prefill and pa_prefill_fp8 with flags.  With flags == 0 they are
- * pa_prefill and pa_prefill_fp8.  The kernel may start while the kernel
- * enqueued just before the call still runs (programmatic launch); by default
- * it waits for that kernel before it reads any input.
+ * pa_prefill and pa_prefill_fp8 with a batch-composition hint and flags.
+ * With num_decode_rows == -1 and flags == 0 they are pa_prefill and
+ * pa_prefill_fp8.
+ *
+ * num_decode_rows: the number of sequences with q_len == 1 (decode rows), or
+ * -1 when the caller does not know it.  Not part of the pages: the launch
+ * is sized from it, so that each one-token row CTA can cover four heads
+ * (one bulk-copy stream through them, one plan and one start-up latency
+ * instead of four) with no idle CTAs.  Used when num_seqs <= 4096 (one
+ * launch); ignored otherwise.  A count other than the true one makes the
+ * launch too large (idle CTAs, correct results) or too small: then the
+ * units past the grid are not computed, their output rows are left as they
+ * were, and PA_ERRBIT_CONTEXT is set.  Outside [-1, min(num_seqs,
+ * num_query_tokens)]: PA_ERR_INVALID_ARG.
+ *
+ * The kernel may start while the kernel enqueued just before the call still
+ * runs (programmatic launch); by default it waits for that kernel before it
+ * reads any input.
  *
  * PA_PREFILL_INPUTS_READY: the kernel enqueued on the stream just before this
  * call writes none of the call's inputs (query, caches, block tables,
@@ -360,14 +378,15 @@ pa_status pa_prefill_ex(void* out, const void* query, const void* key_cache,
                         int max_blocks_per_seq, const int32_t* context_lens,
                         const int32_t* query_start, int num_seqs, int num_query_tokens,
                         int num_heads, int head_dim, int block_size, int num_blocks, float scale,
-                        int max_query_len, unsigned int flags, pa_stream_t stream);
+                        int max_query_len, int num_decode_rows, unsigned int flags,
+                        pa_stream_t stream);
 pa_status pa_prefill_fp8_ex(void* out, const void* query, const void* key_cache,
                             const void* value_cache, const int32_t* block_tables,
                             int max_blocks_per_seq, const int32_t* context_lens,
                             const int32_t* query_start, int num_seqs, int num_query_tokens,
                             int num_heads, int head_dim, int block_size, int num_blocks,
                             float scale, float k_scale, float v_scale, int max_query_len,
-                            unsigned int flags, pa_stream_t stream);
+                            int num_decode_rows, unsigned int flags, pa_stream_t stream);
 
 /*
  * Block swap between the device cache and a host copy [P4 §三: when GPU

@@ -76,10 +76,10 @@ _lib.pa_prefill_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _
                                 _i32, _i32, _f32, _f32, _f32, _i32, _vp]
 _lib.pa_prefill_fp8.restype = _i32
 _lib.pa_prefill_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
-                               _i32, _f32, _i32, ctypes.c_uint32, _vp]
+                               _i32, _f32, _i32, _i32, ctypes.c_uint32, _vp]
 _lib.pa_prefill_ex.restype = _i32
 _lib.pa_prefill_fp8_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
-                                   _i32, _i32, _f32, _f32, _f32, _i32, ctypes.c_uint32, _vp]
+                                   _i32, _i32, _f32, _f32, _f32, _i32, _i32, ctypes.c_uint32, _vp]
 _lib.pa_prefill_fp8_ex.restype = _i32
 _lib.pa_swap_blocks.argtypes = [_vp, _vp, _i32, _vp, _i32, _sz, ctypes.c_int64, ctypes.c_int64, _vp]
 _lib.pa_swap_blocks.restype = _i32
@@ -387,21 +387,23 @@ def pa_prefill(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
 
 def pa_prefill_ex(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
                   value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
-                  query_start: torch.Tensor, scale: float, max_query_len: int, flags: int = 0,
-                  stream=None) -> None:
-    """pa_prefill with flags (PA_PREFILL_INPUTS_READY; see pa_prefill_ex in include/pa.h)."""
+                  query_start: torch.Tensor, scale: float, max_query_len: int,
+                  num_decode_rows: int = -1, flags: int = 0, stream=None) -> None:
+    """pa_prefill with the batch's count of one-token sequences (-1: not known) and flags
+    (PA_PREFILL_INPUTS_READY); see pa_prefill_ex in include/pa.h."""
     _prefill(out, query, key_cache, value_cache, block_tables, context_lens, query_start, scale,
-             max_query_len, stream, None, flags)
+             max_query_len, stream, None, (int(num_decode_rows), int(flags)))
 
 
 def pa_prefill_fp8_ex(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
                       value_cache: torch.Tensor, block_tables: torch.Tensor,
                       context_lens: torch.Tensor, query_start: torch.Tensor, scale: float,
-                      k_scale: float, v_scale: float, max_query_len: int, flags: int = 0,
-                      stream=None) -> None:
-    """pa_prefill_fp8 with flags (see pa_prefill_ex in include/pa.h)."""
+                      k_scale: float, v_scale: float, max_query_len: int,
+                      num_decode_rows: int = -1, flags: int = 0, stream=None) -> None:
+    """pa_prefill_fp8 with the count of one-token sequences and flags (see pa_prefill_ex in
+    include/pa.h)."""
     _prefill(out, query, key_cache, value_cache, block_tables, context_lens, query_start, scale,
-             max_query_len, stream, (float(k_scale), float(v_scale)), flags)
+             max_query_len, stream, (float(k_scale), float(v_scale)), (int(num_decode_rows), int(flags)))
 
 
 def pa_prefill_fp8(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
@@ -414,7 +416,7 @@ def pa_prefill_fp8(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tens
 
 
 def _prefill(out, query, key_cache, value_cache, block_tables, context_lens, query_start, scale,
-             max_query_len, stream, fp8, flags=None) -> None:
+             max_query_len, stream, fp8, ex=None) -> None:
     TQ, H, D = query.shape
     NB, H2, B, D2 = key_cache.shape
     S = context_lens.shape[0]
@@ -430,10 +432,10 @@ def _prefill(out, query, key_cache, value_cache, block_tables, context_lens, que
               _ptr(block_tables, "block_tables", torch.int32), block_tables.shape[1],
               _ptr(context_lens, "context_lens", torch.int32),
               _ptr(query_start, "query_start", torch.int32), S, TQ, H, D, B, NB, float(scale))
-    name = "pa_prefill" + ("_fp8" if fp8 is not None else "") + ("_ex" if flags is not None else "")
+    name = "pa_prefill" + ("_fp8" if fp8 is not None else "") + ("_ex" if ex is not None else "")
     args = common + ((fp8[0], fp8[1]) if fp8 is not None else ()) + (int(max_query_len),)
-    if flags is not None:
-        args += (int(flags),)
+    if ex is not None:  # (num_decode_rows, flags)
+        args += ex
     st = getattr(_lib, name)(*args, _stream(stream))
     _check(st, name)
 

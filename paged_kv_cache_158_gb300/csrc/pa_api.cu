@@ -553,12 +553,14 @@ static pa_status prefill_impl(bool fp8, void* out, const void* query, const void
                               const int32_t* query_start, int num_seqs, int num_query_tokens,
                               int num_heads, int head_dim, int block_size, int num_blocks,
                               float scale, float k_scale, float v_scale, int max_query_len,
-                              unsigned int flags, pa_stream_t stream) {
+                              int num_decode_rows, unsigned int flags, pa_stream_t stream) {
   if (!head_dim_ok(head_dim) || !(block_size == 8 || block_size == 16 || block_size == 32))
     return PA_ERR_UNSUPPORTED;
   if (flags & ~PA_PREFILL_INPUTS_READY) return PA_ERR_INVALID_ARG;
   if (num_seqs < 0 || num_query_tokens < 0 || num_heads <= 0 || num_blocks <= 0 ||
       max_blocks_per_seq <= 0 || max_query_len < 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_decode_rows < -1 || num_decode_rows > num_seqs || num_decode_rows > num_query_tokens)
     return PA_ERR_INVALID_ARG;
   if (fp8 && (!scale_ok(k_scale) || !scale_ok(v_scale))) return PA_ERR_INVALID_ARG;
   if (num_seqs == 0 || num_query_tokens == 0 || max_query_len == 0) return PA_OK;
@@ -596,6 +598,7 @@ static pa_status prefill_impl(bool fp8, void* out, const void* query, const void
   g.scale_log2 = (float)((double)scale * (fp8 ? (double)k_scale : 1.0) *
                          1.4426950408889634073599246810019);
   g.inputs_ready = (flags & PA_PREFILL_INPUTS_READY) != 0;
+  g.num_decode_rows = num_decode_rows;
   return pa::launch_prefill(g, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
@@ -608,7 +611,7 @@ pa_status pa_prefill(void* out, const void* query, const void* key_cache, const 
                      int num_blocks, float scale, int max_query_len, pa_stream_t stream) {
   return prefill_impl(false, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
                       context_lens, query_start, num_seqs, num_query_tokens, num_heads, head_dim,
-                      block_size, num_blocks, scale, 1.f, 1.f, max_query_len, 0u, stream);
+                      block_size, num_blocks, scale, 1.f, 1.f, max_query_len, -1, 0u, stream);
 }
 
 pa_status pa_prefill_ex(void* out, const void* query, const void* key_cache,
@@ -616,10 +619,12 @@ pa_status pa_prefill_ex(void* out, const void* query, const void* key_cache,
                         int max_blocks_per_seq, const int32_t* context_lens,
                         const int32_t* query_start, int num_seqs, int num_query_tokens,
                         int num_heads, int head_dim, int block_size, int num_blocks, float scale,
-                        int max_query_len, unsigned int flags, pa_stream_t stream) {
+                        int max_query_len, int num_decode_rows, unsigned int flags,
+                        pa_stream_t stream) {
   return prefill_impl(false, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
                       context_lens, query_start, num_seqs, num_query_tokens, num_heads, head_dim,
-                      block_size, num_blocks, scale, 1.f, 1.f, max_query_len, flags, stream);
+                      block_size, num_blocks, scale, 1.f, 1.f, max_query_len, num_decode_rows,
+                      flags, stream);
 }
 
 pa_status pa_prefill_fp8(void* out, const void* query, const void* key_cache,
@@ -630,7 +635,8 @@ pa_status pa_prefill_fp8(void* out, const void* query, const void* key_cache,
                          float k_scale, float v_scale, int max_query_len, pa_stream_t stream) {
   return prefill_impl(true, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
                       context_lens, query_start, num_seqs, num_query_tokens, num_heads, head_dim,
-                      block_size, num_blocks, scale, k_scale, v_scale, max_query_len, 0u, stream);
+                      block_size, num_blocks, scale, k_scale, v_scale, max_query_len, -1, 0u,
+                      stream);
 }
 
 pa_status pa_prefill_fp8_ex(void* out, const void* query, const void* key_cache,
@@ -639,11 +645,11 @@ pa_status pa_prefill_fp8_ex(void* out, const void* query, const void* key_cache,
                             const int32_t* query_start, int num_seqs, int num_query_tokens,
                             int num_heads, int head_dim, int block_size, int num_blocks,
                             float scale, float k_scale, float v_scale, int max_query_len,
-                            unsigned int flags, pa_stream_t stream) {
+                            int num_decode_rows, unsigned int flags, pa_stream_t stream) {
   return prefill_impl(true, out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
                       context_lens, query_start, num_seqs, num_query_tokens, num_heads, head_dim,
-                      block_size, num_blocks, scale, k_scale, v_scale, max_query_len, flags,
-                      stream);
+                      block_size, num_blocks, scale, k_scale, v_scale, max_query_len,
+                      num_decode_rows, flags, stream);
 }
 
 pa_status pa_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,

@@ -119,6 +119,7 @@ struct PrefillArgs {
   bool fp8;           // E4M3 caches (uint8 codes)
   float v_scale;      // FP8 caches: value scale
   bool inputs_ready;  // the kernel before the call writes none of its inputs (read before the wait)
+  int num_decode_rows;  // the call's one-token sequences, or -1 when the caller does not say
 };
 cudaError_t launch_prefill(const PrefillArgs& args, cudaStream_t stream);
 // The cache's rows (num_blocks * num_heads * block_size) fit the kernel's int coordinates.

@@ -131,6 +131,8 @@ struct PrefillParams {
   float scale_log2;              // scale * log2(e), times the key scale for FP8 caches
   float v_scale;                 // value scale (1 for fp16 caches)
   int inputs_ready;              // 1: inputs are read before the wait, outputs stored after it
+  int row_heads;                 // heads per decode-row unit (1 .. prows::kMaxRowHeads)
+  int num_query_tokens;          // rows of query and out
 };
 
 // Per-CTA geometry of one query tile (x = 0, 1 of the pair).
@@ -260,12 +262,12 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
   if (a.num_seqs <= 32) {
     if (warp == 1)
       prows::plan_small(a.query_start + a.seq_begin, a.context_lens + a.seq_begin, a.num_seqs, H,
-                        a.qpairs, a.sms, (int)blockIdx.x, unit_s, scratch + 19);
+                        a.row_heads, a.qpairs, a.sms, (int)blockIdx.x, unit_s, scratch + 19);
   } else {
     int tot = 0;
     const prows::Unit u = prows::plan_unit_block(a.query_start + a.seq_begin,
                                                  a.context_lens + a.seq_begin, a.num_seqs, H,
-                                                 a.qpairs, a.sms, (int)blockIdx.x,
+                                                 a.row_heads, a.qpairs, a.sms, (int)blockIdx.x,
                                                  reinterpret_cast<int*>(sm), scratch, &tot);
     if (tid == 0) {
       *unit_s = u;
@@ -287,14 +289,15 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
       pdl_launch_dependents();
       const int s = a.seq_begin + unit.s, q_len = unit.q_len, c = unit.c;
       const bool bad = q_len != 1 || c < 1 || c > a.max_blocks * a.block_size ||
-                       q_len > a.max_query_len;
+                       q_len > a.max_query_len || unit.q0 < 0 ||
+                       unit.q0 > a.num_query_tokens - q_len;
       if (bad && unit.h == 0 && tid == 0) atomicOr(a.err, PA_ERRBIT_CONTEXT);
       if (!bad) {
         const int32_t* bt = a.block_tables + (size_t)s * a.max_blocks;
         uint64_t* dbars = reinterpret_cast<uint64_t*>(sm + T::OFF_RBAR);
         float* pw = reinterpret_cast<float*>(sm + T::OFF_RPW);
-        if (tid == 0) {
-          for (int i = 0; i < prows::kRowWarps * 4; ++i) mbar_init(smem_u32(&dbars[i]), 1);
+        if (tid < prows::kRowWarps * 4) {
+          mbar_init(smem_u32(&dbars[tid]), 1);
           fence_mbar_init();
         }
         __syncthreads();
@@ -302,13 +305,14 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
           constexpr int NST = prows::row_stages<D, 8, F8>(T::ROW_AREA);
           prows::decode_row<D, 8, F8, NST>(a.query, a.key_cache, a.value_cache, bt, H,
                                             a.block_size, a.num_blocks, a.scale_log2, a.v_scale,
-                                            a.err, a.out, unit.h, unit.q0, c, sm, dbars, pw, fail);
+                                            a.err, a.out, unit.h, unit.nh, unit.q0, c, sm, dbars,
+                                            pw, fail);
         } else {
           constexpr int NST = prows::row_stages<D, 16, F8>(T::ROW_AREA);
           prows::decode_row<D, 16, F8, NST>(a.query, a.key_cache, a.value_cache, bt, H,
                                              a.block_size, a.num_blocks, a.scale_log2, a.v_scale,
-                                             a.err, a.out, unit.h, unit.q0, c, sm, dbars, pw,
-                                             fail);
+                                             a.err, a.out, unit.h, unit.nh, unit.q0, c, sm, dbars,
+                                             pw, fail);
         }
       }
     }
@@ -329,7 +333,7 @@ __global__ void __launch_bounds__(PrefillTraits<D, F8>::THREADS, 1)
   const int q_len = __shfl_sync(kFullMask, unit.q_len, 0);
   const int c = __shfl_sync(kFullMask, unit.c, 0);
   const bool bad = q_len < 0 || q_len > c || c > a.max_blocks * a.block_size ||
-                   q_len > a.max_query_len;
+                   q_len > a.max_query_len || q0 < 0 || q0 > a.num_query_tokens - q_len;
   if (bad && pq == 0 && h == 0 && tid == 0) atomicOr(a.err, PA_ERRBIT_CONTEXT);
   QTile qx[2];
 #pragma unroll
@@ -819,17 +823,31 @@ cudaError_t launch_prefill_t(const PrefillArgs& g, cudaStream_t stream) {
   p.scale_log2 = g.scale_log2;
   p.v_scale = F8 ? g.v_scale : 1.f;
   p.inputs_ready = g.inputs_ready ? 1 : 0;
+  p.num_query_tokens = g.num_query_tokens;
   // One launch per window of sequences.  The grid bounds the window's units:
   // a sequence of q tokens needs ceil(q / 256) units per head, at most qpairs,
-  // and over the window sum(ceil(q / 256)) <= (TQ + 255 * n) / 256.
+  // and over the window sum(ceil(q / 256)) <= (TQ + 255 * n) / 256.  A decode
+  // row (q = 1) is one unit per head within that bound.  When the window's
+  // count r of decode rows is known, the rows' units are counted exactly
+  // (RowSplit) and the other n - r sequences hold the other TQ - r tokens; a
+  // unit then covers up to kMaxRowHeads heads of a row.  r
+  // is known when no sequence has more than one token (r <= n; shorter ones
+  // have no units) or from the caller for a call of one window.
   for (int sb = 0; sb < g.num_seqs; sb += kSeqsPerLaunch) {
     const int n = g.num_seqs - sb < kSeqsPerLaunch ? g.num_seqs - sb : kSeqsPerLaunch;
     p.seq_begin = sb;
     p.num_seqs = n;
-    long long per_head = (long long)n * p.qpairs;
-    const long long by_tokens = ((long long)g.num_query_tokens + 255LL * n) / 256;
+    const int r = g.max_query_len == 1 ? n
+                  : g.num_seqs <= kSeqsPerLaunch ? g.num_decode_rows : -1;
+    p.row_heads = r >= 0 ? prows::kMaxRowHeads : 1;
+    const int nc = r >= 0 ? (n > r ? n - r : 0) : n;  // the other sequences and their tokens
+    long long tc = r >= 0 ? (long long)g.num_query_tokens - r : g.num_query_tokens;
+    if (tc < 0) tc = 0;
+    long long per_head = (long long)nc * p.qpairs;
+    const long long by_tokens = (tc + 255LL * nc) / 256;
     if (by_tokens < per_head) per_head = by_tokens;
-    const long long grid = per_head * g.num_heads;
+    long long grid = per_head * g.num_heads;
+    if (r > 0) grid += prows::RowSplit(r, g.num_heads, p.row_heads, p.sms).units(g.num_heads);
     if (grid <= 0) continue;
     const cudaError_t e = launch_pdl(prefill_kernel<D, F8>, dim3((unsigned)grid),
                                      dim3(T::THREADS), (size_t)T::SMEM, stream, tq, tk, tv, p);

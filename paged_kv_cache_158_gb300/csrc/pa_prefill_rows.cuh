@@ -37,6 +37,9 @@ constexpr int kDecodeRowKind = -1;  // table entry of a one-token row (CUDA-core
 constexpr int kNW = 12;             // warps per CTA
 constexpr int kThreads = kNW * 32;
 constexpr int kRowWarps = 12;       // warps that run a decode row
+constexpr int kMaxRowHeads = 4;     // most heads of one decode-row unit
+static_assert(kRowWarps % 2 == 0 && kRowWarps % 3 == 0 && kRowWarps % 4 == 0,
+              "every head count up to kMaxRowHeads divides the row warps");
 
 // Exclusive scan of one int per thread over the block; *total gets the sum.
 // scratch[0..11] is used; ends with a barrier, so scratch may be reused.
@@ -109,12 +112,44 @@ __device__ __forceinline__ int2 block_select(const int* table, int n, int target
 struct Unit {
   int kind;  // 0: none (past the launch's units), 1: pair of query tiles, 2: decode row
   int s;     // sequence within the launch
-  int h;
+  int h;     // head (kind 1); first head (kind 2)
   int pq;    // pair of query tiles (kind 1)
   int q0;    // the sequence's first query row, its query length and context length
   int q_len;
   int c;
+  int nh;    // heads h .. h + nh - 1 (kind 2)
 };
+
+// Decode-row units.  With G heads per unit (G > 1) the rows come first in
+// units of G heads (a row's last unit may hold fewer), except the last
+// `tail` rows, which take one unit per head so that the launch ends on short
+// units; with G == 1 every row is one unit per head.  nd: the launch's decode
+// rows; sms: the SM count.
+struct RowSplit {
+  int ru;    // units of a grouped row
+  int tail;  // rows at one unit per head
+  int gu;    // units of the grouped rows
+  __host__ __device__ RowSplit(int nd, int H, int G, int sms) {
+    ru = (H + G - 1) / G;
+    const int wave = (sms + H - 1) / H;  // rows that fill one wave at one unit per head
+    tail = G == 1 ? nd : (nd < wave ? nd : wave);
+    gu = (nd - tail) * ru;
+  }
+  __host__ __device__ int units(int H) const { return gu + tail * H; }
+};
+
+// Row unit rho (0 <= rho < RowSplit::units): the row's index among the
+// launch's decode rows (sequence order), its first head and head count.
+__device__ __forceinline__ int3 row_unit(const RowSplit& rs, int H, int G, int rho) {
+  if (rho < rs.gu) {
+    const int i = rho / rs.ru;
+    const int h = (rho - i * rs.ru) * G;
+    return make_int3(i, h, min(G, H - h));
+  }
+  rho -= rs.gu;
+  const int i = rho / H;
+  return make_int3(rs.gu / rs.ru + i, rho - i * H, 1);
+}
 
 // Table entry of a sequence with q new tokens: pairs of query tiles, a decode
 // row, or nothing.  A negative length gets one unit, which reports it; a
@@ -143,20 +178,22 @@ __device__ __forceinline__ int2 warp_select(int w, int target) {
 }
 
 // The unit order of plan_unit for at most 32 sequences, on one warp (lane i
-// holds sequence i's table entry k).
-__device__ __forceinline__ Unit plan_unit_warp(int k, int H, int qpairs, int sms, int b,
+// holds sequence i's table entry k).  G: heads per decode-row unit.
+__device__ __forceinline__ Unit plan_unit_warp(int k, int H, int G, int qpairs, int sms, int b,
                                                int* total_units) {
-  Unit u{0, 0, 0, 0, 0, 0, 0};
+  Unit u{0, 0, 0, 0, 0, 0, 0, 0};
   const int lane = threadIdx.x & 31;
   const int cu = __reduce_add_sync(kFullMask, k > 0 ? H * k : 0);
   const int nd = __reduce_add_sync(kFullMask, k == kDecodeRowKind ? 1 : 0);
-  *total_units = cu + nd * H;
-  if (b >= cu + nd * H) return u;
+  const RowSplit rs(nd, H, G, sms);
+  *total_units = cu + rs.units(H);
+  if (b >= cu + rs.units(H)) return u;
   if (b >= cu) {
-    const int2 r = warp_select(k == kDecodeRowKind ? H : 0, b - cu);
+    const int3 r = row_unit(rs, H, G, b - cu);
     u.kind = 2;
-    u.s = r.x;
+    u.s = warp_select(k == kDecodeRowKind ? 1 : 0, r.x).x;
     u.h = r.y;
+    u.nh = r.z;
     return u;
   }
   const int wu = k > 0 ? H * k : 0;
@@ -204,7 +241,7 @@ __device__ __forceinline__ Unit plan_unit_warp(int k, int H, int qpairs, int sms
 // selections (every lane computes the same unit).
 __device__ __forceinline__ Unit plan_unit_uniform(int nseq, int k, int H, int sms, int b,
                                                   int* total_units) {
-  Unit u{0, 0, 0, 0, 0, 0, 0};
+  Unit u{0, 0, 0, 0, 0, 0, 0, 0};
   const int G = H * k;  // units of one sequence
   const int cu = nseq * G;
   *total_units = cu;
@@ -248,24 +285,26 @@ __device__ __forceinline__ Unit plan_unit_uniform(int nseq, int k, int H, int sm
 
 // This CTA's unit over many sequences: the table in shared memory and
 // block-wide selections.  Every thread calls it (block barriers inside).
-__device__ __forceinline__ Unit plan_unit_table(const int32_t* qs, int nseq, int H, int qpairs,
-                                               int sms, int b, int* table, int* scratch,
-                                               int* total_units) {
+__device__ __forceinline__ Unit plan_unit_table(const int32_t* qs, int nseq, int H, int G,
+                                               int qpairs, int sms, int b, int* table,
+                                               int* scratch, int* total_units) {
   for (int i = threadIdx.x; i < nseq; i += kThreads) table[i] = table_entry(qs[i + 1] - qs[i], qpairs);
   __syncthreads();
   auto chunk_units = [H](int, int k) { return k > 0 ? H * k : 0; };
   const int cu = block_sum(table, nseq, chunk_units, scratch);
   const int nd = block_sum(table, nseq, [](int, int k) { return k == kDecodeRowKind ? 1 : 0; },
                            scratch);
-  Unit u{0, 0, 0, 0, 0, 0, 0};
-  *total_units = cu + nd * H;
-  if (b >= cu + nd * H) return u;
+  Unit u{0, 0, 0, 0, 0, 0, 0, 0};
+  const RowSplit rs(nd, H, G, sms);
+  *total_units = cu + rs.units(H);
+  if (b >= cu + rs.units(H)) return u;
   if (b >= cu) {  // a decode row
-    const int2 r = block_select(table, nseq, b - cu,
-                                [H](int, int k) { return k == kDecodeRowKind ? H : 0; }, scratch);
+    const int3 r = row_unit(rs, H, G, b - cu);
     u.kind = 2;
-    u.s = r.x;
+    u.s = block_select(table, nseq, r.x, [](int, int k) { return k == kDecodeRowKind ? 1 : 0; },
+                       scratch).x;
     u.h = r.y;
+    u.nh = r.z;
     return u;
   }
   // Chunk pairs.  First wave: the whole groups whose pairs fit one CTA per SM.
@@ -314,9 +353,9 @@ __device__ __forceinline__ Unit plan_unit_table(const int32_t* qs, int nseq, int
 
 // plan_unit_table with the unit's query rows and context length.
 __device__ __noinline__ Unit plan_unit_block(const int32_t* qs, const int32_t* ctx, int nseq,
-                                             int H, int qpairs, int sms, int b, int* table,
+                                             int H, int G, int qpairs, int sms, int b, int* table,
                                              int* scratch, int* total_units) {
-  Unit u = plan_unit_table(qs, nseq, H, qpairs, sms, b, table, scratch, total_units);
+  Unit u = plan_unit_table(qs, nseq, H, G, qpairs, sms, b, table, scratch, total_units);
   if (u.kind != 0) {
     u.q0 = qs[u.s];
     u.q_len = qs[u.s + 1] - u.q0;
@@ -330,7 +369,8 @@ __device__ __noinline__ Unit plan_unit_block(const int32_t* qs, const int32_t* c
 // context length, and the launch's unit count to *total_units.  qs, ctx:
 // query_start and context_lens of the launch's first sequence.
 __device__ __noinline__ void plan_small(const int32_t* qs, const int32_t* ctx, int nseq, int H,
-                                        int qpairs, int sms, int b, Unit* res, int* total_units) {
+                                        int G, int qpairs, int sms, int b, Unit* res,
+                                        int* total_units) {
   const int lane = threadIdx.x & 31;
   int q0 = 0, q1 = 0, c = 0;
   if (lane < nseq) {
@@ -343,7 +383,7 @@ __device__ __noinline__ void plan_small(const int32_t* qs, const int32_t* ctx, i
   const int kmin = __reduce_min_sync(kFullMask, lane < nseq ? k : 0x7fffffff);
   const int kmax = __reduce_max_sync(kFullMask, lane < nseq ? k : -0x7fffffff);
   Unit u = kmin == kmax && kmin > 0 ? plan_unit_uniform(nseq, kmin, H, sms, b, &tot)
-                                    : plan_unit_warp(k, H, qpairs, sms, b, &tot);
+                                    : plan_unit_warp(k, H, G, qpairs, sms, b, &tot);
   const int src = u.kind != 0 ? u.s : 0;
   u.q0 = __shfl_sync(kFullMask, q0, src);
   u.q_len = __shfl_sync(kFullMask, q1, src) - u.q0;
@@ -363,17 +403,21 @@ constexpr int row_stages(int area) {
              : area / (kRowWarps * DecodeTraits<D, TCB, F8>::STAGE_BYTES);
 }
 
-// One decode row (head h, query/output row q0, context length c) on
-// kRowWarps warps.  ring: shared memory of at least kRowWarps * NST *
-// STAGE_BYTES bytes; bars: kRowWarps * NST initialised mbarriers (count 1);
-// pw: kRowWarps * 16 floats; fail: a shared flag.  Every thread of the CTA
-// calls it (one block barrier inside).
+// One decode row (query/output row q0, context length c) for the nh heads
+// h0 .. h0 + nh - 1 (nh divides kRowWarps) on kRowWarps warps: warp w runs
+// head w mod nh, chunk w / nh, w / nh + kRowWarps / nh, ... of it.  So the
+// heads advance through the row's blocks side by side and their K/V tiles
+// (neighbours in the [block][head] layout) are read together.  ring: shared
+// memory of at least kRowWarps * NST * STAGE_BYTES bytes; bars: kRowWarps *
+// NST initialised mbarriers (count 1); pw: kRowWarps * 16 floats; fail: a
+// shared flag.  Every thread of the CTA calls it (one block barrier inside).
 template <int D, int TCB, bool F8, int NST>
-__device__ __noinline__ void decode_row(const void* query, const void* key_cache, const void* value_cache,
-                           const int32_t* bt, int num_heads, int block_size, int num_blocks,
-                           float scale_log2, float v_scale, unsigned int* err, void* out, int h,
-                           int q0, int c, unsigned char* ring, uint64_t* bars, float* pw,
-                           int* fail) {
+__device__ __noinline__ void decode_row(const void* query, const void* key_cache,
+                                        const void* value_cache, const int32_t* bt, int num_heads,
+                                        int block_size, int num_blocks, float scale_log2,
+                                        float v_scale, unsigned int* err, void* out, int h0,
+                                        int nh, int q0, int c, unsigned char* ring,
+                                        uint64_t* bars, float* pw, int* fail) {
   using T = DecodeTraits<D, TCB, F8>;
   static_assert(NST >= 2 && NST <= 4, "stages");
   constexpr int PR = T::TC / T::BPC;   // rows per piece (a piece lies in one block)
@@ -381,8 +425,11 @@ __device__ __noinline__ void decode_row(const void* query, const void* key_cache
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool leader = lane == 0;
   const int B = block_size, H = num_heads;
+  const int wph = kRowWarps / nh;      // warps per head
+  const int g = warp % nh, wi = warp / nh;
+  const int h = h0 + g;
   const int n_chunks = (c + T::TC - 1) / T::TC;
-  const int n_my = warp < kRowWarps && warp < n_chunks ? (n_chunks - 1 - warp) / kRowWarps + 1 : 0;
+  const int n_my = wi < n_chunks ? (n_chunks - 1 - wi) / wph + 1 : 0;
   const uint64_t policy = policy_evict_first();
   const uint32_t ring_s = smem_u32(ring) + (uint32_t)(warp * NST * T::STAGE_BYTES);
   const uint32_t bar_s = smem_u32(bars) + (uint32_t)(warp * NST * 8);
@@ -395,7 +442,7 @@ __device__ __noinline__ void decode_row(const void* query, const void* key_cache
     const int k = base + lane / T::BPC;
     int id = -1;
     if (k < n_my) {
-      const int t = (warp + k * kRowWarps) * T::TC + (lane % T::BPC) * PR;
+      const int t = (wi + k * wph) * T::TC + (lane % T::BPC) * PR;
       if (t < c) id = bt[t / B];
     }
     return id;
@@ -412,8 +459,7 @@ __device__ __noinline__ void decode_row(const void* query, const void* key_cache
       ids_cur = ids_next;
       ids_next = load_ids(id_base + PPW);
     }
-    const int j = warp + k * kRowWarps;
-    const int t0 = j * T::TC;
+    const int t0 = (wi + k * wph) * T::TC;
     const int rows = min(T::TC, c - t0);
     const int wsel = (k - id_base) / PPW;
     const int src = ((k - id_base) % PPW) * T::BPC;
@@ -470,8 +516,8 @@ __device__ __noinline__ void decode_row(const void* query, const void* key_cache
     const bool ok = __all_sync(kFullMask, mbar_wait_bounded(bar_s + 8 * st, (uint32_t)(k / NST) & 1));
     if (!ok) {
       // Let this warp's other copies in flight land (bounded), then give up.
-      for (int g = k + 1; g < iss; ++g)
-        mbar_wait_bounded(bar_s + 8 * (g % NST), (uint32_t)(g / NST) & 1);
+      for (int i = k + 1; i < iss; ++i)
+        mbar_wait_bounded(bar_s + 8 * (i % NST), (uint32_t)(i / NST) & 1);
       if (leader) {
         atomicOr(err, PA_ERRBIT_TIMEOUT);
         *fail = 1;
@@ -479,7 +525,7 @@ __device__ __noinline__ void decode_row(const void* query, const void* key_cache
       break;
     }
     if (valid & (1u << st)) {
-      const int rows = min(T::TC, c - (warp + k * kRowWarps) * T::TC);
+      const int rows = min(T::TC, c - (wi + k * wph) * T::TC);
       const unsigned char* Ks = ring + (size_t)(warp * NST + st) * T::STAGE_BYTES;
       if (rows == T::TC)
         process_chunk<D, TCB, F8, true>(Ks, Ks + T::CHUNK_BYTES, rows, q, scale_log2, my_pw, lane,
@@ -496,7 +542,8 @@ __device__ __noinline__ void decode_row(const void* query, const void* key_cache
   }
 
   // Combine the row groups, publish the warp's (m, l, o) in its own first
-  // stage (all of its copies have landed), merge the warps, write the row.
+  // stage (all of its copies have landed), merge each head's warps, write the
+  // heads' output rows (contiguous, like the query rows).
 #pragma unroll
   for (int msk = T::LR; msk < 32; msk <<= 1) {
 #pragma unroll
@@ -504,34 +551,35 @@ __device__ __noinline__ void decode_row(const void* query, const void* key_cache
   }
   __syncwarp();
   float* mw = reinterpret_cast<float*>(ring + (size_t)(warp * NST) * T::STAGE_BYTES);
-  if (warp < kRowWarps && rgrp == 0) {
+  if (rgrp == 0) {
 #pragma unroll
     for (int i = 0; i < T::DPL / 4; ++i)
       reinterpret_cast<float4*>(mw + T::DPL * cidx)[i] =
           make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
   }
-  if (warp < kRowWarps && lane == 0) {
+  if (leader) {
     mw[D] = m;
     mw[D + 1] = l;
   }
   __syncthreads();
   if (*fail != 0) return;
-  for (int d = tid; d < D; d += kThreads) {
+  auto slot = [&](int w) {
+    return reinterpret_cast<const float*>(ring + (size_t)(w * NST) * T::STAGE_BYTES);
+  };
+  for (int i = tid; i < nh * D; i += kThreads) {
+    const int gi = i / D, d = i - gi * D;
     float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kRowWarps; ++w)
-      M = fmaxf(M, reinterpret_cast<const float*>(ring + (size_t)(w * NST) * T::STAGE_BYTES)[D]);
+    for (int w = gi; w < kRowWarps; w += nh) M = fmaxf(M, slot(w)[D]);
     float L = 0.f, O = 0.f;
-#pragma unroll
-    for (int w = 0; w < kRowWarps; ++w) {
-      const float* mb = reinterpret_cast<const float*>(ring + (size_t)(w * NST) * T::STAGE_BYTES);
+    for (int w = gi; w < kRowWarps; w += nh) {
+      const float* mb = slot(w);
       const float sc = mb[D] == -INFINITY ? 0.f : exp2_approx(mb[D] - M);
       L = fmaf(sc, mb[D + 1], L);
       O = fmaf(sc, mb[d], O);
     }
     if constexpr (F8) O *= v_scale;
     const float r = (c > 0 && L > 0.f) ? O / L : 0.f;
-    static_cast<__half*>(out)[((size_t)q0 * H + h) * D + d] = __float2half_rn(r);
+    static_cast<__half*>(out)[((size_t)q0 * H + h0) * D + i] = __float2half_rn(r);
   }
 }
 

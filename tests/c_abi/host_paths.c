@@ -54,8 +54,10 @@ int main(void) {
   CHECK(pa_decode_ex(d, d, d, d, i32, 4, i32, 2, 2, 128, 16, 8, 0.1f, 64, d, 1 << 20, 0x4u, 0) ==
         PA_ERR_INVALID_ARG); /* unknown flag */
   CHECK(pa_decode(0, 0, 0, 0, 0, 4, 0, 0, 2, 128, 16, 8, 0.1f, 64, 0, 0, 0) == PA_OK); /* empty */
-  CHECK(pa_prefill_ex(d, d, d, d, i32, 4, i32, i32, 2, 10, 2, 128, 16, 8, 0.1f, 8, 0x1u, 0) ==
+  CHECK(pa_prefill_ex(d, d, d, d, i32, 4, i32, i32, 2, 10, 2, 128, 16, 8, 0.1f, 8, -1, 0x1u, 0) ==
         PA_ERR_INVALID_ARG); /* unknown flag */
+  CHECK(pa_prefill_ex(d, d, d, d, i32, 4, i32, i32, 2, 10, 2, 128, 16, 8, 0.1f, 8, 3, 0u, 0) ==
+        PA_ERR_INVALID_ARG); /* more one-token sequences than sequences */
   CHECK(pa_prefill_fp8(d, d, d, d, i32, 4, i32, i32, 2, 10, 2, 128, 16, 8, 0.1f, 0.0f, 1.0f, 8,
                        0) == PA_ERR_INVALID_ARG); /* key scale 0 */
   printf("ok\n");

@@ -177,16 +177,23 @@ def test_prefill_rejects_bad_arguments_before_any_launch():
               None) == 0
     fx = lib.pa_prefill_ex
     u = ctypes.c_uint
-    fx.argtypes = [vp, vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, ctypes.c_float, i, u, vp]
-    assert fx(g, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, 8, 0x1, None) == 1   # unknown flag
-    assert fx(g, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, 8, 0x6, None) == 1
-    assert fx(g + 8, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, 8, 0x2, None) == 1
-    assert fx(None, None, None, None, None, 4, None, None, 0, 0, 2, 128, 16, 8, 0.1, 8, 0x2,
+    fx.argtypes = [vp, vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, ctypes.c_float, i, i, u, vp]
+    assert fx(g, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, 8, -1, 0x1, None) == 1  # unknown flag
+    assert fx(g, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, 8, -1, 0x6, None) == 1
+    assert fx(g + 8, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, 8, -1, 0x2, None) == 1
+    assert fx(None, None, None, None, None, 4, None, None, 0, 0, 2, 128, 16, 8, 0.1, 8, -1, 0x2,
+              None) == 0
+    # The count of one-token sequences: -1 (unknown) or 0 .. min(num_seqs, num_query_tokens).
+    assert fx(g, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, 8, -2, 0, None) == 1
+    assert fx(g, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, 8, 3, 0, None) == 1
+    assert fx(g, g, g, g, g, 4, g, g, 3, 2, 2, 128, 16, 8, 0.1, 8, 3, 0, None) == 1
+    assert fx(None, None, None, None, None, 4, None, None, 0, 0, 2, 128, 16, 8, 0.1, 8, 0, 0,
               None) == 0
     f8x = lib.pa_prefill_fp8_ex
-    f8x.argtypes = [vp, vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, fl, fl, fl, i, u, vp]
-    assert f8x(g, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, 1.0, 1.0, 8, 0x4, None) == 1
-    assert f8x(g, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, 0.0, 1.0, 8, 0x2, None) == 1
+    f8x.argtypes = [vp, vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, fl, fl, fl, i, i, u, vp]
+    assert f8x(g, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, 1.0, 1.0, 8, -1, 0x4, None) == 1
+    assert f8x(g, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, 0.0, 1.0, 8, -1, 0x2, None) == 1
+    assert f8x(g, g, g, g, g, 4, g, g, 2, 10, 2, 128, 16, 8, 0.1, 1.0, 1.0, 8, 5, 0x2, None) == 1
 
 
 def test_partition_size_follows_batch_size():

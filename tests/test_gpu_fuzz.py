@@ -100,9 +100,11 @@ def test_random_decode_step_against_oracle(i, mode):
 
 @pytest.mark.parametrize("i", range(10))
 @pytest.mark.parametrize("fp8", [False, True])
-def test_random_prefill_against_oracle(i, fp8):
+@pytest.mark.parametrize("count", [False, True])
+def test_random_prefill_against_oracle(i, fp8, count):
     """Random mixes of empty, one-token and longer chunks (some crossing several 128-row
-    tiles) over random contexts."""
+    tiles) over random contexts; count: the call is told how many one-token sequences the
+    batch holds (up to four heads of a row per CTA)."""
     rng = np.random.default_rng(9100 + i)
     D = int(rng.choice([64, 128]))
     B = int(rng.choice([8, 16, 32]))
@@ -125,10 +127,11 @@ def test_random_prefill_against_oracle(i, fp8):
     out = torch.full((tq, H, D), float("nan"), dtype=torch.float16, device=DEV)
     args = (out, dv["query"], dv["key_cache"], dv["value_cache"], dv["block_tables"],
             dv["context_lens"], dv["query_start"], w.scale)
+    n_rows = sum(1 for q in q_lens if q == 1) if count else -1
     if fp8:
-        pa.pa_prefill_fp8(*args, ks, vs, max(q_lens))
+        pa.pa_prefill_fp8_ex(*args, ks, vs, max(q_lens), n_rows)
     else:
-        pa.pa_prefill(*args, max(q_lens))
+        pa.pa_prefill_ex(*args, max(q_lens), n_rows)
     torch.cuda.synchronize()
     kc, vc = gpu.host_pool(w, 0)
     q = gpu.host_queries(w)
@@ -140,5 +143,6 @@ def test_random_prefill_against_oracle(i, fp8):
         _, ref64, rc = oracle.prefill(q, kc, vc, w.block_tables, w.context_lens,
                                       configs.query_start(w), w.scale)
     assert rc == 0
-    prefill_gate(out, ref64, f"random prefill {i} {'fp8' if fp8 else 'fp16'} D{D} B{B} S{S} H{H}")
+    prefill_gate(out, ref64, f"random prefill {i} {'fp8' if fp8 else 'fp16'} D{D} B{B} S{S} H{H} "
+                             f"count {n_rows}")
     assert pa.pa_check_errors() == (pa.PA_OK, 0)

@@ -201,9 +201,9 @@ def test_inputs_ready_back_to_back_calls_match_serial_calls(shape, fp8):
         args = (out, dv["query"], dv["key_cache"], dv["value_cache"], dv["block_tables"],
                 dv["context_lens"], dv["query_start"], w.scale)
         if fp8:
-            pa.pa_prefill_fp8_ex(*args, sc[0], sc[1], max_q, flags)
+            pa.pa_prefill_fp8_ex(*args, sc[0], sc[1], max_q, flags=flags)
         else:
-            pa.pa_prefill_ex(*args, max_q, flags)
+            pa.pa_prefill_ex(*args, max_q, flags=flags)
 
     refs = []
     for dv, sc in zip(copies, scales):
@@ -236,3 +236,96 @@ def test_prefill_uniform_chunks_every_output(nseq, q_len, H):
     torch.cuda.synchronize()
     prefill_gate(out, oracle_prefill(w), f"uniform S{nseq} q{q_len} H{H}")
     assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+def _run_ex(w, dv, n_rows, max_q=None, fp8_scales=None):
+    """pa_prefill_ex / pa_prefill_fp8_ex with the count of one-token sequences."""
+    tq = int(np.sum(w.extra["q_lens"]))
+    out = torch.full((tq, w.num_heads, w.head_dim), float("nan"), dtype=torch.float16, device=DEV)
+    args = (out, dv["query"], dv["key_cache"], dv["value_cache"], dv["block_tables"],
+            dv["context_lens"], dv["query_start"], w.scale)
+    mq = int(max(w.extra["q_lens"])) if max_q is None else max_q
+    if fp8_scales is not None:
+        pa.pa_prefill_fp8_ex(*args, fp8_scales[0], fp8_scales[1], mq, n_rows)
+    else:
+        pa.pa_prefill_ex(*args, mq, n_rows)
+    return out
+
+
+def _oracle_any(w, fp8_scales):
+    if fp8_scales is None:
+        return oracle_prefill(w)
+    kc, vc = gpu.host_pool(w, 0)
+    ks, vs = fp8_scales
+    _, ref64, rc = oracle.prefill_fp8(gpu.host_queries(w), oracle.quantize_e4m3(kc, ks),
+                                      oracle.quantize_e4m3(vc, vs), w.block_tables,
+                                      w.context_lens, configs.query_start(w), w.scale, ks, vs)
+    assert rc == 0
+    return ref64
+
+
+# One-token rows over contexts from 1 token (one chunk: eleven of the twelve warps idle,
+# most heads skipped by most warps) to several hundred, between chunks.
+ROWS_Q = [1, 300, 1, 1, 0, 1, 77, 1, 1, 1]
+ROWS_C = [1, 700, 20, 191, 40, 192, 77, 193, 650, 1000]
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("D,B,H", [(128, 16, 8), (128, 8, 6), (64, 32, 3), (64, 16, 5),
+                                   (128, 32, 1)])
+def test_prefill_decode_rows_grouped_every_output(D, B, H, fp8):
+    """With the count of one-token sequences given, a CTA runs up to four heads of a row as
+    one chunk stream (the last group of a row may be smaller); every output row of the batch
+    against the oracle, with NaN in every slot no live token uses."""
+    w = configs.prefill_workload(f"rows_D{D}_B{B}_H{H}", 4800 + D + B + H, ROWS_Q, ROWS_C, H, D, B)
+    dv = gpu.materialize_prefill(w, DEV)
+    mask = live_slot_mask(w.block_tables, w.context_lens, w.num_blocks, B)
+    poison_dead_slots_device(dv["key_cache"], dv["value_cache"], mask)
+    sc = _fp8_copy(w, dv) if fp8 else None
+    n_rows = sum(1 for q in ROWS_Q if q == 1)
+    out = _run_ex(w, dv, n_rows, fp8_scales=sc)
+    torch.cuda.synchronize()
+    if fp8:
+        ref64 = _oracle_any(w, sc)   # dead slots hold NaN codes only on the device side
+    else:
+        ref64 = oracle_prefill(w, mask)
+    prefill_gate(out, ref64, f"grouped rows D{D} B{B} H{H} {'fp8' if fp8 else 'fp16'}")
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_prefill_all_rows_grouped_without_count(fp8):
+    """max_query_len == 1: every sequence is a decode row or empty, so the launch groups four
+    heads per CTA without being told the count; every output row."""
+    rng = np.random.default_rng(4900 + fp8)
+    S = 70
+    q_lens = [0 if i % 9 == 4 else 1 for i in range(S)]
+    ctx = [int(rng.integers(1, 1500)) for _ in range(S)]
+    w = configs.prefill_workload("all_rows", 4900 + fp8, q_lens, ctx, 10, 128, 16)
+    dv = gpu.materialize_prefill(w, DEV)
+    sc = _fp8_copy(w, dv) if fp8 else None
+    out = _run_ex(w, dv, -1, fp8_scales=sc)
+    torch.cuda.synchronize()
+    prefill_gate(out, _oracle_any(w, sc), f"all rows {'fp8' if fp8 else 'fp16'}")
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+
+
+def test_prefill_wrong_decode_row_count():
+    """A count below the true one still sizes a large enough launch (each row fits the
+    chunks' bound): every output is right.  A count above it leaves the chunk's units past
+    the grid: reported as PA_ERRBIT_CONTEXT (the kernel skips them, nothing is read or
+    written out of range)."""
+    w = configs.prefill_workload("wrong_rows", 4950, [300, 1, 1, 1], [700, 64, 500, 900], 4,
+                                 128, 16)
+    dv = gpu.materialize_prefill(w, DEV)
+    out = _run_ex(w, dv, 0)
+    torch.cuda.synchronize()
+    prefill_gate(out, oracle_prefill(w), "count 0 of 3")
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+    out = _run_ex(w, dv, 2)
+    torch.cuda.synchronize()
+    prefill_gate(out, oracle_prefill(w), "count 2 of 3")
+    assert pa.pa_check_errors() == (pa.PA_OK, 0)
+    _run_ex(w, dv, 4)
+    st, bits = pa.pa_check_errors()
+    assert st == pa.PA_ERR_OUT_OF_RANGE and bits & pa.PA_ERRBIT_CONTEXT
