@@ -3,8 +3,8 @@
 //
 // Units.  A launch covers a window of sequences.  Sequence s with q_len new
 // tokens contributes, for each head, ceil(q_len / 256) units of two 128-row
-// query tiles (tensor cores), or one unit when q_len == 1 (a decode row, run
-// on CUDA cores: "vLLM推理加速深度解读：PagedAttention如何提升10x吞吐量" §4.3,
+// query tiles (tensor cores), or decode-row units when q_len == 1 (run on
+// CUDA cores: "vLLM推理加速深度解读：PagedAttention如何提升10x吞吐量" §4.3,
 // prefill and decode rows share a batch), or none when q_len == 0.  Units are
 // numbered densely, so a batch of many decode rows and a few chunks launches
 // (almost) no CTA without work:
@@ -13,19 +13,29 @@
 //     adjacent and heaviest first (they share K/V tiles through L2); the
 //     other groups follow rank by rank, every group's heaviest remaining pair
 //     before any group's next one;
-//   * the decode rows (sequence, head) follow, sequence-major.
-// Every CTA derives its unit from query_start with the whole block: one pass
-// writes a per-sequence table to shared memory (pairs, or kDecodeRowKind),
-// then weighted selections over it (block-wide scans) find the unit.
+//   * the decode rows follow, sequence-major (RowSplit): one unit per head,
+//     or, when the launch was sized from a known count of decode rows, one
+//     unit per G = kMaxRowHeads heads of a row except for the last wave of
+//     rows, which keeps one unit per head so that the launch ends on short
+//     units.
+// Every CTA derives its unit from query_start: up to 32 sequences on one
+// warp, more with the whole block (one pass writes a per-sequence table to
+// shared memory, pairs or kDecodeRowKind, then weighted selections over it,
+// block-wide scans, find the unit).
 //
-// Decode rows.  The twelve warps of the CTA split the row's context into
-// chunks (chunk j to warp j mod 12) and run the decode kernel's per-chunk
-// step (fp32 online softmax over bulk-copied K/V rows): each warp owns a ring
-// of shared-memory stages with one mbarrier per stage; lane 0 copies a
-// chunk's K rows and V rows with 1-D bulk copies.  The warps' (m, l, o) merge
-// in shared memory at the end and the CTA writes the row's fp16 output.  One
-// CTA per (sequence, head), whole context: no workspace, no merge kernel;
-// the hardware's CTA dispatch balances rows of different lengths.
+// Decode rows.  A unit of nh heads runs on the CTA's twelve warps, 12 / nh
+// per head: warp w takes head w mod nh and every (12 / nh)-th 16-token chunk
+// of its context, and runs the decode kernel's per-chunk step (fp32 online
+// softmax over bulk-copied K/V rows).  Each warp owns a ring of
+// shared-memory stages with one mbarrier per stage; lane 0 copies a chunk's
+// K rows and V rows with 1-D bulk copies.  The heads of a unit advance
+// through the row's blocks side by side, so their K/V tiles, neighbours in
+// the [block][head] layout, are read together.  At the end each head's
+// warps merge their (m, l, o) in shared memory and the CTA writes the heads'
+// fp16 outputs.  No workspace, no merge kernel; the hardware's CTA dispatch
+// balances rows of different lengths.  Grouping heads spreads one plan, one
+// start-up latency and one CTA turnover (together about 6 us against about
+// 6 us of streaming for one head of a 1300-token FP8 row) over four heads.
 #pragma once
 
 #include "pa_decode.cuh"
