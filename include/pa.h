@@ -347,14 +347,15 @@ pa_status pa_prefill_fp8(void* out, const void* query, const void* key_cache,
  *
  * num_decode_rows: the number of sequences with q_len == 1 (decode rows), or
  * -1 when the caller does not know it.  Not part of the pages: the launch
- * is sized from it, so that each one-token row CTA can cover four heads
- * (one bulk-copy stream through them, one plan and one start-up latency
- * instead of four) with no idle CTAs.  Used when num_seqs <= 4096 (one
- * launch); ignored otherwise.  A count other than the true one makes the
- * launch too large (idle CTAs, correct results) or too small: then the
- * units past the grid are not computed, their output rows are left as they
- * were, and PA_ERRBIT_CONTEXT is set.  Outside [-1, min(num_seqs,
- * num_query_tokens)]: PA_ERR_INVALID_ARG.
+ * is sized from it, so that a one-token row CTA can cover up to four heads
+ * of its row (one plan, one start-up latency and one CTA turnover instead
+ * of four; the last wave of rows keeps one head per CTA) with no idle CTAs.
+ * Used when num_seqs <= 4096 (one launch); ignored otherwise.  A count
+ * other than the true one makes the launch either larger than needed (idle
+ * CTAs, correct results) or too small: then the units past the grid are not
+ * computed, their output rows are left as they were, and PA_ERRBIT_CONTEXT
+ * is set.  Outside [-1, min(num_seqs, num_query_tokens)]:
+ * PA_ERR_INVALID_ARG.
  *
  * The kernel may start while the kernel enqueued just before the call still
  * runs (programmatic launch); by default it waits for that kernel before it
